@@ -1,0 +1,324 @@
+// api.cu — the C ABI of libbgq.so (declared in include/bgq.h).
+//
+// Every entry point validates its arguments before it enqueues anything,
+// carves the caller's workspace into the regions its kernels need, and
+// launches on the caller's stream. Nothing here allocates or synchronises.
+#include <stdint.h>
+#include <string.h>
+
+#include "../../include/bgq.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bgq {
+bool route_shape_ok(int d);
+}
+
+using namespace bgq;
+
+namespace {
+
+constexpr int kMaxBatch = 256;
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 8;
+constexpr int kMaxLayers = 128;
+
+inline bool al(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+inline cudaStream_t st(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+inline size_t up256(size_t n) { return (n + 255) & ~(size_t)255; }
+
+int check_qmatrix(const bgq_qmatrix* W) {
+  if (!W || !W->q || !W->sb) return BGQ_ERR_INVALID_ARG;
+  if (W->bits != 4 && W->bits != 2) return BGQ_ERR_INVALID_ARG;
+  if (W->group != kGroup) return BGQ_ERR_UNSUPPORTED;
+  if (W->rows <= 0 || W->cols <= 0 || W->cols % kGroup) return BGQ_ERR_INVALID_ARG;
+  if (!cols_supported(W->cols, W->bits)) return BGQ_ERR_UNSUPPORTED;
+  if (!al(W->q, 16) || !al(W->sb, 4)) return BGQ_ERR_INVALID_ARG;
+  return BGQ_OK;
+}
+
+QMat qm(const bgq_qmatrix* W) { return QMat{W->q, W->sb, W->rows, W->cols, W->bits}; }
+
+// Sequential carving of a 256-byte aligned workspace.
+struct Carver {
+  char* base;
+  size_t off = 0;
+  explicit Carver(void* b) : base(static_cast<char*>(b)) {}
+  template <typename T>
+  T* take(size_t bytes) {
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += up256(bytes);
+    return p;
+  }
+};
+
+struct LayerWs {
+  Ctrl* ctrl;
+  float* logits;  // [B][E+1] then B*K ints of selected experts
+  Plan* plan;
+  int32_t* idx;
+  float* w;
+  float* gamma;
+  float* H;  // [B][K+1][f]
+  float* Y;  // [B][K+1][d]
+  size_t bytes;
+};
+
+LayerWs carve_layer(void* ws, int B, int d, int f, int E, int K) {
+  Carver c(ws);
+  LayerWs L;
+  L.ctrl = c.take<Ctrl>(sizeof(Ctrl));
+  L.logits = c.take<float>((size_t)B * (E + 1) * 4 + (size_t)B * K * 4);
+  L.plan = c.take<Plan>(plan_bytes(B, K));
+  L.idx = c.take<int32_t>((size_t)B * K * 4);
+  L.w = c.take<float>((size_t)B * K * 4);
+  L.gamma = c.take<float>((size_t)B * 4);
+  L.H = c.take<float>((size_t)B * (K + 1) * f * 4);
+  L.Y = c.take<float>((size_t)B * (K + 1) * d * 4);
+  L.bytes = c.off;
+  return L;
+}
+
+int check_layer(const bgq_moe_layer* L) {
+  if (!L || !L->router || !L->expert_q || !L->expert_sb || !L->shared_q || !L->shared_sb) return BGQ_ERR_INVALID_ARG;
+  if (L->bits != 4 && L->bits != 2) return BGQ_ERR_INVALID_ARG;
+  if (L->group != kGroup) return BGQ_ERR_UNSUPPORTED;
+  if (L->d_model <= 0 || L->d_ff <= 0 || L->n_experts <= 0 || L->top_k <= 0) return BGQ_ERR_INVALID_ARG;
+  if (L->top_k > kMaxTopK || L->n_experts > kMaxExperts || L->top_k > L->n_experts) return BGQ_ERR_UNSUPPORTED;
+  if (!cols_supported(L->d_model, L->bits) || !cols_supported(L->d_ff, L->bits)) return BGQ_ERR_UNSUPPORTED;
+  if (!route_shape_ok(L->d_model)) return BGQ_ERR_UNSUPPORTED;
+  const long long mw = (long long)L->d_model * L->d_ff * L->bits / 32;
+  const long long mg = (long long)L->d_model * L->d_ff / kGroup * 2;
+  if (L->expert_q_stride < 3 * mw || L->expert_sb_stride < 3 * mg) return BGQ_ERR_INVALID_ARG;
+  if (L->expert_q_stride % 4 || L->expert_sb_stride % 2) return BGQ_ERR_INVALID_ARG;
+  if (!al(L->router, 16) || !al(L->expert_q, 16) || !al(L->shared_q, 16) || !al(L->expert_sb, 4) ||
+      !al(L->shared_sb, 4) || (L->shared_gate && !al(L->shared_gate, 16)))
+    return BGQ_ERR_INVALID_ARG;
+  return BGQ_OK;
+}
+
+ExpertSet expert_set(const bgq_moe_layer* L) {
+  ExpertSet es;
+  es.pool_q = L->expert_q;
+  es.pool_sb = L->expert_sb;
+  es.q_stride = L->expert_q_stride;
+  es.sb_stride = L->expert_sb_stride;
+  const long long mw = (long long)L->d_model * L->d_ff * L->bits / 32;
+  const long long mg = (long long)L->d_model * L->d_ff / kGroup * 2;
+  es.shared = ExpertRef{L->shared_q, L->shared_sb, L->shared_q + mw, L->shared_sb + mg, L->shared_q + 2 * mw,
+                        L->shared_sb + 2 * mg};
+  es.d = L->d_model;
+  es.f = L->d_ff;
+  es.bits = L->bits;
+  return es;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? BGQ_OK : BGQ_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* bgq_status_string(int32_t s) {
+  switch (s) {
+    case BGQ_OK: return "ok";
+    case BGQ_ERR_INVALID_ARG: return "invalid argument";
+    case BGQ_ERR_UNSUPPORTED: return "unsupported shape or parameter";
+    case BGQ_ERR_CUDA: return "CUDA launch or query failed";
+    case BGQ_ERR_TIMEOUT: return "a bounded device-side wait timed out";
+    case BGQ_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+int32_t bgq_abi_version(void) { return 100; }
+
+static int32_t gemv_common(const bgq_qmatrix* W, const uint16_t* x, uint16_t* y, int32_t batch, int32_t variant,
+                           int want_bits, void* stream) {
+  int r = check_qmatrix(W);
+  if (r) return r;
+  if (want_bits && W->bits != want_bits) return BGQ_ERR_INVALID_ARG;
+  if (!x || !y || !al(x, 16) || !al(y, 16)) return BGQ_ERR_INVALID_ARG;
+  if (batch < 1 || batch > 64) return BGQ_ERR_INVALID_ARG;
+  if (variant < BGQ_DQ_INT16 || variant > BGQ_DQ_HOISTED) return BGQ_ERR_INVALID_ARG;
+  return cuda_status(launch_qgemv(qm(W), x, batch, y, nullptr, variant, st(stream)));
+}
+
+int32_t q4_gemv(const bgq_qmatrix* W, const uint16_t* x, uint16_t* y, int32_t batch, void* stream) {
+  return gemv_common(W, x, y, batch, BGQ_DQ_INT16, 4, stream);
+}
+
+int32_t q2_gemv(const bgq_qmatrix* W, const uint16_t* x, uint16_t* y, int32_t batch, void* stream) {
+  return gemv_common(W, x, y, batch, BGQ_DQ_INT16, 2, stream);
+}
+
+int32_t bgq_qgemv_variant(const bgq_qmatrix* W, const uint16_t* x, uint16_t* y, int32_t batch, int32_t variant,
+                          void* stream) {
+  return gemv_common(W, x, y, batch, variant, 0, stream);
+}
+
+size_t moe_route_workspace_bytes(int32_t batch, int32_t n_experts) {
+  if (batch < 1 || n_experts < 1) return 0;
+  return sizeof(Ctrl) + up256((size_t)batch * (n_experts + 1) * 4 + (size_t)batch * kMaxTopK * 4);
+}
+
+int32_t moe_route_topk(const uint16_t* router, const uint16_t* shared_gate, const uint16_t* x, int32_t batch,
+                       int32_t d_model, int32_t n_experts, int32_t top_k, int32_t* idx, float* w, float* gamma,
+                       float* logits, void* ws, size_t ws_bytes, void* stream) {
+  if (!router || !x || !idx || !w) return BGQ_ERR_INVALID_ARG;
+  if (!al(router, 16) || !al(x, 16) || (shared_gate && !al(shared_gate, 16))) return BGQ_ERR_INVALID_ARG;
+  if (batch < 1 || batch > kMaxBatch || d_model <= 0 || n_experts <= 0 || top_k <= 0) return BGQ_ERR_INVALID_ARG;
+  if (top_k > kMaxTopK || n_experts > kMaxExperts || top_k > n_experts) return BGQ_ERR_UNSUPPORTED;
+  if (!route_shape_ok(d_model)) return BGQ_ERR_UNSUPPORTED;
+  if (!ws || !al(ws, 256) || ws_bytes < moe_route_workspace_bytes(batch, n_experts)) return BGQ_ERR_WORKSPACE;
+  Carver c(ws);
+  Ctrl* ctrl = c.take<Ctrl>(sizeof(Ctrl));
+  float* lg = c.take<float>((size_t)batch * (n_experts + 1) * 4 + (size_t)batch * top_k * 4);
+  return cuda_status(launch_route(router, shared_gate, x, batch, d_model, n_experts, top_k, lg, ctrl, idx, w, gamma,
+                                  logits, nullptr, st(stream)));
+}
+
+size_t moe_expert_workspace_bytes(const bgq_expert* e, int32_t batch) {
+  if (!e || batch < 1) return 0;
+  const int d = e->gate.cols, f = e->gate.rows;
+  return sizeof(Ctrl) + up256(plan_bytes(batch, 0)) + up256((size_t)batch * f * 4) + up256((size_t)batch * d * 4);
+}
+
+int32_t moe_expert_swiglu(const bgq_expert* e, const uint16_t* x, int32_t batch, uint16_t* y, float* y_f32,
+                          void* ws, size_t ws_bytes, void* stream) {
+  if (!e) return BGQ_ERR_INVALID_ARG;
+  int r;
+  if ((r = check_qmatrix(&e->gate)) || (r = check_qmatrix(&e->up)) || (r = check_qmatrix(&e->down))) return r;
+  const int d = e->gate.cols, f = e->gate.rows, bits = e->gate.bits;
+  if (e->up.rows != f || e->up.cols != d || e->down.rows != d || e->down.cols != f) return BGQ_ERR_INVALID_ARG;
+  if (e->up.bits != bits || e->down.bits != bits) return BGQ_ERR_INVALID_ARG;
+  if (!x || !al(x, 16) || (!y && !y_f32) || (y && !al(y, 16)) || (y_f32 && !al(y_f32, 16)))
+    return BGQ_ERR_INVALID_ARG;
+  if (batch < 1 || batch > kMaxBatch) return BGQ_ERR_INVALID_ARG;
+  if (!ws || !al(ws, 256) || ws_bytes < moe_expert_workspace_bytes(e, batch)) return BGQ_ERR_WORKSPACE;
+  Carver c(ws);
+  c.take<Ctrl>(sizeof(Ctrl));
+  Plan* plan = c.take<Plan>(plan_bytes(batch, 0));
+  float* H = c.take<float>((size_t)batch * f * 4);
+  float* Y = c.take<float>((size_t)batch * d * 4);
+  ExpertSet es{};
+  es.shared = ExpertRef{e->gate.q, e->gate.sb, e->up.q, e->up.sb, e->down.q, e->down.sb};
+  es.d = d;
+  es.f = f;
+  es.bits = bits;
+  cudaStream_t s = st(stream);
+  const int ntasks = (batch + kTaskTok - 1) / kTaskTok;
+  if (launch_plan_single(plan, batch, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  if (launch_gateup(es, plan, ntasks, x, H, 1, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  if (launch_down(es, plan, ntasks, H, Y, 1, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  return cuda_status(launch_combine(Y, nullptr, nullptr, batch, 0, d, y, y_f32, s));
+}
+
+size_t moe_layer_workspace_bytes(const bgq_moe_layer* L, int32_t max_batch) {
+  if (!L || max_batch < 1 || L->top_k < 1 || L->n_experts < 1) return 0;
+  return carve_layer(nullptr, max_batch, L->d_model, L->d_ff, L->n_experts, L->top_k).bytes;
+}
+
+static int32_t layer_forward_impl(const bgq_moe_layer* L, const uint16_t* x, int32_t batch, uint16_t* out,
+                                  float* out_f32, int32_t* idx_out, float* w_out, float* gamma_out, const LayerWs& W,
+                                  cudaStream_t s) {
+  const int K = L->top_k, E = L->n_experts;
+  int32_t* idx = idx_out ? idx_out : W.idx;
+  float* w = w_out ? w_out : W.w;
+  float* gamma = gamma_out ? gamma_out : W.gamma;
+  if (launch_route(L->router, L->shared_gate, x, batch, L->d_model, E, K, W.logits, W.ctrl, idx, w, gamma, nullptr,
+                   W.plan, s) != cudaSuccess)
+    return BGQ_ERR_CUDA;
+  const ExpertSet es = expert_set(L);
+  const int max_tasks = batch * K + (batch + kTaskTok - 1) / kTaskTok;
+  if (launch_gateup(es, W.plan, max_tasks, x, W.H, K + 1, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  if (launch_down(es, W.plan, max_tasks, W.H, W.Y, K + 1, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  return cuda_status(launch_combine(W.Y, w, gamma, batch, K, L->d_model, out, out_f32, s));
+}
+
+int32_t moe_layer_forward(const bgq_moe_layer* L, const uint16_t* x, int32_t batch, uint16_t* out, float* out_f32,
+                          int32_t* idx_out, float* w_out, float* gamma_out, void* ws, size_t ws_bytes, void* stream) {
+  int r = check_layer(L);
+  if (r) return r;
+  if (!x || !al(x, 16) || (!out && !out_f32)) return BGQ_ERR_INVALID_ARG;
+  if ((out && !al(out, 16)) || (out_f32 && !al(out_f32, 16))) return BGQ_ERR_INVALID_ARG;
+  if (batch < 1 || batch > kMaxBatch) return BGQ_ERR_INVALID_ARG;
+  if (!ws || !al(ws, 256) || ws_bytes < moe_layer_workspace_bytes(L, batch)) return BGQ_ERR_WORKSPACE;
+  LayerWs W = carve_layer(ws, batch, L->d_model, L->d_ff, L->n_experts, L->top_k);
+  return layer_forward_impl(L, x, batch, out, out_f32, idx_out, w_out, gamma_out, W, st(stream));
+}
+
+int32_t bgq_rmsnorm(const float* h, const uint16_t* rho, int32_t batch, int32_t d, float eps, uint16_t* a,
+                    void* stream) {
+  if (!h || !a || !al(h, 16) || !al(a, 16) || (rho && !al(rho, 16))) return BGQ_ERR_INVALID_ARG;
+  if (batch < 1 || batch > 65535 || d <= 0 || d % 256 || !(eps >= 0.f)) return BGQ_ERR_INVALID_ARG;
+  return cuda_status(launch_rmsnorm(h, rho, batch, d, eps, a, st(stream)));
+}
+
+int32_t bgq_residual_add(float* h, const float* delta, int64_t n, void* stream) {
+  if (!h || !delta || n < 0) return BGQ_ERR_INVALID_ARG;
+  if (n == 0) return BGQ_OK;
+  return cuda_status(launch_residual_add(h, delta, n, st(stream)));
+}
+
+size_t moe_stack_workspace_bytes(const bgq_moe_layer* layers, int32_t n_layers) {
+  if (!layers || n_layers < 1) return 0;
+  const bgq_moe_layer* L = &layers[0];
+  size_t b = moe_layer_workspace_bytes(L, 1);
+  if (!b) return 0;
+  return b + up256((size_t)L->d_model * 4) * 2 + up256((size_t)L->d_model * 2);
+}
+
+int32_t moe_stack_decode(const bgq_moe_layer* layers, const uint16_t* const* rho, int32_t n_layers, float eps,
+                         const uint16_t* x, uint16_t* x_next, float* h_out, int32_t* idx_out, void* ws,
+                         size_t ws_bytes, void* stream) {
+  if (!layers || !rho || n_layers < 1 || n_layers > kMaxLayers) return BGQ_ERR_INVALID_ARG;
+  const bgq_moe_layer* L0 = &layers[0];
+  for (int l = 0; l < n_layers; ++l) {
+    int r = check_layer(&layers[l]);
+    if (r) return r;
+    const bgq_moe_layer* L = &layers[l];
+    if (L->d_model != L0->d_model || L->d_ff != L0->d_ff || L->n_experts != L0->n_experts ||
+        L->top_k != L0->top_k || L->bits != L0->bits)
+      return BGQ_ERR_INVALID_ARG;
+    if (!rho[l] || !al(rho[l], 16)) return BGQ_ERR_INVALID_ARG;
+  }
+  if (!x || !al(x, 16) || (x_next && !al(x_next, 16)) || (h_out && !al(h_out, 16))) return BGQ_ERR_INVALID_ARG;
+  if (!(eps >= 0.f) || L0->d_model % 256) return BGQ_ERR_INVALID_ARG;
+  if (!ws || !al(ws, 256) || ws_bytes < moe_stack_workspace_bytes(layers, n_layers)) return BGQ_ERR_WORKSPACE;
+  const int d = L0->d_model, K = L0->top_k;
+  LayerWs W = carve_layer(ws, 1, d, L0->d_ff, L0->n_experts, K);
+  Carver c(static_cast<char*>(ws) + W.bytes);
+  float* h = c.take<float>((size_t)d * 4);
+  float* o = c.take<float>((size_t)d * 4);
+  uint16_t* a = c.take<uint16_t>((size_t)d * 2);
+  cudaStream_t s = st(stream);
+  if (launch_widen(x, h, d, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  for (int l = 0; l < n_layers; ++l) {
+    if (launch_rmsnorm(h, rho[l], 1, d, eps, a, s) != cudaSuccess) return BGQ_ERR_CUDA;
+    int r = layer_forward_impl(&layers[l], a, 1, nullptr, o, idx_out ? idx_out + (size_t)l * K : nullptr, nullptr,
+                               nullptr, W, s);
+    if (r) return r;
+    if (launch_residual_add(h, o, d, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  }
+  if (x_next && launch_rmsnorm(h, nullptr, 1, d, eps, x_next, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  if (h_out && cudaMemcpyAsync(h_out, h, (size_t)d * 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+    return BGQ_ERR_CUDA;
+  return BGQ_OK;
+}
+
+int32_t bgq_read_device_status(void* ws, void* stream) {
+  if (!ws || !al(ws, 256)) return BGQ_ERR_INVALID_ARG;
+  int v = 0;
+  cudaStream_t s = st(stream);
+  if (cudaMemcpyAsync(&v, ws, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return BGQ_ERR_CUDA;
+  if (v != 0) {
+    int zero = 0;
+    if (cudaMemcpyAsync(ws, &zero, sizeof(int), cudaMemcpyHostToDevice, s) != cudaSuccess) return BGQ_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return BGQ_ERR_CUDA;
+  }
+  return v == 0 ? BGQ_OK : (v == BGQ_ERR_TIMEOUT ? BGQ_ERR_TIMEOUT : BGQ_ERR_CUDA);
+}
+
+}  // extern "C"

@@ -1,0 +1,266 @@
+// common.cuh — device helpers shared by the libbgq kernels.
+//
+// Packed format (Flash-MoE page, "FMA Dequant": w = nibble*scale + bias):
+//   codes  uint32 [rows][cols*BITS/32], column k at word k/(32/BITS), bit offset BITS*(k%(32/BITS));
+//   sb     bf16 pairs [rows][cols/64][2] = (scale, bias) per group of 64 columns.
+//
+// A row is consumed in "parts" of 128 bits of codes (one 16-byte load per lane):
+// 32 columns at 4 bits (half a group), 64 columns at 2 bits (one group).
+// P = cols*BITS/128 parts per row. A warp gives LPR = min(P, 32) lanes to a row,
+// so it covers RPP = 32/LPR rows at once, each in NIT = P/LPR iterations.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace bgq {
+
+constexpr int kGroup = 64;
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+__device__ __forceinline__ float bf16f(uint16_t v) { return __uint_as_float(((uint32_t)v) << 16); }
+__device__ __forceinline__ uint16_t f2bf(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
+
+// 4-way byte dot products (dp4a): unsigned codes times signed / unsigned bytes.
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t dp4a_uu(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Streaming 16-byte / 4-byte global loads that do not allocate in L1.
+__device__ __forceinline__ uint4 ldg_stream16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ldg_stream4(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+
+// 2^e as a float for e in [-126, 127].
+__device__ __forceinline__ float exp2i(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
+
+template <int BITS>
+struct Geo {
+  static constexpr int kPer = 32 / BITS;         // codes per word
+  static constexpr int kNvec = kPer / 4;         // byte vectors per word (4 codes each)
+  static constexpr int kNch = kNvec / 2;         // 16-byte x chunks per word (lo+hi of 2 vectors)
+  static constexpr int kValsPerPart = 128 / BITS;
+  static constexpr uint32_t kByteMask = BITS == 4 ? 0x0f0f0f0fu : 0x03030303u;
+};
+
+// Runtime row geometry for a given column count.
+struct RowGeo {
+  int P;    // parts per row
+  int LPR;  // lanes per row
+  int RPP;  // rows per warp pass
+  int NIT;  // iterations per row
+};
+__host__ __device__ inline RowGeo row_geo(int cols, int bits) {
+  RowGeo g;
+  g.P = cols * bits / 128;
+  g.LPR = g.P >= 32 ? 32 : g.P;
+  g.RPP = 32 / g.LPR;
+  g.NIT = g.P / g.LPR;
+  return g;
+}
+__host__ __device__ inline bool cols_supported(int cols, int bits) {
+  if (cols <= 0 || cols % kGroup) return false;
+  int P = cols * bits / 128;
+  if (P <= 0) return false;
+  return (P % 32 == 0) || (32 % P == 0);
+}
+
+// ---------------------------------------------------------------------------
+// x staging for the integer (dp4a) dot product.
+//
+// Per group of 64 inputs: sh = 14 - floor(log2(max|x|)), X_k = rint(x_k * 2^sh),
+// so |X_k| < 2^15 and every input within 2^7 of the group maximum is exact.
+// X is split into an unsigned low byte and a signed high byte: X = 256*hi + lo.
+// For code word w and byte vector j (codes k = w*per + j + nvec*i, i = 0..3)
+// we store (lo bytes, hi bytes) as two uint32; chunk ch of word w holds vectors
+// 2ch, 2ch+1 as {lo0, hi0, lo1, hi1}.
+// Chunk (t, part p, word c, chunk ch) lives at 16-byte slot
+//   (((t*NIT + p/LPR)*4 + c)*NCH + ch)*LPR + p%LPR
+// so that for fixed (t, iteration, c, ch) the lanes of a row read consecutive
+// slots (no bank conflicts). Part info (2^-sh, 2^-sh * sum_k X_k) is a float2
+// at [t*P + p].
+// ---------------------------------------------------------------------------
+template <int BITS>
+__host__ __device__ constexpr int xstage_bytes_per_token(int cols) {
+  // codes*2 bytes of X (lo+hi) + 8 bytes of part info per part
+  return cols * 2 + (cols * BITS / 128) * 8;
+}
+
+struct XStage {
+  uint4* chunks;    // [T * P * 4 * NCH] 16-byte slots
+  float2* partinfo; // [T * P]
+};
+
+// Input element loaders.
+__device__ __forceinline__ float load_in(const uint16_t* x, int i) { return bf16f(x[i]); }
+__device__ __forceinline__ float load_in(const float* x, int i) { return x[i]; }
+
+// Where the T input vectors of a staging call come from.
+template <typename In>
+struct StridedSrc {  // token t at x + t*ld
+  const In* x;
+  int ld;
+  __device__ const In* ptr(int t) const { return x + (size_t)t * ld; }
+};
+template <typename In>
+struct GatherSrc {  // token t at base + off[t] (off in shared memory)
+  const In* base;
+  const int* off;
+  __device__ const In* ptr(int t) const { return base + off[t]; }
+};
+
+// Stage T inputs of `cols` values into shared memory.
+// `gsh` is scratch shared memory for T*cols/64 ints. All threads of the block
+// must call; ends with __syncthreads().
+template <int BITS, typename In, typename Src>
+__device__ void stage_x_int16(const Src src, int T, int cols, XStage st, int* gsh) {
+  using G = Geo<BITS>;
+  const int ngroups = cols / kGroup;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  // pass 1: per (token, group) exponent shift
+  for (int tg = warp; tg < T * ngroups; tg += nwarps) {
+    int t = tg / ngroups, g = tg - t * ngroups;
+    const In* xp = src.ptr(t) + g * kGroup;
+    float m = fmaxf(fabsf(load_in(xp, lane)), fabsf(load_in(xp, lane + 32)));
+    m = warp_max(m);
+    if (lane == 0) {
+      int sh = 0;
+      if (m > 0.f) {
+        int e = (int)((__float_as_uint(m) >> 23) & 0xff) - 127;  // floor(log2 m) for normal m
+        sh = 14 - e;
+        sh = sh > 126 ? 126 : (sh < -126 ? -126 : sh);
+      }
+      gsh[tg] = sh;
+    }
+  }
+  __syncthreads();
+  // pass 2: one thread per (token, code word)
+  const RowGeo rg = row_geo(cols, BITS);
+  const int words = cols * BITS / 32;
+  const int total = T * words;  // a multiple of 4: each part has 4 words
+  for (int base = 0; base < total; base += blockDim.x) {
+    // Uniform trip count per warp so the 4-lane shuffles below see all lanes.
+    const int tw = base + threadIdx.x;
+    const bool active = tw < total;
+    int t = active ? tw / words : 0, w = active ? tw - t * words : 0;
+    int k0 = w * G::kPer;
+    int sh = gsh[t * ngroups + k0 / kGroup];
+    float sc = exp2i(sh);
+    const In* xp = src.ptr(t) + k0;
+    int X[G::kPer];
+    int xsum = 0;
+#pragma unroll
+    for (int i = 0; i < G::kPer; ++i) {
+      // |x*2^sh| < 2^15; the clamp only matters for fp32 inputs within an
+      // ulp of the next power of two, which round up to 2^15.
+      int v = active ? __float2int_rn(load_in(xp, i) * sc) : 0;
+      X[i] = max(-32767, min(32767, v));
+      xsum += X[i];
+    }
+    uint32_t lo[G::kNvec], hi[G::kNvec];
+#pragma unroll
+    for (int j = 0; j < G::kNvec; ++j) {
+      uint32_t l = 0, h = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        int v = X[j + G::kNvec * i];
+        l |= ((uint32_t)v & 0xffu) << (8 * i);
+        h |= ((uint32_t)(v >> 8) & 0xffu) << (8 * i);
+      }
+      lo[j] = l;
+      hi[j] = h;
+    }
+    int p = w >> 2, c = w & 3;
+    int it = p / rg.LPR, lp = p - it * rg.LPR;
+    if (active) {
+#pragma unroll
+      for (int ch = 0; ch < G::kNch; ++ch) {
+        int slot = (((t * rg.NIT + it) * 4 + c) * G::kNch + ch) * rg.LPR + lp;
+        st.chunks[slot] = make_uint4(lo[2 * ch], hi[2 * ch], lo[2 * ch + 1], hi[2 * ch + 1]);
+      }
+    }
+    // Part sum over the 4 words of part p: they sit on 4 consecutive lanes
+    // (base and blockDim are multiples of 32, words a multiple of 4).
+    xsum += __shfl_xor_sync(kFull, xsum, 1);
+    xsum += __shfl_xor_sync(kFull, xsum, 2);
+    if (active && c == 0) {
+      float inv = exp2i(-sh);
+      st.partinfo[t * rg.P + p] = make_float2(inv, (float)xsum * inv);
+    }
+  }
+  __syncthreads();
+}
+
+// Integer dot product of one part (4 code words) with staged token t.
+// Returns s*2^-sh*sum(q*X) + b*2^-sh*sum(X) added to acc.
+template <int BITS>
+__device__ __forceinline__ float part_dot_int16(const uint4 qv, uint32_t sbw, const uint4* __restrict__ chunks,
+                                                const float2* __restrict__ partinfo, int t, int p, const RowGeo& rg,
+                                                float acc) {
+  using G = Geo<BITS>;
+  int it = p / rg.LPR, lp = p - it * rg.LPR;
+  int acc_h = 0;
+  uint32_t acc_l = 0;
+  const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+#pragma unroll
+    for (int ch = 0; ch < G::kNch; ++ch) {
+      uint4 xc = chunks[(((t * rg.NIT + it) * 4 + c) * G::kNch + ch) * rg.LPR + lp];
+      uint32_t v0 = (qw[c] >> (BITS * (2 * ch))) & G::kByteMask;
+      uint32_t v1 = (qw[c] >> (BITS * (2 * ch + 1))) & G::kByteMask;
+      acc_l = dp4a_uu(v0, xc.x, acc_l);
+      acc_h = dp4a_us(v0, xc.y, acc_h);
+      acc_l = dp4a_uu(v1, xc.z, acc_l);
+      acc_h = dp4a_us(v1, xc.w, acc_h);
+    }
+  }
+  float2 pi = partinfo[t * rg.P + p];
+  int A = acc_h * 256 + (int)acc_l;
+  float s = bf16lo(sbw), b = bf16hi(sbw);
+  return fmaf(s * pi.x, (float)A, fmaf(b, pi.y, acc));
+}
+
+// Group index of part p.
+template <int BITS>
+__device__ __forceinline__ int part_group(int p) {
+  return BITS == 4 ? (p >> 1) : p;
+}
+
+// Sum over the LPR lanes that share a row (lanes l, l^1, ... within the row's span).
+__device__ __forceinline__ float row_reduce(float v, int LPR) {
+  for (int o = LPR >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+}  // namespace bgq

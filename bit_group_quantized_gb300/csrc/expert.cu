@@ -1,0 +1,337 @@
+// expert.cu — grouped SwiGLU experts, combine, RMSNorm and residual add.
+//
+// Flash-MoE page, section "架构设计：SSD当显存用": CMD3 is the selected experts'
+// forward pass, the combine and the norm. An expert is SwiGLU:
+//   h = silu(gate x) * (up x)   (kept in fp32),   y = down h.
+// The kernels run a plan of grouped-GEMV tasks (route.cu): one task is one
+// expert applied to up to 8 tokens, so each weight row is read once for all of
+// them. Rows are split across CTAs; the CTA stages its task's inputs once and
+// keeps them while consecutive work items stay on the same task.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bgq {
+
+constexpr int kExpThreads = 256;
+constexpr int kExpWarps = 8;
+constexpr int kMaxNitE = 4;  // parts per lane and row-dot held in registers
+
+__device__ __forceinline__ ExpertRef resolve(const ExpertSet& es, int e) {
+  if (e < 0) return es.shared;
+  ExpertRef r;
+  const long long mw = (long long)es.d * es.f * es.bits / 32;  // words per matrix
+  const long long mg = (long long)es.d * es.f / kGroup * 2;    // bf16 per matrix
+  const uint32_t* q = es.pool_q + (long long)e * es.q_stride;
+  const uint16_t* sb = es.pool_sb + (long long)e * es.sb_stride;
+  r.gate_q = q;
+  r.up_q = q + mw;
+  r.down_q = q + 2 * mw;
+  r.gate_sb = sb;
+  r.up_sb = sb + mg;
+  r.down_sb = sb + 2 * mg;
+  return r;
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.f + expf(-g)); }
+
+template <int BITS>
+__device__ __forceinline__ void load_row(const uint32_t* qrow, const uint32_t* sbrow, const RowGeo& rg, int lp,
+                                         int it0, bool valid, uint4 (&qv)[kMaxNitE], uint32_t (&sv)[kMaxNitE]) {
+#pragma unroll
+  for (int i = 0; i < kMaxNitE; ++i) {
+    int it = it0 + i;
+    if (valid && it < rg.NIT) {
+      int p = it * rg.LPR + lp;
+      qv[i] = ldg_stream16(qrow + 4 * p);
+      sv[i] = ldg_stream4(sbrow + part_group<BITS>(p));
+    } else {
+      qv[i] = make_uint4(0, 0, 0, 0);
+      sv[i] = 0;
+    }
+  }
+}
+
+// Accumulate the parts of one load round into acc[t] for t < ntok.
+template <int BITS>
+__device__ __forceinline__ void dot_round(const uint4 (&qv)[kMaxNitE], const uint32_t (&sv)[kMaxNitE],
+                                          const XStage& st, const RowGeo& rg, int lp, int it0, int ntok,
+                                          float (&acc)[kTaskTok]) {
+#pragma unroll
+  for (int i = 0; i < kMaxNitE; ++i) {
+    int it = it0 + i;
+    if (it < rg.NIT) {
+      int p = it * rg.LPR + lp;
+#pragma unroll
+      for (int t = 0; t < kTaskTok; ++t)
+        if (t < ntok) acc[t] = part_dot_int16<BITS>(qv[i], sv[i], st.chunks, st.partinfo, t, p, rg, acc[t]);
+    }
+  }
+}
+
+struct ItemRange {
+  int begin, end;
+};
+__device__ __forceinline__ ItemRange my_items(int total) {
+  int per = (total + gridDim.x - 1) / gridDim.x;
+  int b = blockIdx.x * per;
+  int e = b + per;
+  return ItemRange{b < total ? b : total, e < total ? e : total};
+}
+
+// ---------------------------------------------------------------------------
+// gate/up + SiLU*mul. Item = (task, block of rows of d_ff).
+// ---------------------------------------------------------------------------
+template <int BITS>
+__global__ void __launch_bounds__(kExpThreads)
+k_gateup(ExpertSet es, const Plan* __restrict__ plan, const uint16_t* __restrict__ x, float* __restrict__ H,
+         int nslot) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ int s_off[kTaskTok];
+  const int d = es.d, f = es.f;
+  const RowGeo rg = row_geo(d, BITS);
+  const int rows_item = kExpWarps * rg.RPP;
+  const int nrb = (f + rows_item - 1) / rows_item;
+  const int total = plan->ntasks * nrb;
+  const ItemRange ir = my_items(total);
+  XStage st;
+  st.chunks = reinterpret_cast<uint4*>(smem);
+  st.partinfo = reinterpret_cast<float2*>(smem + (size_t)kTaskTok * d * 2);
+  int* gsh = reinterpret_cast<int*>(smem + (size_t)kTaskTok * d * 2 + (size_t)kTaskTok * rg.P * 8);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int rs = lane / rg.LPR, lp = lane - rs * rg.LPR;
+  const int wpr = d * BITS / 32, gpr = d / kGroup;
+  int staged = -1;
+  for (int item = ir.begin; item < ir.end; ++item) {
+    const int ti = item / nrb, rb = item - ti * nrb;
+    const Task& tk = plan->tasks[ti];
+    const int ntok = tk.ntok;
+    const ExpertRef ex = resolve(es, tk.expert);
+    const int row = rb * rows_item + warp * rg.RPP + rs;
+    const bool valid = row < f;
+    const uint32_t* gq = ex.gate_q + (size_t)(valid ? row : 0) * wpr;
+    const uint32_t* uq = ex.up_q + (size_t)(valid ? row : 0) * wpr;
+    const uint32_t* gs = reinterpret_cast<const uint32_t*>(ex.gate_sb) + (size_t)(valid ? row : 0) * gpr;
+    const uint32_t* us = reinterpret_cast<const uint32_t*>(ex.up_sb) + (size_t)(valid ? row : 0) * gpr;
+    uint4 gqv[kMaxNitE], uqv[kMaxNitE];
+    uint32_t gsv[kMaxNitE], usv[kMaxNitE];
+    load_row<BITS>(gq, gs, rg, lp, 0, valid, gqv, gsv);
+    load_row<BITS>(uq, us, rg, lp, 0, valid, uqv, usv);
+    if (ti != staged) {
+      __syncthreads();  // previous item finished reading the staged inputs
+      if (threadIdx.x < kTaskTok) s_off[threadIdx.x] = threadIdx.x < ntok ? tk.tok[threadIdx.x] * d : 0;
+      __syncthreads();
+      stage_x_int16<BITS, uint16_t>(GatherSrc<uint16_t>{x, s_off}, ntok, d, st, gsh);
+      staged = ti;
+    }
+    float ga[kTaskTok], ua[kTaskTok];
+#pragma unroll
+    for (int t = 0; t < kTaskTok; ++t) ga[t] = ua[t] = 0.f;
+    for (int it0 = 0; it0 < rg.NIT; it0 += kMaxNitE) {
+      if (it0 > 0) {
+        load_row<BITS>(gq, gs, rg, lp, it0, valid, gqv, gsv);
+        load_row<BITS>(uq, us, rg, lp, it0, valid, uqv, usv);
+      }
+      dot_round<BITS>(gqv, gsv, st, rg, lp, it0, ntok, ga);
+      dot_round<BITS>(uqv, usv, st, rg, lp, it0, ntok, ua);
+    }
+#pragma unroll
+    for (int t = 0; t < kTaskTok; ++t) {
+      if (t < ntok) {
+        float g = row_reduce(ga[t], rg.LPR), u = row_reduce(ua[t], rg.LPR);
+        if (valid && lp == 0) H[((size_t)tk.tok[t] * nslot + tk.slot[t]) * f + row] = silu_f(g) * u;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// down projection. Item = (task, block of rows of d_model).
+// ---------------------------------------------------------------------------
+template <int BITS>
+__global__ void __launch_bounds__(kExpThreads)
+k_down(ExpertSet es, const Plan* __restrict__ plan, const float* __restrict__ H, float* __restrict__ Y, int nslot) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ int s_off[kTaskTok];
+  const int d = es.d, f = es.f;
+  const RowGeo rg = row_geo(f, BITS);
+  const int rows_item = kExpWarps * rg.RPP;
+  const int nrb = (d + rows_item - 1) / rows_item;
+  const int total = plan->ntasks * nrb;
+  const ItemRange ir = my_items(total);
+  XStage st;
+  st.chunks = reinterpret_cast<uint4*>(smem);
+  st.partinfo = reinterpret_cast<float2*>(smem + (size_t)kTaskTok * f * 2);
+  int* gsh = reinterpret_cast<int*>(smem + (size_t)kTaskTok * f * 2 + (size_t)kTaskTok * rg.P * 8);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int rs = lane / rg.LPR, lp = lane - rs * rg.LPR;
+  const int wpr = f * BITS / 32, gpr = f / kGroup;
+  int staged = -1;
+  for (int item = ir.begin; item < ir.end; ++item) {
+    const int ti = item / nrb, rb = item - ti * nrb;
+    const Task& tk = plan->tasks[ti];
+    const int ntok = tk.ntok;
+    const ExpertRef ex = resolve(es, tk.expert);
+    const int row = rb * rows_item + warp * rg.RPP + rs;
+    const bool valid = row < d;
+    const uint32_t* dq = ex.down_q + (size_t)(valid ? row : 0) * wpr;
+    const uint32_t* ds = reinterpret_cast<const uint32_t*>(ex.down_sb) + (size_t)(valid ? row : 0) * gpr;
+    uint4 qv[kMaxNitE];
+    uint32_t sv[kMaxNitE];
+    load_row<BITS>(dq, ds, rg, lp, 0, valid, qv, sv);
+    if (ti != staged) {
+      __syncthreads();
+      if (threadIdx.x < kTaskTok)
+        s_off[threadIdx.x] = threadIdx.x < ntok ? (tk.tok[threadIdx.x] * nslot + tk.slot[threadIdx.x]) * f : 0;
+      __syncthreads();
+      stage_x_int16<BITS, float>(GatherSrc<float>{H, s_off}, ntok, f, st, gsh);
+      staged = ti;
+    }
+    float acc[kTaskTok];
+#pragma unroll
+    for (int t = 0; t < kTaskTok; ++t) acc[t] = 0.f;
+    for (int it0 = 0; it0 < rg.NIT; it0 += kMaxNitE) {
+      if (it0 > 0) load_row<BITS>(dq, ds, rg, lp, it0, valid, qv, sv);
+      dot_round<BITS>(qv, sv, st, rg, lp, it0, ntok, acc);
+    }
+#pragma unroll
+    for (int t = 0; t < kTaskTok; ++t) {
+      if (t < ntok) {
+        float v = row_reduce(acc[t], rg.LPR);
+        if (valid && lp == 0) Y[((size_t)tk.tok[t] * nslot + tk.slot[t]) * d + row] = v;
+      }
+    }
+  }
+}
+
+template <typename K>
+static cudaError_t set_smem(K kern, size_t sm) {
+  if (sm > 48 * 1024) return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  return cudaSuccess;
+}
+
+static int expert_grid(int max_items) {
+  int g = num_sms() * 2;
+  return max_items < g ? (max_items > 0 ? max_items : 1) : g;
+}
+
+cudaError_t launch_gateup(const ExpertSet& es, const Plan* plan, int max_tasks, const uint16_t* x, float* H, int nslot,
+                          cudaStream_t s) {
+  size_t sm = qgemv_int16_smem(es.d, es.bits, kTaskTok);
+  RowGeo rg = row_geo(es.d, es.bits);
+  int nrb = (es.f + kExpWarps * rg.RPP - 1) / (kExpWarps * rg.RPP);
+  int grid = expert_grid(max_tasks * nrb);
+  cudaError_t e;
+  if (es.bits == 4) {
+    if ((e = set_smem(k_gateup<4>, sm)) != cudaSuccess) return e;
+    k_gateup<4><<<grid, kExpThreads, sm, s>>>(es, plan, x, H, nslot);
+  } else {
+    if ((e = set_smem(k_gateup<2>, sm)) != cudaSuccess) return e;
+    k_gateup<2><<<grid, kExpThreads, sm, s>>>(es, plan, x, H, nslot);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_down(const ExpertSet& es, const Plan* plan, int max_tasks, const float* H, float* Y, int nslot,
+                        cudaStream_t s) {
+  size_t sm = qgemv_int16_smem(es.f, es.bits, kTaskTok);
+  RowGeo rg = row_geo(es.f, es.bits);
+  int nrb = (es.d + kExpWarps * rg.RPP - 1) / (kExpWarps * rg.RPP);
+  int grid = expert_grid(max_tasks * nrb);
+  cudaError_t e;
+  if (es.bits == 4) {
+    if ((e = set_smem(k_down<4>, sm)) != cudaSuccess) return e;
+    k_down<4><<<grid, kExpThreads, sm, s>>>(es, plan, H, Y, nslot);
+  } else {
+    if ((e = set_smem(k_down<2>, sm)) != cudaSuccess) return e;
+    k_down<2><<<grid, kExpThreads, sm, s>>>(es, plan, H, Y, nslot);
+  }
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// combine, RMSNorm, residual
+// ---------------------------------------------------------------------------
+__global__ void k_combine(const float* __restrict__ Y, const float* __restrict__ w, const float* __restrict__ gamma,
+                          int B, int K, int d, uint16_t* __restrict__ out, float* __restrict__ out_f32) {
+  const long long n = (long long)B * d;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(i / d), r = (int)(i - (long long)t * d);
+    const float* yt = Y + (size_t)t * (K + 1) * d + r;
+    float acc = 0.f;
+    for (int k = 0; k < K; ++k) acc = fmaf(w[t * K + k], yt[(size_t)k * d], acc);
+    const float g = gamma ? gamma[t] : 1.f;
+    acc = fmaf(g, yt[(size_t)K * d], acc);
+    if (out) out[i] = f2bf(acc);
+    if (out_f32) out_f32[i] = acc;
+  }
+}
+
+cudaError_t launch_combine(const float* Y, const float* w, const float* gamma, int batch, int K, int d,
+                           uint16_t* out, float* out_f32, cudaStream_t s) {
+  long long n = (long long)batch * d;
+  int grid = (int)((n + 255) / 256);
+  int cap = num_sms() * 8;
+  if (grid > cap) grid = cap;
+  k_combine<<<grid, 256, 0, s>>>(Y, w, gamma, batch, K, d, out, out_f32);
+  return cudaGetLastError();
+}
+
+// One CTA per token: a = bf16(h * (1/sqrt(mean(h^2) + eps)) * rho).
+__global__ void __launch_bounds__(256) k_rmsnorm(const float* __restrict__ h, const uint16_t* __restrict__ rho, int d,
+                                                 float eps, uint16_t* __restrict__ a) {
+  __shared__ float red[8];
+  const float* ht = h + (size_t)blockIdx.x * d;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) ss = fmaf(ht[i], ht[i], ss);
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += red[i];
+  const float r = 1.f / sqrtf(tot / (float)d + eps);
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    float v = ht[i] * r;
+    if (rho) v *= bf16f(rho[i]);
+    a[(size_t)blockIdx.x * d + i] = f2bf(v);
+  }
+}
+
+cudaError_t launch_rmsnorm(const float* h, const uint16_t* rho, int batch, int d, float eps, uint16_t* a,
+                           cudaStream_t s) {
+  k_rmsnorm<<<batch, 256, 0, s>>>(h, rho, d, eps, a);
+  return cudaGetLastError();
+}
+
+__global__ void k_residual(float* __restrict__ h, const float* __restrict__ delta, long long n) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+    h[i] += delta[i];
+}
+
+cudaError_t launch_residual_add(float* h, const float* delta, long long n, cudaStream_t s) {
+  int grid = (int)((n + 255) / 256);
+  int cap = num_sms() * 8;
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  k_residual<<<grid, 256, 0, s>>>(h, delta, n);
+  return cudaGetLastError();
+}
+
+__global__ void k_widen(const uint16_t* __restrict__ x, float* __restrict__ h, int n) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) h[i] = bf16f(x[i]);
+}
+
+cudaError_t launch_widen(const uint16_t* x, float* h, int n, cudaStream_t s) {
+  int grid = (n + 255) / 256;
+  if (grid > 1024) grid = 1024;
+  k_widen<<<grid, 256, 0, s>>>(x, h, n);
+  return cudaGetLastError();
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 132;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 132;
+  return n;
+}
+
+}  // namespace bgq

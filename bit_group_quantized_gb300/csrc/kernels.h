@@ -1,0 +1,97 @@
+// kernels.h — internal launcher interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace bgq {
+
+struct QMat {
+  const uint32_t* q;
+  const uint16_t* sb;
+  int rows, cols, bits;
+};
+
+// Device-resolvable reference to one SwiGLU expert.
+struct ExpertRef {
+  const uint32_t* gate_q;
+  const uint16_t* gate_sb;
+  const uint32_t* up_q;
+  const uint16_t* up_sb;
+  const uint32_t* down_q;
+  const uint16_t* down_sb;
+};
+
+// The experts a plan can name: pool expert e >= 0, or `shared` for e == -1.
+struct ExpertSet {
+  const uint32_t* pool_q;
+  const uint16_t* pool_sb;
+  long long q_stride;   // words between experts
+  long long sb_stride;  // bf16 elements between experts
+  ExpertRef shared;
+  int d, f, bits;
+};
+
+constexpr int kTaskTok = 8;  // tokens per task (grouped GEMV width)
+
+// One grouped-GEMV task: expert `expert` applied to up to 8 tokens; token i's
+// result goes to slot slot[i] of token tok[i].
+struct Task {
+  int expert;
+  int ntok;
+  int tok[kTaskTok];
+  int slot[kTaskTok];
+};
+
+struct Plan {
+  int ntasks;
+  int pad[3];
+  Task tasks[1];  // [ntasks]
+};
+
+inline size_t plan_bytes(int batch, int top_k) {
+  size_t maxtasks = (size_t)batch * top_k + (batch + kTaskTok - 1) / kTaskTok + 1;
+  return sizeof(Plan) + maxtasks * sizeof(Task);
+}
+
+// Workspace control block (first 256 bytes of every workspace).
+struct Ctrl {
+  int status;         // 0 = ok, 4 = a bounded wait timed out
+  int pad0[15];
+  int route_counter;  // last-CTA detection of the router kernel
+  int pad1[15];
+  int misc[32];
+};
+static_assert(sizeof(Ctrl) == 256, "control block is 256 bytes");
+
+size_t qgemv_int16_smem(int cols, int bits, int T);
+cudaError_t launch_qgemv(const QMat& W, const uint16_t* x, int batch, uint16_t* y, float* yf, int variant,
+                         cudaStream_t s);
+
+// Router + softmax + top-K (+ optional grouping plan).
+cudaError_t launch_route(const uint16_t* router, const uint16_t* sgate, const uint16_t* x, int batch, int d,
+                         int E, int K, float* logits_ws, Ctrl* ctrl, int32_t* idx, float* w, float* gamma,
+                         float* logits_out, Plan* plan, cudaStream_t s);
+
+// Builds the plan of one explicit expert over `batch` tokens (slot 0).
+cudaError_t launch_plan_single(Plan* plan, int batch, cudaStream_t s);
+
+// Grouped gate/up + SiLU*mul: H[(tok*nslot + slot)*f + row].
+cudaError_t launch_gateup(const ExpertSet& es, const Plan* plan, int max_tasks, const uint16_t* x, float* H,
+                          int nslot, cudaStream_t s);
+// Grouped down projection: Y[(tok*nslot + slot)*d + row].
+cudaError_t launch_down(const ExpertSet& es, const Plan* plan, int max_tasks, const float* H, float* Y, int nslot,
+                        cudaStream_t s);
+// out[t][r] = sum_{k<K} w[t][k] Y[t][k][r] + gamma[t] Y[t][K][r]  (K may be 0; gamma NULL => 1).
+cudaError_t launch_combine(const float* Y, const float* w, const float* gamma, int batch, int K, int d,
+                           uint16_t* out, float* out_f32, cudaStream_t s);
+
+cudaError_t launch_rmsnorm(const float* h, const uint16_t* rho, int batch, int d, float eps, uint16_t* a,
+                           cudaStream_t s);
+cudaError_t launch_residual_add(float* h, const float* delta, long long n, cudaStream_t s);
+cudaError_t launch_widen(const uint16_t* x, float* h, int n, cudaStream_t s);
+
+int num_sms();
+
+}  // namespace bgq

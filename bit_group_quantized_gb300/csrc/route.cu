@@ -1,0 +1,318 @@
+// route.cu — fused router GEMV + softmax + top-K + renormalise (+ grouping plan).
+//
+// Flash-MoE page, section "架构设计：SSD当显存用": after the routing logits are
+// computed, softmax and top-K select the experts (K = 4 of 512 per section
+// "先搞清楚为什么这件事很难"). The page runs softmax + topK on the CPU; here it
+// is the tail of the router kernel: every CTA computes a slice of the logits,
+// and the last CTA to finish (atomic counter, no waiting) selects the experts.
+//
+//   l[e] = router[e] . x (fp32), p = softmax(l) (fp32, max-subtracted),
+//   top-K by logit, ties to the lower index, largest first,
+//   w_k = p[idx_k] / sum_j p[idx_j],  gamma = sigmoid(shared_gate . x).
+//
+// With a plan pointer, the last CTA also groups the (token, slot) pairs by
+// expert (counting sort, stable by token then slot) into grouped-GEMV tasks of
+// at most 8 tokens, routed experts in ascending order, then the shared expert.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bgq {
+
+constexpr int kRouteThreads = 256;
+constexpr int kRouteWarps = 8;
+constexpr int kRouteTok = 8;       // tokens per x chunk in shared memory
+constexpr int kRouteMaxVec = 8;    // 16-byte weight vectors per lane held in registers
+constexpr int kMaxExperts = 1024;  // top-K registers: 32 logits per lane
+constexpr int kMaxTopK = 8;
+
+struct RouteGeo {
+  int sk;        // warps per row (split-K)
+  int rows_cta;  // rows per CTA
+  int nvec;      // 16-byte vectors per lane per row slice
+};
+__host__ __device__ inline RouteGeo route_geo(int d) {
+  RouteGeo g;
+  g.sk = (d + 2047) / 2048;
+  g.rows_cta = kRouteWarps / g.sk;
+  g.nvec = d / g.sk / 256;
+  return g;
+}
+bool route_shape_ok(int d) {
+  if (d <= 0 || d % 256) return false;
+  RouteGeo g = route_geo(d);
+  return g.sk <= kRouteWarps && d % (256 * g.sk) == 0;
+}
+
+__device__ void topk_one_token(const float* __restrict__ lg, int E, int K, float zgate, bool has_gate, int t,
+                               int32_t* idx, float* w, float* gamma, float* logits_out, int* sel_out) {
+  const int lane = threadIdx.x & 31;
+  float v[kMaxExperts / 32];
+  const int per = (E + 31) / 32;
+#pragma unroll
+  for (int i = 0; i < kMaxExperts / 32; ++i) {
+    int e = i * 32 + lane;
+    v[i] = (i < per && e < E) ? __ldcg(lg + e) : -INFINITY;
+    if (logits_out && i < per && e < E) logits_out[(size_t)t * E + e] = v[i];
+  }
+  // softmax denominator over all experts
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < kMaxExperts / 32; ++i) m = fmaxf(m, v[i]);
+  m = warp_max(m);
+  float ssum = 0.f;
+#pragma unroll
+  for (int i = 0; i < kMaxExperts / 32; ++i)
+    if (i < per && i * 32 + lane < E) ssum += expf(v[i] - m);
+  ssum = warp_sum(ssum);
+  // K rounds of arg-max; (value, index) order: larger value, then lower index.
+  unsigned taken = 0u;
+  int sel[kMaxTopK];
+  float selv[kMaxTopK];
+  for (int k = 0; k < K; ++k) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < kMaxExperts / 32; ++i) {
+      int e = i * 32 + lane;
+      bool ok = i < per && e < E && !((taken >> i) & 1u);
+      if (ok && (v[i] > bv || (v[i] == bv && e < bi))) {
+        bv = v[i];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      float ov = __shfl_xor_sync(kFull, bv, o);
+      int oi = __shfl_xor_sync(kFull, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    sel[k] = bi;
+    selv[k] = bv;
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+  }
+  if (lane == 0) {
+    float p[kMaxTopK], ps = 0.f;
+    for (int k = 0; k < K; ++k) {
+      p[k] = expf(selv[k] - m) / ssum;
+      ps += p[k];
+    }
+    for (int k = 0; k < K; ++k) {
+      idx[t * K + k] = sel[k];
+      w[t * K + k] = p[k] / ps;
+      if (sel_out) sel_out[t * K + k] = sel[k];
+    }
+    if (gamma) gamma[t] = has_gate ? 1.f / (1.f + expf(-zgate)) : 1.f;
+  }
+}
+
+// Block-wide exclusive scan of n <= 4*blockDim ints in shared memory (in place).
+__device__ void block_exclusive_scan(int* a, int n, int* tmp /* >= 33 ints */) {
+  const int per = (n + blockDim.x - 1) / blockDim.x;
+  const int lo = threadIdx.x * per;
+  int local = 0;
+  for (int i = 0; i < per; ++i)
+    if (lo + i < n) local += a[lo + i];
+  // scan of per-thread totals
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = local;
+  for (int o = 1; o < 32; o <<= 1) {
+    int v = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) tmp[warp] = incl;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) {
+      int v = tmp[i];
+      tmp[i] = run;
+      run += v;
+    }
+    tmp[32] = run;
+  }
+  __syncthreads();
+  int run = tmp[warp] + incl - local;
+  for (int i = 0; i < per; ++i) {
+    if (lo + i < n) {
+      int v = a[lo + i];
+      a[lo + i] = run;
+      run += v;
+    }
+  }
+  __syncthreads();
+}
+
+__device__ void build_plan(const int* sel, int B, int K, int E, Plan* plan, int* s_cnt, int* s_tmp) {
+  const int npairs = B * K;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < npairs; i += blockDim.x) atomicAdd(&s_cnt[sel[i]], 1);
+  __syncthreads();
+  // chunks of <= 8 tokens per expert, then their starting task index
+  int* s_first = s_cnt + E;  // E ints: task index of each expert's first chunk
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_first[e] = (s_cnt[e] + kTaskTok - 1) / kTaskTok;
+  __syncthreads();
+  block_exclusive_scan(s_first, E, s_tmp);
+  const int nrouted = s_tmp[32];
+  for (int i = threadIdx.x; i < npairs; i += blockDim.x) {
+    int e = sel[i];
+    int r = 0;
+    for (int j = 0; j < i; ++j) r += (sel[j] == e);
+    Task& tk = plan->tasks[s_first[e] + r / kTaskTok];
+    int pos = r % kTaskTok;
+    tk.tok[pos] = i / K;
+    tk.slot[pos] = i % K;
+    if (pos == 0) {
+      tk.expert = e;
+      int left = s_cnt[e] - (r / kTaskTok) * kTaskTok;
+      tk.ntok = left < kTaskTok ? left : kTaskTok;
+    }
+  }
+  const int nshared = (B + kTaskTok - 1) / kTaskTok;
+  for (int c = threadIdx.x; c < nshared; c += blockDim.x) {
+    Task& tk = plan->tasks[nrouted + c];
+    tk.expert = -1;
+    int n = B - c * kTaskTok;
+    tk.ntok = n < kTaskTok ? n : kTaskTok;
+    for (int i = 0; i < tk.ntok; ++i) {
+      tk.tok[i] = c * kTaskTok + i;
+      tk.slot[i] = K;
+    }
+  }
+  if (threadIdx.x == 0) plan->ntasks = nrouted + nshared;
+}
+
+__global__ void __launch_bounds__(kRouteThreads)
+k_route(const uint16_t* __restrict__ router, const uint16_t* __restrict__ sgate, const uint16_t* __restrict__ x, int B,
+        int d, int E, int K, float* __restrict__ lg, Ctrl* ctrl, int32_t* __restrict__ idx, float* __restrict__ w,
+        float* __restrict__ gamma, float* __restrict__ logits_out, Plan* plan, int* __restrict__ sel_ws) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);                       // [kRouteTok][d]
+  float* red = reinterpret_cast<float*>(smem + (size_t)kRouteTok * d * 2);  // [warps][kRouteTok]
+  __shared__ int s_last;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const RouteGeo g = route_geo(d);
+  const int nrows = E + (sgate ? 1 : 0);
+  const int rloc = warp / g.sk, half = warp - rloc * g.sk;
+  const int row = blockIdx.x * g.rows_cta + rloc;
+  const bool valid = rloc < g.rows_cta && row < nrows;
+  const uint16_t* wrow = (row < E) ? router + (size_t)row * d : sgate;
+  const int c0 = half * (d / g.sk);
+
+  uint4 wv[kRouteMaxVec];
+#pragma unroll
+  for (int i = 0; i < kRouteMaxVec; ++i)
+    wv[i] = (valid && i < g.nvec) ? ldg_stream16(wrow + c0 + (i * 32 + lane) * 8) : make_uint4(0, 0, 0, 0);
+
+  for (int t0 = 0; t0 < B; t0 += kRouteTok) {
+    const int T = B - t0 < kRouteTok ? B - t0 : kRouteTok;
+    __syncthreads();
+    for (int i = threadIdx.x; i < T * d / 8; i += blockDim.x)
+      reinterpret_cast<uint4*>(xs)[i] = reinterpret_cast<const uint4*>(x + (size_t)t0 * d)[i];
+    __syncthreads();
+    float acc[kRouteTok];
+#pragma unroll
+    for (int t = 0; t < kRouteTok; ++t) acc[t] = 0.f;
+#pragma unroll
+    for (int i = 0; i < kRouteMaxVec; ++i) {
+      if (i < g.nvec) {
+        const float wf[8] = {bf16lo(wv[i].x), bf16hi(wv[i].x), bf16lo(wv[i].y), bf16hi(wv[i].y),
+                             bf16lo(wv[i].z), bf16hi(wv[i].z), bf16lo(wv[i].w), bf16hi(wv[i].w)};
+        const int col = c0 + (i * 32 + lane) * 8;
+#pragma unroll
+        for (int t = 0; t < kRouteTok; ++t) {
+          if (t < T) {
+            uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)t * d + col);
+            float a = acc[t];
+            a = fmaf(wf[0], bf16lo(xv.x), a);
+            a = fmaf(wf[1], bf16hi(xv.x), a);
+            a = fmaf(wf[2], bf16lo(xv.y), a);
+            a = fmaf(wf[3], bf16hi(xv.y), a);
+            a = fmaf(wf[4], bf16lo(xv.z), a);
+            a = fmaf(wf[5], bf16hi(xv.z), a);
+            a = fmaf(wf[6], bf16lo(xv.w), a);
+            a = fmaf(wf[7], bf16hi(xv.w), a);
+            acc[t] = a;
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < kRouteTok; ++t) {
+      float v = warp_sum(acc[t]);
+      if (lane == 0) red[warp * kRouteTok + t] = v;
+    }
+    __syncthreads();
+    if (valid && half == 0 && lane < T) {
+      float v = 0.f;
+      for (int h = 0; h < g.sk; ++h) v += red[(rloc * g.sk + h) * kRouteTok + lane];
+      lg[(size_t)(t0 + lane) * (E + 1) + row] = v;
+    }
+  }
+  // last CTA selects the experts
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    int prev = atomicAdd(&ctrl->route_counter, 1);
+    s_last = (prev == (int)gridDim.x - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int t = warp; t < B; t += kRouteWarps) {
+    float z = sgate ? __ldcg(lg + (size_t)t * (E + 1) + E) : 0.f;
+    topk_one_token(lg + (size_t)t * (E + 1), E, K, z, sgate != nullptr, t, idx, w, gamma, logits_out, sel_ws);
+  }
+  if (plan) {
+    __syncthreads();
+    __threadfence_block();
+    int* s_cnt = reinterpret_cast<int*>(smem);  // reuse: 2*E ints + scan scratch
+    build_plan(sel_ws, B, K, E, plan, s_cnt, s_cnt + 2 * E);
+  }
+  if (threadIdx.x == 0) ctrl->route_counter = 0;  // ready for the next launch
+}
+
+cudaError_t launch_route(const uint16_t* router, const uint16_t* sgate, const uint16_t* x, int batch, int d, int E,
+                         int K, float* logits_ws, Ctrl* ctrl, int32_t* idx, float* w, float* gamma,
+                         float* logits_out, Plan* plan, cudaStream_t s) {
+  RouteGeo g = route_geo(d);
+  int nrows = E + (sgate ? 1 : 0);
+  int grid = (nrows + g.rows_cta - 1) / g.rows_cta;
+  size_t sm = (size_t)kRouteTok * d * 2 + kRouteWarps * kRouteTok * sizeof(float);
+  size_t sm_plan = (size_t)(2 * E + 40) * sizeof(int);
+  if (sm_plan > sm) sm = sm_plan;
+  if (sm > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k_route, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+  }
+  // selected experts scratch for the plan: right after the logits
+  int* sel_ws = reinterpret_cast<int*>(logits_ws + (size_t)batch * (E + 1));
+  k_route<<<grid, kRouteThreads, sm, s>>>(router, sgate, x, batch, d, E, K, logits_ws, ctrl, idx, w, gamma,
+                                          logits_out, plan, sel_ws);
+  return cudaGetLastError();
+}
+
+__global__ void k_plan_single(Plan* plan, int B) {
+  const int n = (B + kTaskTok - 1) / kTaskTok;
+  for (int c = threadIdx.x; c < n; c += blockDim.x) {
+    Task& tk = plan->tasks[c];
+    tk.expert = -1;
+    int m = B - c * kTaskTok;
+    tk.ntok = m < kTaskTok ? m : kTaskTok;
+    for (int i = 0; i < tk.ntok; ++i) {
+      tk.tok[i] = c * kTaskTok + i;
+      tk.slot[i] = 0;
+    }
+  }
+  if (threadIdx.x == 0) plan->ntasks = n;
+}
+
+cudaError_t launch_plan_single(Plan* plan, int batch, cudaStream_t s) {
+  k_plan_single<<<1, 64, 0, s>>>(plan, batch);
+  return cudaGetLastError();
+}
+
+}  // namespace bgq

@@ -244,3 +244,16 @@ def rho(seed: int, layer: int, d_model: int, device="cpu"):
 def activations(seed: int, stream: int, batch: int, d_model: int, device="cpu"):
     k = stream_keys(seed, TAG_X, stream)
     return normal_at(k, _arange(0, batch * d_model, device)).to(torch.bfloat16).view(batch, d_model)
+
+
+def layer_tensors(seed: int, layer: int, shape: PoolShape, device="cpu", with_gate: bool = True):
+    """All tensors of one synthetic MoE layer.
+
+    Returns a dict: router bf16 [E][d], shared_gate bf16 [d] (or None),
+    pool_q int32 [E+1][q_stride], pool_sb bf16 [E+1][sb_stride] (routed experts
+    0..E-1, the shared expert at index E).
+    """
+    pool_q, pool_sb = expert_pool(seed, layer, shape, device)
+    return dict(router=router(seed, layer, shape.E, shape.d, device),
+                shared_gate=shared_gate(seed, layer, shape.d, device) if with_gate else None,
+                pool_q=pool_q, pool_sb=pool_sb)

@@ -1,0 +1,214 @@
+/*
+ * bgq.h — C ABI of libbgq.so: 4-bit / 2-bit group-quantized Mixture-of-Experts
+ * decode on one NVIDIA GB300 (sm_103a).
+ *
+ * Method (source: "397B参数的模型跑在48GB笔记本上：Flash-MoE用纯C打爆Python推理框架",
+ * blog.js-css.com/topics/2026/03/23/519):
+ *   - layer shape, section "先搞清楚为什么这件事很难": 512 routed experts per layer,
+ *     each token uses 4 of them plus 1 shared expert;
+ *   - per-token pipeline, section "架构设计：SSD当显存用": routing logits, softmax +
+ *     top-K, the selected experts' forward pass, combine, norm;
+ *   - weight format, section "FMA Dequant：一条指令省12%": every weight is
+ *     nibble*scale + bias, and the product with x is reordered into
+ *     fma(nibble, scale*x, bias*x);
+ *   - section "2-bit vs 4-bit": the same layer at 2 bits per weight.
+ * Values the page leaves open are fixed by the workload definition: a group of
+ * 64 consecutive columns shares one bf16 scale and one bf16 bias; codes are
+ * packed least-significant-first, 8 (4-bit) or 16 (2-bit) per uint32 along a
+ * row; the top-K weights are renormalised to sum to 1; equal router logits go
+ * to the lower expert index; the shared expert is scaled by sigmoid(g . x);
+ * every accumulation is fp32 and API outputs are rounded once to bf16.
+ *
+ * Conventions for every entry point
+ *   - All array pointers are DEVICE pointers owned by the caller, unless the
+ *     argument is documented as a host pointer. The library allocates no
+ *     memory, keeps no state between calls and never synchronises the host.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream). Outputs are valid once the stream reaches that point.
+ *   - Arguments are validated before anything is enqueued; a failed check
+ *     returns BGQ_ERR_INVALID_ARG / BGQ_ERR_UNSUPPORTED / BGQ_ERR_WORKSPACE and
+ *     launches nothing. A failed launch returns BGQ_ERR_CUDA.
+ *   - Conditions only the GPU can see (a bounded wait that ran out) are written
+ *     to the workspace status word; read it with bgq_read_device_status().
+ *   - Device pointers must be 16-byte aligned (codes, x, outputs) and 4-byte
+ *     aligned (scale/bias). Workspaces must be 256-byte aligned and zero-filled
+ *     once before first use (the kernels leave their counters at zero).
+ *   - bf16 values are passed as their uint16 bit patterns.
+ *   - Calls sharing one workspace must not run concurrently.
+ */
+#ifndef BGQ_H
+#define BGQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+enum {
+  BGQ_OK = 0,
+  BGQ_ERR_INVALID_ARG = 1, /* NULL pointer, bad size, misalignment, bad enum */
+  BGQ_ERR_UNSUPPORTED = 2, /* valid but not implemented shape (see each call) */
+  BGQ_ERR_CUDA = 3,        /* a CUDA launch or query failed */
+  BGQ_ERR_TIMEOUT = 4,     /* a bounded device-side wait ran out (status word) */
+  BGQ_ERR_WORKSPACE = 5    /* workspace pointer NULL or smaller than required */
+};
+
+/* Dequantisation variants of the GEMV (bgq_qgemv_variant).
+ * BGQ_DQ_INT16     production: per group, y += s*sum(q*x) + b*sum(x), the inner
+ *                  sum in exact integer arithmetic on x held as 16-bit fixed point
+ *                  with one power-of-two exponent per group of 64 (dp4a).
+ * BGQ_DQ_STANDARD  per weight: acc += (q*s + b) * x        (the page's "standard").
+ * BGQ_DQ_REORDERED per weight: acc += fma(q, s*x, b*x)     (the page's reordering).
+ * BGQ_DQ_HOISTED   per group:  y += s*sum(q*x) + b*sum(x), fp32 FMAs per weight
+ *                  (the reordering summed over a group, where s and b are constant). */
+enum { BGQ_DQ_INT16 = 0, BGQ_DQ_STANDARD = 1, BGQ_DQ_REORDERED = 2, BGQ_DQ_HOISTED = 3 };
+
+/* One group-quantized matrix W [rows x cols] (host struct, device arrays).
+ *   q  : codes, uint32 [rows][cols*bits/32]; column k of a row is in word
+ *        k/(32/bits) at bit offset bits*(k%(32/bits)).
+ *   sb : bf16 pairs [rows][cols/64][2] = (scale, bias) of each group of 64.
+ *   W[n][k] = q[n][k]*scale[n][k/64] + bias[n][k/64].
+ *   bits is 4 or 2; group must be 64; cols a multiple of 64 such that
+ *   P = cols*bits/128 divides 32 or is a multiple of 32 (e.g. 64..1024 by powers
+ *   of two, and any multiple of 1024 (4-bit) / 2048 (2-bit)). */
+typedef struct bgq_qmatrix {
+  const uint32_t* q;
+  const uint16_t* sb;
+  int32_t rows;
+  int32_t cols;
+  int32_t bits;
+  int32_t group;
+} bgq_qmatrix;
+
+/* One SwiGLU expert: y = down( silu(gate x) * (up x) ).
+ * gate and up are [d_ff x d_model], down is [d_model x d_ff]. */
+typedef struct bgq_expert {
+  bgq_qmatrix gate;
+  bgq_qmatrix up;
+  bgq_qmatrix down;
+} bgq_expert;
+
+/* One MoE layer (host struct, device arrays).
+ *   router      : bf16 [n_experts][d_model].
+ *   shared_gate : bf16 [d_model]; gamma = sigmoid(shared_gate . x). NULL: gamma = 1.
+ *   expert_q/sb : pool of routed experts. Expert e starts at
+ *                 expert_q + e*expert_q_stride (uint32 words) and
+ *                 expert_sb + e*expert_sb_stride (bf16 elements). Inside an
+ *                 expert the matrices follow each other: gate, up, down, each
+ *                 in the bgq_qmatrix layout (gate at word 0, up at word
+ *                 d_ff*d_model*bits/32, down at twice that; the same order for
+ *                 sb with d_ff*(d_model/64)*2 elements per matrix).
+ *   shared_q/sb : the shared expert, same internal layout.
+ *   Limits: 1 <= top_k <= 8, top_k <= n_experts <= 1024, d_model and d_ff
+ *   valid bgq_qmatrix column counts, bits 4 or 2, group 64. */
+typedef struct bgq_moe_layer {
+  int32_t d_model;
+  int32_t d_ff;
+  int32_t n_experts;
+  int32_t top_k;
+  int32_t bits;
+  int32_t group;
+  const uint16_t* router;
+  const uint16_t* shared_gate;
+  const uint32_t* expert_q;
+  const uint16_t* expert_sb;
+  int64_t expert_q_stride;
+  int64_t expert_sb_stride;
+  const uint32_t* shared_q;
+  const uint16_t* shared_sb;
+} bgq_moe_layer;
+
+/* Human-readable name of a status code (static string). */
+const char* bgq_status_string(int32_t status);
+
+/* ABI version of this header (major*100 + minor). */
+int32_t bgq_abi_version(void);
+
+/* y[b][n] = bf16( sum_k W[n][k] * x[b][k] ), b < batch, fp32 accumulation.
+ * The standalone GEMV of the format (Flash-MoE page, "FMA Dequant").
+ * W->bits must be 4 for q4_gemv and 2 for q2_gemv. x: bf16 [batch][cols],
+ * y: bf16 [batch][rows]. 1 <= batch <= 64. Production variant BGQ_DQ_INT16. */
+int32_t q4_gemv(const bgq_qmatrix* W, const uint16_t* x, uint16_t* y, int32_t batch, void* stream);
+int32_t q2_gemv(const bgq_qmatrix* W, const uint16_t* x, uint16_t* y, int32_t batch, void* stream);
+
+/* The same GEMV with an explicit dequantisation variant (BGQ_DQ_*), for the
+ * page's standard-vs-reordered comparison. Any bits (4 or 2). */
+int32_t bgq_qgemv_variant(const bgq_qmatrix* W, const uint16_t* x, uint16_t* y, int32_t batch,
+                          int32_t variant, void* stream);
+
+/* Router of a batch of tokens (Flash-MoE page, "架构设计": routing, then
+ * softmax + top-K on the logits).
+ *   logits_l[b][e] = router[e] . x[b] (fp32), p = softmax_fp32(l[b]),
+ *   idx[b][0..top_k) = the top_k experts by logit, largest first, equal logits
+ *   to the lower index; w[b][k] = p[idx] / sum_j p[idx_j];
+ *   gamma[b] = sigmoid(shared_gate . x[b]) (1 if shared_gate is NULL).
+ * x: bf16 [batch][d_model]. idx: int32 [batch][top_k]. w: fp32 [batch][top_k].
+ * gamma (nullable): fp32 [batch]. logits (nullable): fp32 [batch][n_experts].
+ * ws: workspace of moe_route_workspace_bytes(batch, n_experts) bytes.
+ * 1 <= batch <= 256; d_model a multiple of 256. */
+size_t moe_route_workspace_bytes(int32_t batch, int32_t n_experts);
+int32_t moe_route_topk(const uint16_t* router, const uint16_t* shared_gate, const uint16_t* x,
+                       int32_t batch, int32_t d_model, int32_t n_experts, int32_t top_k,
+                       int32_t* idx, float* w, float* gamma, float* logits,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* One SwiGLU expert on a batch (Flash-MoE page, "架构设计": expert forward):
+ *   h = silu(gate x) * (up x) (fp32, never rounded), y = down h.
+ * x: bf16 [batch][d_model]; y (nullable): bf16 [batch][d_model];
+ * y_f32 (nullable): fp32 [batch][d_model]. 1 <= batch <= 256.
+ * ws: moe_expert_workspace_bytes(e, batch) bytes. */
+size_t moe_expert_workspace_bytes(const bgq_expert* e, int32_t batch);
+int32_t moe_expert_swiglu(const bgq_expert* e, const uint16_t* x, int32_t batch,
+                          uint16_t* y, float* y_f32, void* ws, size_t ws_bytes, void* stream);
+
+/* One MoE layer on a batch of decode tokens:
+ *   out[b] = sum_k w[b][k] * expert_{idx[b][k]}(x[b]) + gamma[b] * shared(x[b]),
+ * summed in fp32 in the order k = 0..top_k-1, then the shared expert.
+ * For batch > 1 the (token, expert) pairs are grouped by expert so each expert's
+ * weights are read once per call.
+ * x: bf16 [batch][d_model]. out (nullable): bf16 [batch][d_model].
+ * out_f32 (nullable): fp32 [batch][d_model] (unrounded). idx_out (nullable):
+ * int32 [batch][top_k]. w_out (nullable): fp32 [batch][top_k].
+ * gamma_out (nullable): fp32 [batch]. 1 <= batch <= 256.
+ * ws: moe_layer_workspace_bytes(L, batch) bytes. */
+size_t moe_layer_workspace_bytes(const bgq_moe_layer* L, int32_t max_batch);
+int32_t moe_layer_forward(const bgq_moe_layer* L, const uint16_t* x, int32_t batch,
+                          uint16_t* out, float* out_f32, int32_t* idx_out, float* w_out,
+                          float* gamma_out, void* ws, size_t ws_bytes, void* stream);
+
+/* a[b] = bf16( h[b] / sqrt(mean(h[b]^2) + eps) * rho ) — the RMSNorm placed
+ * before each layer of a decode stack (Flash-MoE page, "架构设计": "norm").
+ * h: fp32 [batch][d]; rho (nullable => 1): bf16 [d]; a: bf16 [batch][d].
+ * d a multiple of 256, 1 <= batch <= 65535. */
+int32_t bgq_rmsnorm(const float* h, const uint16_t* rho, int32_t batch, int32_t d, float eps,
+                    uint16_t* a, void* stream);
+
+/* h[b] += delta[b] (fp32 residual add between layers), n = batch*d elements. */
+int32_t bgq_residual_add(float* h, const float* delta, int64_t n, void* stream);
+
+/* One decode token through a stack of n_layers resident layers (batch 1):
+ *   h = x (widened to fp32); for each layer l:
+ *     a = bf16(rmsnorm(h, rho[l], eps)); h += layer_l(a)  (fp32, unrounded);
+ *   x_next = bf16(rmsnorm(h, none, eps)).
+ * layers: HOST array of n_layers bgq_moe_layer (all with the same shape).
+ * rho: HOST array of n_layers device pointers to bf16 [d_model].
+ * x: bf16 [d_model]. x_next (nullable): bf16 [d_model]. h_out (nullable):
+ * fp32 [d_model]. idx_out (nullable): int32 [n_layers][top_k].
+ * 1 <= n_layers <= 128. ws: moe_stack_workspace_bytes(layers, n_layers). */
+size_t moe_stack_workspace_bytes(const bgq_moe_layer* layers, int32_t n_layers);
+int32_t moe_stack_decode(const bgq_moe_layer* layers, const uint16_t* const* rho, int32_t n_layers,
+                         float eps, const uint16_t* x, uint16_t* x_next, float* h_out,
+                         int32_t* idx_out, void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, then returns the status word that the kernels of the
+ * calls above left in workspace `ws` (BGQ_OK or BGQ_ERR_TIMEOUT), and clears it. */
+int32_t bgq_read_device_status(void* ws, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BGQ_H */

@@ -1,0 +1,85 @@
+"""Shared test helpers: oracle input marshalling and error metrics."""
+
+import numpy as np
+import torch
+
+from bit_group_quantized_gb300 import synth
+from oracle import bgq_oracle as O
+
+REL_L2_TOL = 2e-3  # max relative L2 error of an output vector (bf16 out, fp32 accumulate)
+TIE_GAP = 1e-3  # K-th vs (K+1)-th logit gap below which several expert sets are correct
+
+
+def bits16(t: torch.Tensor) -> np.ndarray:
+    """bf16 tensor -> uint16 numpy bit patterns (host copy)."""
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().astype(np.uint16)
+
+
+def f64(t: torch.Tensor) -> np.ndarray:
+    if t.dtype == torch.bfloat16:
+        return O.bf16_to_f64(bits16(t))
+    return t.detach().cpu().double().numpy()
+
+
+def rel_l2(got, ref) -> float:
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    den = np.linalg.norm(ref)
+    return float(np.linalg.norm(got - ref) / (den if den > 0 else 1.0))
+
+
+class ExpertSource:
+    """Regenerates single experts of a synthetic layer on the host, with a cache."""
+
+    def __init__(self, seed, layer, shape: synth.PoolShape):
+        self.seed, self.layer, self.shape = seed, layer, shape
+        self.cache = {}
+
+    def __call__(self, e: int):
+        if e not in self.cache:
+            q, sb = synth.expert_pool_range(self.seed, self.layer, self.shape, e, 1, "cpu")
+            mats = synth.expert_matrices(q[0], sb[0], self.shape)
+            self.cache[e] = [(m[0].numpy(), bits16(m[1])) for m in mats]
+        return self.cache[e]
+
+
+def topk_gap(logits: np.ndarray, k: int) -> float:
+    s = np.sort(logits)[::-1]
+    return float(s[k - 1] - s[k]) if len(s) > k else np.inf
+
+
+def check_topk_valid(gpu_idx, oracle_logits, k, gap=TIE_GAP):
+    """gpu_idx is a correct top-k within `gap`: every chosen logit >= every
+    unchosen logit - gap, all distinct."""
+    gi = [int(i) for i in gpu_idx]
+    assert len(set(gi)) == k
+    chosen = oracle_logits[gi]
+    others = np.delete(oracle_logits, gi)
+    assert chosen.min() >= others.max() - gap
+
+
+def bf16_ulp(v) -> np.ndarray:
+    """Spacing of bf16 numbers at |v| (8 significant bits)."""
+    a = np.maximum(np.abs(np.asarray(v, dtype=np.float64)), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(a)) - 7)
+
+
+def assert_bf16_output(got_bf16, ref_f64, what="", own_tol=1e-3):
+    """A bf16 output vector against its float64 oracle value.
+
+    * rel-L2 <= 2e-3 against the unrounded oracle (the workload tolerance),
+      asserted for vectors of at least 512 elements: the output rounding
+      alone costs about 1.5e-3 on average and varies more on short vectors;
+    * rel-L2 <= own_tol (1e-3) against the oracle rounded to bf16 (the
+      kernel's own error, beyond the output rounding), for every length;
+    * every element within one bf16 spacing of the oracle value (plus 1e-3
+      of the vector's largest magnitude for elements near zero).
+    """
+    got = np.asarray(got_bf16, dtype=np.float64)
+    ref = np.asarray(ref_f64, dtype=np.float64)
+    if got.size >= 512:
+        assert rel_l2(got, ref) <= REL_L2_TOL, (what, rel_l2(got, ref))
+    assert rel_l2(got, O.round_bf16(ref)) <= own_tol, (what, rel_l2(got, O.round_bf16(ref)))
+    tol = bf16_ulp(ref) + 1e-3 * np.abs(ref).max()
+    bad = np.abs(got - ref) > tol
+    assert not bad.any(), (what, np.flatnonzero(bad)[:10], got[bad][:5], ref[bad][:5])

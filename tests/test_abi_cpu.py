@@ -1,0 +1,147 @@
+"""C ABI checks that need no GPU: the library builds, loads and exports every
+entry point declared in include/bgq.h, and argument validation rejects bad
+calls before anything is launched (no CUDA call is reached on these paths)."""
+
+import ctypes as C
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bgq.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bit_group_quantized_gb300 import build, lib as L
+
+    build.build()
+    return L
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?(?:int32_t|size_t|char\s*\*|const char\s*\*)\s*\*?\s*(\w+)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ["q4_gemv", "q2_gemv", "moe_route_topk", "moe_expert_swiglu", "moe_layer_forward",
+              "moe_layer_workspace_bytes", "moe_stack_decode", "bgq_status_string", "bgq_read_device_status"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    out = subprocess.run(["nm", "-D", "--defined-only", lib.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if l.strip()}
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    L = lib.load()
+    for n in names:
+        assert hasattr(L, n)
+    assert set(lib._SIGS) >= set(names)
+
+
+def test_status_strings(lib):
+    assert lib.status_string(0) == "ok"
+    assert "workspace" in lib.status_string(5)
+    assert lib.load().bgq_abi_version() == 100
+
+
+FAKE = 0x10000000  # 256-byte aligned, never dereferenced: validation fails first
+
+
+def qmat(lib, rows=1024, cols=4096, bits=4, q=FAKE, sb=FAKE, group=64):
+    return lib.bgq_qmatrix(q, sb, rows, cols, bits, group)
+
+
+def test_gemv_validation(lib):
+    L = lib.load()
+    W = qmat(lib)
+    assert L.q4_gemv(None, FAKE, FAKE, 1, None) == lib.ERR_INVALID_ARG
+    assert L.q4_gemv(C.byref(W), None, FAKE, 1, None) == lib.ERR_INVALID_ARG
+    assert L.q4_gemv(C.byref(W), FAKE + 2, FAKE, 1, None) == lib.ERR_INVALID_ARG  # misaligned x
+    assert L.q4_gemv(C.byref(W), FAKE, FAKE, 0, None) == lib.ERR_INVALID_ARG  # batch 0
+    assert L.q4_gemv(C.byref(W), FAKE, FAKE, 65, None) == lib.ERR_INVALID_ARG
+    W2 = qmat(lib, bits=2)
+    assert L.q4_gemv(C.byref(W2), FAKE, FAKE, 1, None) == lib.ERR_INVALID_ARG  # wrong bits for q4
+    assert L.q2_gemv(C.byref(W), FAKE, FAKE, 1, None) == lib.ERR_INVALID_ARG
+    assert L.q4_gemv(C.byref(qmat(lib, group=128)), FAKE, FAKE, 1, None) == lib.ERR_UNSUPPORTED
+    assert L.q4_gemv(C.byref(qmat(lib, cols=100)), FAKE, FAKE, 1, None) == lib.ERR_INVALID_ARG
+    assert L.q4_gemv(C.byref(qmat(lib, cols=192)), FAKE, FAKE, 1, None) == lib.ERR_UNSUPPORTED
+    assert L.q4_gemv(C.byref(qmat(lib, bits=3)), FAKE, FAKE, 1, None) == lib.ERR_INVALID_ARG
+    assert L.q4_gemv(C.byref(qmat(lib, q=FAKE + 4)), FAKE, FAKE, 1, None) == lib.ERR_INVALID_ARG
+    assert L.q4_gemv(C.byref(qmat(lib, rows=0)), FAKE, FAKE, 1, None) == lib.ERR_INVALID_ARG
+    assert L.bgq_qgemv_variant(C.byref(W), FAKE, FAKE, 1, 7, None) == lib.ERR_INVALID_ARG
+
+
+def layer_struct(lib, **kw):
+    d, f, E, K, bits = kw.get("d", 4096), kw.get("f", 1024), kw.get("E", 512), kw.get("K", 4), kw.get("bits", 4)
+    mw = d * f * bits // 32
+    mg = d * f // 64 * 2
+    return lib.bgq_moe_layer(d, f, E, K, bits, kw.get("group", 64), FAKE, FAKE, FAKE, FAKE,
+                             kw.get("qs", 3 * mw), kw.get("sbs", 3 * mg), FAKE, FAKE)
+
+
+def test_layer_validation_and_workspace(lib):
+    L = lib.load()
+    Ls = layer_struct(lib)
+    need = L.moe_layer_workspace_bytes(C.byref(Ls), 1)
+    assert need > 0 and need % 256 == 0
+    assert L.moe_layer_workspace_bytes(C.byref(Ls), 64) > need
+    args = lambda ws, n: (C.byref(Ls), FAKE, 1, FAKE, None, None, None, None, ws, n, None)
+    assert L.moe_layer_forward(*args(None, need)) == lib.ERR_WORKSPACE
+    assert L.moe_layer_forward(*args(FAKE, need - 256)) == lib.ERR_WORKSPACE
+    assert L.moe_layer_forward(*args(FAKE + 16, need)) == lib.ERR_WORKSPACE  # misaligned ws
+    for bad in (dict(K=9), dict(E=2000), dict(K=600, E=512), dict(group=32), dict(d=4000)):
+        Lb = layer_struct(lib, **bad)
+        r = L.moe_layer_forward(C.byref(Lb), FAKE, 1, FAKE, None, None, None, None, FAKE, 1 << 30, None)
+        assert r in (lib.ERR_UNSUPPORTED, lib.ERR_INVALID_ARG), bad
+    Lb = layer_struct(lib, qs=100)  # expert stride shorter than one expert
+    assert L.moe_layer_forward(C.byref(Lb), FAKE, 1, FAKE, None, None, None, None, FAKE, 1 << 30, None) == \
+        lib.ERR_INVALID_ARG
+    assert L.moe_layer_forward(C.byref(Ls), FAKE, 0, FAKE, None, None, None, None, FAKE, 1 << 30, None) == \
+        lib.ERR_INVALID_ARG
+    assert L.moe_layer_forward(C.byref(Ls), FAKE, 257, FAKE, None, None, None, None, FAKE, 1 << 30, None) == \
+        lib.ERR_INVALID_ARG
+    assert L.moe_layer_forward(C.byref(Ls), FAKE, 1, None, None, None, None, None, FAKE, 1 << 30, None) == \
+        lib.ERR_INVALID_ARG  # no output at all
+
+
+def test_route_and_expert_validation(lib):
+    L = lib.load()
+    need = L.moe_route_workspace_bytes(1, 512)
+    assert need > 0
+    r = L.moe_route_topk(FAKE, None, FAKE, 1, 4096, 512, 4, FAKE, FAKE, None, None, FAKE, need - 1, None)
+    assert r == lib.ERR_WORKSPACE
+    r = L.moe_route_topk(FAKE, None, FAKE, 1, 4096, 512, 9, FAKE, FAKE, None, None, FAKE, need, None)
+    assert r == lib.ERR_UNSUPPORTED
+    r = L.moe_route_topk(FAKE, None, FAKE, 1, 4000, 512, 4, FAKE, FAKE, None, None, FAKE, need, None)
+    assert r == lib.ERR_UNSUPPORTED
+    e = lib.bgq_expert(qmat(lib, 1024, 4096), qmat(lib, 1024, 4096), qmat(lib, 4096, 1024))
+    need = L.moe_expert_workspace_bytes(C.byref(e), 1)
+    assert L.moe_expert_swiglu(C.byref(e), FAKE, 1, FAKE, None, FAKE, need - 256, None) == lib.ERR_WORKSPACE
+    bad = lib.bgq_expert(qmat(lib, 1024, 4096), qmat(lib, 1024, 4096), qmat(lib, 4096, 2048))
+    assert L.moe_expert_swiglu(C.byref(bad), FAKE, 1, FAKE, None, FAKE, 1 << 30, None) == lib.ERR_INVALID_ARG
+
+
+def test_stack_validation(lib):
+    L = lib.load()
+    layers = (lib.bgq_moe_layer * 2)(layer_struct(lib), layer_struct(lib, f=2048))
+    rho = (C.c_void_p * 2)(FAKE, FAKE)
+    r = L.moe_stack_decode(layers, rho, 2, 1e-6, FAKE, FAKE, None, None, FAKE, 1 << 30, None)
+    assert r == lib.ERR_INVALID_ARG  # mixed shapes
+    layers = (lib.bgq_moe_layer * 1)(layer_struct(lib))
+    assert L.moe_stack_decode(layers, rho, 0, 1e-6, FAKE, FAKE, None, None, FAKE, 1 << 30, None) == \
+        lib.ERR_INVALID_ARG
+    need = L.moe_stack_workspace_bytes(layers, 1)
+    assert L.moe_stack_decode(layers, rho, 1, 1e-6, FAKE, FAKE, None, None, FAKE, need - 256, None) == \
+        lib.ERR_WORKSPACE
+    assert L.bgq_rmsnorm(FAKE, None, 1, 100, 1e-6, FAKE, None) == lib.ERR_INVALID_ARG
+    assert L.bgq_read_device_status(None, None) == lib.ERR_INVALID_ARG

@@ -1,0 +1,204 @@
+"""GPU parity of the SwiGLU expert, the MoE layer and the decode stack
+against the fp64 oracle (same tolerances as the GEMV tests)."""
+
+import numpy as np
+import pytest
+import torch
+
+from bit_group_quantized_gb300 import lib, synth
+from oracle import bgq_oracle as O
+from tests.helpers import (REL_L2_TOL, TIE_GAP, ExpertSource, assert_bf16_output, bits16, check_topk_valid, f64,
+                           rel_l2, topk_gap)
+
+pytestmark = pytest.mark.gpu
+
+
+def expert_binding(q_row, sb_row, shape):
+    mats = synth.expert_matrices(q_row, sb_row, shape)
+    dims = [(shape.f, shape.d), (shape.f, shape.d), (shape.d, shape.f)]
+    return lib.Expert(*[lib.QMatrix(m[0], m[1], r, c, shape.bits) for m, (r, c) in zip(mats, dims)])
+
+
+@pytest.mark.parametrize("d,f,bits,B", [(4096, 1024, 4, 1), (4096, 1024, 4, 11), (4096, 1024, 2, 3),
+                                        (512, 256, 4, 17), (1024, 2048, 2, 1)])
+def test_expert_matches_oracle(cuda_device, d, f, bits, B):
+    shape = synth.PoolShape(d, f, 1, bits)
+    q, sb = synth.expert_pool_range(77, 0, shape, 0, 1, device=cuda_device)
+    ex = expert_binding(q[0], sb[0], shape)
+    x = synth.activations(77, d, B, d, device=cuda_device)
+    y, yf = lib.moe_expert_swiglu(ex, x, want_f32=True)
+    torch.cuda.synchronize()
+    mats = [(m[0].cpu().numpy(), bits16(m[1])) for m in synth.expert_matrices(q[0], sb[0], shape)]
+    xd = f64(x)
+    for t in range(B):
+        ref = O.expert_swiglu(*mats, bits, xd[t])
+        assert_bf16_output(f64(y)[t], ref, t)
+        assert rel_l2(f64(yf)[t], ref) <= 2e-4  # unrounded fp32 output
+    assert torch.equal(y, yf.to(torch.bfloat16))
+
+
+def build_layer(seed, layer, shape, K, dev, with_gate=True):
+    t = synth.layer_tensors(seed, layer, shape, device=dev, with_gate=with_gate)
+    E = shape.E
+    L = lib.MoELayer(shape.d, shape.f, E, K, shape.bits, t["router"], t["shared_gate"], t["pool_q"][:E],
+                     t["pool_sb"][:E], t["pool_q"][E], t["pool_sb"][E])
+    return L, t
+
+
+def oracle_layer_token(t, src, shape, K, x_tok, gpu_idx=None):
+    """Oracle layer output for one token; near-tie tokens use the GPU's expert set."""
+    Rb = bits16(t["router"])
+    Gb = None if t["shared_gate"] is None else bits16(t["shared_gate"])
+    logits = O.route(Rb, x_tok, K, Gb)[0]
+    force = None
+    if gpu_idx is not None and topk_gap(logits, K) <= TIE_GAP:
+        check_topk_valid(gpu_idx, logits, K)
+        force = gpu_idx
+    out, idx, w, gamma = O.moe_layer(Rb, Gb, src, src(shape.E), shape.bits, x_tok, K, force_idx=force)
+    return out, idx, w, gamma, logits
+
+
+@pytest.mark.parametrize("E,d,f,K,bits,B", [
+    (16, 256, 128, 4, 4, 1),
+    (16, 256, 128, 4, 4, 40),  # several 8-token tasks per expert
+    (8, 512, 256, 2, 2, 13),
+    (64, 1024, 512, 4, 4, 64),
+    (32, 2048, 1024, 8, 4, 5),
+])
+def test_small_layer_matches_oracle(cuda_device, E, d, f, K, bits, B):
+    shape = synth.PoolShape(d, f, E, bits)
+    L, t = build_layer(5, 0, shape, K, cuda_device)
+    # spread the tiny router's logits like the 4096-wide one
+    t["router"].copy_((t["router"].float() * np.sqrt(4096 / d)).to(torch.bfloat16))
+    x = synth.activations(5, 2, B, d, device=cuda_device)
+    out, out_f32, idx, w, gamma = lib.moe_layer_forward(L, x, want_f32=True, want_route=True)
+    torch.cuda.synchronize()
+    src = ExpertSource(5, 0, shape)
+    xd = f64(x)
+    for tok in range(B):
+        gi = idx[tok].cpu().numpy()
+        ref, oi, ow, og, logits = oracle_layer_token(t, src, shape, K, xd[tok], gi)
+        if topk_gap(logits, K) > TIE_GAP:
+            assert gi.tolist() == oi.tolist()
+        assert_bf16_output(f64(out)[tok], ref, tok)
+        assert rel_l2(f64(out_f32)[tok], ref) <= 5e-4, tok
+        assert abs(float(gamma[tok]) - og) <= 1e-6
+
+
+@pytest.fixture(scope="module")
+def full_layer(cuda_device):
+    shape = synth.PoolShape(4096, 1024, 512, 4)
+    L, t = build_layer(0, 0, shape, 4, cuda_device)
+    return shape, L, t
+
+
+@pytest.mark.parametrize("B,sample", [(1, [0]), (4, [0, 3]), (16, [0, 9, 15]), (64, [0, 31, 63])])
+def test_full_layer_matches_oracle_on_sampled_tokens(cuda_device, full_layer, B, sample):
+    shape, L, t = full_layer
+    x = synth.activations(0, 100 + B, B, shape.d, device=cuda_device)
+    out, _, idx, w, gamma = lib.moe_layer_forward(L, x, want_route=True)
+    torch.cuda.synchronize()
+    src = ExpertSource(0, 0, shape)
+    xd = f64(x)
+    for tok in sample:
+        gi = idx[tok].cpu().numpy()
+        ref, oi, ow, og, logits = oracle_layer_token(t, src, shape, 4, xd[tok], gi)
+        if topk_gap(logits, 4) > TIE_GAP:
+            assert gi.tolist() == oi.tolist()
+            assert np.allclose(w[tok].cpu().numpy(), ow, rtol=1e-5, atol=1e-6)
+        assert_bf16_output(f64(out)[tok], ref, tok)
+    # every token: valid routing, weights sum to 1
+    assert torch.all((idx >= 0) & (idx < 512))
+    assert torch.allclose(w.sum(dim=1), torch.ones(B, device=cuda_device), atol=1e-6)
+
+
+def test_layer_batch_equals_single_bitwise(cuda_device, full_layer):
+    """Grouping tokens by expert does not change any token's result."""
+    shape, L, t = full_layer
+    x = synth.activations(0, 900, 12, shape.d, device=cuda_device)
+    ob = lib.moe_layer_forward(L, x)[0]
+    for tok in range(12):
+        o1 = lib.moe_layer_forward(L, x[tok:tok + 1].contiguous())[0]
+        assert torch.equal(ob[tok].view(torch.int16), o1[0].view(torch.int16)), tok
+
+
+def test_layer_deterministic(cuda_device, full_layer):
+    shape, L, t = full_layer
+    x = synth.activations(0, 901, 16, shape.d, device=cuda_device)
+    ws = lib.workspace(lib.moe_layer_workspace_bytes(L, 16), cuda_device)
+    a = lib.moe_layer_forward(L, x, ws=ws)[0].clone()
+    b = lib.moe_layer_forward(L, x, ws=ws)[0]
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert lib.read_device_status(ws) == lib.OK
+
+
+def test_layer_expert_permutation(cuda_device):
+    """Permuting the router rows together with the expert pool leaves the output unchanged."""
+    shape = synth.PoolShape(512, 256, 16, 4)
+    L, t = build_layer(8, 0, shape, 4, cuda_device)
+    x = synth.activations(8, 0, 6, shape.d, device=cuda_device)
+    out, _, idx, _, _ = lib.moe_layer_forward(L, x, want_route=True)
+    perm = torch.randperm(16, generator=torch.Generator().manual_seed(0)).to(cuda_device)
+    R2 = t["router"][perm].contiguous()
+    q2 = t["pool_q"][:16][perm].contiguous()
+    sb2 = t["pool_sb"][:16][perm].contiguous()
+    L2 = lib.MoELayer(shape.d, shape.f, 16, 4, 4, R2, t["shared_gate"], q2, sb2, t["pool_q"][16], t["pool_sb"][16])
+    out2, _, idx2, _, _ = lib.moe_layer_forward(L2, x, want_route=True)
+    torch.cuda.synchronize()
+    assert torch.equal(perm[idx2.long()], idx.long())
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+
+
+# ------------------------------------------------------------------ stack
+def stack_case(dev, seed, n_layers, shape, K):
+    built = [build_layer(seed, l, shape, K, dev) for l in range(n_layers)]
+    rhos = [synth.rho(seed, l, shape.d, device=dev) for l in range(n_layers)]
+    return built, rhos
+
+
+def oracle_stack(seed, built, rhos, shape, K, x_bits, gpu_idx):
+    layers = []
+    for l, (L, t) in enumerate(built):
+        layers.append(dict(router=bits16(t["router"]), shared_gate=bits16(t["shared_gate"]), rho=bits16(rhos[l]),
+                           get_expert=ExpertSource(seed, l, shape), shared=None))
+        layers[-1]["shared"] = layers[-1]["get_expert"](shape.E)
+    # near ties: evaluate with the GPU's expert set (checked valid inside)
+    h = O.bf16_to_f64(x_bits)
+    force = []
+    for l, L in enumerate(layers):
+        a = O.round_bf16(O.rmsnorm(h, L["rho"]))
+        logits = O.route(L["router"], a, K, L["shared_gate"])[0]
+        if topk_gap(logits, K) <= TIE_GAP:
+            check_topk_valid(gpu_idx[l], logits, K)
+            force.append(np.asarray(gpu_idx[l]))
+        else:
+            force.append(None)
+        out, _, _, _ = O.moe_layer(L["router"], L["shared_gate"], L["get_expert"], L["shared"], shape.bits, a, K,
+                                   force_idx=force[-1])
+        h = h + out
+    return O.stack_token(layers, x_bits, shape.bits, K, force_idx=force)
+
+
+@pytest.mark.parametrize("n_layers,d,f,E,bits", [(6, 512, 256, 16, 4), (4, 4096, 1024, 512, 4),
+                                                 (3, 4096, 1024, 512, 2)])
+def test_stack_matches_oracle(cuda_device, n_layers, d, f, E, bits):
+    K = 4
+    shape = synth.PoolShape(d, f, E, bits)
+    built, rhos = stack_case(cuda_device, 3, n_layers, shape, K)
+    if d != 4096:
+        for L, t in built:
+            t["router"].copy_((t["router"].float() * np.sqrt(4096 / d)).to(torch.bfloat16))
+    st = lib.Stack([b[0] for b in built], rhos)
+    x = synth.activations(3, 5, 1, d, device=cuda_device)[0]
+    x_next = torch.empty_like(x)
+    h = torch.empty(d, dtype=torch.float32, device=cuda_device)
+    idx = torch.empty((n_layers, K), dtype=torch.int32, device=cuda_device)
+    lib.moe_stack_decode(st, x, 1e-6, x_next=x_next, h_out=h, idx_out=idx)
+    torch.cuda.synchronize()
+    xo, ho, oidx = oracle_stack(3, built, rhos, shape, K, bits16(x), idx.cpu().numpy())
+    assert rel_l2(f64(h), ho) <= REL_L2_TOL
+    # x_next against the oracle's unrounded normalised residual. Every layer
+    # rounds its normalised input to bf16 on both sides, from slightly
+    # different values, so the stack's own error may exceed one layer's.
+    assert_bf16_output(O.bf16_to_f64(bits16(x_next)), O.rmsnorm(ho, None), "x_next", own_tol=REL_L2_TOL)
+    assert rel_l2(O.bf16_to_f64(bits16(x_next)), O.bf16_to_f64(xo)) <= REL_L2_TOL
