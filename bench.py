@@ -1,0 +1,364 @@
+#!/usr/bin/env python3
+"""Benchmark of the group-quantized MoE decode path on GB300.
+
+Default workload: batch-1 decode through a stack of 24 resident MoE layers
+(d_model 4096, d_ff 1024, 512 routed experts + 1 shared expert, top-4,
+4-bit codes with a bf16 scale and bias per group of 64; 87 GB of weights,
+far larger than L2). One step = one token through all 24 layers (RMSNorm,
+router, softmax/top-4, SwiGLU experts, shared expert, combine, residual).
+Seeded synthetic weights and activations (no trained model exists here).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload stack4|stack2|layer|gemv] [--layers L] [--batch B]
+
+Prints one JSON line. With N > 1 (torchrun) every rank runs its own decode
+stream on its own GPU (replicas; no data-path collective); the slowest
+rank's time is reported and `value` counts all ranks' tokens.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer decode µs/layer and tokens/s; q4 GEMV HBM GB/s vs ~8 TB/s peak"
+D_MODEL, D_FF, N_EXPERTS, TOP_K = 4096, 1024, 512, 4
+EPS = 1e-6
+
+
+# ------------------------------------------------------------------ helpers
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def layer_weight_bytes(bits: int) -> int:
+    from bit_group_quantized_gb300 import synth
+
+    shape = synth.PoolShape(D_MODEL, D_FF, N_EXPERTS, bits)
+    # router + shared-gate vector + 4 routed experts + 1 shared expert
+    return N_EXPERTS * D_MODEL * 2 + D_MODEL * 2 + (TOP_K + 1) * shape.expert_bytes
+
+
+def layer_algorithmic_bytes(bits: int) -> int:
+    # weights + RMSNorm weight + normalised input (bf16) + residual read/write (fp32)
+    return layer_weight_bytes(bits) + D_MODEL * 2 + D_MODEL * 2 + D_MODEL * 4 * 2
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ oracle (CPU) timing
+def oracle_sample(bits: int, n_layers: int, seed: int = 0):
+    """Time the fp64 oracle on one token through `n_layers` layers of the stack.
+
+    Runs in this process on the host cores (numpy/BLAS threads). Expert
+    regeneration on the host is excluded from the timed part.
+    """
+    import numpy as np
+    import torch
+
+    from bit_group_quantized_gb300 import synth
+    from oracle import bgq_oracle as O
+
+    shape = synth.PoolShape(D_MODEL, D_FF, N_EXPERTS, bits)
+
+    def b16(t):
+        return t.contiguous().view(torch.int16).numpy().astype(np.uint16)
+
+    h = O.bf16_to_f64(b16(synth.activations(seed, 0, 1, D_MODEL)[0]))
+    total = 0.0
+    for l in range(n_layers):
+        R = b16(synth.router(seed, l, N_EXPERTS, D_MODEL))
+        G = b16(synth.shared_gate(seed, l, D_MODEL))
+        rho = b16(synth.rho(seed, l, D_MODEL))
+        t0 = time.perf_counter()
+        a = O.round_bf16(O.rmsnorm(h, rho, EPS))
+        idx = O.route(R, a, TOP_K, G)[2]
+        total += time.perf_counter() - t0
+        cache = {}
+        for e in list(idx) + [N_EXPERTS]:
+            q, sb = synth.expert_pool_range(seed, l, shape, int(e), 1)
+            cache[int(e)] = [(m[0].numpy(), b16(m[1])) for m in synth.expert_matrices(q[0], sb[0], shape)]
+        t0 = time.perf_counter()
+        out, _, _, _ = O.moe_layer(R, G, lambda e: cache[e], cache[N_EXPERTS], bits, a, TOP_K)
+        h = h + out
+        total += time.perf_counter() - t0
+    return total / n_layers  # seconds per layer-token
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    """The oracle as the reference arm: fp64 on the host cores, bounded sample per step."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    bits = 2 if args.workload == "stack2" else 4
+    n_layers = args.layers
+    per_step_layers = 1  # each step: one layer of the stack for one token (bounded sample)
+    for _ in range(args.warmup):
+        oracle_sample(bits, per_step_layers)
+    times = [oracle_sample(bits, per_step_layers, seed=s + 1) for s in range(args.steps)]
+    s_layer = statistics.mean(times)
+    tok_s = 1.0 / (s_layer * n_layers)
+    cores = cpu_cores()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(tok_s, 4), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(s_layer * n_layers * 1000, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_name(args), "us_per_layer": round(s_layer * 1e6, 1)},
+        "cpu_baseline": {"value": round(tok_s, 4), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step: 1 of {n_layers} layers for one token (router + 4 experts + shared),"
+                                   " scaled to the full stack"},
+        "e2e": {"value": round(tok_s, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_name(args) -> str:
+    if args.workload in ("stack4", "stack2"):
+        bits = 4 if args.workload == "stack4" else 2
+        return (f"moe_decode_stack: {args.layers} layers x (512 routed + 1 shared SwiGLU experts, d_model 4096, "
+                f"d_ff 1024, top-4), {bits}-bit codes, group 64 bf16 scale+bias, batch 1")
+    if args.workload == "layer":
+        return f"moe_layer: 512 routed + 1 shared experts, d_model 4096, d_ff 1024, top-4, 4-bit, batch {args.batch}"
+    return "q4_gemv: 1024x4096 4-bit, group 64, batch 1"
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from bit_group_quantized_gb300 import lib, synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    torch.cuda.set_device(local)
+    dev = torch.device(f"cuda:{local}")
+    lib.load()
+
+    bits = 2 if args.workload == "stack2" else 4
+    n_layers = args.layers
+    shape = synth.PoolShape(D_MODEL, D_FF, N_EXPERTS, bits)
+    layers, rhos, keep = [], [], []
+    for l in range(n_layers):
+        t = synth.layer_tensors(args.seed + rank, l, shape, device=dev)
+        keep.append(t)
+        layers.append(lib.MoELayer(D_MODEL, D_FF, N_EXPERTS, TOP_K, bits, t["router"], t["shared_gate"],
+                                   t["pool_q"][:N_EXPERTS], t["pool_sb"][:N_EXPERTS], t["pool_q"][N_EXPERTS],
+                                   t["pool_sb"][N_EXPERTS]))
+        rhos.append(synth.rho(args.seed + rank, l, D_MODEL, device=dev))
+    stack = lib.Stack(layers, rhos)
+    ws = lib.workspace(stack.ws_bytes, dev)
+    x_in = synth.activations(args.seed + rank, 0, 1, D_MODEL, device=dev)[0].clone()
+    x_out = torch.empty_like(x_in)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+
+    def step():
+        lib.moe_stack_decode(stack, x_in, EPS, ws=ws, x_next=x_out, stream=stream)
+        x_in.copy_(x_out)
+
+    graph = None
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+        stream.synchronize()
+        if not args.no_graph:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                step()
+
+    def run(n):
+        with torch.cuda.stream(stream):
+            for _ in range(n):
+                if graph is not None:
+                    graph.replay()
+                else:
+                    step()
+
+    run(args.warmup)
+    stream.synchronize()
+    status = lib.read_device_status(ws, stream)
+    if status != lib.OK:
+        raise RuntimeError(f"device status after warm-up: {lib.status_string(status)}")
+
+    # ---- timed region (device time, CUDA events on the launching stream)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    run(args.steps)
+    e1.record(stream)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    clock = clocks.stop()
+    if world > 1:
+        dist.barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---- end to end through the public API with host buffers
+    xh = torch.empty(D_MODEL, dtype=torch.bfloat16, pin_memory=True)
+    xh.copy_(x_in.cpu())
+    oh = torch.empty(D_MODEL, dtype=torch.bfloat16, pin_memory=True)
+    e2e_steps = max(1, min(args.steps, 500))
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(e2e_steps):
+            x_in.copy_(xh, non_blocking=True)
+            lib.moe_stack_decode(stack, x_in, EPS, ws=ws, x_next=x_out, stream=stream)
+            oh.copy_(x_out, non_blocking=True)
+            stream.synchronize()
+            xh.copy_(oh)
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        n_s = 2
+        s_layer = oracle_sample(bits, n_s, seed=args.seed)
+        cpu = {"value": round(1.0 / (s_layer * n_layers), 5), "unit": "tokens/s", "cores": cpu_cores(),
+               "kind": "oracle",
+               "sample": f"one token through {n_s} of the {n_layers} layers (fp64 numpy/BLAS), scaled to the stack"}
+
+    if rank == 0:
+        peak, peak_kind = peaks()
+        layer_bytes = layer_algorithmic_bytes(bits)
+        step_bytes = n_layers * layer_bytes
+        us_layer = ms * 1000 / n_layers
+        achieved = step_bytes / (ms * 1e-3) / 1e9
+        launches = 1 + 6 * n_layers + 1
+        line = {
+            "metric": METRIC, "value": round(world * 1000.0 / ms, 2), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int8x4-dot/f32" if bits else "f32",
+            "data": "synthetic (seeded counter-based generator; no trained weights)",
+            "config": {"workload": workload_name(args), "us_per_layer": round(us_layer, 3),
+                       "gbs_per_layer": round(achieved, 1), "bytes_per_layer": layer_bytes,
+                       "l2": "inputs larger than L2 (the stack holds %.1f GB of weights)" % (
+                           n_layers * shape.expert_bytes * (N_EXPERTS + 1) / 1e9),
+                       "graph": graph is not None, "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "kernel": "moe_stack_decode step (all launches of one token)",
+                         "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
+                         "frac_of_8tbs": round(achieved / 8000.0, 4), "traffic": None},
+            "e2e": {"value": round(world / e2e_s, 2), "unit": "tokens/s", "h2d_bytes_per_step": D_MODEL * 2,
+                    "d2h_bytes_per_step": D_MODEL * 2},
+            "gpu_launches": launches * args.steps,
+            "clocks": clock,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="stack4", choices=["stack4", "stack2"])
+    ap.add_argument("--layers", type=int, default=24)
+    ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
