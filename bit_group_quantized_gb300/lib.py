@@ -61,6 +61,7 @@ _SIGS = {
     "moe_expert_swiglu": (_I, [C.POINTER(bgq_expert), _P, _I, _P, _P, _P, _S, _P]),
     "moe_layer_workspace_bytes": (_S, [C.POINTER(bgq_moe_layer), _I]),
     "moe_layer_forward": (_I, [C.POINTER(bgq_moe_layer), _P, _I, _P, _P, _P, _P, _P, _P, _S, _P]),
+    "moe_layer_forward_noalloc": (_I, [C.POINTER(bgq_moe_layer), _P, _I, _P, _P, _P, _P, _P, _P]),
     "bgq_rmsnorm": (_I, [_P, _P, _I, _I, C.c_float, _P, _P]),
     "bgq_residual_add": (_I, [_P, _P, C.c_int64, _P]),
     "moe_stack_workspace_bytes": (_S, [C.POINTER(bgq_moe_layer), _I]),
@@ -237,6 +238,18 @@ def moe_layer_forward(layer: MoELayer, x: torch.Tensor, ws=None, out=None, out_f
         ws = workspace(lib.moe_layer_workspace_bytes(C.byref(s), B), dev)
     _check(lib.moe_layer_forward(C.byref(s), _ptr(x), B, _ptr(out), _ptr(out_f32), _ptr(idx), _ptr(w),
                                  _ptr(gamma), _ptr(ws), ws.numel(), _stream(stream)), "moe_layer_forward")
+    return out, out_f32, idx, w, gamma
+
+
+def moe_layer_forward_noalloc(layer: MoELayer, x: torch.Tensor, out=None, out_f32=None, idx=None, w=None,
+                              gamma=None, stream=None):
+    """moe_layer_forward with the library's fixed scratch array instead of a
+    workspace: for callers that cannot allocate device memory at call time.
+    Output buffers given as None are not written (pass tensors to receive them)."""
+    B = x.shape[0]
+    s = layer.struct()
+    _check(load().moe_layer_forward_noalloc(C.byref(s), _ptr(x), B, _ptr(out), _ptr(out_f32), _ptr(idx), _ptr(w),
+                                            _ptr(gamma), _stream(stream)), "moe_layer_forward_noalloc")
     return out, out_f32, idx, w, gamma
 
 

@@ -22,7 +22,8 @@
  * Conventions for every entry point
  *   - All array pointers are DEVICE pointers owned by the caller, unless the
  *     argument is documented as a host pointer. The library allocates no
- *     memory, keeps no state between calls and never synchronises the host.
+ *     memory, keeps no state between calls (moe_layer_forward_noalloc's fixed
+ *     scratch array is the one exception) and never synchronises the host.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream). Outputs are valid once the stream reaches that point.
  *   - Arguments are validated before anything is enqueued; a failed check
@@ -178,6 +179,27 @@ size_t moe_layer_workspace_bytes(const bgq_moe_layer* L, int32_t max_batch);
 int32_t moe_layer_forward(const bgq_moe_layer* L, const uint16_t* x, int32_t batch,
                           uint16_t* out, float* out_f32, int32_t* idx_out, float* w_out,
                           float* gamma_out, void* ws, size_t ws_bytes, void* stream);
+
+/* moe_layer_forward without a workspace argument. The Flash-MoE page has no
+ * counterpart: this entry point exists for callers that cannot allocate device
+ * memory at the point where they run a layer (a plugin inside a framework that
+ * owns the allocator and gives it no workspace, a process whose memory budget
+ * is fixed after start-up, a foreign-function caller that can pass buffers but
+ * not create them).
+ * Same arguments, kernels and results as moe_layer_forward; the scratch memory
+ * is a 4 MiB array inside the library (held on every GPU that loads the
+ * library until the process exits), enough for batch <= 40 at d_model 4096,
+ * d_ff 1024, 512 experts, top-4. A call whose moe_layer_workspace_bytes(L,
+ * batch) exceeds 4 MiB returns BGQ_ERR_WORKSPACE and launches nothing.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture. Each call clears the array's 256-byte control block on
+ * `stream`, then runs the layer. All calls on a device share the one array,
+ * which keeps the last call's contents: calls that can overlap on the GPU (on
+ * different streams, or from different host threads) race and must be
+ * serialised by the caller. Allocates nothing. */
+int32_t moe_layer_forward_noalloc(const bgq_moe_layer* L, const uint16_t* x, int32_t batch, uint16_t* out,
+                                  float* out_f32, int32_t* idx_out, float* w_out, float* gamma_out, void* stream);
 
 /* a[b] = bf16( h[b] / sqrt(mean(h[b]^2) + eps) * rho ) — the RMSNorm placed
  * before each layer of a decode stack (Flash-MoE page, "架构设计": "norm").
