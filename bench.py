@@ -313,18 +313,24 @@ def run_ours(args):
         step_bytes = n_layers * layer_bytes
         us_layer = ms * 1000 / n_layers
         achieved = step_bytes / (ms * 1e-3) / 1e9
-        launches = 1 + 6 * n_layers + 1
+        # the persistent kernel runs a whole token in one launch; the multi-kernel
+        # fallback launches widen + 6 per layer + the final norm
+        fused = lib.load().moe_stack_trace_entries(stack.c_layers, n_layers) > 0
+        launches = 1 if fused else 1 + 6 * n_layers + 1
         line = {
             "metric": METRIC, "value": round(world * 1000.0 / ms, 2), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "int8x4-dot/f32" if bits else "f32",
+            "scaling": "weak", "vs_baseline": None, "dtype": "u4 codes x s16 fixed-point x (dp4a), f32 accumulate" if bits == 4
+            else "u2 codes x s16 fixed-point x (dp4a), f32 accumulate",
             "data": "synthetic (seeded counter-based generator; no trained weights)",
             "config": {"workload": workload_name(args), "us_per_layer": round(us_layer, 3),
                        "gbs_per_layer": round(achieved, 1), "bytes_per_layer": layer_bytes,
                        "l2": "inputs larger than L2 (the stack holds %.1f GB of weights)" % (
                            n_layers * shape.expert_bytes * (N_EXPERTS + 1) / 1e9),
                        "graph": graph is not None, "parallelism": f"replicas x{world}"},
-            "roofline": {"bound": "hbm", "kernel": "moe_stack_decode step (all launches of one token)",
+            "roofline": {"bound": "hbm",
+                         "kernel": ("k_fused_decode (one launch per token, all %d layers)" % n_layers) if fused
+                         else "moe_stack_decode step (multi-kernel path)",
                          "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
                          "frac_of_8tbs": round(achieved / 8000.0, 4), "traffic": None},

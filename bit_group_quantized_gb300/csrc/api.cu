@@ -8,6 +8,7 @@
 
 #include "../../include/bgq.h"
 #include "common.cuh"
+#include "fused.h"
 #include "kernels.h"
 
 namespace bgq {
@@ -61,6 +62,11 @@ struct LayerWs {
   float* gamma;
   float* H;  // [B][K+1][f]
   float* Y;  // [B][K+1][d]
+  // batch-1 persistent kernel scratch
+  float* fh;        // [d] residual stream
+  float* fpart;     // [2][1024] per-CTA sums of squares
+  int32_t* fidx;    // [16]
+  float* fw;        // [16]
   size_t bytes;
 };
 
@@ -75,6 +81,10 @@ LayerWs carve_layer(void* ws, int B, int d, int f, int E, int K) {
   L.gamma = c.take<float>((size_t)B * 4);
   L.H = c.take<float>((size_t)B * (K + 1) * f * 4);
   L.Y = c.take<float>((size_t)B * (K + 1) * d * 4);
+  L.fh = c.take<float>((size_t)d * 4);
+  L.fpart = c.take<float>(2 * 1024 * 4);
+  L.fidx = c.take<int32_t>(16 * 4);
+  L.fw = c.take<float>(16 * 4);
   L.bytes = c.off;
   return L;
 }
@@ -114,6 +124,45 @@ ExpertSet expert_set(const bgq_moe_layer* L) {
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? BGQ_OK : BGQ_ERR_CUDA; }
+
+constexpr long long kFusedTimeoutNs = 2000000000ll;  // bounded waits inside the persistent kernel
+
+// The persistent kernel streams weight rows with 16-byte bulk copies.
+bool use_fused(const bgq_moe_layer* L) {
+  if (!al(L->router, 16) || !al(L->expert_sb, 16) || !al(L->shared_sb, 16)) return false;
+  if (L->shared_gate && !al(L->shared_gate, 16)) return false;
+  if (L->expert_sb_stride % 8) return false;
+  return fused_supported(L->d_model, L->d_ff, L->n_experts, L->top_k, L->bits) && num_sms() <= 1024;
+}
+
+void fill_fused_common(FusedParams& P, const bgq_moe_layer* L0, const LayerWs& W) {
+  P.d = L0->d_model;
+  P.f = L0->d_ff;
+  P.E = L0->n_experts;
+  P.K = L0->top_k;
+  P.timeout_ns = kFusedTimeoutNs;
+  P.ctrl = W.ctrl;
+  P.h = W.fh;
+  P.hk = W.H;
+  P.logits = W.logits;
+  P.part_ss = W.fpart;
+  P.route_idx = W.fidx;
+  P.route_w = W.fw;
+}
+
+FusedLayer fused_layer(const bgq_moe_layer* L, const uint16_t* rho) {
+  FusedLayer f;
+  f.router = L->router;
+  f.sgate = L->shared_gate;
+  f.pool_q = L->expert_q;
+  f.pool_sb = L->expert_sb;
+  f.q_stride = L->expert_q_stride;
+  f.sb_stride = L->expert_sb_stride;
+  f.shared_q = L->shared_q;
+  f.shared_sb = L->shared_sb;
+  f.rho = rho;
+  return f;
+}
 
 }  // namespace
 
@@ -245,6 +294,22 @@ int32_t moe_layer_forward(const bgq_moe_layer* L, const uint16_t* x, int32_t bat
   if (batch < 1 || batch > kMaxBatch) return BGQ_ERR_INVALID_ARG;
   if (!ws || !al(ws, 256) || ws_bytes < moe_layer_workspace_bytes(L, batch)) return BGQ_ERR_WORKSPACE;
   LayerWs W = carve_layer(ws, batch, L->d_model, L->d_ff, L->n_experts, L->top_k);
+  if (batch == 1 && use_fused(L)) {
+    static_assert(sizeof(FusedParams) < 32000, "kernel parameter space");
+    FusedParams P{};
+    fill_fused_common(P, L, W);
+    P.n_layers = 1;
+    P.stack = 0;
+    P.eps = 0.f;
+    P.x_in = x;
+    P.out = out;
+    P.out_f32 = out_f32;
+    P.idx_out = idx_out;
+    P.w_out = w_out;
+    P.gamma_out = gamma_out;
+    P.layers[0] = fused_layer(L, nullptr);
+    return cuda_status(launch_fused(P, L->bits, st(stream)));
+  }
   return layer_forward_impl(L, x, batch, out, out_f32, idx_out, w_out, gamma_out, W, st(stream));
 }
 
@@ -269,9 +334,32 @@ size_t moe_stack_workspace_bytes(const bgq_moe_layer* layers, int32_t n_layers) 
   return b + up256((size_t)L->d_model * 4) * 2 + up256((size_t)L->d_model * 2);
 }
 
+static int32_t stack_decode_impl(const bgq_moe_layer* layers, const uint16_t* const* rho, int32_t n_layers,
+                                 float eps, const uint16_t* x, uint16_t* x_next, float* h_out, int32_t* idx_out,
+                                 void* ws, size_t ws_bytes, uint64_t* trace, void* stream);
+
 int32_t moe_stack_decode(const bgq_moe_layer* layers, const uint16_t* const* rho, int32_t n_layers, float eps,
                          const uint16_t* x, uint16_t* x_next, float* h_out, int32_t* idx_out, void* ws,
                          size_t ws_bytes, void* stream) {
+  return stack_decode_impl(layers, rho, n_layers, eps, x, x_next, h_out, idx_out, ws, ws_bytes, nullptr, stream);
+}
+
+size_t moe_stack_trace_entries(const bgq_moe_layer* layers, int32_t n_layers) {
+  if (!layers || n_layers < 1 || !use_fused(&layers[0])) return 0;
+  return (size_t)n_layers * num_sms() * kTraceEvents;
+}
+
+int32_t moe_stack_decode_traced(const bgq_moe_layer* layers, const uint16_t* const* rho, int32_t n_layers, float eps,
+                                const uint16_t* x, uint16_t* x_next, float* h_out, int32_t* idx_out, void* ws,
+                                size_t ws_bytes, uint64_t* trace, void* stream) {
+  if (!trace || !al(trace, 16)) return BGQ_ERR_INVALID_ARG;
+  if (!layers || n_layers < 1 || !use_fused(&layers[0])) return BGQ_ERR_UNSUPPORTED;
+  return stack_decode_impl(layers, rho, n_layers, eps, x, x_next, h_out, idx_out, ws, ws_bytes, trace, stream);
+}
+
+static int32_t stack_decode_impl(const bgq_moe_layer* layers, const uint16_t* const* rho, int32_t n_layers,
+                                 float eps, const uint16_t* x, uint16_t* x_next, float* h_out, int32_t* idx_out,
+                                 void* ws, size_t ws_bytes, uint64_t* trace, void* stream) {
   if (!layers || !rho || n_layers < 1 || n_layers > kMaxLayers) return BGQ_ERR_INVALID_ARG;
   const bgq_moe_layer* L0 = &layers[0];
   for (int l = 0; l < n_layers; ++l) {
@@ -288,6 +376,20 @@ int32_t moe_stack_decode(const bgq_moe_layer* layers, const uint16_t* const* rho
   if (!ws || !al(ws, 256) || ws_bytes < moe_stack_workspace_bytes(layers, n_layers)) return BGQ_ERR_WORKSPACE;
   const int d = L0->d_model, K = L0->top_k;
   LayerWs W = carve_layer(ws, 1, d, L0->d_ff, L0->n_experts, K);
+  if (use_fused(L0)) {
+    FusedParams P{};
+    fill_fused_common(P, L0, W);
+    P.n_layers = n_layers;
+    P.stack = 1;
+    P.eps = eps;
+    P.x_in = x;
+    P.x_next = x_next;
+    P.h_out = h_out;
+    P.idx_out = idx_out;
+    P.trace = reinterpret_cast<unsigned long long*>(trace);
+    for (int l = 0; l < n_layers; ++l) P.layers[l] = fused_layer(&layers[l], rho[l]);
+    return cuda_status(launch_fused(P, L0->bits, st(stream)));
+  }
   Carver c(static_cast<char*>(ws) + W.bytes);
   float* h = c.take<float>((size_t)d * 4);
   float* o = c.take<float>((size_t)d * 4);
@@ -305,6 +407,14 @@ int32_t moe_stack_decode(const bgq_moe_layer* layers, const uint16_t* const* rho
   if (h_out && cudaMemcpyAsync(h_out, h, (size_t)d * 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
     return BGQ_ERR_CUDA;
   return BGQ_OK;
+}
+
+int32_t bgq_wait_selftest(void* ws, size_t ws_bytes, int64_t timeout_ns, void* stream) {
+  if (!ws || !al(ws, 256) || ws_bytes < sizeof(Ctrl)) return BGQ_ERR_WORKSPACE;
+  if (timeout_ns < 1000 || timeout_ns > 1000000000ll) return BGQ_ERR_INVALID_ARG;
+  cudaStream_t s = st(stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(Ctrl), s) != cudaSuccess) return BGQ_ERR_CUDA;
+  return cuda_status(launch_wait_selftest(static_cast<Ctrl*>(ws), timeout_ns, s));
 }
 
 int32_t bgq_read_device_status(void* ws, void* stream) {

@@ -125,96 +125,120 @@ struct XStage {
 __device__ __forceinline__ float load_in(const uint16_t* x, int i) { return bf16f(x[i]); }
 __device__ __forceinline__ float load_in(const float* x, int i) { return x[i]; }
 
-// Where the T input vectors of a staging call come from.
+// Where the T input vectors of a staging call come from. load8(t, k0, v)
+// reads values k0..k0+7 of vector t (k0 a multiple of 8).
+__device__ __forceinline__ void unpack_bf16x8(const uint4 u, float* v) {
+  v[0] = bf16lo(u.x); v[1] = bf16hi(u.x); v[2] = bf16lo(u.y); v[3] = bf16hi(u.y);
+  v[4] = bf16lo(u.z); v[5] = bf16hi(u.z); v[6] = bf16lo(u.w); v[7] = bf16hi(u.w);
+}
+__device__ __forceinline__ void load8_from(const uint16_t* p, float* v) {
+  unpack_bf16x8(*reinterpret_cast<const uint4*>(p), v);
+}
+__device__ __forceinline__ void load8_from(const float* p, float* v) {
+  const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
 template <typename In>
-struct StridedSrc {  // token t at x + t*ld
+struct StridedSrc {  // token t at x + t*ld (16-byte aligned rows)
   const In* x;
   int ld;
-  __device__ const In* ptr(int t) const { return x + (size_t)t * ld; }
+  __device__ void load8(int t, int k0, float* v) const { load8_from(x + (size_t)t * ld + k0, v); }
 };
 template <typename In>
 struct GatherSrc {  // token t at base + off[t] (off in shared memory)
   const In* base;
   const int* off;
-  __device__ const In* ptr(int t) const { return base + off[t]; }
+  __device__ void load8(int t, int k0, float* v) const { load8_from(base + off[t] + k0, v); }
 };
 
-// Stage T inputs of `cols` values into shared memory.
-// `gsh` is scratch shared memory for T*cols/64 ints. All threads of the block
-// must call; ends with __syncthreads().
-template <int BITS, typename In, typename Src>
+struct CgSrc {  // fp32 vectors written by other CTAs of the same launch: read through L2
+  const float* x;
+  int ld;
+  __device__ void load8(int t, int k0, float* v) const {
+    const float4* p = reinterpret_cast<const float4*>(x + (size_t)t * ld + k0);
+    const float4 a = __ldcg(p), b = __ldcg(p + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+};
+
+// Pack the low bytes and the second bytes of four int16-range values.
+__device__ __forceinline__ void pack_lohi(int x0, int x1, int x2, int x3, uint32_t& lo, uint32_t& hi) {
+  const uint32_t t01 = __byte_perm((uint32_t)x0, (uint32_t)x1, 0x5140);  // x0.b0 x1.b0 x0.b1 x1.b1
+  const uint32_t t23 = __byte_perm((uint32_t)x2, (uint32_t)x3, 0x5140);
+  lo = __byte_perm(t01, t23, 0x5410);
+  hi = __byte_perm(t01, t23, 0x7632);
+}
+
+// Stage T inputs of `cols` values into shared memory, one thread per code
+// word: the 64/kPer consecutive threads of a group find the group maximum with
+// shuffles, so a single pass with no block barrier inside does the job.
+// `gsh` is unused (kept for the call sites' shared-memory layout). All threads
+// of the block must call; ends with __syncthreads().
+template <int BITS, typename Src>
 __device__ void stage_x_int16(const Src src, int T, int cols, XStage st, int* gsh) {
   using G = Geo<BITS>;
-  const int ngroups = cols / kGroup;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  // pass 1: per (token, group) exponent shift
-  for (int tg = warp; tg < T * ngroups; tg += nwarps) {
-    int t = tg / ngroups, g = tg - t * ngroups;
-    const In* xp = src.ptr(t) + g * kGroup;
-    float m = fmaxf(fabsf(load_in(xp, lane)), fabsf(load_in(xp, lane + 32)));
-    m = warp_max(m);
-    if (lane == 0) {
-      int sh = 0;
-      if (m > 0.f) {
-        int e = (int)((__float_as_uint(m) >> 23) & 0xff) - 127;  // floor(log2 m) for normal m
-        sh = 14 - e;
-        sh = sh > 126 ? 126 : (sh < -126 ? -126 : sh);
-      }
-      gsh[tg] = sh;
-    }
-  }
-  __syncthreads();
-  // pass 2: one thread per (token, code word)
+  constexpr int kGW = kGroup / G::kPer;  // threads (words) per group: 8 at 4 bits, 4 at 2 bits
+  (void)gsh;
   const RowGeo rg = row_geo(cols, BITS);
   const int words = cols * BITS / 32;
-  const int total = T * words;  // a multiple of 4: each part has 4 words
+  const int total = T * words;  // a multiple of kGW: groups never straddle a warp
   for (int base = 0; base < total; base += blockDim.x) {
-    // Uniform trip count per warp so the 4-lane shuffles below see all lanes.
+    // uniform trip count per warp so that every shuffle sees all lanes
     const int tw = base + threadIdx.x;
     const bool active = tw < total;
-    int t = active ? tw / words : 0, w = active ? tw - t * words : 0;
-    int k0 = w * G::kPer;
-    int sh = gsh[t * ngroups + k0 / kGroup];
-    float sc = exp2i(sh);
-    const In* xp = src.ptr(t) + k0;
+    const int t = active ? tw / words : 0, w = active ? tw - t * words : 0;
+    const int k0 = w * G::kPer;
+    float v[G::kPer];
+#pragma unroll
+    for (int i = 0; i < G::kPer; i += 8) {
+      if (active) {
+        src.load8(t, k0 + i, v + i);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[i + j] = 0.f;
+      }
+    }
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < G::kPer; ++i) m = fmaxf(m, fabsf(v[i]));
+#pragma unroll
+    for (int o = kGW / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+    int sh = 0;
+    if (m > 0.f) {
+      const int e = (int)((__float_as_uint(m) >> 23) & 0xff) - 127;  // floor(log2 m) for normal m
+      sh = 14 - e;
+      sh = sh > 126 ? 126 : (sh < -126 ? -126 : sh);
+    }
+    const float sc = exp2i(sh);
     int X[G::kPer];
     int xsum = 0;
 #pragma unroll
     for (int i = 0; i < G::kPer; ++i) {
-      // |x*2^sh| < 2^15; the clamp only matters for fp32 inputs within an
-      // ulp of the next power of two, which round up to 2^15.
-      int v = active ? __float2int_rn(load_in(xp, i) * sc) : 0;
-      X[i] = max(-32767, min(32767, v));
+      // rint(v*2^sh) by the 1.5*2^23 addition (|v*2^sh| < 2^15, product exact);
+      // the clamp only matters for fp32 inputs within an ulp of a power of
+      // two, which round up to 2^15.
+      const int q = __float_as_int(fmaf(v[i], sc, 12582912.f)) - 0x4B400000;
+      X[i] = max(-32767, min(32767, q));
       xsum += X[i];
     }
     uint32_t lo[G::kNvec], hi[G::kNvec];
 #pragma unroll
-    for (int j = 0; j < G::kNvec; ++j) {
-      uint32_t l = 0, h = 0;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        int v = X[j + G::kNvec * i];
-        l |= ((uint32_t)v & 0xffu) << (8 * i);
-        h |= ((uint32_t)(v >> 8) & 0xffu) << (8 * i);
-      }
-      lo[j] = l;
-      hi[j] = h;
-    }
-    int p = w >> 2, c = w & 3;
-    int it = p / rg.LPR, lp = p - it * rg.LPR;
+    for (int j = 0; j < G::kNvec; ++j)
+      pack_lohi(X[j], X[j + G::kNvec], X[j + 2 * G::kNvec], X[j + 3 * G::kNvec], lo[j], hi[j]);
+    const int p = w >> 2, c = w & 3;
+    const int it = p / rg.LPR, lp = p - it * rg.LPR;
     if (active) {
 #pragma unroll
       for (int ch = 0; ch < G::kNch; ++ch) {
-        int slot = (((t * rg.NIT + it) * 4 + c) * G::kNch + ch) * rg.LPR + lp;
+        const int slot = (((t * rg.NIT + it) * 4 + c) * G::kNch + ch) * rg.LPR + lp;
         st.chunks[slot] = make_uint4(lo[2 * ch], hi[2 * ch], lo[2 * ch + 1], hi[2 * ch + 1]);
       }
     }
-    // Part sum over the 4 words of part p: they sit on 4 consecutive lanes
-    // (base and blockDim are multiples of 32, words a multiple of 4).
+    // part sum over the 4 words of part p (4 consecutive lanes)
     xsum += __shfl_xor_sync(kFull, xsum, 1);
     xsum += __shfl_xor_sync(kFull, xsum, 2);
     if (active && c == 0) {
-      float inv = exp2i(-sh);
+      const float inv = exp2i(-sh);
       st.partinfo[t * rg.P + p] = make_float2(inv, (float)xsum * inv);
     }
   }
@@ -222,21 +246,22 @@ __device__ void stage_x_int16(const Src src, int T, int cols, XStage st, int* gs
 }
 
 // Integer dot product of one part (4 code words) with staged token t.
+// The part is p = it*LPR + lp (iteration it of lane lp of the row).
 // Returns s*2^-sh*sum(q*X) + b*2^-sh*sum(X) added to acc.
 template <int BITS>
 __device__ __forceinline__ float part_dot_int16(const uint4 qv, uint32_t sbw, const uint4* __restrict__ chunks,
-                                                const float2* __restrict__ partinfo, int t, int p, const RowGeo& rg,
-                                                float acc) {
+                                                const float2* __restrict__ partinfo, int t, int it, int lp,
+                                                const RowGeo& rg, float acc) {
   using G = Geo<BITS>;
-  int it = p / rg.LPR, lp = p - it * rg.LPR;
   int acc_h = 0;
   uint32_t acc_l = 0;
   const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+  const uint4* xb = chunks + ((t * rg.NIT + it) * 4 * G::kNch) * rg.LPR + lp;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
 #pragma unroll
     for (int ch = 0; ch < G::kNch; ++ch) {
-      uint4 xc = chunks[(((t * rg.NIT + it) * 4 + c) * G::kNch + ch) * rg.LPR + lp];
+      uint4 xc = xb[(c * G::kNch + ch) * rg.LPR];
       uint32_t v0 = (qw[c] >> (BITS * (2 * ch))) & G::kByteMask;
       uint32_t v1 = (qw[c] >> (BITS * (2 * ch + 1))) & G::kByteMask;
       acc_l = dp4a_uu(v0, xc.x, acc_l);
@@ -245,7 +270,7 @@ __device__ __forceinline__ float part_dot_int16(const uint4 qv, uint32_t sbw, co
       acc_h = dp4a_us(v1, xc.w, acc_h);
     }
   }
-  float2 pi = partinfo[t * rg.P + p];
+  float2 pi = partinfo[t * rg.P + it * rg.LPR + lp];
   int A = acc_h * 256 + (int)acc_l;
   float s = bf16lo(sbw), b = bf16hi(sbw);
   return fmaf(s * pi.x, (float)A, fmaf(b, pi.y, acc));

@@ -60,10 +60,9 @@ __device__ __forceinline__ void dot_round(const uint4 (&qv)[kMaxNitE], const uin
   for (int i = 0; i < kMaxNitE; ++i) {
     int it = it0 + i;
     if (it < rg.NIT) {
-      int p = it * rg.LPR + lp;
 #pragma unroll
       for (int t = 0; t < kTaskTok; ++t)
-        if (t < ntok) acc[t] = part_dot_int16<BITS>(qv[i], sv[i], st.chunks, st.partinfo, t, p, rg, acc[t]);
+        if (t < ntok) acc[t] = part_dot_int16<BITS>(qv[i], sv[i], st.chunks, st.partinfo, t, it, lp, rg, acc[t]);
     }
   }
 }
@@ -120,7 +119,7 @@ k_gateup(ExpertSet es, const Plan* __restrict__ plan, const uint16_t* __restrict
       __syncthreads();  // previous item finished reading the staged inputs
       if (threadIdx.x < kTaskTok) s_off[threadIdx.x] = threadIdx.x < ntok ? tk.tok[threadIdx.x] * d : 0;
       __syncthreads();
-      stage_x_int16<BITS, uint16_t>(GatherSrc<uint16_t>{x, s_off}, ntok, d, st, gsh);
+      stage_x_int16<BITS>(GatherSrc<uint16_t>{x, s_off}, ntok, d, st, gsh);
       staged = ti;
     }
     float ga[kTaskTok], ua[kTaskTok];
@@ -183,7 +182,7 @@ k_down(ExpertSet es, const Plan* __restrict__ plan, const float* __restrict__ H,
       if (threadIdx.x < kTaskTok)
         s_off[threadIdx.x] = threadIdx.x < ntok ? (tk.tok[threadIdx.x] * nslot + tk.slot[threadIdx.x]) * f : 0;
       __syncthreads();
-      stage_x_int16<BITS, float>(GatherSrc<float>{H, s_off}, ntok, f, st, gsh);
+      stage_x_int16<BITS>(GatherSrc<float>{H, s_off}, ntok, f, st, gsh);
       staged = ti;
     }
     float acc[kTaskTok];

@@ -1,0 +1,1038 @@
+// fused.cu — one persistent kernel for batch-1 decode: a whole token through
+// one MoE layer or a stack of layers per launch.
+//
+// Flash-MoE page, section "架构设计：SSD当显存用": per token and layer the path
+// is routing logits -> softmax + top-K -> the selected experts' forward pass
+// -> combine (-> norm). At batch 1 every step is a matrix-vector product whose
+// weights are read exactly once, so a layer is bound by HBM bandwidth and by
+// the latency of its three dependent steps. One cooperative launch with one
+// CTA per SM keeps the token on chip and replaces kernel boundaries by
+// grid-wide counters:
+//
+//   A  RMSNorm of the residual (stack mode), router rows (bf16) and the shared
+//      expert's gate/up rows; the last CTA to finish its router rows selects
+//      the top-K experts and publishes them (nobody waits for it here);
+//   B  the selected experts' gate/up rows (after the selection);
+//   C  the down rows of the K selected experts and of the shared expert,
+//      combined per output row in a fixed order (after every h is written),
+//      plus the residual add in stack mode.
+//
+// Data movement. Each CTA owns a fixed slice of every phase. Its router rows,
+// shared gate/up rows (phase A) and selected-expert gate/up rows (phase B)
+// are streamed into shared memory with bulk async copies (cp.async.bulk, one
+// mbarrier per work unit), all issued the moment they are known: phase B's
+// right after the selection, the next layer's phase A right after it, so HBM
+// keeps streaming while the grid waits at its counters. Phase C's down rows
+// (of experts known after the selection) are prefetched into L2 at that same
+// moment and read from L2 into registers. Consumers start on a unit as soon
+// as its own mbarrier completes.
+//
+// Every wait is bounded (an iteration count and %globaltimer). On expiry the
+// CTA sets BGQ_ERR_TIMEOUT in the status word and an abort flag that makes
+// every CTA leave at its next grid-wide wait; before leaving, thread 0 waits
+// (again with a limit) for the bulk copies its CTA still has in flight.
+#include <climits>
+
+#include "../../include/bgq.h"
+#include "common.cuh"
+#include "fused.h"
+#include "kernels.h"
+
+namespace bgq {
+
+constexpr int kFThreads = 512;
+constexpr int kFWarps = kFThreads / 32;
+constexpr int kMaxS1 = 16;   // shared gate/up units per CTA
+constexpr int kMaxB = 32;    // selected gate/up units per CTA
+constexpr int kCH = 4;       // units per bulk-copy chunk (one mbarrier per chunk)
+constexpr int kMaxSC = 4;    // shared gate/up chunks per CTA
+constexpr int kMaxBC = 16;   // selected gate/up chunks per CTA
+constexpr long long kMaxSpin = 1ll << 26;
+constexpr long long kDrainNs = 200000000ll;
+
+// --------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t* m, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(m)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* m, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(m)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* m, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(m)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// global -> shared bulk copy, completion counted on mbarrier m (16-byte aligned, size % 16 == 0)
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* m) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(m))
+      : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+
+__device__ __forceinline__ bool aborted(Ctrl* ctrl) { return *(volatile int*)&ctrl->misc[0] != 0; }
+__device__ __forceinline__ void raise_timeout(Ctrl* ctrl) {
+  atomicExch(&ctrl->status, BGQ_ERR_TIMEOUT);
+  atomicExch(&ctrl->misc[0], 1);
+}
+
+// Bounded wait for mbarrier phase `parity`; false on timeout or abort.
+__device__ bool mbar_wait(uint64_t* m, uint32_t parity, Ctrl* ctrl, long long timeout_ns) {
+  if (mbar_try_wait(m, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  long long it = 0;
+  while (!mbar_try_wait(m, parity)) {
+    if ((++it & 31) == 0) {
+      if (aborted(ctrl)) return false;
+      if (it > kMaxSpin || (long long)(globaltimer() - t0) > timeout_ns) {
+        raise_timeout(ctrl);
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+// --------------------------------------------------------------- geometry
+// Row shapes handled here: rows of d (router, gate, up) are read by all 32
+// lanes (d*bits/128 parts, a multiple of 32, at most 4 per lane); rows of f
+// (down) have at most 32 parts, one per lane.
+struct FGeo {
+  int nC;          // CTAs
+  int qr;          // warps per router row (1024 columns each)
+  int rpc;         // router rows per CTA
+  int nRouter;     // CTAs holding router rows
+  int s1_nr;       // shared gate/up units per CTA without router rows
+  int nit_d;       // parts per lane of a d-row
+  int wpr, gpr;    // words / groups per d-row
+  int unit;        // bytes of one gate+up unit in shared memory
+  int nBmax;       // selected gate/up units per CTA (max)
+  int bufA, bufB;  // shared-memory buffer bytes
+};
+
+__host__ __device__ inline void fsplit(int n, int part, int nparts, int& b, int& e) {
+  b = (int)((long long)n * part / nparts);
+  e = (int)((long long)n * (part + 1) / nparts);
+}
+
+__host__ __device__ inline FGeo fgeo(int nC, int d, int f, int E, int K, int bits) {
+  FGeo g;
+  g.nC = nC;
+  g.qr = (d >= 1024 && d % 1024 == 0) ? d / 1024 : 1;
+  g.rpc = kFWarps / g.qr;
+  g.nRouter = (E + 1 + g.rpc - 1) / g.rpc;
+  g.nit_d = d * bits / 128 / 32;
+  g.wpr = d * bits / 32;
+  g.gpr = d / kGroup;
+  g.unit = 2 * (g.wpr + g.gpr) * 4;
+  g.nBmax = (K * f + nC - 1) / nC;
+  const int n_nr = nC - g.nRouter;
+  g.s1_nr = 0;
+  if (n_nr > 0) {
+    // balance phase A's bytes: a router row is 2d bytes, a gate+up unit `unit` bytes
+    double total = (double)(E + 1) * 2 * d + (double)f * g.unit;
+    int a = (int)(total / nC / g.unit + 0.5);
+    if (a * n_nr > f) a = f / n_nr;
+    if (a > kMaxS1) a = kMaxS1;
+    g.s1_nr = a < 0 ? 0 : a;
+  }
+  const int rest = f - n_nr * g.s1_nr;
+  const int nparts = g.s1_nr > 0 ? g.nRouter : nC;
+  const int s1_router = (rest + nparts - 1) / nparts;
+  int a_router = g.rpc * 2 * d + s1_router * g.unit;
+  int a_nr = g.s1_nr * g.unit;
+  g.bufA = a_router > a_nr ? a_router : a_nr;
+  g.bufB = g.nBmax * g.unit;
+  // phase C reuses bufB for its down rows (K+1 experts x the CTA's rows) and partial results
+  const int rows_c = (d + nC - 1) / nC;
+  const int c_bytes = (K + 1) * rows_c * (f * bits / 8 + (f / kGroup) * 4) + (K + 1) * rows_c * 4 + 16;
+  if (g.bufB < c_bytes) g.bufB = c_bytes;
+  return g;
+}
+
+// Shared-memory layout (byte offsets; every region 128-byte aligned).
+struct FLayout {
+  size_t misc, rho, a_s, sta_chunks, sta_pi, gsh_a, sth_chunks, sth_pi, gsh_h, bufA, bufB, total;
+};
+__host__ __device__ inline size_t fl_take(size_t& o, size_t bytes) {
+  size_t r = o;
+  o += (bytes + 127) & ~(size_t)127;
+  return r;
+}
+__host__ __device__ inline FLayout flayout(const FGeo& g, int d, int f, int K, int bits) {
+  FLayout L;
+  size_t o = 0;
+  fl_take(o, (3 + kMaxSC + kMaxBC) * 8);  // mbarriers at offset 0
+  L.misc = fl_take(o, 256);
+  L.rho = fl_take(o, (size_t)d * 2);  // apar, bpar, s_idx[8], s_w[9], red[kFWarps]
+  L.a_s = fl_take(o, (size_t)d * 2);
+  L.sta_chunks = fl_take(o, (size_t)d * 2);
+  L.sta_pi = fl_take(o, (size_t)(d * bits / 128) * 8);
+  L.gsh_a = fl_take(o, (size_t)(d / kGroup) * 4);
+  L.sth_chunks = fl_take(o, (size_t)(K + 1) * f * 2);
+  L.sth_pi = fl_take(o, (size_t)(K + 1) * (f * bits / 128) * 8);
+  L.gsh_h = fl_take(o, (size_t)(K + 1) * (f / kGroup) * 4);
+  L.bufA = fl_take(o, (size_t)g.bufA);
+  L.bufB = fl_take(o, (size_t)g.bufB);
+  L.total = o;
+  return L;
+}
+
+// This CTA's shared gate/up unit range.
+__device__ __forceinline__ void s1_range(const FGeo& g, int f, int& b, int& e) {
+  const int n_nr = g.nC - g.nRouter;
+  if (g.s1_nr > 0 && (int)blockIdx.x >= g.nRouter) {
+    b = ((int)blockIdx.x - g.nRouter) * g.s1_nr;
+    e = b + g.s1_nr;
+    return;
+  }
+  const int rest0 = g.s1_nr > 0 ? n_nr * g.s1_nr : 0;
+  fsplit(f - rest0, blockIdx.x, g.s1_nr > 0 ? g.nRouter : g.nC, b, e);
+  b += rest0;
+  e += rest0;
+}
+
+// Offset of the shared gate/up units in bufA: after the router rows on CTAs
+// that hold router rows, at 0 on the others (bufA is sized for both cases).
+__device__ __forceinline__ size_t s1_base(const FGeo& g, int d) {
+  return (int)blockIdx.x < g.nRouter ? (size_t)g.rpc * 2 * d : 0;
+}
+
+// Units [b, e) are copied in chunks of up to kCH consecutive rows that never
+// cross a multiple of `seg` (an expert boundary). Chunk c holds n units laid
+// out as [gate q rows][up q rows][gate sb rows][up sb rows] starting at byte
+// (start - b) * unit of its buffer.
+struct Chunk {
+  int start, n, idx;
+};
+__device__ __forceinline__ Chunk chunk_at(int c, int b, int e, int seg) {
+  int start = b;
+  for (int i = 0; i < c && start < e; ++i) {
+    int lim = min(min(start + kCH, e), (start / seg + 1) * seg);
+    start = lim;
+  }
+  const int lim = min(min(start + kCH, e), (start / seg + 1) * seg);
+  return Chunk{start, start < e ? lim - start : 0, c};
+}
+__device__ __forceinline__ Chunk chunk_of(int u, int b, int e, int seg) {
+  int start = b, idx = 0;
+  while (true) {
+    const int lim = min(min(start + kCH, e), (start / seg + 1) * seg);
+    if (u < lim) return Chunk{start, lim - start, idx};
+    start = lim;
+    ++idx;
+  }
+}
+
+// --------------------------------------------------------------- compute helpers
+// gate and up rows of one unit (in shared memory) against staged input 0:
+// two dot products that share every x chunk. Lane l reads part it*32 + l.
+template <int BITS>
+__device__ __noinline__ void unit_gateup(const unsigned char* cbase, int n, int pos, const XStage st, const FGeo g,
+                                         int lane, float& gv, float& uv) {
+  using G = Geo<BITS>;
+  const int wq = g.wpr * 4, ws = g.gpr * 4;
+  const uint4* qg = reinterpret_cast<const uint4*>(cbase + pos * wq);
+  const uint4* qu = reinterpret_cast<const uint4*>(cbase + (n + pos) * wq);
+  const uint32_t* sg = reinterpret_cast<const uint32_t*>(cbase + 2 * n * wq + pos * ws);
+  const uint32_t* su = reinterpret_cast<const uint32_t*>(cbase + 2 * n * wq + (n + pos) * ws);
+  float ag = 0.f, au = 0.f;
+#pragma unroll 1
+  for (int it = 0; it < 4; ++it) {
+    if (it < g.nit_d) {
+      const int p = it * 32 + lane;
+      const uint4 wg = qg[p], wu = qu[p];
+      const uint32_t sbg = sg[part_group<BITS>(p)], sbu = su[part_group<BITS>(p)];
+      const uint32_t gw[4] = {wg.x, wg.y, wg.z, wg.w}, uw[4] = {wu.x, wu.y, wu.z, wu.w};
+      const uint4* xb = st.chunks + (it * 4 * G::kNch) * 32 + lane;
+      int hg = 0, hu = 0;
+      uint32_t lg = 0, lu = 0;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+#pragma unroll
+        for (int ch = 0; ch < G::kNch; ++ch) {
+          const uint4 xc = xb[(c * G::kNch + ch) * 32];
+          const int s0 = BITS * (2 * ch), s1 = BITS * (2 * ch + 1);
+          const uint32_t g0 = (gw[c] >> s0) & G::kByteMask, g1 = (gw[c] >> s1) & G::kByteMask;
+          const uint32_t u0 = (uw[c] >> s0) & G::kByteMask, u1 = (uw[c] >> s1) & G::kByteMask;
+          lg = dp4a_uu(g0, xc.x, lg);
+          hg = dp4a_us(g0, xc.y, hg);
+          lg = dp4a_uu(g1, xc.z, lg);
+          hg = dp4a_us(g1, xc.w, hg);
+          lu = dp4a_uu(u0, xc.x, lu);
+          hu = dp4a_us(u0, xc.y, hu);
+          lu = dp4a_uu(u1, xc.z, lu);
+          hu = dp4a_us(u1, xc.w, hu);
+        }
+      }
+      const float2 pi = st.partinfo[p];
+      ag = fmaf(bf16lo(sbg) * pi.x, (float)(hg * 256 + (int)lg), fmaf(bf16hi(sbg), pi.y, ag));
+      au = fmaf(bf16lo(sbu) * pi.x, (float)(hu * 256 + (int)lu), fmaf(bf16hi(sbu), pi.y, au));
+    }
+  }
+  gv = warp_sum(ag);
+  uv = warp_sum(au);
+}
+
+// A slice (<= 1024 columns) of a bf16 router row in shared memory dotted with
+// the bf16 input in shared memory.
+__device__ __forceinline__ float router_dot(const uint16_t* wrow, const uint16_t* a_s, int c0, int nvec, int lane) {
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if (i < nvec) {
+      const uint4 w = *reinterpret_cast<const uint4*>(wrow + c0 + (i * 32 + lane) * 8);
+      const uint4 x = *reinterpret_cast<const uint4*>(a_s + c0 + (i * 32 + lane) * 8);
+      acc = fmaf(bf16lo(w.x), bf16lo(x.x), acc);
+      acc = fmaf(bf16hi(w.x), bf16hi(x.x), acc);
+      acc = fmaf(bf16lo(w.y), bf16lo(x.y), acc);
+      acc = fmaf(bf16hi(w.y), bf16hi(x.y), acc);
+      acc = fmaf(bf16lo(w.z), bf16lo(x.z), acc);
+      acc = fmaf(bf16hi(w.z), bf16hi(x.z), acc);
+      acc = fmaf(bf16lo(w.w), bf16lo(x.w), acc);
+      acc = fmaf(bf16hi(w.w), bf16hi(x.w), acc);
+    }
+  }
+  return warp_sum(acc);
+}
+
+// Order-preserving map of a float to a signed int (larger float, larger int).
+__device__ __forceinline__ int fkey(float v) {
+  const int i = __float_as_int(v == 0.f ? 0.f : v);  // -0 and +0 compare equal
+  return i >= 0 ? i : i ^ 0x7fffffff;
+}
+__device__ __forceinline__ int redux_max(int v) {
+  int r;
+  asm volatile("redux.sync.max.s32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+  return r;
+}
+__device__ __forceinline__ int redux_min(int v) {
+  int r;
+  asm volatile("redux.sync.min.s32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+  return r;
+}
+
+// Top-K selection, run by every CTA on the logits in shared memory (lg[0..E),
+// lg[E] = shared-gate logit), E <= 1024, K <= 8.
+//   selection: order (larger logit, then lower index) — a total order, so the
+//   set and its order are the same as the router kernel's per-warp selection.
+//   Each warp takes the top K of its 64 logits (K rounds of redux.sync on an
+//   order-preserving integer key, ties to the lowest index), then warp 0
+//   merges the 16 x K candidates the same way.
+//   weights: the softmax denominator is summed in the router kernel's order
+//   (lane j adds elements j, j+32, ... in turn, then a butterfly), so the
+//   weights are bit-identical to the multi-kernel path's.
+// Writes s_idx[0..K), s_w[0..K) and s_w[K] = gamma. `scratch` holds E floats
+// plus 16*8 (key, index) pairs.
+__device__ void block_topk(const float* lg, float* scratch, int E, int K, bool has_gate, float* red, int* red_i,
+                           int* s_idx, float* s_w) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int* cand_k = reinterpret_cast<int*>(scratch + E);  // [16][8] keys
+  int* cand_i = cand_k + kFWarps * 8;                 // [16][8] indices
+  // this warp's elements: e0 = warp*64 + lane, e1 = e0 + 32
+  const int e0 = warp * 64 + lane, e1 = e0 + 32;
+  int k0 = e0 < E ? fkey(lg[e0]) : INT_MIN;
+  int k1 = e1 < E ? fkey(lg[e1]) : INT_MIN;
+  // max for the softmax, and exp(l - max) of every logit
+  {
+    int m = redux_max(max(k0, k1));
+    if (lane == 0) red_i[warp] = m;
+  }
+  __syncthreads();
+  int mk = red_i[0];
+  for (int w = 1; w < kFWarps; ++w) mk = max(mk, red_i[w]);
+  const float m = __int_as_float(mk >= 0 ? mk : mk ^ 0x7fffffff);
+  if (e0 < E) scratch[e0] = expf(lg[e0] - m);
+  if (e1 < E) scratch[e1] = expf(lg[e1] - m);
+  // per-warp top K
+  for (int k = 0; k < K; ++k) {
+    const int best = redux_max(max(k0, k1));
+    const int i0 = (k0 == best && e0 < E) ? e0 : INT_MAX;
+    const int i1 = (k1 == best && e1 < E) ? e1 : INT_MAX;
+    const int bi = redux_min(min(i0, i1));
+    if (lane == 0) {
+      cand_k[warp * 8 + k] = best;
+      cand_i[warp * 8 + k] = bi;
+    }
+    if (bi == e0) k0 = INT_MIN;
+    if (bi == e1) k1 = INT_MIN;
+  }
+  __syncthreads();
+  // merge: lane j of warp 0 holds candidates j*... (16 warps x K <= 128 entries, 4 per lane)
+  if (warp == 0) {
+    int ck[4], ci[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = j * 32 + lane;  // candidate slot c = w*8 + k
+      const bool ok = c < kFWarps * 8 && (c & 7) < K;
+      ck[j] = ok ? cand_k[c] : INT_MIN;
+      ci[j] = ok ? cand_i[c] : INT_MAX;
+    }
+    for (int k = 0; k < K; ++k) {
+      int lb = INT_MIN;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) lb = max(lb, ck[j]);
+      const int best = redux_max(lb);
+      int li = INT_MAX;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (ck[j] == best) li = min(li, ci[j]);
+      const int bi = redux_min(li);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (ci[j] == bi) ck[j] = INT_MIN;
+      if (lane == 0) s_idx[k] = bi;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    float ssum = 0.f;
+    for (int i = 0; i * 32 + lane < E; ++i) ssum += scratch[i * 32 + lane];
+    ssum = warp_sum(ssum);
+    if (lane == 0) {
+      float p[8], ps = 0.f;
+      for (int k = 0; k < K; ++k) {
+        p[k] = scratch[s_idx[k]] / ssum;
+        ps += p[k];
+      }
+      for (int k = 0; k < K; ++k) s_w[k] = p[k] / ps;
+      s_w[K] = has_gate ? 1.f / (1.f + expf(-lg[E])) : 1.f;
+    }
+  }
+  __syncthreads();
+  (void)red;
+}
+
+// x staging from fp32 values in shared memory (the layer input).
+template <int BITS>
+__device__ __noinline__ void stage_f32(const float* src, int ld, int T, int cols, const XStage st) {
+  stage_x_int16<BITS>(StridedSrc<float>{src, ld}, T, cols, st, nullptr);
+}
+// x staging from fp32 values other CTAs wrote to global memory (the SwiGLU outputs).
+template <int BITS>
+__device__ __noinline__ void stage_cg(const float* src, int ld, int T, int cols, const XStage st) {
+  stage_x_int16<BITS>(CgSrc{src, ld}, T, cols, st, nullptr);
+}
+
+// Thread 0 stamps event ev of layer l (no-op without a trace buffer).
+__device__ __forceinline__ void stamp(const FusedParams& P, int l, int ev) {
+  if (P.trace && threadIdx.x == 0)
+    P.trace[((size_t)l * gridDim.x + blockIdx.x) * kTraceEvents + ev] = globaltimer();
+}
+
+__device__ __forceinline__ float h_in(const FusedParams& P, int l, int k) {
+  return l == 0 ? bf16f(P.x_in[k]) : __ldcg(P.h + k);
+}
+
+// Shared-memory state of the kernel.
+struct FSmem {
+  uint64_t* mR;    // router rows
+  uint64_t* mRho;  // RMSNorm weight
+  uint64_t* mC;    // down rows of phase C
+  uint16_t* rho;
+  uint64_t* mS;  // [kMaxSC] shared gate/up chunks
+  uint64_t* mB;  // [kMaxBC] selected gate/up chunks
+  unsigned char* bufA;
+  unsigned char* bufB;
+  int* apar;  // parity of the last issued A batch (-1: none)
+  int* bpar;  // parity of the last issued B batch (-1: none)
+  int* cpar;  // parity of the last issued C batch (-1: none)
+};
+
+// Thread 0: wait (bounded) for every bulk copy this CTA still has in flight.
+__device__ void drain_copies(const FSmem& S) {
+  const unsigned long long t0 = globaltimer();
+  const int ap = *S.apar, bp = *S.bpar, cp = *S.cpar;
+  if (cp >= 0)
+    while (!mbar_try_wait(S.mC, (uint32_t)cp) && (long long)(globaltimer() - t0) < kDrainNs) {
+    }
+  if (ap >= 0) {
+    while (!mbar_try_wait(S.mR, (uint32_t)ap) && (long long)(globaltimer() - t0) < kDrainNs) {
+    }
+    while (!mbar_try_wait(S.mRho, (uint32_t)ap) && (long long)(globaltimer() - t0) < kDrainNs) {
+    }
+    for (int j = 0; j < kMaxSC; ++j)
+      while (!mbar_try_wait(&S.mS[j], (uint32_t)ap) && (long long)(globaltimer() - t0) < kDrainNs) {
+      }
+  }
+  if (bp >= 0)
+    for (int j = 0; j < kMaxBC; ++j)
+      while (!mbar_try_wait(&S.mB[j], (uint32_t)bp) && (long long)(globaltimer() - t0) < kDrainNs) {
+      }
+}
+
+// Grid-wide wait: thread 0 waits until *p >= target. False for the whole CTA
+// on abort or timeout (after thread 0 drained the CTA's copies in flight).
+__device__ bool cta_wait(const int* p, int target, Ctrl* ctrl, long long timeout_ns, const FSmem& S) {
+  __shared__ int s_ok;
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    const unsigned long long t0 = globaltimer();
+    long long it = 0;
+    while (ld_acquire(p) < target) {
+      if (aborted(ctrl)) {
+        ok = 0;
+        break;
+      }
+      if (++it > kMaxSpin || (long long)(globaltimer() - t0) > timeout_ns) {
+        raise_timeout(ctrl);
+        ok = 0;
+        break;
+      }
+      if (it > 16) __nanosleep(32);
+    }
+    if (ok && aborted(ctrl)) ok = 0;
+    if (!ok) drain_copies(S);
+    s_ok = ok;
+  }
+  __syncthreads();
+  return s_ok != 0;
+}
+
+// All threads: publish this CTA's global writes, then count it in *p
+// (block barrier, then one release reduction by thread 0).
+__device__ void cta_arrive(int* p) {
+  __syncthreads();
+  if (threadIdx.x == 0) asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p) : "memory");
+}
+
+// Warp 0: issue layer l's phase-A copies (router rows by lane 0, shared
+// gate/up chunk i by lane i).
+__device__ void issue_A(const FusedParams& P, const FGeo& g, int l, const FSmem& S) {
+  const FusedLayer& L = P.layers[l];
+  const int d = P.d, E = P.E, f = P.f, lane = threadIdx.x & 31;
+  fence_proxy_async();
+  if (lane == 0) {
+    // router rows [r0, r1) of rows 0..E (row E is the shared-gate vector)
+    const int r0 = (int)blockIdx.x * g.rpc;
+    int r1 = r0 + g.rpc;
+    const int nrows = E + (L.sgate ? 1 : 0);
+    if (r1 > nrows) r1 = nrows;
+    const int nr = r1 > r0 ? r1 - r0 : 0;
+    mbar_expect_tx(S.mR, (uint32_t)nr * 2 * d);
+    if (nr > 0) {
+      const int nE = (r1 < E ? r1 : E) - r0;  // rows taken from the router matrix
+      if (nE > 0) bulk_g2s(S.bufA, L.router + (size_t)r0 * d, (uint32_t)nE * 2 * d, S.mR);
+      if (nr > nE) bulk_g2s(S.bufA + (size_t)nE * 2 * d, L.sgate, 2 * d, S.mR);
+    }
+  }
+  if (lane == 1) {  // RMSNorm weight of the layer (stack mode)
+    const bool has = P.stack && L.rho;
+    mbar_expect_tx(S.mRho, has ? (uint32_t)d * 2 : 0u);
+    if (has) bulk_g2s(S.rho, L.rho, d * 2, S.mRho);
+  }
+  if (lane < kMaxSC) {
+    int b, e;
+    s1_range(g, f, b, e);
+    const Chunk ch = chunk_at(lane, b, e, f);
+    uint64_t* m = &S.mS[lane];
+    if (ch.n > 0) {
+      const int wq = g.wpr * 4, ws = g.gpr * 4;
+      unsigned char* cb = S.bufA + s1_base(g, d) + (size_t)(ch.start - b) * g.unit;
+      const uint32_t* gq = L.shared_q + (size_t)ch.start * g.wpr;
+      const uint32_t* uq = L.shared_q + (size_t)(f + ch.start) * g.wpr;
+      const uint32_t* gs = reinterpret_cast<const uint32_t*>(L.shared_sb) + (size_t)ch.start * g.gpr;
+      const uint32_t* us = reinterpret_cast<const uint32_t*>(L.shared_sb) + (size_t)(f + ch.start) * g.gpr;
+      mbar_expect_tx(m, (uint32_t)ch.n * g.unit);
+      bulk_g2s(cb, gq, ch.n * wq, m);
+      bulk_g2s(cb + ch.n * wq, uq, ch.n * wq, m);
+      bulk_g2s(cb + 2 * ch.n * wq, gs, ch.n * ws, m);
+      bulk_g2s(cb + 2 * ch.n * wq + ch.n * ws, us, ch.n * ws, m);
+    } else {
+      mbar_expect_tx(m, 0);  // every barrier completes one phase per layer
+    }
+  }
+  if (lane == 0) *S.apar = l & 1;
+}
+
+// Warp 0: issue layer l's phase-B copies (gate/up rows of the selected
+// experts), chunk i by lane i.
+__device__ void issue_B(const FusedParams& P, const FGeo& g, int l, const FSmem& S, const int* s_idx) {
+  const FusedLayer& L = P.layers[l];
+  const int f = P.f, lane = threadIdx.x & 31;
+  fence_proxy_async();
+  if (lane < kMaxBC) {
+    int b, e;
+    fsplit(P.K * f, blockIdx.x, g.nC, b, e);
+    const Chunk ch = chunk_at(lane, b, e, f);
+    uint64_t* m = &S.mB[lane];
+    if (ch.n > 0) {
+      const int wq = g.wpr * 4, ws = g.gpr * 4;
+      const int k = ch.start / f, r = ch.start - k * f;
+      const uint32_t* eq = L.pool_q + (size_t)s_idx[k] * L.q_stride;
+      const uint32_t* es = reinterpret_cast<const uint32_t*>(L.pool_sb + (size_t)s_idx[k] * L.sb_stride);
+      unsigned char* cb = S.bufB + (size_t)(ch.start - b) * g.unit;
+      mbar_expect_tx(m, (uint32_t)ch.n * g.unit);
+      bulk_g2s(cb, eq + (size_t)r * g.wpr, ch.n * wq, m);
+      bulk_g2s(cb + ch.n * wq, eq + (size_t)(f + r) * g.wpr, ch.n * wq, m);
+      bulk_g2s(cb + 2 * ch.n * wq, es + (size_t)r * g.gpr, ch.n * ws, m);
+      bulk_g2s(cb + 2 * ch.n * wq + ch.n * ws, es + (size_t)(f + r) * g.gpr, ch.n * ws, m);
+    } else {
+      mbar_expect_tx(m, 0);
+    }
+  }
+  if (lane == 0) *S.bpar = l & 1;
+}
+
+// Phase C's shared-memory layout in bufB for rows [c_b, c_b + n) of d:
+// q rows of slot k at k*n*wqf, scale/bias rows at (K+1)*n*wqf + k*n*wsf,
+// partial results ys[k][r] after both.
+struct CLayout {
+  int n, wqf, wsf;
+  __device__ size_t q(int k) const { return (size_t)k * n * wqf; }
+  __device__ size_t sb(int K, int k) const { return (size_t)(K + 1) * n * wqf + (size_t)k * n * wsf; }
+  __device__ size_t ys(int K) const { return ((size_t)(K + 1) * n * (wqf + wsf) + 15) & ~(size_t)15; }
+};
+
+// Warp 0: issue phase C's copies (the CTA's down rows of the K selected
+// experts and of the shared expert) into bufB; lane k copies slot k.
+template <int BITS>
+__device__ void issue_C(const FusedParams& P, const FGeo& g, int l, const FSmem& S, const int* s_idx, int c_b,
+                        const CLayout& cl) {
+  const FusedLayer& L = P.layers[l];
+  const int f = P.f, K = P.K, lane = threadIdx.x & 31;
+  fence_proxy_async();
+  if (lane == 0) mbar_expect_tx(S.mC, (uint32_t)((K + 1) * cl.n * (cl.wqf + cl.wsf)));
+  __syncwarp();
+  if (lane <= K && cl.n > 0) {
+    const uint32_t* q;
+    const uint16_t* sb;
+    if (lane < K) {
+      q = L.pool_q + (size_t)s_idx[lane] * L.q_stride;
+      sb = L.pool_sb + (size_t)s_idx[lane] * L.sb_stride;
+    } else {
+      q = L.shared_q;
+      sb = L.shared_sb;
+    }
+    q += 2 * (size_t)f * g.wpr + (size_t)c_b * (f * BITS / 32);
+    sb += 2 * (size_t)f * g.gpr * 2 + (size_t)c_b * (f / kGroup) * 2;
+    bulk_g2s(S.bufB + cl.q(lane), q, (uint32_t)cl.n * cl.wqf, S.mC);
+    bulk_g2s(S.bufB + cl.sb(K, lane), sb, (uint32_t)cl.n * cl.wsf, S.mC);
+  }
+  if (lane == 0) *S.cpar = l & 1;
+}
+
+// --------------------------------------------------------------- the kernel
+template <int BITS>
+__global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_constant__ FusedParams P) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int d = P.d, f = P.f, E = P.E, K = P.K;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const FGeo g = fgeo(gridDim.x, d, f, E, K, BITS);
+  Ctrl* ctrl = P.ctrl;
+  const RowGeo rgd = row_geo(d, BITS);
+  const RowGeo rgf = row_geo(f, BITS);
+
+  // ---- shared memory
+  const FLayout FL = flayout(g, d, f, K, BITS);
+  FSmem S;
+  S.mR = reinterpret_cast<uint64_t*>(smem);
+  S.mRho = S.mR + 1;
+  S.mC = S.mR + 2;
+  S.mS = S.mR + 3;
+  S.rho = reinterpret_cast<uint16_t*>(smem + FL.rho);
+  S.mB = S.mS + kMaxSC;
+  S.apar = reinterpret_cast<int*>(smem + FL.misc);
+  S.bpar = S.apar + 1;
+  S.cpar = S.apar + 52;
+  int* s_idx = S.apar + 2;                              // [8]   ints 2..9
+  float* s_w = reinterpret_cast<float*>(S.apar + 10);  // [9]   ints 10..18
+  float* red = reinterpret_cast<float*>(S.apar + 20);  // [16]  ints 20..35 (< 64)
+  uint16_t* a_s = reinterpret_cast<uint16_t*>(smem + FL.a_s);
+  XStage sta;
+  sta.chunks = reinterpret_cast<uint4*>(smem + FL.sta_chunks);
+  sta.partinfo = reinterpret_cast<float2*>(smem + FL.sta_pi);
+  XStage sth;
+  sth.chunks = reinterpret_cast<uint4*>(smem + FL.sth_chunks);
+  sth.partinfo = reinterpret_cast<float2*>(smem + FL.sth_pi);
+  S.bufA = smem + FL.bufA;
+  S.bufB = smem + FL.bufB;
+  __shared__ float s_r;
+
+  if (tid == 0) {
+    mbar_init(S.mR, 1);
+    mbar_init(S.mRho, 1);
+    mbar_init(S.mC, 1);
+    for (int j = 0; j < kMaxSC; ++j) mbar_init(&S.mS[j], 1);
+    for (int j = 0; j < kMaxBC; ++j) mbar_init(&S.mB[j], 1);
+    *S.apar = -1;
+    *S.bpar = -1;
+    *S.cpar = -1;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (warp == 0) issue_A(P, g, 0, S);
+
+  for (int l = 0; l < P.n_layers; ++l) {
+    const FusedLayer& L = P.layers[l];
+    const uint32_t par = (uint32_t)(l & 1);
+    const bool has_gate = L.sgate != nullptr;
+    stamp(P, l, 0);
+
+    // ---------------- A0: layer input (RMSNorm of the residual in stack mode)
+    if (P.stack) {
+      if (l > 0 && !cta_wait(&ctrl->misc[4], g.nC * l, ctrl, P.timeout_ns, S)) return;
+      stamp(P, l, 1);
+      // one round trip: this thread's 8-element slices of the residual and of rho,
+      // and (warp 0) the per-CTA sums of squares of the previous layer
+      constexpr int kA0 = 2;  // slices per thread (d <= 8192)
+      float hv[kA0][8];
+      uint4 rv[kA0];
+#pragma unroll
+      for (int i = 0; i < kA0; ++i) {
+        const int c = tid + i * kFThreads;
+        rv[i] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) hv[i][j] = 0.f;
+        if (c < d / 8) {
+          if (l == 0) {
+            const uint4 xv = *reinterpret_cast<const uint4*>(P.x_in + 8 * c);
+            hv[i][0] = bf16lo(xv.x); hv[i][1] = bf16hi(xv.x); hv[i][2] = bf16lo(xv.y); hv[i][3] = bf16hi(xv.y);
+            hv[i][4] = bf16lo(xv.z); hv[i][5] = bf16hi(xv.z); hv[i][6] = bf16lo(xv.w); hv[i][7] = bf16hi(xv.w);
+          } else {
+            const float4 h0 = __ldcg(reinterpret_cast<const float4*>(P.h + 8 * c));
+            const float4 h1 = __ldcg(reinterpret_cast<const float4*>(P.h + 8 * c + 4));
+            hv[i][0] = h0.x; hv[i][1] = h0.y; hv[i][2] = h0.z; hv[i][3] = h0.w;
+            hv[i][4] = h1.x; hv[i][5] = h1.y; hv[i][6] = h1.z; hv[i][7] = h1.w;
+          }
+        }
+      }
+      mbar_wait(S.mRho, par, ctrl, P.timeout_ns);
+#pragma unroll
+      for (int i = 0; i < kA0; ++i) {
+        const int c = tid + i * kFThreads;
+        if (c < d / 8) rv[i] = *reinterpret_cast<const uint4*>(S.rho + 8 * c);
+      }
+      if (l == 0) {
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < kA0; ++i)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) ss = fmaf(hv[i][j], hv[i][j], ss);
+        ss = warp_sum(ss);
+        if (lane == 0) red[warp] = ss;
+        __syncthreads();
+        if (tid == 0) {
+          float s = 0.f;
+          for (int w = 0; w < kFWarps; ++w) s += red[w];
+          s_r = 1.f / sqrtf(s / (float)d + P.eps);
+        }
+      } else if (warp == 0) {
+        const float* part = P.part_ss + (l & 1) * g.nC;
+        float s = 0.f;
+        for (int c = lane; c < g.nC; c += 32) s += __ldcg(part + c);
+        s = warp_sum(s);
+        if (lane == 0) s_r = 1.f / sqrtf(s / (float)d + P.eps);
+      }
+      __syncthreads();
+      const float r = s_r;
+#pragma unroll
+      for (int i = 0; i < kA0; ++i) {
+        const int c = tid + i * kFThreads;
+        if (c < d / 8) {
+          const float rho[8] = {bf16lo(rv[i].x), bf16hi(rv[i].x), bf16lo(rv[i].y), bf16hi(rv[i].y),
+                                bf16lo(rv[i].z), bf16hi(rv[i].z), bf16lo(rv[i].w), bf16hi(rv[i].w)};
+          uint32_t o[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t lo = f2bf((hv[i][2 * j] * r) * rho[2 * j]);
+            const uint32_t hi = f2bf((hv[i][2 * j + 1] * r) * rho[2 * j + 1]);
+            o[j] = lo | (hi << 16);
+          }
+          *reinterpret_cast<uint4*>(a_s + 8 * c) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+    } else {
+      for (int k = tid; k < d / 8; k += kFThreads)
+        reinterpret_cast<uint4*>(a_s)[k] = reinterpret_cast<const uint4*>(P.x_in)[k];
+    }
+    __syncthreads();
+    {  // fp32 copy of the input in bufB (free until the selection), then staged
+      float* af = reinterpret_cast<float*>(S.bufB);
+      for (int k = tid; k < d; k += kFThreads) af[k] = bf16f(a_s[k]);
+      __syncthreads();
+      stage_f32<BITS>(af, d, 1, d, sta);
+    }
+    stamp(P, l, 2);
+
+    // ---------------- A1: router rows (in bufA)
+    {
+      const int rloc = warp / g.qr, qtr = warp - rloc * g.qr;
+      const int row = (int)blockIdx.x * g.rpc + rloc;
+      const bool valid = rloc < g.rpc && row < E + (has_gate ? 1 : 0);
+      float v = 0.f;
+      if (valid) {
+        mbar_wait(S.mR, par, ctrl, P.timeout_ns);
+        const int c0 = qtr * (d / g.qr);
+        v = router_dot(reinterpret_cast<const uint16_t*>(S.bufA) + (size_t)rloc * d, a_s, c0, d / g.qr / 256, lane);
+      }
+      if (lane == 0) red[warp] = v;
+      __syncthreads();
+      if (valid && qtr == 0 && lane == 0) {
+        float s = 0.f;
+        for (int q = 0; q < g.qr; ++q) s += red[warp + q];
+        P.logits[row] = s;
+      }
+    }
+    stamp(P, l, 3);
+    cta_arrive(&ctrl->misc[1]);
+
+    // ---------------- A2: shared expert gate/up units (in bufA)
+    {
+      int b, e;
+      s1_range(g, f, b, e);
+      unsigned char* base = S.bufA + s1_base(g, d);
+      for (int j = warp; j < e - b; j += kFWarps) {
+        const Chunk ch = chunk_of(b + j, b, e, f);
+        mbar_wait(&S.mS[ch.idx], par, ctrl, P.timeout_ns);
+        float gv, uv;
+        unit_gateup<BITS>(base + (size_t)(ch.start - b) * g.unit, ch.n, b + j - ch.start, sta, g, lane, gv, uv);
+        if (lane == 0) P.hk[(size_t)K * f + b + j] = gv / (1.f + expf(-gv)) * uv;
+      }
+    }
+
+    // ---------------- selection: every CTA selects from the complete logits
+    stamp(P, l, 4);
+    if (!cta_wait(&ctrl->misc[1], g.nC * (l + 1), ctrl, P.timeout_ns, S)) return;
+    stamp(P, l, 5);
+    {
+      float* lg_s = reinterpret_cast<float*>(S.bufB);  // bufB is free until the B copies
+      for (int e = tid; e <= E; e += kFThreads) lg_s[e] = __ldcg(P.logits + e);
+      __syncthreads();
+      block_topk(lg_s, lg_s + E + 1, E, K, has_gate, red, reinterpret_cast<int*>(red + kFWarps), s_idx, s_w);
+      stamp(P, l, 11);
+      if (blockIdx.x == 0 && tid < K) {
+        if (P.idx_out) P.idx_out[l * K + tid] = s_idx[tid];
+        if (P.w_out) P.w_out[l * K + tid] = s_w[tid];
+      }
+      if (blockIdx.x == 0 && tid == 0 && P.gamma_out) P.gamma_out[l] = s_w[K];
+    }
+
+    // ---------------- B: the selected experts' gate/up units (in bufB)
+    if (warp == 0) issue_B(P, g, l, S, s_idx);
+    {
+      int b, e;
+      fsplit(K * f, blockIdx.x, g.nC, b, e);
+      for (int j = warp; j < e - b; j += kFWarps) {
+        const Chunk ch = chunk_of(b + j, b, e, f);
+        mbar_wait(&S.mB[ch.idx], par, ctrl, P.timeout_ns);
+        float gv, uv;
+        unit_gateup<BITS>(S.bufB + (size_t)(ch.start - b) * g.unit, ch.n, b + j - ch.start, sta, g, lane, gv, uv);
+        if (lane == 0) P.hk[b + j] = gv / (1.f + expf(-gv)) * uv;  // unit u = k*f + row
+      }
+    }
+    stamp(P, l, 6);
+    // Phase C: this CTA's output rows [c_b, c_e). Once every warp is done with
+    // bufB, warp 0 streams the down rows of the K+1 experts into it (and the
+    // next layer's phase-A data into bufA); both land during the grid-wide wait.
+    int c_b, c_e;
+    fsplit(d, blockIdx.x, g.nC, c_b, c_e);
+    CLayout cl;
+    cl.n = c_e - c_b;
+    cl.wqf = f * BITS / 8;
+    cl.wsf = (f / kGroup) * 4;
+    cta_arrive(&ctrl->misc[3]);
+    if (warp == 0) {
+      issue_C<BITS>(P, g, l, S, s_idx, c_b, cl);
+      if (l + 1 < P.n_layers) issue_A(P, g, l + 1, S);
+    }
+
+    // ---------------- C: down rows + combine (+ residual)
+    if (!cta_wait(&ctrl->misc[3], g.nC * (l + 1), ctrl, P.timeout_ns, S)) return;
+    stamp(P, l, 7);
+    {
+      stage_cg<BITS>(P.hk, f, K + 1, f, sth);  // the SwiGLU outputs of every CTA, through L2
+      stamp(P, l, 13);
+      mbar_wait(S.mC, par, ctrl, P.timeout_ns);
+      const int nrg = (cl.n + rgf.RPP - 1) / rgf.RPP;  // row groups
+      const int np = nrg * (K + 1);
+      const int lp = lane % rgf.LPR, rs = lane / rgf.LPR;
+      float* ys = reinterpret_cast<float*>(S.bufB + cl.ys(K));
+      const int nrows = cl.n;
+#pragma unroll 1
+      for (int pair = warp; pair < np; pair += kFWarps) {
+        const int k = pair / nrg, rgi = pair - k * nrg;
+        const int rloc = rgi * rgf.RPP + rs;
+        uint4 q = make_uint4(0, 0, 0, 0);
+        uint32_t sbw = 0;
+        if (rloc < nrows) {
+          q = *reinterpret_cast<const uint4*>(S.bufB + cl.q(k) + (size_t)rloc * cl.wqf + lp * 16);
+          sbw = *reinterpret_cast<const uint32_t*>(S.bufB + cl.sb(K, k) + (size_t)rloc * cl.wsf +
+                                                   part_group<BITS>(lp) * 4);
+        }
+        const float acc = part_dot_int16<BITS>(q, sbw, sth.chunks, sth.partinfo, k, 0, lp, rgf, 0.f);
+        const float y = row_reduce(acc, rgf.LPR);
+        if (lp == 0 && rloc < nrows) ys[k * nrows + rloc] = y;
+      }
+      __syncthreads();
+      // combine in fixed order: routed experts k = 0..K-1, then the shared expert (k = K)
+      float ss = 0.f;
+      for (int rl = tid; rl < nrows; rl += kFThreads) {
+        const int row = c_b + rl;
+        float o = 0.f;
+        for (int k = 0; k <= K; ++k) o = fmaf(s_w[k], ys[k * nrows + rl], o);
+        if (P.stack) {
+          const float hv = h_in(P, l, row) + o;
+          P.h[row] = hv;
+          ss = fmaf(hv, hv, ss);
+        } else {
+          if (P.out) P.out[row] = f2bf(o);
+          if (P.out_f32) P.out_f32[row] = o;
+        }
+      }
+      stamp(P, l, 14);
+      if (P.stack) {
+        ss = warp_sum(ss);
+        if (lane == 0) red[warp] = ss;
+        __syncthreads();
+        if (tid == 0) {
+          float s = 0.f;
+          for (int w = 0; w < kFWarps; ++w) s += red[w];
+          P.part_ss[((l + 1) & 1) * g.nC + blockIdx.x] = s;
+        }
+      }
+    }
+    stamp(P, l, 8);
+    cta_arrive(&ctrl->misc[4]);
+  }
+
+  // ---------------- stack output: x_next = bf16(rmsnorm(h)), h_out
+  if (P.stack) {
+    if (!cta_wait(&ctrl->misc[4], g.nC * P.n_layers, ctrl, P.timeout_ns, S)) return;
+    if (warp == 0) {
+      const float* part = P.part_ss + (P.n_layers & 1) * g.nC;
+      float s = 0.f;
+      for (int c = lane; c < g.nC; c += 32) s += __ldcg(part + c);
+      s = warp_sum(s);
+      if (lane == 0) s_r = 1.f / sqrtf(s / (float)d + P.eps);
+    }
+    __syncthreads();
+    int b, e;
+    fsplit(d, blockIdx.x, g.nC, b, e);
+    for (int k = b + tid; k < e; k += kFThreads) {
+      float hv = __ldcg(P.h + k);
+      if (P.x_next) P.x_next[k] = f2bf(hv * s_r);
+      if (P.h_out) P.h_out[k] = hv;
+    }
+  }
+  // the last CTA out resets the counters for the next launch
+  __syncthreads();
+  int prev = 0;
+  if (tid == 0) prev = atomicAdd(&ctrl->misc[5], 1);
+  if (tid == 0 && prev == g.nC - 1) {
+    for (int i = 1; i <= 5; ++i) ctrl->misc[i] = 0;
+    __threadfence();
+  }
+}
+
+// --------------------------------------------------------------- wait self-test
+// Two CTAs wait on a counter nothing increments, with a short limit: the
+// bounded wait must give up, write BGQ_ERR_TIMEOUT and return. Exercises the
+// same grid-wide wait the decode kernel uses, without faulting anything.
+__global__ void k_wait_selftest(Ctrl* ctrl, long long timeout_ns) {
+  FSmem S{};
+  __shared__ int par[3];
+  if (threadIdx.x == 0) {
+    par[0] = -1;
+    par[1] = -1;
+    par[2] = -1;
+  }
+  __syncthreads();
+  S.apar = &par[0];
+  S.bpar = &par[1];
+  S.cpar = &par[2];
+  if (!cta_wait(&ctrl->misc[6], 1 << 30, ctrl, timeout_ns, S)) return;
+  if (threadIdx.x == 0) atomicExch(&ctrl->status, BGQ_OK);  // not reached: nothing sets misc[6]
+}
+
+cudaError_t launch_wait_selftest(Ctrl* ctrl, long long timeout_ns, cudaStream_t s) {
+  k_wait_selftest<<<2, 64, 0, s>>>(ctrl, timeout_ns);
+  return cudaGetLastError();
+}
+
+// --------------------------------------------------------------- host side
+static size_t fused_smem_for(const FGeo& g, int d, int f, int K, int bits) {
+  return flayout(g, d, f, K, bits).total;
+}
+
+size_t fused_smem_bytes(int d, int f, int K, int bits) {
+  FGeo g = fgeo(num_sms(), d, f, 1024, K, bits);
+  return fused_smem_for(g, d, f, K, bits);
+}
+
+bool fused_supported(int d, int f, int E, int K, int bits) {
+  if (K < 1 || K > 8 || E < K || E > 1024) return false;
+  if (d % 256 || f % 256) return false;  // scale/bias rows of 16-byte multiples (bulk copies)
+  if (d > 2048 && d % 1024) return false;  // router slices of 1024 columns, or one slice of <= 2048
+  const int Pd = d * bits / 128, Pf = f * bits / 128;
+  if (Pd < 32 || Pd % 32 || Pd / 32 > 4) return false;  // d-rows: all lanes, <= 4 parts each
+  if (Pf < 1 || Pf > 32 || 32 % Pf) return false;       // f-rows: one part per lane
+  const int nC = num_sms();
+  FGeo g = fgeo(nC, d, f, E, K, bits);
+  if (g.nRouter > nC) return false;  // every router row owned by one CTA
+  if (g.nBmax > kMaxB) return false;
+  // bulk-copy chunks per CTA
+  for (int c = 0; c < nC; ++c) {
+    int b, e;
+    fsplit(K * f, c, nC, b, e);
+    int start = b, nch = 0;
+    while (start < e) {
+      int lim = start + kCH < e ? start + kCH : e;
+      int seg = (start / f + 1) * f;
+      if (seg < lim) lim = seg;
+      start = lim;
+      ++nch;
+    }
+    if (nch > kMaxBC) return false;
+  }
+  // largest shared gate/up range of any CTA
+  int mx = g.s1_nr;
+  const int n_nr = nC - g.nRouter;
+  const int rest0 = g.s1_nr > 0 ? n_nr * g.s1_nr : 0;
+  const int nparts = g.s1_nr > 0 ? g.nRouter : nC;
+  for (int c = 0; c < nparts; ++c) {
+    int b, e;
+    fsplit(f - rest0, c, nparts, b, e);
+    if (e - b > mx) mx = e - b;
+  }
+  if (mx > kMaxS1 || (mx + kCH - 1) / kCH > kMaxSC) return false;
+  int dev = 0, optin = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return false;
+  return fused_smem_for(g, d, f, K, bits) + 1024 <= (size_t)optin;
+}
+
+cudaError_t launch_fused(const FusedParams& P, int bits, cudaStream_t s) {
+  const int nC = num_sms();
+  FGeo g = fgeo(nC, P.d, P.f, P.E, P.K, bits);
+  size_t sm = fused_smem_for(g, P.d, P.f, P.K, bits);
+  void* kern = bits == 4 ? (void*)k_fused_decode<4> : (void*)k_fused_decode<2>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  void* args[] = {(void*)&P};
+  return cudaLaunchCooperativeKernel(kern, dim3(nC), dim3(kFThreads), args, sm, s);
+}
+
+}  // namespace bgq

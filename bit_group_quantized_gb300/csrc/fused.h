@@ -1,0 +1,58 @@
+// fused.h — parameters of the persistent batch-1 decode kernel (fused.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kernels.h"
+
+namespace bgq {
+
+constexpr int kMaxFusedLayers = 128;
+
+struct FusedLayer {
+  const uint16_t* router;  // bf16 [E][d]
+  const uint16_t* sgate;   // bf16 [d] or null
+  const uint32_t* pool_q;
+  const uint16_t* pool_sb;
+  long long q_stride, sb_stride;
+  const uint32_t* shared_q;
+  const uint16_t* shared_sb;
+  const uint16_t* rho;  // bf16 [d] (stack mode)
+};
+
+struct FusedParams {
+  int n_layers, d, f, E, K;
+  int stack;  // 1: RMSNorm + residual per layer, x_next output; 0: one layer, out = layer(x)
+  float eps;
+  long long timeout_ns;
+  const uint16_t* x_in;  // bf16 [d]
+  // outputs (nullable)
+  uint16_t* x_next;    // stack: bf16 [d]
+  float* h_out;        // stack: fp32 [d]
+  uint16_t* out;       // layer: bf16 [d]
+  float* out_f32;      // layer: fp32 [d]
+  int32_t* idx_out;    // [n_layers][K]
+  float* w_out;        // [n_layers][K]
+  float* gamma_out;    // [n_layers]
+  // scratch (workspace)
+  Ctrl* ctrl;
+  float* h;          // [d] residual stream
+  float* hk;         // [K+1][f] SwiGLU outputs (slot K: shared expert)
+  float* logits;     // [E+1]
+  float* part_ss;    // [2][nCTA] per-CTA sums of h^2
+  int32_t* route_idx;  // [K]
+  float* route_w;      // [K+1] (K: gamma)
+  // optional phase timestamps (%globaltimer, ns): [n_layers][nCTA][kTraceEvents]
+  unsigned long long* trace;
+  FusedLayer layers[kMaxFusedLayers];
+};
+
+constexpr int kTraceEvents = 16;
+
+size_t fused_smem_bytes(int d, int f, int K, int bits);
+bool fused_supported(int d, int f, int E, int K, int bits);
+cudaError_t launch_fused(const FusedParams& P, int bits, cudaStream_t s);
+cudaError_t launch_wait_selftest(Ctrl* ctrl, long long timeout_ns, cudaStream_t s);
+
+}  // namespace bgq

@@ -60,7 +60,7 @@ k_qgemv_int16(const uint32_t* __restrict__ q, const uint32_t* __restrict__ sb, i
     }
   }
 
-  stage_x_int16<BITS, uint16_t>(StridedSrc<uint16_t>{x, ldx}, T, cols, st, gsh);
+  stage_x_int16<BITS>(StridedSrc<uint16_t>{x, ldx}, T, cols, st, gsh);
 
   float acc[T];
 #pragma unroll
@@ -82,9 +82,8 @@ k_qgemv_int16(const uint32_t* __restrict__ q, const uint32_t* __restrict__ sb, i
     for (int i = 0; i < kMaxNit; ++i) {
       int it = it0 + i;
       if (it < rg.NIT) {
-        int p = it * rg.LPR + lp;
 #pragma unroll
-        for (int t = 0; t < T; ++t) acc[t] = part_dot_int16<BITS>(qv[i], sv[i], st.chunks, st.partinfo, t, p, rg, acc[t]);
+        for (int t = 0; t < T; ++t) acc[t] = part_dot_int16<BITS>(qv[i], sv[i], st.chunks, st.partinfo, t, it, lp, rg, acc[t]);
       }
     }
   }

@@ -30,9 +30,12 @@ struct RouteGeo {
   int rows_cta;  // rows per CTA
   int nvec;      // 16-byte vectors per lane per row slice
 };
+// Rows are cut into slices of 1024 columns when d is a multiple of 1024 (the
+// same cut as the persistent batch-1 kernel, so both sum a logit in the same
+// order and give bit-identical results), else one slice per row.
 __host__ __device__ inline RouteGeo route_geo(int d) {
   RouteGeo g;
-  g.sk = (d + 2047) / 2048;
+  g.sk = (d >= 1024 && d % 1024 == 0) ? d / 1024 : 1;
   g.rows_cta = kRouteWarps / g.sk;
   g.nvec = d / g.sk / 256;
   return g;
@@ -40,7 +43,7 @@ __host__ __device__ inline RouteGeo route_geo(int d) {
 bool route_shape_ok(int d) {
   if (d <= 0 || d % 256) return false;
   RouteGeo g = route_geo(d);
-  return g.sk <= kRouteWarps && d % (256 * g.sk) == 0;
+  return g.sk <= kRouteWarps && d % (256 * g.sk) == 0 && g.nvec <= kRouteMaxVec;
 }
 
 __device__ void topk_one_token(const float* __restrict__ lg, int E, int K, float zgate, bool has_gate, int t,

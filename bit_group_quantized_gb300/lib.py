@@ -67,6 +67,10 @@ _SIGS = {
     "moe_stack_workspace_bytes": (_S, [C.POINTER(bgq_moe_layer), _I]),
     "moe_stack_decode": (_I, [C.POINTER(bgq_moe_layer), C.POINTER(_P), _I, C.c_float, _P, _P, _P, _P, _P, _S,
                               _P]),
+    "moe_stack_trace_entries": (_S, [C.POINTER(bgq_moe_layer), _I]),
+    "moe_stack_decode_traced": (_I, [C.POINTER(bgq_moe_layer), C.POINTER(_P), _I, C.c_float, _P, _P, _P, _P, _P,
+                                     _S, _P, _P]),
+    "bgq_wait_selftest": (_I, [_P, _S, C.c_int64, _P]),
     "bgq_read_device_status": (_I, [_P, _P]),
 }
 
@@ -286,6 +290,33 @@ def moe_stack_decode(stack: Stack, x: torch.Tensor, eps: float = 1e-6, ws=None, 
     _check(lib.moe_stack_decode(stack.c_layers, stack.c_rho, n, eps, _ptr(x), _ptr(x_next), _ptr(h_out),
                                 _ptr(idx_out), _ptr(ws), ws.numel(), _stream(stream)), "moe_stack_decode")
     return x_next, h_out, idx_out
+
+
+def wait_selftest(ws: torch.Tensor, timeout_ns: int, stream=None) -> None:
+    _check(load().bgq_wait_selftest(_ptr(ws), ws.numel(), timeout_ns, _stream(stream)), "bgq_wait_selftest")
+
+
+TRACE_EVENTS = ("layer_start", "prev_layer_done", "input_staged", "router_done", "shared_gateup_done",
+                "logits_visible", "selected_gateup_done", "swiglu_visible", "down_combine_done", "unused9",
+                "unused10", "selected", "unused12", "swiglu_staged", "down_rows_done", "unused15")
+
+
+def moe_stack_decode_traced(stack: Stack, x: torch.Tensor, eps: float = 1e-6, ws=None, x_next=None, h_out=None,
+                            idx_out=None, stream=None):
+    """moe_stack_decode plus per-SM phase timestamps; returns the trace as an
+    int64 tensor [n_layers][n_sm][10] of %globaltimer nanoseconds."""
+    lib = load()
+    n = len(stack.layers)
+    ent = lib.moe_stack_trace_entries(stack.c_layers, n)
+    if ent == 0:
+        raise BGQError(ERR_UNSUPPORTED, "moe_stack_trace_entries")
+    trace = torch.zeros(ent, dtype=torch.int64, device=x.device)
+    if ws is None:
+        ws = workspace(stack.ws_bytes, x.device)
+    _check(lib.moe_stack_decode_traced(stack.c_layers, stack.c_rho, n, eps, _ptr(x), _ptr(x_next), _ptr(h_out),
+                                       _ptr(idx_out), _ptr(ws), ws.numel(), _ptr(trace), _stream(stream)),
+           "moe_stack_decode_traced")
+    return trace.view(n, -1, len(TRACE_EVENTS))
 
 
 def read_device_status(ws: torch.Tensor, stream=None) -> int:

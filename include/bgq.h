@@ -225,6 +225,30 @@ int32_t moe_stack_decode(const bgq_moe_layer* layers, const uint16_t* const* rho
                          float eps, const uint16_t* x, uint16_t* x_next, float* h_out,
                          int32_t* idx_out, void* ws, size_t ws_bytes, void* stream);
 
+/* moe_stack_decode that also records when each phase of each layer starts on
+ * each SM (the device-side counterpart of a per-layer --timing report).
+ * trace: device uint64 [n_layers][n_sm][16] of %globaltimer values (ns),
+ * moe_stack_trace_entries(layers, n_layers) entries, 16-byte aligned. Events:
+ * 0 layer start, 1 previous layer complete (grid-wide), 2 input staged,
+ * 3 router rows done, 4 shared gate/up done, 5 all logits visible,
+ * 11 experts selected, 6 selected gate/up done, 7 all SwiGLU outputs visible,
+ * 13 SwiGLU outputs staged, 14 down rows done, 8 down+combine done;
+ * 9, 10, 12, 15 unused.
+ * Available when the layers take the persistent batch-1 kernel (otherwise
+ * moe_stack_trace_entries returns 0 and the call BGQ_ERR_UNSUPPORTED). */
+size_t moe_stack_trace_entries(const bgq_moe_layer* layers, int32_t n_layers);
+int32_t moe_stack_decode_traced(const bgq_moe_layer* layers, const uint16_t* const* rho, int32_t n_layers,
+                                float eps, const uint16_t* x, uint16_t* x_next, float* h_out, int32_t* idx_out,
+                                void* ws, size_t ws_bytes, uint64_t* trace, void* stream);
+
+/* Self-test of the bounded device-side wait used by the persistent decode
+ * kernel: clears the control block of `ws` (>= 256 bytes) and launches two
+ * CTAs that wait on a counter nothing increments. The wait gives up after
+ * timeout_ns (1e3 .. 1e9), writes BGQ_ERR_TIMEOUT to the status word and the
+ * kernel returns; bgq_read_device_status(ws) then reports BGQ_ERR_TIMEOUT.
+ * Nothing faults or hangs. Leaves the workspace needing a re-zero. */
+int32_t bgq_wait_selftest(void* ws, size_t ws_bytes, int64_t timeout_ns, void* stream);
+
 /* Synchronises `stream`, then returns the status word that the kernels of the
  * calls above left in workspace `ws` (BGQ_OK or BGQ_ERR_TIMEOUT), and clears it. */
 int32_t bgq_read_device_status(void* ws, void* stream);

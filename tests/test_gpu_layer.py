@@ -64,6 +64,10 @@ def oracle_layer_token(t, src, shape, K, x_tok, gpu_idx=None):
     (8, 512, 256, 2, 2, 13),
     (64, 1024, 512, 4, 4, 64),
     (32, 2048, 1024, 8, 4, 5),
+    # batch 1 at shapes the persistent kernel takes (rows of d read by all 32 lanes)
+    (16, 1024, 256, 4, 4, 1),
+    (8, 2048, 512, 2, 2, 1),
+    (64, 1024, 512, 8, 4, 1),
 ])
 def test_small_layer_matches_oracle(cuda_device, E, d, f, K, bits, B):
     shape = synth.PoolShape(d, f, E, bits)
@@ -179,8 +183,8 @@ def oracle_stack(seed, built, rhos, shape, K, x_bits, gpu_idx):
     return O.stack_token(layers, x_bits, shape.bits, K, force_idx=force)
 
 
-@pytest.mark.parametrize("n_layers,d,f,E,bits", [(6, 512, 256, 16, 4), (4, 4096, 1024, 512, 4),
-                                                 (3, 4096, 1024, 512, 2)])
+@pytest.mark.parametrize("n_layers,d,f,E,bits", [(6, 512, 256, 16, 4), (6, 1024, 256, 16, 4),
+                                                 (4, 4096, 1024, 512, 4), (3, 4096, 1024, 512, 2)])
 def test_stack_matches_oracle(cuda_device, n_layers, d, f, E, bits):
     K = 4
     shape = synth.PoolShape(d, f, E, bits)
@@ -202,3 +206,14 @@ def test_stack_matches_oracle(cuda_device, n_layers, d, f, E, bits):
     # different values, so the stack's own error may exceed one layer's.
     assert_bf16_output(O.bf16_to_f64(bits16(x_next)), O.rmsnorm(ho, None), "x_next", own_tol=REL_L2_TOL)
     assert rel_l2(O.bf16_to_f64(bits16(x_next)), O.bf16_to_f64(xo)) <= REL_L2_TOL
+
+
+def test_bounded_wait_times_out_cleanly(cuda_device):
+    """A grid-wide wait on a counter nothing sets gives up after its limit and
+    reports BGQ_ERR_TIMEOUT through the status word; the context stays usable."""
+    ws = lib.workspace(4096, cuda_device)
+    lib.wait_selftest(ws, 2_000_000)  # 2 ms
+    assert lib.read_device_status(ws) == lib.ERR_TIMEOUT
+    assert lib.read_device_status(ws) == lib.OK  # reading clears it
+    x = torch.ones(16, device=cuda_device)
+    assert float((x * 2).sum()) == 32.0
