@@ -58,6 +58,29 @@ def layer_algorithmic_bytes(bits: int) -> int:
     return layer_weight_bytes(bits) + D_MODEL * 2 + D_MODEL * 2 + D_MODEL * 4 * 2
 
 
+def profiled_traffic(n_layers: int):
+    """DRAM bytes of one k_fused_decode launch, from the committed 1-layer ncu
+    capture scaled by the number of layers (each layer reads the same bytes);
+    None if the kernel sources changed since the capture."""
+    import hashlib
+
+    prof = os.path.join(ROOT, "profiles", "k_fused_decode_stack1_full.md")
+    if not os.path.exists(prof):
+        return None
+    fields = {}
+    for line in open(prof, encoding="utf-8"):
+        if ":" in line and line.split(":", 1)[0] in ("traffic_bytes_per_layer", "kernel_sources_sha256_16"):
+            k, v = line.split(":", 1)
+            fields[k] = v.strip()
+    csrc = os.path.join(ROOT, "bit_group_quantized_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in ("fused.cu", "common.cuh"):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    if fields.get("kernel_sources_sha256_16") != h.hexdigest()[:16] or "traffic_bytes_per_layer" not in fields:
+        return None
+    return int(fields["traffic_bytes_per_layer"]) * n_layers
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle sampling in the background during the timed region."""
 
@@ -333,7 +356,10 @@ def run_ours(args):
                          else "moe_stack_decode step (multi-kernel path)",
                          "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
-                         "frac_of_8tbs": round(achieved / 8000.0, 4), "traffic": None},
+                         "frac_of_8tbs": round(achieved / 8000.0, 4),
+                         "traffic": profiled_traffic(n_layers) if (fused and bits == 4) else None,
+                         "traffic_source": "ncu dram__bytes_read+write of a 1-layer capture "
+                                           "(profiles/k_fused_decode_stack1_full.md) x layers"},
             "e2e": {"value": round(world / e2e_s, 2), "unit": "tokens/s", "h2d_bytes_per_step": D_MODEL * 2,
                     "d2h_bytes_per_step": D_MODEL * 2},
             "gpu_launches": launches * args.steps,
