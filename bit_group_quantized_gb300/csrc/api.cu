@@ -246,7 +246,7 @@ int32_t moe_expert_swiglu(const bgq_expert* e, const uint16_t* x, int32_t batch,
   if (batch < 1 || batch > kMaxBatch) return BGQ_ERR_INVALID_ARG;
   if (!ws || !al(ws, 256) || ws_bytes < moe_expert_workspace_bytes(e, batch)) return BGQ_ERR_WORKSPACE;
   Carver c(ws);
-  c.take<Ctrl>(sizeof(Ctrl));
+  Ctrl* ctrl = c.take<Ctrl>(sizeof(Ctrl));
   Plan* plan = c.take<Plan>(plan_bytes(batch, 0));
   float* H = c.take<float>((size_t)batch * f * 4);
   float* Y = c.take<float>((size_t)batch * d * 4);
@@ -259,7 +259,9 @@ int32_t moe_expert_swiglu(const bgq_expert* e, const uint16_t* x, int32_t batch,
   const int ntasks = (batch + kTaskTok - 1) / kTaskTok;
   if (launch_plan_single(plan, batch, s) != cudaSuccess) return BGQ_ERR_CUDA;
   if (launch_gateup(es, plan, ntasks, x, H, 1, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  if (launch_gateup_tc(es, plan, batch, 0, x, H, 1, ctrl, s) != cudaSuccess) return BGQ_ERR_CUDA;
   if (launch_down(es, plan, ntasks, H, Y, 1, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  if (launch_down_tc(es, plan, batch, 0, H, Y, 1, ctrl, s) != cudaSuccess) return BGQ_ERR_CUDA;
   return cuda_status(launch_combine(Y, nullptr, nullptr, batch, 0, d, y, y_f32, s));
 }
 
@@ -279,9 +281,12 @@ static int32_t layer_forward_impl(const bgq_moe_layer* L, const uint16_t* x, int
                    W.plan, s) != cudaSuccess)
     return BGQ_ERR_CUDA;
   const ExpertSet es = expert_set(L);
-  const int max_tasks = batch * K + (batch + kTaskTok - 1) / kTaskTok;
+  const int max_tasks = plan_max_tasks(batch, K);
+  // experts with < 16 tokens: grouped GEMV; with >= 16: tensor-core GEMM
   if (launch_gateup(es, W.plan, max_tasks, x, W.H, K + 1, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  if (launch_gateup_tc(es, W.plan, batch, K, x, W.H, K + 1, W.ctrl, s) != cudaSuccess) return BGQ_ERR_CUDA;
   if (launch_down(es, W.plan, max_tasks, W.H, W.Y, K + 1, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  if (launch_down_tc(es, W.plan, batch, K, W.H, W.Y, K + 1, W.ctrl, s) != cudaSuccess) return BGQ_ERR_CUDA;
   return cuda_status(launch_combine(W.Y, w, gamma, batch, K, L->d_model, out, out_f32, s));
 }
 

@@ -102,7 +102,7 @@ k_gateup(ExpertSet es, const Plan* __restrict__ plan, const uint16_t* __restrict
   int staged = -1;
   for (int item = ir.begin; item < ir.end; ++item) {
     const int ti = item / nrb, rb = item - ti * nrb;
-    const Task& tk = plan->tasks[ti];
+    const Task& tk = plan_tasks(plan)[ti];
     const int ntok = tk.ntok;
     const ExpertRef ex = resolve(es, tk.expert);
     const int row = rb * rows_item + warp * rg.RPP + rs;
@@ -167,7 +167,7 @@ k_down(ExpertSet es, const Plan* __restrict__ plan, const float* __restrict__ H,
   int staged = -1;
   for (int item = ir.begin; item < ir.end; ++item) {
     const int ti = item / nrb, rb = item - ti * nrb;
-    const Task& tk = plan->tasks[ti];
+    const Task& tk = plan_tasks(plan)[ti];
     const int ntok = tk.ntok;
     const ExpertRef ex = resolve(es, tk.expert);
     const int row = rb * rows_item + warp * rg.RPP + rs;

@@ -34,6 +34,7 @@ struct ExpertSet {
 };
 
 constexpr int kTaskTok = 8;  // tokens per task (grouped GEMV width)
+constexpr int kBigTok = 16;  // an expert with at least this many tokens goes to the tensor-core path
 
 // One grouped-GEMV task: expert `expert` applied to up to 8 tokens; token i's
 // result goes to slot slot[i] of token tok[i].
@@ -44,15 +45,47 @@ struct Task {
   int slot[kTaskTok];
 };
 
-struct Plan {
-  int ntasks;
-  int pad[3];
-  Task tasks[1];  // [ntasks]
+// One tensor-core task: expert `expert` (-1: shared) applied to ntok tokens,
+// listed at ptok[first..first+ntok) with their slots at pslot[...].
+struct BigTask {
+  int expert;
+  int ntok;
+  int first;
+  int pad;
 };
 
+// Plan header; followed by Task[max_tasks], BigTask[max_big], int ptok[max_pairs], int pslot[max_pairs].
+struct Plan {
+  int ntasks;  // grouped-GEMV tasks
+  int nbig;    // tensor-core tasks
+  int pad[2];
+};
+
+__host__ __device__ inline int plan_max_tasks(int B, int K) { return B * K + (B + kTaskTok - 1) / kTaskTok + 1; }
+__host__ __device__ inline int plan_max_big(int B, int K) { return (B * K) / kBigTok + 2; }
+__host__ __device__ inline int plan_max_pairs(int B, int K) { return B * K + B; }
+__host__ __device__ inline Task* plan_tasks(Plan* p) { return reinterpret_cast<Task*>(p + 1); }
+__host__ __device__ inline const Task* plan_tasks(const Plan* p) { return reinterpret_cast<const Task*>(p + 1); }
+__host__ __device__ inline BigTask* plan_big(Plan* p, int B, int K) {
+  return reinterpret_cast<BigTask*>(plan_tasks(p) + plan_max_tasks(B, K));
+}
+__host__ __device__ inline const BigTask* plan_big(const Plan* p, int B, int K) {
+  return reinterpret_cast<const BigTask*>(plan_tasks(p) + plan_max_tasks(B, K));
+}
+__host__ __device__ inline int* plan_ptok(Plan* p, int B, int K) {
+  return reinterpret_cast<int*>(plan_big(p, B, K) + plan_max_big(B, K));
+}
+__host__ __device__ inline const int* plan_ptok(const Plan* p, int B, int K) {
+  return reinterpret_cast<const int*>(plan_big(p, B, K) + plan_max_big(B, K));
+}
+__host__ __device__ inline int* plan_pslot(Plan* p, int B, int K) { return plan_ptok(p, B, K) + plan_max_pairs(B, K); }
+__host__ __device__ inline const int* plan_pslot(const Plan* p, int B, int K) {
+  return plan_ptok(p, B, K) + plan_max_pairs(B, K);
+}
+
 inline size_t plan_bytes(int batch, int top_k) {
-  size_t maxtasks = (size_t)batch * top_k + (batch + kTaskTok - 1) / kTaskTok + 1;
-  return sizeof(Plan) + maxtasks * sizeof(Task);
+  return sizeof(Plan) + (size_t)plan_max_tasks(batch, top_k) * sizeof(Task) +
+         (size_t)plan_max_big(batch, top_k) * sizeof(BigTask) + (size_t)plan_max_pairs(batch, top_k) * 8;
 }
 
 // Workspace control block (first 256 bytes of every workspace).
@@ -76,6 +109,13 @@ cudaError_t launch_route(const uint16_t* router, const uint16_t* sgate, const ui
 
 // Builds the plan of one explicit expert over `batch` tokens (slot 0).
 cudaError_t launch_plan_single(Plan* plan, int batch, cudaStream_t s);
+
+// Tensor-core (tcgen05) gate/up + SiLU*mul and down projection for the plan's
+// big tasks (experts with >= kBigTok tokens). B, K: the plan's batch and top_k.
+cudaError_t launch_gateup_tc(const ExpertSet& es, const Plan* plan, int B, int K, const uint16_t* x, float* H,
+                             int nslot, Ctrl* ctrl, cudaStream_t s);
+cudaError_t launch_down_tc(const ExpertSet& es, const Plan* plan, int B, int K, const float* H, float* Y, int nslot,
+                           Ctrl* ctrl, cudaStream_t s);
 
 // Grouped gate/up + SiLU*mul: H[(tok*nslot + slot)*f + row].
 cudaError_t launch_gateup(const ExpertSet& es, const Plan* plan, int max_tasks, const uint16_t* x, float* H,

@@ -150,42 +150,77 @@ __device__ void block_exclusive_scan(int* a, int n, int* tmp /* >= 33 ints */) {
 
 __device__ void build_plan(const int* sel, int B, int K, int E, Plan* plan, int* s_cnt, int* s_tmp) {
   const int npairs = B * K;
+  Task* tasks = plan_tasks(plan);
+  BigTask* big = plan_big(plan, B, K);
+  int* ptok = plan_ptok(plan, B, K);
+  int* pslot = plan_pslot(plan, B, K);
+  int* s_first = s_cnt + E;    // task index of each small expert's first chunk
+  int* s_pfirst = s_cnt + 2 * E;  // pair offset of each big expert
+  int* s_bidx = s_cnt + 3 * E;    // big-task index of each big expert
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
   __syncthreads();
   for (int i = threadIdx.x; i < npairs; i += blockDim.x) atomicAdd(&s_cnt[sel[i]], 1);
   __syncthreads();
-  // chunks of <= 8 tokens per expert, then their starting task index
-  int* s_first = s_cnt + E;  // E ints: task index of each expert's first chunk
-  for (int e = threadIdx.x; e < E; e += blockDim.x) s_first[e] = (s_cnt[e] + kTaskTok - 1) / kTaskTok;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int c = s_cnt[e];
+    const bool bigc = c >= kBigTok;
+    s_first[e] = bigc ? 0 : (c + kTaskTok - 1) / kTaskTok;
+    s_pfirst[e] = bigc ? c : 0;
+    s_bidx[e] = bigc ? 1 : 0;
+  }
   __syncthreads();
   block_exclusive_scan(s_first, E, s_tmp);
-  const int nrouted = s_tmp[32];
+  const int nsmall = s_tmp[32];
+  block_exclusive_scan(s_pfirst, E, s_tmp);
+  const int nbigpairs = s_tmp[32];
+  block_exclusive_scan(s_bidx, E, s_tmp);
+  const int nbigr = s_tmp[32];
   for (int i = threadIdx.x; i < npairs; i += blockDim.x) {
-    int e = sel[i];
+    const int e = sel[i];
     int r = 0;
     for (int j = 0; j < i; ++j) r += (sel[j] == e);
-    Task& tk = plan->tasks[s_first[e] + r / kTaskTok];
-    int pos = r % kTaskTok;
-    tk.tok[pos] = i / K;
-    tk.slot[pos] = i % K;
-    if (pos == 0) {
-      tk.expert = e;
-      int left = s_cnt[e] - (r / kTaskTok) * kTaskTok;
-      tk.ntok = left < kTaskTok ? left : kTaskTok;
+    if (s_cnt[e] >= kBigTok) {
+      ptok[s_pfirst[e] + r] = i / K;
+      pslot[s_pfirst[e] + r] = i % K;
+      if (r == 0) big[s_bidx[e]] = BigTask{e, s_cnt[e], s_pfirst[e], 0};
+    } else {
+      Task& tk = tasks[s_first[e] + r / kTaskTok];
+      const int pos = r % kTaskTok;
+      tk.tok[pos] = i / K;
+      tk.slot[pos] = i % K;
+      if (pos == 0) {
+        tk.expert = e;
+        const int left = s_cnt[e] - (r / kTaskTok) * kTaskTok;
+        tk.ntok = left < kTaskTok ? left : kTaskTok;
+      }
     }
   }
-  const int nshared = (B + kTaskTok - 1) / kTaskTok;
-  for (int c = threadIdx.x; c < nshared; c += blockDim.x) {
-    Task& tk = plan->tasks[nrouted + c];
-    tk.expert = -1;
-    int n = B - c * kTaskTok;
-    tk.ntok = n < kTaskTok ? n : kTaskTok;
-    for (int i = 0; i < tk.ntok; ++i) {
-      tk.tok[i] = c * kTaskTok + i;
-      tk.slot[i] = K;
+  // the shared expert takes every token (slot K)
+  int nshared = 0, nbig = nbigr;
+  if (B >= kBigTok) {
+    for (int t = threadIdx.x; t < B; t += blockDim.x) {
+      ptok[nbigpairs + t] = t;
+      pslot[nbigpairs + t] = K;
+    }
+    if (threadIdx.x == 0) big[nbigr] = BigTask{-1, B, nbigpairs, 0};
+    nbig = nbigr + 1;
+  } else {
+    nshared = (B + kTaskTok - 1) / kTaskTok;
+    for (int c = threadIdx.x; c < nshared; c += blockDim.x) {
+      Task& tk = tasks[nsmall + c];
+      tk.expert = -1;
+      const int n = B - c * kTaskTok;
+      tk.ntok = n < kTaskTok ? n : kTaskTok;
+      for (int i = 0; i < tk.ntok; ++i) {
+        tk.tok[i] = c * kTaskTok + i;
+        tk.slot[i] = K;
+      }
     }
   }
-  if (threadIdx.x == 0) plan->ntasks = nrouted + nshared;
+  if (threadIdx.x == 0) {
+    plan->ntasks = nsmall + nshared;
+    plan->nbig = nbig;
+  }
 }
 
 __global__ void __launch_bounds__(kRouteThreads)
@@ -272,8 +307,8 @@ k_route(const uint16_t* __restrict__ router, const uint16_t* __restrict__ sgate,
   if (plan) {
     __syncthreads();
     __threadfence_block();
-    int* s_cnt = reinterpret_cast<int*>(smem);  // reuse: 2*E ints + scan scratch
-    build_plan(sel_ws, B, K, E, plan, s_cnt, s_cnt + 2 * E);
+    int* s_cnt = reinterpret_cast<int*>(smem);  // reuse: 4*E ints + scan scratch
+    build_plan(sel_ws, B, K, E, plan, s_cnt, s_cnt + 4 * E);
   }
   if (threadIdx.x == 0) ctrl->route_counter = 0;  // ready for the next launch
 }
@@ -285,7 +320,7 @@ cudaError_t launch_route(const uint16_t* router, const uint16_t* sgate, const ui
   int nrows = E + (sgate ? 1 : 0);
   int grid = (nrows + g.rows_cta - 1) / g.rows_cta;
   size_t sm = (size_t)kRouteTok * d * 2 + kRouteWarps * kRouteTok * sizeof(float);
-  size_t sm_plan = (size_t)(2 * E + 40) * sizeof(int);
+  size_t sm_plan = (size_t)(4 * E + 40) * sizeof(int);
   if (sm_plan > sm) sm = sm_plan;
   if (sm > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(k_route, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
@@ -298,10 +333,27 @@ cudaError_t launch_route(const uint16_t* router, const uint16_t* sgate, const ui
   return cudaGetLastError();
 }
 
+// Plan of one explicit expert over B tokens (slot 0): one tensor-core task for
+// B >= kBigTok, else grouped-GEMV tasks of up to 8 tokens. Plan sized for (B, 0).
 __global__ void k_plan_single(Plan* plan, int B) {
+  if (B >= kBigTok) {
+    BigTask* big = plan_big(plan, B, 0);
+    int* ptok = plan_ptok(plan, B, 0);
+    int* pslot = plan_pslot(plan, B, 0);
+    for (int t = threadIdx.x; t < B; t += blockDim.x) {
+      ptok[t] = t;
+      pslot[t] = 0;
+    }
+    if (threadIdx.x == 0) {
+      big[0] = BigTask{-1, B, 0, 0};
+      plan->nbig = 1;
+      plan->ntasks = 0;
+    }
+    return;
+  }
   const int n = (B + kTaskTok - 1) / kTaskTok;
   for (int c = threadIdx.x; c < n; c += blockDim.x) {
-    Task& tk = plan->tasks[c];
+    Task& tk = plan_tasks(plan)[c];
     tk.expert = -1;
     int m = B - c * kTaskTok;
     tk.ntok = m < kTaskTok ? m : kTaskTok;
@@ -310,7 +362,10 @@ __global__ void k_plan_single(Plan* plan, int B) {
       tk.slot[i] = 0;
     }
   }
-  if (threadIdx.x == 0) plan->ntasks = n;
+  if (threadIdx.x == 0) {
+    plan->ntasks = n;
+    plan->nbig = 0;
+  }
 }
 
 cudaError_t launch_plan_single(Plan* plan, int batch, cudaStream_t s) {

@@ -1,0 +1,496 @@
+// umma.cu — tensor-core (tcgen05) grouped GEMM for experts with many tokens.
+//
+// When a batch routes kBigTok (16) or more tokens to one expert (always true for
+// the shared expert at batch >= 16), the expert's three matrices are a dense
+// contraction: rows x K weights against K x tokens activations. Here the
+// weights are dequantised (w = q*scale + bias, Flash-MoE page, "FMA Dequant")
+// to fp16 in shared memory, the tokens' inputs are converted to fp16 next to
+// them, and tcgen05.mma (kind::f16, fp32 accumulation in tensor memory)
+// multiplies them. fp16 keeps 11 significant bits, so each dequantised weight
+// carries one fp16 rounding (about 2^-12 relative), far inside the layer's
+// tolerance; the accumulation is fp32.
+//
+// Tile: 128 weight rows (M) x Npad tokens (N = the task's tokens rounded up
+// to 16), K in steps of 64 (one quantisation group). Two shared-memory stages:
+// while the tensor core multiplies one stage, the 128 threads fill the other.
+// Operands use the canonical no-swizzle K-major layout: 8x16-byte core
+// matrices, the next core matrix along K 128 bytes on (LBO), the next 8 rows
+// 1024 bytes on (SBO). Within each 16-column block the columns are stored in
+// the order the code extraction produces them; activations use the same order,
+// so every dot product is unchanged.
+//
+// One thread issues the MMAs and commits them to a per-stage mbarrier; every
+// wait is bounded (on expiry: BGQ_ERR_TIMEOUT in the status word, a second
+// bounded wait for the tensor core, tensor memory freed, return).
+#include <cuda_fp16.h>
+
+#include "../../include/bgq.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bgq {
+
+constexpr int kTcThreads = 128;
+constexpr int kTcM = 128;
+constexpr int kTcBK = 64;
+constexpr long long kTcTimeoutNs = 1000000000ll;
+
+__device__ __forceinline__ uint32_t tc_smem(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ unsigned long long tc_time() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void tc_mbar_init(uint64_t* m) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem(m)) : "memory");
+}
+__device__ __forceinline__ bool tc_mbar_try(uint64_t* m, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(tc_smem(m)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait; false on timeout.
+__device__ bool tc_mbar_wait(uint64_t* m, uint32_t parity, long long limit_ns) {
+  if (tc_mbar_try(m, parity)) return true;
+  const unsigned long long t0 = tc_time();
+  long long it = 0;
+  while (!tc_mbar_try(m, parity)) {
+    if ((++it & 63) == 0 && ((long long)(tc_time() - t0) > limit_ns || it > (1ll << 28))) return false;
+  }
+  return true;
+}
+__device__ __forceinline__ void tc_fence_proxy() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Tensor memory: allocation and release by one whole warp.
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tc_smem(slot)), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_free(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, no swizzle.
+__device__ __forceinline__ uint64_t tc_desc(const void* base) {
+  const uint64_t addr = (tc_smem(base) >> 4) & 0x3FFF;
+  const uint64_t lbo = (128 >> 4);   // next core matrix along K
+  const uint64_t sbo = (1024 >> 4);  // next 8 rows
+  return addr | (lbo << 16) | (sbo << 32) | (1ull << 46);  // version 1, base offset 0, no swizzle
+}
+// Instruction descriptor: fp16 A and B (K-major), fp32 D, M = 128, N = n.
+__device__ __forceinline__ uint32_t tc_idesc(int n) {
+  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kTcM >> 4) << 24);
+}
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint64_t* m) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(tc_smem(m))
+               : "memory");
+}
+// 8 consecutive fp32 columns of this warp's 32 tensor-memory lanes (one row per thread).
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Byte offset of element (row r, 16-column block kb, slot s in 0..15) in a
+// K-major no-swizzle operand tile of 64 columns.
+__device__ __forceinline__ int tc_off(int r, int kb, int s) {
+  return (r >> 3) * 1024 + (kb * 2 + (s >> 3)) * 128 + (r & 7) * 16 + (s & 7) * 2;
+}
+// Slot of column k (0..15) inside its 16-column block, matching the order in
+// which dequant_row() writes codes (4-bit: pairs (j, j+4) per 8 columns;
+// 2-bit: pairs (j, j+8) per 16 columns).
+template <int BITS>
+__device__ __forceinline__ int tc_slot(int k) {
+  if (BITS == 4) {
+    const int h = k >> 3, j = k & 7;
+    return h * 8 + (j < 4 ? 2 * j : 2 * (j - 4) + 1);
+  } else {
+    return k < 8 ? (k >> 2) * 8 + 2 * (k & 3) : ((k - 8) >> 2) * 8 + 2 * ((k - 8) & 3) + 1;
+  }
+}
+
+// Dequantise one row's 64 codes (group g) to fp16 into the tile.
+template <int BITS>
+__device__ __forceinline__ void dequant_row(const uint32_t* qrow, uint32_t sbw, unsigned char* tile, int r) {
+  const __half2 s2 = __float2half2_rn(bf16lo(sbw));
+  const __half2 b2 = __float2half2_rn(bf16hi(sbw));
+  const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f);
+  constexpr int kWords = 64 * BITS / 32;  // 8 (4-bit) or 4 (2-bit)
+  uint32_t w[kWords];
+  if (BITS == 4) {
+    const uint4 a = *reinterpret_cast<const uint4*>(qrow), b = *reinterpret_cast<const uint4*>(qrow + 4);
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+    w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+  } else {
+    const uint4 a = *reinterpret_cast<const uint4*>(qrow);
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+  }
+  // each 16-byte chunk (8 slots) = 4 half2 pairs
+  constexpr int kChunks = 8;  // 64 columns = 8 chunks of 8
+#pragma unroll
+  for (int c = 0; c < kChunks; ++c) {
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t v;
+      if (BITS == 4) {
+        v = (w[c] >> (4 * j)) & 0x000F000Fu;  // codes j and j+4 of word c
+      } else {
+        const int wi = c >> 1, base = (c & 1) * 4;  // chunk c: half (c&1) of word c/2
+        v = (w[wi] >> (2 * (base + j))) & 0x00030003u;  // codes base+j and base+j+8
+      }
+      const uint32_t m = v | 0x64006400u;                                // fp16 1024 + code
+      __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&m), k1024);  // exact code values
+      h = __hfma2(h, s2, b2);                                      // q*s + b, one rounding
+      o[j] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    // chunk c covers columns 8c..8c+7: block kb = c/2, slots (c%2)*8 ..
+    *reinterpret_cast<uint4*>(tile + tc_off(r, c >> 1, (c & 1) * 8)) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// Write 16 activation values (columns 16*kb .. +15 of token row n) into the
+// tile in tc_slot order.
+template <int BITS>
+__device__ __forceinline__ void put_act16(unsigned char* tile, int n, int kb, const float (&v)[16]) {
+  __half h[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) h[tc_slot<BITS>(k)] = __float2half_rn(v[k]);
+  uint4 c0, c1;
+  c0.x = (uint32_t)__half_as_ushort(h[0]) | ((uint32_t)__half_as_ushort(h[1]) << 16);
+  c0.y = (uint32_t)__half_as_ushort(h[2]) | ((uint32_t)__half_as_ushort(h[3]) << 16);
+  c0.z = (uint32_t)__half_as_ushort(h[4]) | ((uint32_t)__half_as_ushort(h[5]) << 16);
+  c0.w = (uint32_t)__half_as_ushort(h[6]) | ((uint32_t)__half_as_ushort(h[7]) << 16);
+  c1.x = (uint32_t)__half_as_ushort(h[8]) | ((uint32_t)__half_as_ushort(h[9]) << 16);
+  c1.y = (uint32_t)__half_as_ushort(h[10]) | ((uint32_t)__half_as_ushort(h[11]) << 16);
+  c1.z = (uint32_t)__half_as_ushort(h[12]) | ((uint32_t)__half_as_ushort(h[13]) << 16);
+  c1.w = (uint32_t)__half_as_ushort(h[14]) | ((uint32_t)__half_as_ushort(h[15]) << 16);
+  *reinterpret_cast<uint4*>(tile + tc_off(n, kb, 0)) = c0;
+  *reinterpret_cast<uint4*>(tile + tc_off(n, kb, 8)) = c1;
+}
+
+__device__ __forceinline__ ExpertRef tc_resolve(const ExpertSet& es, int e) {
+  if (e < 0) return es.shared;
+  ExpertRef r;
+  const long long mw = (long long)es.d * es.f * es.bits / 32;
+  const long long mg = (long long)es.d * es.f / kGroup * 2;
+  const uint32_t* q = es.pool_q + (long long)e * es.q_stride;
+  const uint16_t* sb = es.pool_sb + (long long)e * es.sb_stride;
+  r.gate_q = q;
+  r.up_q = q + mw;
+  r.down_q = q + 2 * mw;
+  r.gate_sb = sb;
+  r.up_sb = sb + mg;
+  r.down_sb = sb + 2 * mg;
+  return r;
+}
+
+// Shared memory of one CTA: [mbar x2][tmem slot] then two stages of
+// NA weight tiles (16 KB each) and one activation tile (Npad*128 bytes).
+struct TcSmem {
+  uint64_t* mbar;
+  uint32_t* tslot;
+  unsigned char* stage[2];
+  int a_bytes, b_off;
+};
+__device__ __forceinline__ TcSmem tc_carve(unsigned char* smem, int na, int npad) {
+  TcSmem S;
+  S.mbar = reinterpret_cast<uint64_t*>(smem);
+  S.tslot = reinterpret_cast<uint32_t*>(smem + 16);
+  S.a_bytes = kTcM * kTcBK * 2;  // 16 KB
+  S.b_off = na * S.a_bytes;
+  const int stage_bytes = S.b_off + npad * kTcBK * 2;
+  S.stage[0] = smem + 1024;
+  S.stage[1] = smem + 1024 + stage_bytes;
+  return S;
+}
+size_t tc_smem_bytes(int na, int npad) { return 1024 + 2 * ((size_t)na * kTcM * kTcBK * 2 + (size_t)npad * kTcBK * 2); }
+
+__device__ __forceinline__ void tc_fail(Ctrl* ctrl) { atomicExch(&ctrl->status, BGQ_ERR_TIMEOUT); }
+
+// ---------------------------------------------------------------------------
+// gate/up + SiLU*mul: blockIdx.x = tile of 128 rows of d_ff, blockIdx.y = big task.
+// ---------------------------------------------------------------------------
+template <int BITS>
+__global__ void __launch_bounds__(kTcThreads, 1)
+k_gateup_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const uint16_t* __restrict__ x,
+            float* __restrict__ H, int nslot, Ctrl* ctrl) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  if ((int)blockIdx.y >= plan->nbig) return;
+  const BigTask bt = plan_big(plan, B, K)[blockIdx.y];
+  const int* ptok = plan_ptok(plan, B, K) + bt.first;
+  const int* pslot = plan_pslot(plan, B, K) + bt.first;
+  const int d = es.d, f = es.f;
+  const int npad = (bt.ntok + 15) & ~15;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int m0 = blockIdx.x * kTcM;
+  TcSmem S = tc_carve(smem, 2, npad);
+  const ExpertRef ex = tc_resolve(es, bt.expert);
+  const int wpr = d * BITS / 32, gpr = d / kGroup;
+  uint32_t ncols = 32;
+  while ((int)ncols < 2 * npad) ncols <<= 1;
+
+  if (tid == 0) {
+    tc_mbar_init(&S.mbar[0]);
+    tc_mbar_init(&S.mbar[1]);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) tmem_alloc(S.tslot, ncols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *S.tslot;
+  const uint32_t idesc = tc_idesc(npad);
+  const int nk = d / kTcBK;
+  bool ok = true;
+
+  for (int kb = 0; kb < nk; ++kb) {
+    const int s = kb & 1;
+    unsigned char* st = S.stage[s];
+    if (kb >= 2 && !tc_mbar_wait(&S.mbar[s], (uint32_t)((kb / 2 - 1) & 1), kTcTimeoutNs)) {
+      ok = false;
+      break;
+    }
+    // weights: thread t dequantises row m0 + t of gate and of up
+    {
+      const int r = m0 + tid;
+      if (r < f) {
+        const uint32_t* gq = ex.gate_q + (size_t)r * wpr + kb * (kTcBK * BITS / 32);
+        const uint32_t* uq = ex.up_q + (size_t)r * wpr + kb * (kTcBK * BITS / 32);
+        const uint32_t gs = reinterpret_cast<const uint32_t*>(ex.gate_sb)[(size_t)r * gpr + kb];
+        const uint32_t us = reinterpret_cast<const uint32_t*>(ex.up_sb)[(size_t)r * gpr + kb];
+        dequant_row<BITS>(gq, gs, st, tid);
+        dequant_row<BITS>(uq, us, st + S.a_bytes, tid);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          *reinterpret_cast<uint4*>(st + tc_off(tid, c >> 1, (c & 1) * 8)) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(st + S.a_bytes + tc_off(tid, c >> 1, (c & 1) * 8)) = make_uint4(0, 0, 0, 0);
+        }
+      }
+    }
+    // activations: (token n, 16-column block) per thread
+    for (int i = tid; i < npad * 4; i += kTcThreads) {
+      const int n = i >> 2, blk = i & 3;
+      float v[16];
+      if (n < bt.ntok) {
+        const uint16_t* xp = x + (size_t)ptok[n] * d + kb * kTcBK + blk * 16;
+        unpack_bf16x8(*reinterpret_cast<const uint4*>(xp), v);
+        unpack_bf16x8(*reinterpret_cast<const uint4*>(xp + 8), v + 8);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[k] = 0.f;
+      }
+      put_act16<BITS>(st + S.b_off, n, blk, v);
+    }
+    tc_fence_proxy();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int j = 0; j < kTcBK / 16; ++j) {
+        const uint64_t bd = tc_desc(st + S.b_off + j * 256);
+        tc_mma(tbase, tc_desc(st + j * 256), bd, idesc, (kb | j) ? 1u : 0u);
+        tc_mma(tbase + npad, tc_desc(st + S.a_bytes + j * 256), bd, idesc, (kb | j) ? 1u : 0u);
+      }
+      tc_commit(&S.mbar[s]);
+    }
+  }
+  // the last commit covers every MMA
+  if (ok) ok = tc_mbar_wait(&S.mbar[(nk - 1) & 1], (uint32_t)(((nk - 1) / 2) & 1), kTcTimeoutNs);
+  if (ok) {
+    tc_fence_after();
+    const int row = m0 + warp * 32 + (tid & 31);
+    for (int c0 = 0; c0 < npad; c0 += 8) {
+      float g[8], u[8];
+      const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+      tmem_ld8(tbase + lane_off + c0, g);
+      tmem_ld8(tbase + lane_off + npad + c0, u);
+      if (row < f) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int n = c0 + i;
+          if (n < bt.ntok) H[((size_t)ptok[n] * nslot + pslot[n]) * f + row] = g[i] / (1.f + expf(-g[i])) * u[i];
+        }
+      }
+    }
+  } else {
+    if (tid == 0) tc_fail(ctrl);
+    // give the tensor core a last bounded chance to finish before the memory is freed
+    tc_mbar_wait(&S.mbar[0], 0, kTcTimeoutNs / 4);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_free(tbase, ncols);
+}
+
+// ---------------------------------------------------------------------------
+// down projection: blockIdx.x = tile of 128 rows of d_model, blockIdx.y = big task.
+// ---------------------------------------------------------------------------
+template <int BITS>
+__global__ void __launch_bounds__(kTcThreads, 1)
+k_down_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const float* __restrict__ H,
+          float* __restrict__ Y, int nslot, Ctrl* ctrl) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  if ((int)blockIdx.y >= plan->nbig) return;
+  const BigTask bt = plan_big(plan, B, K)[blockIdx.y];
+  const int* ptok = plan_ptok(plan, B, K) + bt.first;
+  const int* pslot = plan_pslot(plan, B, K) + bt.first;
+  const int d = es.d, f = es.f;
+  const int npad = (bt.ntok + 15) & ~15;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int m0 = blockIdx.x * kTcM;
+  TcSmem S = tc_carve(smem, 1, npad);
+  const ExpertRef ex = tc_resolve(es, bt.expert);
+  const int wpr = f * BITS / 32, gpr = f / kGroup;
+  uint32_t ncols = 32;
+  while ((int)ncols < npad) ncols <<= 1;
+
+  if (tid == 0) {
+    tc_mbar_init(&S.mbar[0]);
+    tc_mbar_init(&S.mbar[1]);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) tmem_alloc(S.tslot, ncols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *S.tslot;
+  const uint32_t idesc = tc_idesc(npad);
+  const int nk = f / kTcBK;
+  bool ok = true;
+
+  for (int kb = 0; kb < nk; ++kb) {
+    const int s = kb & 1;
+    unsigned char* st = S.stage[s];
+    if (kb >= 2 && !tc_mbar_wait(&S.mbar[s], (uint32_t)((kb / 2 - 1) & 1), kTcTimeoutNs)) {
+      ok = false;
+      break;
+    }
+    {
+      const int r = m0 + tid;
+      if (r < d) {
+        const uint32_t* dq = ex.down_q + (size_t)r * wpr + kb * (kTcBK * BITS / 32);
+        const uint32_t ds = reinterpret_cast<const uint32_t*>(ex.down_sb)[(size_t)r * gpr + kb];
+        dequant_row<BITS>(dq, ds, st, tid);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(st + tc_off(tid, c >> 1, (c & 1) * 8)) = make_uint4(0, 0, 0, 0);
+      }
+    }
+    for (int i = tid; i < npad * 4; i += kTcThreads) {
+      const int n = i >> 2, blk = i & 3;
+      float v[16];
+      if (n < bt.ntok) {
+        const float* hp = H + ((size_t)ptok[n] * nslot + pslot[n]) * f + kb * kTcBK + blk * 16;
+#pragma unroll
+        for (int k = 0; k < 16; k += 4) {
+          const float4 a = *reinterpret_cast<const float4*>(hp + k);
+          v[k] = a.x;
+          v[k + 1] = a.y;
+          v[k + 2] = a.z;
+          v[k + 3] = a.w;
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[k] = 0.f;
+      }
+      put_act16<BITS>(st + S.b_off, n, blk, v);
+    }
+    tc_fence_proxy();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int j = 0; j < kTcBK / 16; ++j)
+        tc_mma(tbase, tc_desc(st + j * 256), tc_desc(st + S.b_off + j * 256), idesc, (kb | j) ? 1u : 0u);
+      tc_commit(&S.mbar[s]);
+    }
+  }
+  if (ok) ok = tc_mbar_wait(&S.mbar[(nk - 1) & 1], (uint32_t)(((nk - 1) / 2) & 1), kTcTimeoutNs);
+  if (ok) {
+    tc_fence_after();
+    const int row = m0 + warp * 32 + (tid & 31);
+    for (int c0 = 0; c0 < npad; c0 += 8) {
+      float y[8];
+      tmem_ld8(tbase + ((uint32_t)(warp * 32) << 16) + c0, y);
+      if (row < d) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int n = c0 + i;
+          if (n < bt.ntok) Y[((size_t)ptok[n] * nslot + pslot[n]) * d + row] = y[i];
+        }
+      }
+    }
+  } else {
+    if (tid == 0) tc_fail(ctrl);
+    tc_mbar_wait(&S.mbar[0], 0, kTcTimeoutNs / 4);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_free(tbase, ncols);
+}
+
+// ---------------------------------------------------------------------------
+static int tc_npad_max(int B) {
+  int n = B < 256 ? B : 256;
+  return (n + 15) & ~15;
+}
+
+cudaError_t launch_gateup_tc(const ExpertSet& es, const Plan* plan, int B, int K, const uint16_t* x, float* H,
+                             int nslot, Ctrl* ctrl, cudaStream_t s) {
+  if (B < kBigTok) return cudaSuccess;  // no task can have 16 tokens
+  const int npad = tc_npad_max(B);
+  const size_t sm = tc_smem_bytes(2, npad);
+  dim3 grid((es.f + kTcM - 1) / kTcM, plan_max_big(B, K));
+  void* kern = es.bits == 4 ? (void*)k_gateup_tc<4> : (void*)k_gateup_tc<2>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  if (es.bits == 4)
+    k_gateup_tc<4><<<grid, kTcThreads, sm, s>>>(es, plan, B, K, x, H, nslot, ctrl);
+  else
+    k_gateup_tc<2><<<grid, kTcThreads, sm, s>>>(es, plan, B, K, x, H, nslot, ctrl);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_down_tc(const ExpertSet& es, const Plan* plan, int B, int K, const float* H, float* Y, int nslot,
+                           Ctrl* ctrl, cudaStream_t s) {
+  if (B < kBigTok) return cudaSuccess;
+  const int npad = tc_npad_max(B);
+  const size_t sm = tc_smem_bytes(1, npad);
+  dim3 grid((es.d + kTcM - 1) / kTcM, plan_max_big(B, K));
+  void* kern = es.bits == 4 ? (void*)k_down_tc<4> : (void*)k_down_tc<2>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  if (es.bits == 4)
+    k_down_tc<4><<<grid, kTcThreads, sm, s>>>(es, plan, B, K, H, Y, nslot, ctrl);
+  else
+    k_down_tc<2><<<grid, kTcThreads, sm, s>>>(es, plan, B, K, H, Y, nslot, ctrl);
+  return cudaGetLastError();
+}
+
+}  // namespace bgq

@@ -8,6 +8,20 @@ from oracle import bgq_oracle as O
 
 REL_L2_TOL = 2e-3  # max relative L2 error of an output vector (bf16 out, fp32 accumulate)
 TIE_GAP = 1e-3  # K-th vs (K+1)-th logit gap below which several expert sets are correct
+BIG_TOK = 16  # experts with at least this many tokens run on the tensor-core (fp16 operand) path
+# The tensor-core path rounds three operands to fp16 (11 significant bits):
+# the dequantised weights, the inputs and the SwiGLU outputs. Each adds about
+# 2^-11/sqrt(3) ~ 2.8e-4 relative L2, so the kernel's own error (against the
+# oracle rounded to bf16, which also counts bf16 rounding flips) is bounded at
+# 1.5e-3 there instead of 1e-3; the workload tolerance (2e-3 against the
+# unrounded oracle) is the same for every path.
+TC_OWN_TOL = 1.5e-3
+
+
+def own_tol_for(batch: int) -> float:
+    """Kernel-own-error bound for a call on `batch` tokens (the shared expert
+    takes every token, so batch >= 16 puts it on the tensor-core path)."""
+    return TC_OWN_TOL if batch >= BIG_TOK else 1e-3
 
 
 def bits16(t: torch.Tensor) -> np.ndarray:
