@@ -212,8 +212,9 @@ def workload_name(args) -> str:
         return (f"moe_decode_stack: {args.layers} layers x (512 routed + 1 shared SwiGLU experts, d_model 4096, "
                 f"d_ff 1024, top-4), {bits}-bit codes, group 64 bf16 scale+bias, batch 1")
     if args.workload == "layer":
-        return f"moe_layer: 512 routed + 1 shared experts, d_model 4096, d_ff 1024, top-4, 4-bit, batch {args.batch}"
-    return "q4_gemv: 1024x4096 4-bit, group 64, batch 1"
+        return (f"moe_layer: 512 routed + 1 shared experts, d_model 4096, d_ff 1024, top-4, 4-bit, batch {args.batch}"
+                f", ring of {args.ring} distinct layers")
+    return f"q4_gemv: 1024x4096 4-bit, group 64, batch 1, variant {args.variant}, ring of {args.ring} matrices"
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -372,13 +373,132 @@ def run_ours(args):
     return 0
 
 
+def _timed_graph(torch, stream, body, n_replays, warmup):
+    """Capture body() once in a CUDA graph, warm up, then time n_replays
+    replays with CUDA events on `stream`; returns ms per replay."""
+    with torch.cuda.stream(stream):
+        body()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            body()
+        for _ in range(warmup):
+            g.replay()
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_replays):
+            g.replay()
+        e1.record(stream)
+        e1.synchronize()
+    return e0.elapsed_time(e1) / n_replays
+
+
+def run_layer(args):
+    """One MoE layer at batch B per step, cycling through `ring` distinct
+    resident layers and inputs (so router and shared weights are not L2 hits)."""
+    import torch
+
+    from bit_group_quantized_gb300 import lib, synth
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    lib.load()
+    B, R = args.batch, args.ring
+    shape = synth.PoolShape(D_MODEL, D_FF, N_EXPERTS, 4)
+    layers, keep, xs, outs = [], [], [], []
+    for r in range(R):
+        t = synth.layer_tensors(args.seed + 100, r, shape, device=dev)
+        keep.append(t)
+        layers.append(lib.MoELayer(D_MODEL, D_FF, N_EXPERTS, TOP_K, 4, t["router"], t["shared_gate"],
+                                   t["pool_q"][:N_EXPERTS], t["pool_sb"][:N_EXPERTS], t["pool_q"][N_EXPERTS],
+                                   t["pool_sb"][N_EXPERTS]))
+        xs.append(synth.activations(args.seed + 100, r, B, D_MODEL, device=dev))
+        outs.append(torch.empty((B, D_MODEL), dtype=torch.bfloat16, device=dev))
+    ws = lib.workspace(lib.moe_layer_workspace_bytes(layers[0], B), dev)
+    distinct = []
+    for r in range(R):
+        idx = lib.moe_layer_forward(layers[r], xs[r], ws=ws, want_route=True)[2]
+        distinct.append(len(set(idx.flatten().tolist())))
+    stream = torch.cuda.Stream(device=dev)
+
+    def body():
+        for r in range(R):
+            lib.moe_layer_forward(layers[r], xs[r], ws=ws, out=outs[r], stream=stream)
+
+    n_rep = max(1, args.steps // R)
+    clocks = ClockSampler(0)
+    ms = _timed_graph(torch, stream, body, n_rep, args.warmup) / R
+    clock = clocks.stop()
+    dmean = sum(distinct) / len(distinct)
+    layer_bytes = N_EXPERTS * D_MODEL * 2 + D_MODEL * 2 + (dmean + 1) * shape.expert_bytes + B * D_MODEL * 4
+    achieved = layer_bytes / (ms * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+    print(json.dumps({
+        "metric": METRIC, "value": round(B * 1000.0 / ms, 2), "unit": "tokens/s", "n_gpus": 1,
+        "steps": n_rep * R, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u4 codes; dp4a / tcgen05 f16, f32 accumulate",
+        "data": "synthetic", "config": {"workload": workload_name(args), "us_per_layer": round(ms * 1000, 3),
+                                        "distinct_experts_mean": dmean, "bytes_per_layer": int(layer_bytes)},
+        "roofline": {"bound": "hbm", "kernel": "moe_layer_forward (all launches)", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "traffic": None},
+        "clocks": clock}), flush=True)
+    return 0
+
+
+def run_gemv(args):
+    """q4_gemv (1024x4096, batch 1) per step, cycling through `ring` distinct matrices."""
+    import torch
+
+    from bit_group_quantized_gb300 import lib, synth
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    lib.load()
+    R = args.ring = max(args.ring, 64)  # 64 x 2.2 MB: the ring exceeds L2
+    rows, cols = 1024, 4096
+    mats = []
+    for r in range(R):
+        q, sb = synth.qmatrix(args.seed + r, rows, cols, 4, device=dev)
+        mats.append(lib.QMatrix(q, sb, rows, cols, 4))
+    xs = [synth.activations(args.seed, 1000 + r, 1, cols, device=dev) for r in range(R)]
+    ys = [torch.empty((1, rows), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    stream = torch.cuda.Stream(device=dev)
+
+    def body():
+        for r in range(R):
+            if args.variant == 0:
+                lib.q4_gemv(mats[r], xs[r], y=ys[r], stream=stream)
+            else:
+                lib.qgemv_variant(mats[r], xs[r], args.variant, y=ys[r], stream=stream)
+
+    n_rep = max(1, args.steps // R)
+    ms = _timed_graph(torch, stream, body, n_rep, args.warmup) / R
+    nbytes = rows * cols // 2 + rows * cols // 64 * 4 + cols * 2 + rows * 2
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+    print(json.dumps({
+        "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": 1, "steps": n_rep * R,
+        "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u4 codes", "data": "synthetic",
+        "config": {"workload": workload_name(args), "us_per_gemv": round(ms * 1000, 3), "bytes": nbytes},
+        "roofline": {"bound": "hbm", "kernel": "k_qgemv", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gbs / peak, 4), "peak_kind": peak_kind, "traffic": None}}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="stack4", choices=["stack4", "stack2"])
+    ap.add_argument("--workload", default="stack4", choices=["stack4", "stack2", "layer", "gemv"])
+    ap.add_argument("--variant", type=int, default=0, help="gemv: 0 integer (production), 1 standard, "
+                                                            "2 reordered (the page's fma form), 3 hoisted fp32")
+    ap.add_argument("--ring", type=int, default=8, help="layer/gemv: distinct weight copies cycled through")
     ap.add_argument("--layers", type=int, default=24)
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--seed", type=int, default=0)
@@ -389,6 +509,10 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "layer":
+        return run_layer(args)
+    if args.workload == "gemv":
+        return run_gemv(args)
     return run_ours(args)
 
 

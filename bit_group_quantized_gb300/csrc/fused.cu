@@ -866,6 +866,7 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
       stage_cg<BITS>(P.hk, f, K + 1, f, sth);  // the SwiGLU outputs of every CTA, through L2
       stamp(P, l, 13);
       mbar_wait(S.mC, par, ctrl, P.timeout_ns);
+      stamp(P, l, 9);
       const int nrg = (cl.n + rgf.RPP - 1) / rgf.RPP;  // row groups
       const int np = nrg * (K + 1);
       const int lp = lane % rgf.LPR, rs = lane / rgf.LPR;
@@ -887,6 +888,7 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
         if (lp == 0 && rloc < nrows) ys[k * nrows + rloc] = y;
       }
       __syncthreads();
+      stamp(P, l, 10);
       // combine in fixed order: routed experts k = 0..K-1, then the shared expert (k = K)
       float ss = 0.f;
       for (int rl = tid; rl < nrows; rl += kFThreads) {
