@@ -169,6 +169,60 @@ __device__ __forceinline__ void pack_lohi(int x0, int x1, int x2, int x3, uint32
   hi = __byte_perm(t01, t23, 0x7632);
 }
 
+// Stage code word w of token t from its kPer input values v (inactive
+// threads pass zeros). The kGW = 64/kPer threads holding the words of one
+// group must be kGW consecutive, aligned lanes of one warp, and all 32 lanes
+// must call (the group maximum and the part sum are lane shuffles).
+// lpr_shift = log2(LPR) (LPR is a power of two).
+template <int BITS>
+__device__ __forceinline__ void stage_word(const float (&v)[Geo<BITS>::kPer], bool active, int t, int w,
+                                           const RowGeo& rg, int lpr_shift, const XStage& st) {
+  using G = Geo<BITS>;
+  constexpr int kGW = kGroup / G::kPer;
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < G::kPer; ++i) m = fmaxf(m, fabsf(v[i]));
+#pragma unroll
+  for (int o = kGW / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+  int sh = 0;
+  if (m > 0.f) {
+    const int e = (int)((__float_as_uint(m) >> 23) & 0xff) - 127;  // floor(log2 m) for normal m
+    sh = 14 - e;
+    sh = sh > 126 ? 126 : (sh < -126 ? -126 : sh);
+  }
+  const float sc = exp2i(sh);
+  int X[G::kPer];
+  int xsum = 0;
+#pragma unroll
+  for (int i = 0; i < G::kPer; ++i) {
+    // rint(v*2^sh) by the 1.5*2^23 addition (|v*2^sh| < 2^15, product
+    // exact). Only +2^15 can come out (an fp32 input within an ulp below a
+    // power of two rounds up); -2^15 is representable as (hi, lo) = (-128, 0).
+    const int q = __float_as_int(fmaf(v[i], sc, 12582912.f)) - 0x4B400000;
+    X[i] = min(q, 32767);
+    xsum += X[i];
+  }
+  uint32_t lo[G::kNvec], hi[G::kNvec];
+#pragma unroll
+  for (int j = 0; j < G::kNvec; ++j)
+    pack_lohi(X[j], X[j + G::kNvec], X[j + 2 * G::kNvec], X[j + 3 * G::kNvec], lo[j], hi[j]);
+  const int p = w >> 2, c = w & 3;
+  const int it = p >> lpr_shift, lp = p & (rg.LPR - 1);
+  if (active) {
+    uint4* dst = st.chunks + ((((t * rg.NIT + it) * 4 + c) * G::kNch) << lpr_shift) + lp;
+#pragma unroll
+    for (int ch = 0; ch < G::kNch; ++ch)
+      dst[ch << lpr_shift] = make_uint4(lo[2 * ch], hi[2 * ch], lo[2 * ch + 1], hi[2 * ch + 1]);
+  }
+  // part sum over the 4 words of part p (4 consecutive lanes)
+  xsum += __shfl_xor_sync(kFull, xsum, 1);
+  xsum += __shfl_xor_sync(kFull, xsum, 2);
+  if (active && c == 0) {
+    const float inv = exp2i(-sh);
+    st.partinfo[t * rg.P + p] = make_float2(inv, (float)xsum * inv);
+  }
+}
+
 // Stage T inputs of `cols` values into shared memory, one thread per code
 // word: the 64/kPer consecutive threads of a group find the group maximum with
 // shuffles, so a single pass with no block barrier inside does the job.
@@ -177,103 +231,100 @@ __device__ __forceinline__ void pack_lohi(int x0, int x1, int x2, int x3, uint32
 template <int BITS, typename Src>
 __device__ void stage_x_int16(const Src src, int T, int cols, XStage st, int* gsh) {
   using G = Geo<BITS>;
-  constexpr int kGW = kGroup / G::kPer;  // threads (words) per group: 8 at 4 bits, 4 at 2 bits
   (void)gsh;
   const RowGeo rg = row_geo(cols, BITS);
+  const int lpr_shift = __ffs(rg.LPR) - 1;
   const int words = cols * BITS / 32;
-  const int total = T * words;  // a multiple of kGW: groups never straddle a warp
+  const int total = T * words;  // a multiple of the group's words: groups never straddle a warp
+  // t = floor(tw / words) through a float reciprocal: exact while total < 2^20
+  // (the fraction of (tw + 0.5) / words stays >= 0.5 / words from an integer)
+  const float inv_words = 1.f / (float)words;
   for (int base = 0; base < total; base += blockDim.x) {
     // uniform trip count per warp so that every shuffle sees all lanes
     const int tw = base + threadIdx.x;
     const bool active = tw < total;
-    const int t = active ? tw / words : 0, w = active ? tw - t * words : 0;
-    const int k0 = w * G::kPer;
+    const int t = active ? (int)(((float)tw + 0.5f) * inv_words) : 0;
+    const int w = active ? tw - t * words : 0;
     float v[G::kPer];
 #pragma unroll
     for (int i = 0; i < G::kPer; i += 8) {
       if (active) {
-        src.load8(t, k0 + i, v + i);
+        src.load8(t, w * G::kPer + i, v + i);
       } else {
 #pragma unroll
         for (int j = 0; j < 8; ++j) v[i + j] = 0.f;
       }
     }
-    float m = 0.f;
-#pragma unroll
-    for (int i = 0; i < G::kPer; ++i) m = fmaxf(m, fabsf(v[i]));
-#pragma unroll
-    for (int o = kGW / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-    int sh = 0;
-    if (m > 0.f) {
-      const int e = (int)((__float_as_uint(m) >> 23) & 0xff) - 127;  // floor(log2 m) for normal m
-      sh = 14 - e;
-      sh = sh > 126 ? 126 : (sh < -126 ? -126 : sh);
-    }
-    const float sc = exp2i(sh);
-    int X[G::kPer];
-    int xsum = 0;
-#pragma unroll
-    for (int i = 0; i < G::kPer; ++i) {
-      // rint(v*2^sh) by the 1.5*2^23 addition (|v*2^sh| < 2^15, product exact);
-      // the clamp only matters for fp32 inputs within an ulp of a power of
-      // two, which round up to 2^15.
-      const int q = __float_as_int(fmaf(v[i], sc, 12582912.f)) - 0x4B400000;
-      X[i] = max(-32767, min(32767, q));
-      xsum += X[i];
-    }
-    uint32_t lo[G::kNvec], hi[G::kNvec];
-#pragma unroll
-    for (int j = 0; j < G::kNvec; ++j)
-      pack_lohi(X[j], X[j + G::kNvec], X[j + 2 * G::kNvec], X[j + 3 * G::kNvec], lo[j], hi[j]);
-    const int p = w >> 2, c = w & 3;
-    const int it = p / rg.LPR, lp = p - it * rg.LPR;
-    if (active) {
-#pragma unroll
-      for (int ch = 0; ch < G::kNch; ++ch) {
-        const int slot = (((t * rg.NIT + it) * 4 + c) * G::kNch + ch) * rg.LPR + lp;
-        st.chunks[slot] = make_uint4(lo[2 * ch], hi[2 * ch], lo[2 * ch + 1], hi[2 * ch + 1]);
-      }
-    }
-    // part sum over the 4 words of part p (4 consecutive lanes)
-    xsum += __shfl_xor_sync(kFull, xsum, 1);
-    xsum += __shfl_xor_sync(kFull, xsum, 2);
-    if (active && c == 0) {
-      const float inv = exp2i(-sh);
-      st.partinfo[t * rg.P + p] = make_float2(inv, (float)xsum * inv);
-    }
+    stage_word<BITS>(v, active, t, w, rg, lpr_shift, st);
   }
   __syncthreads();
 }
 
+// Integer dot product of one part (4 code words) with its staged input chunks
+// xc[c*NCH + ch] and part info pi. Returns s*2^-sh*sum(q*X) + b*2^-sh*sum(X)
+// added to acc.
+template <int BITS>
+__device__ __forceinline__ float part_dot_x(const uint4 qv, uint32_t sbw, const uint4 (&xc)[4 * Geo<BITS>::kNch],
+                                            const float2 pi, float acc) {
+  using G = Geo<BITS>;
+  const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+  int A;
+  if (BITS == 4) {
+    // odd codes stay in the high nibbles (16x their value) and get their own
+    // accumulators, divided by 16 at the end (exact: every term is a multiple
+    // of 16); saves the shift per word.
+    int h0 = 0, h1 = 0;
+    uint32_t l0 = 0, l1 = 0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint4 x = xc[c];
+      const uint32_t v0 = qw[c] & 0x0f0f0f0fu, v1 = qw[c] & 0xf0f0f0f0u;
+      l0 = dp4a_uu(v0, x.x, l0);
+      h0 = dp4a_us(v0, x.y, h0);
+      l1 = dp4a_uu(v1, x.z, l1);
+      h1 = dp4a_us(v1, x.w, h1);
+    }
+    A = (h0 + (h1 >> 4)) * 256 + (int)(l0 + (l1 >> 4));
+  } else {
+    int acc_h = 0;
+    uint32_t acc_l = 0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+      for (int ch = 0; ch < G::kNch; ++ch) {
+        const uint4 x = xc[c * G::kNch + ch];
+        uint32_t v0 = (qw[c] >> (BITS * (2 * ch))) & G::kByteMask;
+        uint32_t v1 = (qw[c] >> (BITS * (2 * ch + 1))) & G::kByteMask;
+        acc_l = dp4a_uu(v0, x.x, acc_l);
+        acc_h = dp4a_us(v0, x.y, acc_h);
+        acc_l = dp4a_uu(v1, x.z, acc_l);
+        acc_h = dp4a_us(v1, x.w, acc_h);
+      }
+    }
+    A = acc_h * 256 + (int)acc_l;
+  }
+  float s = bf16lo(sbw), b = bf16hi(sbw);
+  return fmaf(s * pi.x, (float)A, fmaf(b, pi.y, acc));
+}
+
+// The staged input chunks of part p = it*LPR + lp of token t.
+template <int BITS>
+__device__ __forceinline__ void load_part_x(const uint4* __restrict__ chunks, int t, int it, int lp, const RowGeo& rg,
+                                            uint4 (&xc)[4 * Geo<BITS>::kNch]) {
+  const uint4* xb = chunks + ((t * rg.NIT + it) * 4 * Geo<BITS>::kNch) * rg.LPR + lp;
+#pragma unroll
+  for (int i = 0; i < 4 * Geo<BITS>::kNch; ++i) xc[i] = xb[i * rg.LPR];
+}
+
 // Integer dot product of one part (4 code words) with staged token t.
 // The part is p = it*LPR + lp (iteration it of lane lp of the row).
-// Returns s*2^-sh*sum(q*X) + b*2^-sh*sum(X) added to acc.
 template <int BITS>
 __device__ __forceinline__ float part_dot_int16(const uint4 qv, uint32_t sbw, const uint4* __restrict__ chunks,
                                                 const float2* __restrict__ partinfo, int t, int it, int lp,
                                                 const RowGeo& rg, float acc) {
-  using G = Geo<BITS>;
-  int acc_h = 0;
-  uint32_t acc_l = 0;
-  const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
-  const uint4* xb = chunks + ((t * rg.NIT + it) * 4 * G::kNch) * rg.LPR + lp;
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-#pragma unroll
-    for (int ch = 0; ch < G::kNch; ++ch) {
-      uint4 xc = xb[(c * G::kNch + ch) * rg.LPR];
-      uint32_t v0 = (qw[c] >> (BITS * (2 * ch))) & G::kByteMask;
-      uint32_t v1 = (qw[c] >> (BITS * (2 * ch + 1))) & G::kByteMask;
-      acc_l = dp4a_uu(v0, xc.x, acc_l);
-      acc_h = dp4a_us(v0, xc.y, acc_h);
-      acc_l = dp4a_uu(v1, xc.z, acc_l);
-      acc_h = dp4a_us(v1, xc.w, acc_h);
-    }
-  }
-  float2 pi = partinfo[t * rg.P + it * rg.LPR + lp];
-  int A = acc_h * 256 + (int)acc_l;
-  float s = bf16lo(sbw), b = bf16hi(sbw);
-  return fmaf(s * pi.x, (float)A, fmaf(b, pi.y, acc));
+  uint4 xc[4 * Geo<BITS>::kNch];
+  load_part_x<BITS>(chunks, t, it, lp, rg, xc);
+  return part_dot_x<BITS>(qv, sbw, xc, partinfo[t * rg.P + it * rg.LPR + lp], acc);
 }
 
 // Group index of part p.
@@ -286,6 +337,59 @@ __device__ __forceinline__ int part_group(int p) {
 __device__ __forceinline__ float row_reduce(float v, int LPR) {
   for (int o = LPR >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
   return v;
+}
+
+// row_reduce of four values at once (LPR >= 4), the same scheme as
+// row_reduce8 below with two halving stages. Returns the sum of value
+// u = 2*[lane & LPR/2] + [lane & LPR/4].
+__device__ __forceinline__ float row_reduce4(float (&v)[4], int LPR, int lane) {
+  int o = LPR >> 1;
+  bool up = (lane & o) != 0;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const float keep = up ? v[j + 2] : v[j], send = up ? v[j] : v[j + 2];
+    v[j] = keep + __shfl_xor_sync(kFull, send, o);
+  }
+  o >>= 1;
+  up = (lane & o) != 0;
+  {
+    const float keep = up ? v[1] : v[0], send = up ? v[0] : v[1];
+    v[0] = keep + __shfl_xor_sync(kFull, send, o);
+  }
+  for (o >>= 1; o > 0; o >>= 1) v[0] += __shfl_xor_sync(kFull, v[0], o);
+  return v[0];
+}
+
+// row_reduce of eight values at once (LPR >= 8). Each of the first three
+// stages halves the values a lane holds: the lane keeps one half, sends the
+// other to its partner and adds the partner's copy of the half it kept. Every
+// addition pairs the same two lanes' partial sums as row_reduce does, in the
+// same order, so each result is bit-identical to row_reduce(v[u], LPR).
+// Returns the sum of value u = 4*[lane & LPR/2] + 2*[lane & LPR/4] +
+// [lane & LPR/8] (each bracket 0 or 1), held by every lane with those bits.
+__device__ __forceinline__ float row_reduce8(float (&v)[8], int LPR, int lane) {
+  int o = LPR >> 1;
+  bool up = (lane & o) != 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float keep = up ? v[j + 4] : v[j], send = up ? v[j] : v[j + 4];
+    v[j] = keep + __shfl_xor_sync(kFull, send, o);
+  }
+  o >>= 1;
+  up = (lane & o) != 0;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const float keep = up ? v[j + 2] : v[j], send = up ? v[j] : v[j + 2];
+    v[j] = keep + __shfl_xor_sync(kFull, send, o);
+  }
+  o >>= 1;
+  up = (lane & o) != 0;
+  {
+    const float keep = up ? v[1] : v[0], send = up ? v[0] : v[1];
+    v[0] = keep + __shfl_xor_sync(kFull, send, o);
+  }
+  for (o >>= 1; o > 0; o >>= 1) v[0] += __shfl_xor_sync(kFull, v[0], o);
+  return v[0];
 }
 
 }  // namespace bgq

@@ -10,22 +10,25 @@
 // grid-wide counters:
 //
 //   A  RMSNorm of the residual (stack mode), router rows (bf16) and the shared
-//      expert's gate/up rows; the last CTA to finish its router rows selects
-//      the top-K experts and publishes them (nobody waits for it here);
-//   B  the selected experts' gate/up rows (after the selection);
-//   C  the down rows of the K selected experts and of the shared expert,
-//      combined per output row in a fixed order (after every h is written),
-//      plus the residual add in stack mode.
+//      expert's gate/up rows; every CTA publishes its logits;
+//   B  after the logits counter, every CTA selects the same top-K experts from
+//      all logits and computes its share of their gate/up rows;
+//   C  after the SwiGLU counter, every CTA computes its output rows: the down
+//      rows of the K selected experts and of the shared expert, combined in a
+//      fixed order, plus the residual add in stack mode.
 //
 // Data movement. Each CTA owns a fixed slice of every phase. Its router rows,
-// shared gate/up rows (phase A) and selected-expert gate/up rows (phase B)
-// are streamed into shared memory with bulk async copies (cp.async.bulk, one
-// mbarrier per work unit), all issued the moment they are known: phase B's
-// right after the selection, the next layer's phase A right after it, so HBM
-// keeps streaming while the grid waits at its counters. Phase C's down rows
-// (of experts known after the selection) are prefetched into L2 at that same
-// moment and read from L2 into registers. Consumers start on a unit as soon
-// as its own mbarrier completes.
+// shared gate/up rows (phase A), selected-expert gate/up rows (phase B) and
+// down rows (phase C) are streamed into shared memory with bulk async copies
+// (cp.async.bulk, one mbarrier per work unit), each issued the moment it is
+// known and its buffer is free: phase B's right after the selection, phase C's
+// and the next layer's phase A's right after phase B, so HBM keeps streaming
+// while the grid waits at its counters. Consumers start on a unit as soon as
+// its own mbarrier completes.
+//
+// (A variant that exchanged logits, SwiGLU outputs and the residual as
+// 64-bit {value, tag} words polled by every CTA, with no counters, measured
+// 29.5 us per layer against 24.8 us for this design on the 24-layer stack.)
 //
 // Every wait is bounded (an iteration count and %globaltimer). On expiry the
 // CTA sets BGQ_ERR_TIMEOUT in the status word and an abort flag that makes
@@ -247,53 +250,62 @@ __device__ __forceinline__ Chunk chunk_of(int u, int b, int e, int seg) {
 }
 
 // --------------------------------------------------------------- compute helpers
-// gate and up rows of one unit (in shared memory) against staged input 0:
-// two dot products that share every x chunk. Lane l reads part it*32 + l.
+// Gate and up rows of two units (in shared memory) against staged input 0:
+// four dot products that share every x chunk load. Unit i is at position
+// p_i of a chunk of n_i units starting at c_i. Lane l reads part it*32 + l.
+// Returns silu(gate) * up of unit 0 in lane 0 and of unit 1 in lane 16.
 template <int BITS>
-__device__ __noinline__ void unit_gateup(const unsigned char* cbase, int n, int pos, const XStage st, const FGeo g,
-                                         int lane, float& gv, float& uv) {
+__device__ __noinline__ float units_gateup2(const unsigned char* c0, int n0, int p0, const unsigned char* c1, int n1,
+                                            int p1, const XStage st, const FGeo g, int lane) {
   using G = Geo<BITS>;
   const int wq = g.wpr * 4, ws = g.gpr * 4;
-  const uint4* qg = reinterpret_cast<const uint4*>(cbase + pos * wq);
-  const uint4* qu = reinterpret_cast<const uint4*>(cbase + (n + pos) * wq);
-  const uint32_t* sg = reinterpret_cast<const uint32_t*>(cbase + 2 * n * wq + pos * ws);
-  const uint32_t* su = reinterpret_cast<const uint32_t*>(cbase + 2 * n * wq + (n + pos) * ws);
-  float ag = 0.f, au = 0.f;
+  const uint4* qg0 = reinterpret_cast<const uint4*>(c0 + p0 * wq);
+  const uint4* qu0 = reinterpret_cast<const uint4*>(c0 + (n0 + p0) * wq);
+  const uint32_t* sg0 = reinterpret_cast<const uint32_t*>(c0 + 2 * n0 * wq + p0 * ws);
+  const uint32_t* su0 = reinterpret_cast<const uint32_t*>(c0 + 2 * n0 * wq + (n0 + p0) * ws);
+  const uint4* qg1 = reinterpret_cast<const uint4*>(c1 + p1 * wq);
+  const uint4* qu1 = reinterpret_cast<const uint4*>(c1 + (n1 + p1) * wq);
+  const uint32_t* sg1 = reinterpret_cast<const uint32_t*>(c1 + 2 * n1 * wq + p1 * ws);
+  const uint32_t* su1 = reinterpret_cast<const uint32_t*>(c1 + 2 * n1 * wq + (n1 + p1) * ws);
+  const RowGeo rg{g.nit_d * 32, 32, 1, g.nit_d};
+  float v[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
-  for (int it = 0; it < 4; ++it) {
-    if (it < g.nit_d) {
-      const int p = it * 32 + lane;
-      const uint4 wg = qg[p], wu = qu[p];
-      const uint32_t sbg = sg[part_group<BITS>(p)], sbu = su[part_group<BITS>(p)];
-      const uint32_t gw[4] = {wg.x, wg.y, wg.z, wg.w}, uw[4] = {wu.x, wu.y, wu.z, wu.w};
-      const uint4* xb = st.chunks + (it * 4 * G::kNch) * 32 + lane;
-      int hg = 0, hu = 0;
-      uint32_t lg = 0, lu = 0;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-#pragma unroll
-        for (int ch = 0; ch < G::kNch; ++ch) {
-          const uint4 xc = xb[(c * G::kNch + ch) * 32];
-          const int s0 = BITS * (2 * ch), s1 = BITS * (2 * ch + 1);
-          const uint32_t g0 = (gw[c] >> s0) & G::kByteMask, g1 = (gw[c] >> s1) & G::kByteMask;
-          const uint32_t u0 = (uw[c] >> s0) & G::kByteMask, u1 = (uw[c] >> s1) & G::kByteMask;
-          lg = dp4a_uu(g0, xc.x, lg);
-          hg = dp4a_us(g0, xc.y, hg);
-          lg = dp4a_uu(g1, xc.z, lg);
-          hg = dp4a_us(g1, xc.w, hg);
-          lu = dp4a_uu(u0, xc.x, lu);
-          hu = dp4a_us(u0, xc.y, hu);
-          lu = dp4a_uu(u1, xc.z, lu);
-          hu = dp4a_us(u1, xc.w, hu);
-        }
-      }
-      const float2 pi = st.partinfo[p];
-      ag = fmaf(bf16lo(sbg) * pi.x, (float)(hg * 256 + (int)lg), fmaf(bf16hi(sbg), pi.y, ag));
-      au = fmaf(bf16lo(sbu) * pi.x, (float)(hu * 256 + (int)lu), fmaf(bf16hi(sbu), pi.y, au));
-    }
+  for (int it = 0; it < g.nit_d; ++it) {
+    const int p = it * 32 + lane, pg = part_group<BITS>(p);
+    const uint4 a = qg0[p], b = qu0[p], c = qg1[p], d = qu1[p];
+    const uint32_t sa = sg0[pg], sb = su0[pg], sc = sg1[pg], sd = su1[pg];
+    uint4 xc[4 * G::kNch];
+    load_part_x<BITS>(st.chunks, 0, it, lane, rg, xc);
+    const float2 pi = st.partinfo[p];
+    v[0] = part_dot_x<BITS>(a, sa, xc, pi, v[0]);
+    v[1] = part_dot_x<BITS>(b, sb, xc, pi, v[1]);
+    v[2] = part_dot_x<BITS>(c, sc, xc, pi, v[2]);
+    v[3] = part_dot_x<BITS>(d, sd, xc, pi, v[3]);
   }
-  gv = warp_sum(ag);
-  uv = warp_sum(au);
+  // lanes 0-7: gate 0, 8-15: up 0, 16-23: gate 1, 24-31: up 1 (bit-identical to warp_sum)
+  const float r = row_reduce4(v, 32, lane);
+  const float up = __shfl_down_sync(kFull, r, 8);
+  return r / (1.f + expf(-r)) * up;
+}
+
+// Units [b, e) of a phase (chunks of kCH units that never cross a multiple of
+// seg, chunk i complete on mbars[i]), two per warp: exchange word hk_dst[j] =
+// silu(gate) * up of unit b + j. An odd last unit is computed twice, written once.
+template <int BITS>
+__device__ __forceinline__ void run_units(const unsigned char* base, int b, int e, int seg, uint64_t* mbars,
+                                          uint32_t par, Ctrl* ctrl, long long timeout_ns, const XStage& st,
+                                          const FGeo& g, float* hk_dst, int warp, int lane) {
+  const int nu = e - b;
+  for (int j0 = 2 * warp; j0 < nu; j0 += 2 * kFWarps) {
+    const int j1 = min(j0 + 1, nu - 1);
+    const Chunk c0 = chunk_of(b + j0, b, e, seg), c1 = chunk_of(b + j1, b, e, seg);
+    mbar_wait(&mbars[c0.idx], par, ctrl, timeout_ns);
+    if (c1.idx != c0.idx) mbar_wait(&mbars[c1.idx], par, ctrl, timeout_ns);
+    const float h = units_gateup2<BITS>(base + (size_t)(c0.start - b) * g.unit, c0.n, b + j0 - c0.start,
+                                        base + (size_t)(c1.start - b) * g.unit, c1.n, b + j1 - c1.start, st, g, lane);
+    if (lane == 0) hk_dst[j0] = h;
+    if (lane == 16 && j1 != j0) hk_dst[j1] = h;
+  }
 }
 
 // A slice (<= 1024 columns) of a bf16 router row in shared memory dotted with
@@ -341,32 +353,19 @@ __device__ __forceinline__ int redux_min(int v) {
 //   Each warp takes the top K of its 64 logits (K rounds of redux.sync on an
 //   order-preserving integer key, ties to the lowest index), then warp 0
 //   merges the 16 x K candidates the same way.
-//   weights: the softmax denominator is summed in the router kernel's order
-//   (lane j adds elements j, j+32, ... in turn, then a butterfly), so the
-//   weights are bit-identical to the multi-kernel path's.
-// Writes s_idx[0..K), s_w[0..K) and s_w[K] = gamma. `scratch` holds E floats
-// plus 16*8 (key, index) pairs.
-__device__ void block_topk(const float* lg, float* scratch, int E, int K, bool has_gate, float* red, int* red_i,
-                           int* s_idx, float* s_w) {
+//   weights: softmax over all E logits followed by renormalisation over the
+//   selected K equals a softmax over the selected logits alone (the full
+//   denominator cancels), so w_k = exp(l_k - l_0) / sum_j exp(l_j - l_0) with
+//   l_0 the largest logit, summed in k order exactly as the router kernel does.
+// Writes s_idx[0..K), s_w[0..K) and s_w[K] = gamma. `cand` holds 2*16*8 ints.
+__device__ void block_topk(const float* lg, int* cand, int E, int K, bool has_gate, int* s_idx, float* s_w) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int* cand_k = reinterpret_cast<int*>(scratch + E);  // [16][8] keys
-  int* cand_i = cand_k + kFWarps * 8;                 // [16][8] indices
+  int* cand_k = cand;                  // [16][8] keys
+  int* cand_i = cand_k + kFWarps * 8;  // [16][8] indices
   // this warp's elements: e0 = warp*64 + lane, e1 = e0 + 32
   const int e0 = warp * 64 + lane, e1 = e0 + 32;
   int k0 = e0 < E ? fkey(lg[e0]) : INT_MIN;
   int k1 = e1 < E ? fkey(lg[e1]) : INT_MIN;
-  // max for the softmax, and exp(l - max) of every logit
-  {
-    int m = redux_max(max(k0, k1));
-    if (lane == 0) red_i[warp] = m;
-  }
-  __syncthreads();
-  int mk = red_i[0];
-  for (int w = 1; w < kFWarps; ++w) mk = max(mk, red_i[w]);
-  const float m = __int_as_float(mk >= 0 ? mk : mk ^ 0x7fffffff);
-  if (e0 < E) scratch[e0] = expf(lg[e0] - m);
-  if (e1 < E) scratch[e1] = expf(lg[e1] - m);
-  // per-warp top K
   for (int k = 0; k < K; ++k) {
     const int best = redux_max(max(k0, k1));
     const int i0 = (k0 == best && e0 < E) ? e0 : INT_MAX;
@@ -380,16 +379,17 @@ __device__ void block_topk(const float* lg, float* scratch, int E, int K, bool h
     if (bi == e1) k1 = INT_MIN;
   }
   __syncthreads();
-  // merge: lane j of warp 0 holds candidates j*... (16 warps x K <= 128 entries, 4 per lane)
+  // merge: lane j of warp 0 holds candidate slots j, j+32, j+64, j+96 (slot = w*8 + k)
   if (warp == 0) {
     int ck[4], ci[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int c = j * 32 + lane;  // candidate slot c = w*8 + k
+      const int c = j * 32 + lane;
       const bool ok = c < kFWarps * 8 && (c & 7) < K;
       ck[j] = ok ? cand_k[c] : INT_MIN;
       ci[j] = ok ? cand_i[c] : INT_MAX;
     }
+    int mine = 0;
     for (int k = 0; k < K; ++k) {
       int lb = INT_MIN;
 #pragma unroll
@@ -403,18 +403,15 @@ __device__ void block_topk(const float* lg, float* scratch, int E, int K, bool h
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         if (ci[j] == bi) ck[j] = INT_MIN;
-      if (lane == 0) s_idx[k] = bi;
+      if (lane == k) mine = bi;
     }
-  }
-  __syncthreads();
-  if (warp == 0) {
-    float ssum = 0.f;
-    for (int i = 0; i * 32 + lane < E; ++i) ssum += scratch[i * 32 + lane];
-    ssum = warp_sum(ssum);
+    if (lane < K) s_idx[lane] = mine;
+    __syncwarp();
     if (lane == 0) {
       float p[8], ps = 0.f;
+      const float l0 = lg[s_idx[0]];
       for (int k = 0; k < K; ++k) {
-        p[k] = scratch[s_idx[k]] / ssum;
+        p[k] = expf(lg[s_idx[k]] - l0);
         ps += p[k];
       }
       for (int k = 0; k < K; ++k) s_w[k] = p[k] / ps;
@@ -422,7 +419,6 @@ __device__ void block_topk(const float* lg, float* scratch, int E, int K, bool h
     }
   }
   __syncthreads();
-  (void)red;
 }
 
 // x staging from fp32 values in shared memory (the layer input).
@@ -634,6 +630,73 @@ __device__ void issue_C(const FusedParams& P, const FGeo& g, int l, const FSmem&
   if (lane == 0) *S.cpar = l & 1;
 }
 
+// Phase C's dot products: rows [0, cl.n) of the down matrices of slots
+// 0..K (staged SwiGLU outputs of token k = slot k). The (slot, row group)
+// work is cut into chunks of at most kCU row groups of one slot (as few
+// chunks per slot as that allows, of near-equal size). A warp loads the
+// slot's staged chunks for its part once, runs the chunk's rows as
+// independent chains and reduces them together; ys[k * cl.n + r] = row r of
+// slot k.
+constexpr int kCU = 9;
+
+template <int BITS>
+__device__ __forceinline__ void down_rows(const unsigned char* buf, const CLayout& cl, int K, const XStage& sth,
+                                          const RowGeo& rgf, float* ys, int warp, int lane) {
+  using G = Geo<BITS>;
+  const int nrows = cl.n;
+  const int nrg = (nrows + rgf.RPP - 1) / rgf.RPP;
+  const int cpk = (nrg + kCU - 1) / kCU;  // chunks per slot
+  const int nch = cpk * (K + 1);
+  const int lp = lane % rgf.LPR, rs = lane / rgf.LPR;
+  const int rstep = rgf.RPP * cl.wqf, sstep = rgf.RPP * cl.wsf;
+#pragma unroll 1
+  for (int c = warp; c < nch; c += kFWarps) {
+    const int k = c / cpk, ci = c - k * cpk;
+    const int g0 = nrg * ci / cpk, g1 = nrg * (ci + 1) / cpk;  // at most kCU row groups
+    uint4 xc[4 * G::kNch];
+    load_part_x<BITS>(sth.chunks, k, 0, lp, rgf, xc);
+    const float2 pi = sth.partinfo[k * rgf.P + lp];
+    const int r0 = g0 * rgf.RPP + rs;
+    const unsigned char* qb = buf + cl.q(k) + (size_t)r0 * cl.wqf + lp * 16;
+    const unsigned char* sbb = buf + cl.sb(K, k) + (size_t)r0 * cl.wsf + part_group<BITS>(lp) * 4;
+    float v[kCU];
+#pragma unroll
+    for (int u = 0; u < kCU; ++u) {
+      v[u] = 0.f;
+      if (g0 + u < g1 && r0 + u * rgf.RPP < nrows) {
+        const uint4 q = *reinterpret_cast<const uint4*>(qb + u * rstep);
+        const uint32_t sbw = *reinterpret_cast<const uint32_t*>(sbb + u * sstep);
+        v[u] = part_dot_x<BITS>(q, sbw, xc, pi, 0.f);
+      }
+    }
+    if (rgf.LPR >= 8) {
+      float w8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) w8[u] = v[u];
+      const float y = row_reduce8(w8, rgf.LPR, lane);
+      const int o1 = rgf.LPR >> 1, o2 = o1 >> 1, o3 = o2 >> 1;
+      if ((lp & (o3 - 1)) == 0) {
+        const int u = ((lp & o1) ? 4 : 0) + ((lp & o2) ? 2 : 0) + ((lp & o3) ? 1 : 0);
+        const int rloc = r0 + u * rgf.RPP;
+        if (g0 + u < g1 && rloc < nrows) ys[k * nrows + rloc] = y;
+      }
+#pragma unroll
+      for (int u = 8; u < kCU; ++u) {
+        const float y2 = row_reduce(v[u], rgf.LPR);
+        const int rloc = r0 + u * rgf.RPP;
+        if (lp == 0 && g0 + u < g1 && rloc < nrows) ys[k * nrows + rloc] = y2;
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < kCU; ++u) {
+        const float y = row_reduce(v[u], rgf.LPR);
+        const int rloc = r0 + u * rgf.RPP;
+        if (lp == 0 && g0 + u < g1 && rloc < nrows) ys[k * nrows + rloc] = y;
+      }
+    }
+  }
+}
+
 // --------------------------------------------------------------- the kernel
 template <int BITS>
 __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_constant__ FusedParams P) {
@@ -803,14 +866,8 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
     {
       int b, e;
       s1_range(g, f, b, e);
-      unsigned char* base = S.bufA + s1_base(g, d);
-      for (int j = warp; j < e - b; j += kFWarps) {
-        const Chunk ch = chunk_of(b + j, b, e, f);
-        mbar_wait(&S.mS[ch.idx], par, ctrl, P.timeout_ns);
-        float gv, uv;
-        unit_gateup<BITS>(base + (size_t)(ch.start - b) * g.unit, ch.n, b + j - ch.start, sta, g, lane, gv, uv);
-        if (lane == 0) P.hk[(size_t)K * f + b + j] = gv / (1.f + expf(-gv)) * uv;
-      }
+      run_units<BITS>(S.bufA + s1_base(g, d), b, e, f, S.mS, par, ctrl, P.timeout_ns, sta, g,
+                      P.hk + (size_t)K * f + b, warp, lane);
     }
 
     // ---------------- selection: every CTA selects from the complete logits
@@ -821,7 +878,7 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
       float* lg_s = reinterpret_cast<float*>(S.bufB);  // bufB is free until the B copies
       for (int e = tid; e <= E; e += kFThreads) lg_s[e] = __ldcg(P.logits + e);
       __syncthreads();
-      block_topk(lg_s, lg_s + E + 1, E, K, has_gate, red, reinterpret_cast<int*>(red + kFWarps), s_idx, s_w);
+      block_topk(lg_s, reinterpret_cast<int*>(lg_s + ((E + 4) & ~3)), E, K, has_gate, s_idx, s_w);
       stamp(P, l, 11);
       if (blockIdx.x == 0 && tid < K) {
         if (P.idx_out) P.idx_out[l * K + tid] = s_idx[tid];
@@ -835,13 +892,7 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
     {
       int b, e;
       fsplit(K * f, blockIdx.x, g.nC, b, e);
-      for (int j = warp; j < e - b; j += kFWarps) {
-        const Chunk ch = chunk_of(b + j, b, e, f);
-        mbar_wait(&S.mB[ch.idx], par, ctrl, P.timeout_ns);
-        float gv, uv;
-        unit_gateup<BITS>(S.bufB + (size_t)(ch.start - b) * g.unit, ch.n, b + j - ch.start, sta, g, lane, gv, uv);
-        if (lane == 0) P.hk[b + j] = gv / (1.f + expf(-gv)) * uv;  // unit u = k*f + row
-      }
+      run_units<BITS>(S.bufB, b, e, f, S.mB, par, ctrl, P.timeout_ns, sta, g, P.hk + b, warp, lane);
     }
     stamp(P, l, 6);
     // Phase C: this CTA's output rows [c_b, c_e). Once every warp is done with
@@ -867,26 +918,9 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
       stamp(P, l, 13);
       mbar_wait(S.mC, par, ctrl, P.timeout_ns);
       stamp(P, l, 9);
-      const int nrg = (cl.n + rgf.RPP - 1) / rgf.RPP;  // row groups
-      const int np = nrg * (K + 1);
-      const int lp = lane % rgf.LPR, rs = lane / rgf.LPR;
       float* ys = reinterpret_cast<float*>(S.bufB + cl.ys(K));
+      down_rows<BITS>(S.bufB, cl, K, sth, rgf, ys, warp, lane);
       const int nrows = cl.n;
-#pragma unroll 1
-      for (int pair = warp; pair < np; pair += kFWarps) {
-        const int k = pair / nrg, rgi = pair - k * nrg;
-        const int rloc = rgi * rgf.RPP + rs;
-        uint4 q = make_uint4(0, 0, 0, 0);
-        uint32_t sbw = 0;
-        if (rloc < nrows) {
-          q = *reinterpret_cast<const uint4*>(S.bufB + cl.q(k) + (size_t)rloc * cl.wqf + lp * 16);
-          sbw = *reinterpret_cast<const uint32_t*>(S.bufB + cl.sb(K, k) + (size_t)rloc * cl.wsf +
-                                                   part_group<BITS>(lp) * 4);
-        }
-        const float acc = part_dot_int16<BITS>(q, sbw, sth.chunks, sth.partinfo, k, 0, lp, rgf, 0.f);
-        const float y = row_reduce(acc, rgf.LPR);
-        if (lp == 0 && rloc < nrows) ys[k * nrows + rloc] = y;
-      }
       __syncthreads();
       stamp(P, l, 10);
       // combine in fixed order: routed experts k = 0..K-1, then the shared expert (k = K)

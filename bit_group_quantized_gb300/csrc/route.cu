@@ -6,9 +6,11 @@
 // is the tail of the router kernel: every CTA computes a slice of the logits,
 // and the last CTA to finish (atomic counter, no waiting) selects the experts.
 //
-//   l[e] = router[e] . x (fp32), p = softmax(l) (fp32, max-subtracted),
-//   top-K by logit, ties to the lower index, largest first,
-//   w_k = p[idx_k] / sum_j p[idx_j],  gamma = sigmoid(shared_gate . x).
+//   l[e] = router[e] . x (fp32), top-K by logit, ties to the lower index,
+//   largest first, w_k = p[idx_k] / sum_j p[idx_j] with p = softmax(l), which
+//   is computed as exp(l_k - l_max) / sum_j exp(l_j - l_max) over the selected
+//   logits (the full softmax denominator cancels),
+//   gamma = sigmoid(shared_gate . x).
 //
 // With a plan pointer, the last CTA also groups the (token, slot) pairs by
 // expert (counting sort, stable by token then slot) into grouped-GEMV tasks of
@@ -57,16 +59,6 @@ __device__ void topk_one_token(const float* __restrict__ lg, int E, int K, float
     v[i] = (i < per && e < E) ? __ldcg(lg + e) : -INFINITY;
     if (logits_out && i < per && e < E) logits_out[(size_t)t * E + e] = v[i];
   }
-  // softmax denominator over all experts
-  float m = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < kMaxExperts / 32; ++i) m = fmaxf(m, v[i]);
-  m = warp_max(m);
-  float ssum = 0.f;
-#pragma unroll
-  for (int i = 0; i < kMaxExperts / 32; ++i)
-    if (i < per && i * 32 + lane < E) ssum += expf(v[i] - m);
-  ssum = warp_sum(ssum);
   // K rounds of arg-max; (value, index) order: larger value, then lower index.
   unsigned taken = 0u;
   int sel[kMaxTopK];
@@ -97,9 +89,12 @@ __device__ void topk_one_token(const float* __restrict__ lg, int E, int K, float
     if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
   }
   if (lane == 0) {
+    // softmax over all E followed by renormalisation over the K selected is a
+    // softmax over the selected logits (the full denominator cancels); selv[0]
+    // is the largest logit.
     float p[kMaxTopK], ps = 0.f;
     for (int k = 0; k < K; ++k) {
-      p[k] = expf(selv[k] - m) / ssum;
+      p[k] = expf(selv[k] - selv[0]);
       ps += p[k];
     }
     for (int k = 0; k < K; ++k) {
