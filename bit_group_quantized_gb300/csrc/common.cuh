@@ -151,16 +151,6 @@ struct GatherSrc {  // token t at base + off[t] (off in shared memory)
   __device__ void load8(int t, int k0, float* v) const { load8_from(base + off[t] + k0, v); }
 };
 
-struct CgSrc {  // fp32 vectors written by other CTAs of the same launch: read through L2
-  const float* x;
-  int ld;
-  __device__ void load8(int t, int k0, float* v) const {
-    const float4* p = reinterpret_cast<const float4*>(x + (size_t)t * ld + k0);
-    const float4 a = __ldcg(p), b = __ldcg(p + 1);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-  }
-};
-
 // Pack the low bytes and the second bytes of four int16-range values.
 __device__ __forceinline__ void pack_lohi(int x0, int x1, int x2, int x3, uint32_t& lo, uint32_t& hi) {
   const uint32_t t01 = __byte_perm((uint32_t)x0, (uint32_t)x1, 0x5140);  // x0.b0 x1.b0 x0.b1 x1.b1

@@ -47,7 +47,7 @@ constexpr int kFThreads = 512;
 constexpr int kFWarps = kFThreads / 32;
 constexpr int kMaxS1 = 16;   // shared gate/up units per CTA
 constexpr int kMaxB = 32;    // selected gate/up units per CTA
-constexpr int kCH = 4;       // units per bulk-copy chunk (one mbarrier per chunk)
+constexpr int kCH = 14;      // units per bulk-copy chunk (one mbarrier per chunk)
 constexpr int kMaxSC = 4;    // shared gate/up chunks per CTA
 constexpr int kMaxBC = 16;   // selected gate/up chunks per CTA
 constexpr long long kMaxSpin = 1ll << 26;
@@ -170,7 +170,9 @@ __host__ __device__ inline FGeo fgeo(int nC, int d, int f, int E, int K, int bit
   g.bufB = g.nBmax * g.unit;
   // phase C reuses bufB for its down rows (K+1 experts x the CTA's rows) and partial results
   const int rows_c = (d + nC - 1) / nC;
-  const int c_bytes = (K + 1) * rows_c * (f * bits / 8 + (f / kGroup) * 4) + (K + 1) * rows_c * 4 + 16;
+  // ... followed by the SwiGLU outputs gathered as fp32 before staging
+  const int c_bytes = (K + 1) * rows_c * (f * bits / 8 + (f / kGroup) * 4) + (K + 1) * rows_c * 4 + 32 +
+                      (K + 1) * f * 4;
   if (g.bufB < c_bytes) g.bufB = c_bytes;
   return g;
 }
@@ -426,12 +428,6 @@ template <int BITS>
 __device__ __noinline__ void stage_f32(const float* src, int ld, int T, int cols, const XStage st) {
   stage_x_int16<BITS>(StridedSrc<float>{src, ld}, T, cols, st, nullptr);
 }
-// x staging from fp32 values other CTAs wrote to global memory (the SwiGLU outputs).
-template <int BITS>
-__device__ __noinline__ void stage_cg(const float* src, int ld, int T, int cols, const XStage st) {
-  stage_x_int16<BITS>(CgSrc{src, ld}, T, cols, st, nullptr);
-}
-
 // Thread 0 stamps event ev of layer l (no-op without a trace buffer).
 __device__ __forceinline__ void stamp(const FusedParams& P, int l, int ev) {
   if (P.trace && threadIdx.x == 0)
@@ -514,8 +510,8 @@ __device__ void cta_arrive(int* p) {
   if (threadIdx.x == 0) asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p) : "memory");
 }
 
-// Warp 0: issue layer l's phase-A copies (router rows by lane 0, shared
-// gate/up chunk i by lane i).
+// Warp 0: issue layer l's phase-A copies (router rows by lane 0, the RMSNorm
+// weight by lane 1, then the shared gate/up chunks).
 __device__ void issue_A(const FusedParams& P, const FGeo& g, int l, const FSmem& S) {
   const FusedLayer& L = P.layers[l];
   const int d = P.d, E = P.E, f = P.f, lane = threadIdx.x & 31;
@@ -527,11 +523,12 @@ __device__ void issue_A(const FusedParams& P, const FGeo& g, int l, const FSmem&
     const int nrows = E + (L.sgate ? 1 : 0);
     if (r1 > nrows) r1 = nrows;
     const int nr = r1 > r0 ? r1 - r0 : 0;
+    uint64_t* m = S.mR;
     mbar_expect_tx(S.mR, (uint32_t)nr * 2 * d);
     if (nr > 0) {
       const int nE = (r1 < E ? r1 : E) - r0;  // rows taken from the router matrix
-      if (nE > 0) bulk_g2s(S.bufA, L.router + (size_t)r0 * d, (uint32_t)nE * 2 * d, S.mR);
-      if (nr > nE) bulk_g2s(S.bufA + (size_t)nE * 2 * d, L.sgate, 2 * d, S.mR);
+      if (nE > 0) bulk_g2s(S.bufA, L.router + (size_t)r0 * d, (uint32_t)nE * 2 * d, m);
+      if (nr > nE) bulk_g2s(S.bufA + (size_t)nE * 2 * d, L.sgate, 2 * d, m);
     }
   }
   if (lane == 1) {  // RMSNorm weight of the layer (stack mode)
@@ -539,54 +536,60 @@ __device__ void issue_A(const FusedParams& P, const FGeo& g, int l, const FSmem&
     mbar_expect_tx(S.mRho, has ? (uint32_t)d * 2 : 0u);
     if (has) bulk_g2s(S.rho, L.rho, d * 2, S.mRho);
   }
-  if (lane < kMaxSC) {
+  // shared gate/up chunks, one piece per lane (see issue_B)
+  static_assert(kMaxSC <= 8, "one instruction issues up to 8 chunks");
+  {
     int b, e;
     s1_range(g, f, b, e);
-    const Chunk ch = chunk_at(lane, b, e, f);
-    uint64_t* m = &S.mS[lane];
-    if (ch.n > 0) {
+    const int c = lane >> 2, piece = lane & 3;
+    const Chunk ch = chunk_at(c < kMaxSC ? c : 0, b, e, f);
+    uint64_t* m = &S.mS[c < kMaxSC ? c : 0];
+    if (c < kMaxSC && piece == 0) mbar_expect_tx(m, (uint32_t)ch.n * g.unit);  // 0: completes empty
+    __syncwarp();
+    if (c < kMaxSC && ch.n > 0) {
       const int wq = g.wpr * 4, ws = g.gpr * 4;
       unsigned char* cb = S.bufA + s1_base(g, d) + (size_t)(ch.start - b) * g.unit;
-      const uint32_t* gq = L.shared_q + (size_t)ch.start * g.wpr;
-      const uint32_t* uq = L.shared_q + (size_t)(f + ch.start) * g.wpr;
-      const uint32_t* gs = reinterpret_cast<const uint32_t*>(L.shared_sb) + (size_t)ch.start * g.gpr;
-      const uint32_t* us = reinterpret_cast<const uint32_t*>(L.shared_sb) + (size_t)(f + ch.start) * g.gpr;
-      mbar_expect_tx(m, (uint32_t)ch.n * g.unit);
-      bulk_g2s(cb, gq, ch.n * wq, m);
-      bulk_g2s(cb + ch.n * wq, uq, ch.n * wq, m);
-      bulk_g2s(cb + 2 * ch.n * wq, gs, ch.n * ws, m);
-      bulk_g2s(cb + 2 * ch.n * wq + ch.n * ws, us, ch.n * ws, m);
-    } else {
-      mbar_expect_tx(m, 0);  // every barrier completes one phase per layer
+      const int row = (piece & 1) ? f + ch.start : ch.start;  // gate rows, then up rows
+      if (piece < 2)
+        bulk_g2s(cb + piece * ch.n * wq, L.shared_q + (size_t)row * g.wpr, ch.n * wq, m);
+      else
+        bulk_g2s(cb + 2 * ch.n * wq + (piece - 2) * ch.n * ws,
+              reinterpret_cast<const uint32_t*>(L.shared_sb) + (size_t)row * g.gpr, ch.n * ws, m);
     }
   }
   if (lane == 0) *S.apar = l & 1;
 }
 
-// Warp 0: issue layer l's phase-B copies (gate/up rows of the selected
-// experts), chunk i by lane i.
+// One warp: issue layer l's phase-B copies (gate/up rows of the selected
+// experts).
 __device__ void issue_B(const FusedParams& P, const FGeo& g, int l, const FSmem& S, const int* s_idx) {
   const FusedLayer& L = P.layers[l];
   const int f = P.f, lane = threadIdx.x & 31;
   fence_proxy_async();
-  if (lane < kMaxBC) {
-    int b, e;
-    fsplit(P.K * f, blockIdx.x, g.nC, b, e);
-    const Chunk ch = chunk_at(lane, b, e, f);
-    uint64_t* m = &S.mB[lane];
+  // One copy per lane: lanes 4c..4c+3 issue chunk c's four pieces (gate rows,
+  // up rows, their scale/bias rows), eight chunks per instruction. A copy
+  // instruction costs its thread ~0.1 us to issue, so one lane per piece
+  // issues fastest, and chunk-major order lets chunk 0 land first.
+  int b, e;
+  fsplit(P.K * f, blockIdx.x, g.nC, b, e);
+  for (int c0 = 0; c0 < kMaxBC; c0 += 8) {
+    const int c = c0 + (lane >> 2), piece = lane & 3;
+    const Chunk ch = chunk_at(c, b, e, f);
+    uint64_t* m = &S.mB[c];
+    if (piece == 0) mbar_expect_tx(m, (uint32_t)ch.n * g.unit);  // 0: completes empty
+    __syncwarp();
     if (ch.n > 0) {
       const int wq = g.wpr * 4, ws = g.gpr * 4;
       const int k = ch.start / f, r = ch.start - k * f;
-      const uint32_t* eq = L.pool_q + (size_t)s_idx[k] * L.q_stride;
-      const uint32_t* es = reinterpret_cast<const uint32_t*>(L.pool_sb + (size_t)s_idx[k] * L.sb_stride);
+      const int row = (piece & 1) ? f + r : r;  // gate rows, then up rows
       unsigned char* cb = S.bufB + (size_t)(ch.start - b) * g.unit;
-      mbar_expect_tx(m, (uint32_t)ch.n * g.unit);
-      bulk_g2s(cb, eq + (size_t)r * g.wpr, ch.n * wq, m);
-      bulk_g2s(cb + ch.n * wq, eq + (size_t)(f + r) * g.wpr, ch.n * wq, m);
-      bulk_g2s(cb + 2 * ch.n * wq, es + (size_t)r * g.gpr, ch.n * ws, m);
-      bulk_g2s(cb + 2 * ch.n * wq + ch.n * ws, es + (size_t)(f + r) * g.gpr, ch.n * ws, m);
-    } else {
-      mbar_expect_tx(m, 0);
+      if (piece < 2)
+        bulk_g2s(cb + piece * ch.n * wq, L.pool_q + (size_t)s_idx[k] * L.q_stride + (size_t)row * g.wpr, ch.n * wq,
+                 m);
+      else
+        bulk_g2s(cb + 2 * ch.n * wq + (piece - 2) * ch.n * ws,
+                 reinterpret_cast<const uint32_t*>(L.pool_sb + (size_t)s_idx[k] * L.sb_stride) + (size_t)row * g.gpr,
+                 ch.n * ws, m);
     }
   }
   if (lane == 0) *S.bpar = l & 1;
@@ -600,6 +603,7 @@ struct CLayout {
   __device__ size_t q(int k) const { return (size_t)k * n * wqf; }
   __device__ size_t sb(int K, int k) const { return (size_t)(K + 1) * n * wqf + (size_t)k * n * wsf; }
   __device__ size_t ys(int K) const { return ((size_t)(K + 1) * n * (wqf + wsf) + 15) & ~(size_t)15; }
+  __device__ size_t hk(int K) const { return (ys(K) + (size_t)(K + 1) * n * 4 + 15) & ~(size_t)15; }
 };
 
 // Warp 0: issue phase C's copies (the CTA's down rows of the K selected
@@ -862,16 +866,7 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
     stamp(P, l, 3);
     cta_arrive(&ctrl->misc[1]);
 
-    // ---------------- A2: shared expert gate/up units (in bufA)
-    {
-      int b, e;
-      s1_range(g, f, b, e);
-      run_units<BITS>(S.bufA + s1_base(g, d), b, e, f, S.mS, par, ctrl, P.timeout_ns, sta, g,
-                      P.hk + (size_t)K * f + b, warp, lane);
-    }
-
     // ---------------- selection: every CTA selects from the complete logits
-    stamp(P, l, 4);
     if (!cta_wait(&ctrl->misc[1], g.nC * (l + 1), ctrl, P.timeout_ns, S)) return;
     stamp(P, l, 5);
     {
@@ -888,11 +883,18 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
     }
 
     // ---------------- B: the selected experts' gate/up units (in bufB)
-    if (warp == 0) issue_B(P, g, l, S, s_idx);
+    if (warp == kFWarps - 1) issue_B(P, g, l, S, s_idx);  // the last warp: its phase-B units (if any) come last
     {
+      // The shared expert's gate/up units (phase A's data, in bufA) do not
+      // gate the selection, so they run here, while phase B's rows stream in;
+      // they go to the last warps, whose phase-B chunks land last.
       int b, e;
+      s1_range(g, f, b, e);
+      run_units<BITS>(S.bufA + s1_base(g, d), b, e, f, S.mS, par, ctrl, P.timeout_ns, sta, g,
+                      P.hk + (size_t)K * f + b, kFWarps - 1 - warp, lane);
+      stamp(P, l, 4);
       fsplit(K * f, blockIdx.x, g.nC, b, e);
-      run_units<BITS>(S.bufB, b, e, f, S.mB, par, ctrl, P.timeout_ns, sta, g, P.hk + b, warp, lane);
+      run_units<BITS>(S.bufB, b, e, f, S.mB, par, ctrl, P.timeout_ns, sta, g, P.hk + b, warp, lane);  // unit k*f + row
     }
     stamp(P, l, 6);
     // Phase C: this CTA's output rows [c_b, c_e). Once every warp is done with
@@ -914,7 +916,22 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
     if (!cta_wait(&ctrl->misc[3], g.nC * (l + 1), ctrl, P.timeout_ns, S)) return;
     stamp(P, l, 7);
     {
-      stage_cg<BITS>(P.hk, f, K + 1, f, sth);  // the SwiGLU outputs of every CTA, through L2
+      {  // the SwiGLU outputs of every CTA, through L2: all loads in flight, then staged
+        float4* hks = reinterpret_cast<float4*>(S.bufB + cl.hk(K));
+        const float4* src = reinterpret_cast<const float4*>(P.hk);
+        const int n4 = (K + 1) * f / 4;
+        for (int i0 = tid; i0 < n4; i0 += 4 * kFThreads) {
+          float4 v[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (i0 + j * kFThreads < n4) v[j] = __ldcg(src + i0 + j * kFThreads);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (i0 + j * kFThreads < n4) hks[i0 + j * kFThreads] = v[j];
+        }
+        __syncthreads();
+        stage_f32<BITS>(reinterpret_cast<const float*>(hks), f, K + 1, f, sth);
+      }
       stamp(P, l, 13);
       mbar_wait(S.mC, par, ctrl, P.timeout_ns);
       stamp(P, l, 9);
