@@ -807,9 +807,16 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
           s_r = 1.f / sqrtf(s / (float)d + P.eps);
         }
       } else if (warp == 0) {
+        // the previous layer's per-CTA sums of squares: all loads in flight, then summed in order
         const float* part = P.part_ss + (l & 1) * g.nC;
         float s = 0.f;
-        for (int c = lane; c < g.nC; c += 32) s += __ldcg(part + c);
+        for (int c0 = 0; c0 < g.nC; c0 += 8 * 32) {
+          float v[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[i] = c0 + i * 32 + lane < g.nC ? __ldcg(part + c0 + i * 32 + lane) : 0.f;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) s += v[i];
+        }
         s = warp_sum(s);
         if (lane == 0) s_r = 1.f / sqrtf(s / (float)d + P.eps);
       }
@@ -836,12 +843,6 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
         reinterpret_cast<uint4*>(a_s)[k] = reinterpret_cast<const uint4*>(P.x_in)[k];
     }
     __syncthreads();
-    {  // fp32 copy of the input in bufB (free until the selection), then staged
-      float* af = reinterpret_cast<float*>(S.bufB);
-      for (int k = tid; k < d; k += kFThreads) af[k] = bf16f(a_s[k]);
-      __syncthreads();
-      stage_f32<BITS>(af, d, 1, d, sta);
-    }
     stamp(P, l, 2);
 
     // ---------------- A1: router rows (in bufA)
@@ -865,6 +866,15 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
     }
     stamp(P, l, 3);
     cta_arrive(&ctrl->misc[1]);
+    {  // Staged integer copy of the input for the gate/up rows, while the
+       // logits of the other CTAs arrive: fp32 copy in bufB (free until the
+       // selection), then staged.
+      float* af = reinterpret_cast<float*>(S.bufB);
+      for (int k = tid; k < d; k += kFThreads) af[k] = bf16f(a_s[k]);
+      __syncthreads();
+      stage_f32<BITS>(af, d, 1, d, sta);
+    }
+    stamp(P, l, 12);
 
     // ---------------- selection: every CTA selects from the complete logits
     if (!cta_wait(&ctrl->misc[1], g.nC * (l + 1), ctrl, P.timeout_ns, S)) return;
