@@ -258,9 +258,9 @@ int32_t moe_expert_swiglu(const bgq_expert* e, const uint16_t* x, int32_t batch,
   cudaStream_t s = st(stream);
   const int ntasks = (batch + kTaskTok - 1) / kTaskTok;
   if (launch_plan_single(plan, batch, s) != cudaSuccess) return BGQ_ERR_CUDA;
-  if (launch_gateup(es, plan, ntasks, x, H, 1, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  if (launch_gateup(es, plan, ntasks, batch, x, H, 1, s) != cudaSuccess) return BGQ_ERR_CUDA;
   if (launch_gateup_tc(es, plan, batch, 0, x, H, 1, ctrl, s) != cudaSuccess) return BGQ_ERR_CUDA;
-  if (launch_down(es, plan, ntasks, H, Y, 1, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  if (launch_down(es, plan, ntasks, batch, H, Y, 1, s) != cudaSuccess) return BGQ_ERR_CUDA;
   if (launch_down_tc(es, plan, batch, 0, H, Y, 1, ctrl, s) != cudaSuccess) return BGQ_ERR_CUDA;
   return cuda_status(launch_combine(Y, nullptr, nullptr, batch, 0, d, y, y_f32, s));
 }
@@ -283,9 +283,9 @@ static int32_t layer_forward_impl(const bgq_moe_layer* L, const uint16_t* x, int
   const ExpertSet es = expert_set(L);
   const int max_tasks = plan_max_tasks(batch, K);
   // experts with < 16 tokens: grouped GEMV; with >= 16: tensor-core GEMM
-  if (launch_gateup(es, W.plan, max_tasks, x, W.H, K + 1, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  if (launch_gateup(es, W.plan, max_tasks, batch, x, W.H, K + 1, s) != cudaSuccess) return BGQ_ERR_CUDA;
   if (launch_gateup_tc(es, W.plan, batch, K, x, W.H, K + 1, W.ctrl, s) != cudaSuccess) return BGQ_ERR_CUDA;
-  if (launch_down(es, W.plan, max_tasks, W.H, W.Y, K + 1, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  if (launch_down(es, W.plan, max_tasks, batch, W.H, W.Y, K + 1, s) != cudaSuccess) return BGQ_ERR_CUDA;
   if (launch_down_tc(es, W.plan, batch, K, W.H, W.Y, K + 1, W.ctrl, s) != cudaSuccess) return BGQ_ERR_CUDA;
   return cuda_status(launch_combine(W.Y, w, gamma, batch, K, L->d_model, out, out_f32, s));
 }

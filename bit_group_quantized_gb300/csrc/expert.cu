@@ -202,6 +202,186 @@ k_down(ExpertSet es, const Plan* __restrict__ plan, const float* __restrict__ H,
   }
 }
 
+// ---------------------------------------------------------------------------
+// Small batches (all inputs fit in shared memory): one 512-thread CTA per SM
+// stages every token's input once, then walks its share of the rows of every
+// task. A warp keeps the weight rows of its next work item in flight while it
+// computes the current one, so each SM has ~100 KB of row loads outstanding
+// (the HBM latency-bandwidth product per SM), and no CTA restages inputs when
+// the task changes. Per-row arithmetic (part order, accumulation, butterfly)
+// is the same as in k_gateup / k_down and the persistent kernel, so results
+// are bit-identical across the three.
+// ---------------------------------------------------------------------------
+constexpr int kAllThreads = 384;  // 12 warps: two work items of row loads per warp fit in registers
+constexpr int kAllWarps = kAllThreads / 32;
+constexpr int kAllRows = 8;  // rows per down-projection work item
+
+struct RowSpan {
+  int b, e;
+};
+__device__ __forceinline__ RowSpan cta_rows(int n) {
+  return RowSpan{(int)((long long)n * blockIdx.x / gridDim.x), (int)((long long)n * (blockIdx.x + 1) / gridDim.x)};
+}
+
+// Gate and up rows (all parts of one row per lane group; d-rows have LPR = 32).
+struct GateUpRows {
+  uint4 g[kMaxNitE], u[kMaxNitE];
+  uint32_t gs[kMaxNitE], us[kMaxNitE];
+};
+
+template <int BITS>
+__device__ __forceinline__ void load_gateup(const ExpertSet& es, const Plan* plan, int item, int nr, int r0,
+                                            const RowGeo& rg, int lane, GateUpRows& R) {
+  const Task& tk = plan_tasks(plan)[item / nr];
+  const int row = r0 + item % nr;
+  const ExpertRef ex = resolve(es, tk.expert);
+  const int wpr = es.d * BITS / 32, gpr = es.d / kGroup;
+  load_row<BITS>(ex.gate_q + (size_t)row * wpr, reinterpret_cast<const uint32_t*>(ex.gate_sb) + (size_t)row * gpr,
+                 rg, lane, 0, true, R.g, R.gs);
+  load_row<BITS>(ex.up_q + (size_t)row * wpr, reinterpret_cast<const uint32_t*>(ex.up_sb) + (size_t)row * gpr, rg,
+                 lane, 0, true, R.u, R.us);
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kAllThreads, 1)
+k_gateup_all(ExpertSet es, const Plan* __restrict__ plan, const uint16_t* __restrict__ x, int B,
+             float* __restrict__ H, int nslot) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int d = es.d, f = es.f;
+  const RowGeo rg = row_geo(d, BITS);  // LPR == 32, NIT <= kMaxNitE (checked by the launcher)
+  XStage st;
+  st.chunks = reinterpret_cast<uint4*>(smem);
+  st.partinfo = reinterpret_cast<float2*>(smem + (size_t)B * d * 2);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const RowSpan rs = cta_rows(f);
+  const int nr = rs.e - rs.b;
+  const int total = plan->ntasks * nr;
+  GateUpRows cur, nxt;
+  if (warp < total) load_gateup<BITS>(es, plan, warp, nr, rs.b, rg, lane, cur);  // in flight during staging
+  stage_x_int16<BITS>(StridedSrc<uint16_t>{x, d}, B, d, st, nullptr);
+  for (int item = warp; item < total; item += kAllWarps) {
+    if (item + kAllWarps < total) load_gateup<BITS>(es, plan, item + kAllWarps, nr, rs.b, rg, lane, nxt);
+    const Task& tk = plan_tasks(plan)[item / nr];
+    const int row = rs.b + item % nr;
+    for (int i = 0; i < tk.ntok; ++i) {
+      const int t = tk.tok[i];
+      float ga = 0.f, ua = 0.f;
+#pragma unroll
+      for (int it = 0; it < kMaxNitE; ++it) {
+        if (it < rg.NIT) {
+          uint4 xc[4 * Geo<BITS>::kNch];
+          load_part_x<BITS>(st.chunks, t, it, lane, rg, xc);
+          const float2 pi = st.partinfo[t * rg.P + it * 32 + lane];
+          ga = part_dot_x<BITS>(cur.g[it], cur.gs[it], xc, pi, ga);
+          ua = part_dot_x<BITS>(cur.u[it], cur.us[it], xc, pi, ua);
+        }
+      }
+      ga = warp_sum(ga);
+      ua = warp_sum(ua);
+      if (lane == 0) H[((size_t)t * nslot + tk.slot[i]) * f + row] = silu_f(ga) * ua;
+    }
+    cur = nxt;
+  }
+}
+
+// Up to kAllRows down rows of one task (f-rows: one part per lane, RPP rows per warp pass).
+struct DownRows {
+  uint4 q[kAllRows];
+  uint32_t s[kAllRows];
+};
+
+// Work item i: task i / nch, row groups [g0, g1) of the CTA's rows (chunks of
+// at most kAllRows row groups, near-equal sizes).
+struct DownItem {
+  int task, g0, g1;
+};
+__device__ __forceinline__ DownItem down_item(int i, int nch, int nrg) {
+  const int ti = i / nch, ci = i - ti * nch;
+  return DownItem{ti, nrg * ci / nch, nrg * (ci + 1) / nch};
+}
+
+template <int BITS>
+__device__ __forceinline__ void load_down(const ExpertSet& es, const Plan* plan, const DownItem& it, int r0, int nrows,
+                                          const RowGeo& rg, int lp, int rsub, DownRows& R) {
+  const ExpertRef ex = resolve(es, plan_tasks(plan)[it.task].expert);
+  const int wpr = es.f * BITS / 32, gpr = es.f / kGroup;
+#pragma unroll
+  for (int u = 0; u < kAllRows; ++u) {
+    const int r = (it.g0 + u) * rg.RPP + rsub;  // local row
+    if (it.g0 + u < it.g1 && r < nrows) {
+      const size_t row = (size_t)(r0 + r);
+      R.q[u] = ldg_stream16(ex.down_q + row * wpr + 4 * lp);
+      R.s[u] = ldg_stream4(reinterpret_cast<const uint32_t*>(ex.down_sb) + row * gpr + part_group<BITS>(lp));
+    } else {
+      R.q[u] = make_uint4(0, 0, 0, 0);
+      R.s[u] = 0;
+    }
+  }
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kAllThreads, 1)
+k_down_all(ExpertSet es, const Plan* __restrict__ plan, const float* __restrict__ H, int B,
+           float* __restrict__ Y, int nslot) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int d = es.d, f = es.f;
+  const RowGeo rg = row_geo(f, BITS);  // NIT == 1 (checked by the launcher)
+  const int T = B * nslot;             // staged vector (tok, slot) at index tok * nslot + slot
+  XStage st;
+  st.chunks = reinterpret_cast<uint4*>(smem);
+  st.partinfo = reinterpret_cast<float2*>(smem + (size_t)T * f * 2);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lp = lane % rg.LPR, rsub = lane / rg.LPR;
+  const RowSpan rs = cta_rows(d);
+  const int nrows = rs.e - rs.b;
+  const int nrg = (nrows + rg.RPP - 1) / rg.RPP;
+  const int nch = (nrg + kAllRows - 1) / kAllRows;
+  const int total = plan->ntasks * nch;
+  DownRows cur, nxt;
+  if (warp < total) load_down<BITS>(es, plan, down_item(warp, nch, nrg), rs.b, nrows, rg, lp, rsub, cur);
+  stage_x_int16<BITS>(StridedSrc<float>{H, f}, T, f, st, nullptr);
+  for (int i = warp; i < total; i += kAllWarps) {
+    if (i + kAllWarps < total)
+      load_down<BITS>(es, plan, down_item(i + kAllWarps, nch, nrg), rs.b, nrows, rg, lp, rsub, nxt);
+    const DownItem it = down_item(i, nch, nrg);
+    const Task& tk = plan_tasks(plan)[it.task];
+    for (int j = 0; j < tk.ntok; ++j) {
+      const int v = tk.tok[j] * nslot + tk.slot[j];
+      uint4 xc[4 * Geo<BITS>::kNch];
+      load_part_x<BITS>(st.chunks, v, 0, lp, rg, xc);
+      const float2 pi = st.partinfo[v * rg.P + lp];
+      float acc[kAllRows];
+#pragma unroll
+      for (int u = 0; u < kAllRows; ++u) acc[u] = part_dot_x<BITS>(cur.q[u], cur.s[u], xc, pi, 0.f);
+      float* yv = Y + (size_t)v * d + rs.b;
+      if (rg.LPR >= 8) {
+        const float y = row_reduce8(acc, rg.LPR, lane);
+        const int o1 = rg.LPR >> 1, o2 = o1 >> 1, o3 = o2 >> 1;
+        if ((lp & (o3 - 1)) == 0) {
+          const int u = ((lp & o1) ? 4 : 0) + ((lp & o2) ? 2 : 0) + ((lp & o3) ? 1 : 0);
+          const int r = (it.g0 + u) * rg.RPP + rsub;
+          if (it.g0 + u < it.g1 && r < nrows) yv[r] = y;
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < kAllRows; ++u) {
+          const float y = row_reduce(acc[u], rg.LPR);
+          const int r = (it.g0 + u) * rg.RPP + rsub;
+          if (lp == 0 && it.g0 + u < it.g1 && r < nrows) yv[r] = y;
+        }
+      }
+    }
+    cur = nxt;
+  }
+}
+
+// Shared memory of the small-batch kernels: T staged vectors of `cols` values.
+static size_t all_smem(int cols, int bits, int T) {
+  const RowGeo rg = row_geo(cols, bits);
+  return (size_t)T * cols * 2 + (size_t)T * rg.P * 8;
+}
+constexpr size_t kAllSmemMax = 200 * 1024;
+
 template <typename K>
 static cudaError_t set_smem(K kern, size_t sm) {
   if (sm > 48 * 1024) return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
@@ -213,10 +393,22 @@ static int expert_grid(int max_items) {
   return max_items < g ? (max_items > 0 ? max_items : 1) : g;
 }
 
-cudaError_t launch_gateup(const ExpertSet& es, const Plan* plan, int max_tasks, const uint16_t* x, float* H, int nslot,
-                          cudaStream_t s) {
-  size_t sm = qgemv_int16_smem(es.d, es.bits, kTaskTok);
+cudaError_t launch_gateup(const ExpertSet& es, const Plan* plan, int max_tasks, int batch, const uint16_t* x, float* H,
+                          int nslot, cudaStream_t s) {
   RowGeo rg = row_geo(es.d, es.bits);
+  if (rg.LPR == 32 && rg.NIT <= kMaxNitE && all_smem(es.d, es.bits, batch) <= kAllSmemMax) {
+    const size_t sm = all_smem(es.d, es.bits, batch);
+    cudaError_t e;
+    if (es.bits == 4) {
+      if ((e = set_smem(k_gateup_all<4>, sm)) != cudaSuccess) return e;
+      k_gateup_all<4><<<num_sms(), kAllThreads, sm, s>>>(es, plan, x, batch, H, nslot);
+    } else {
+      if ((e = set_smem(k_gateup_all<2>, sm)) != cudaSuccess) return e;
+      k_gateup_all<2><<<num_sms(), kAllThreads, sm, s>>>(es, plan, x, batch, H, nslot);
+    }
+    return cudaGetLastError();
+  }
+  size_t sm = qgemv_int16_smem(es.d, es.bits, kTaskTok);
   int nrb = (es.f + kExpWarps * rg.RPP - 1) / (kExpWarps * rg.RPP);
   int grid = expert_grid(max_tasks * nrb);
   cudaError_t e;
@@ -230,10 +422,22 @@ cudaError_t launch_gateup(const ExpertSet& es, const Plan* plan, int max_tasks, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_down(const ExpertSet& es, const Plan* plan, int max_tasks, const float* H, float* Y, int nslot,
-                        cudaStream_t s) {
-  size_t sm = qgemv_int16_smem(es.f, es.bits, kTaskTok);
+cudaError_t launch_down(const ExpertSet& es, const Plan* plan, int max_tasks, int batch, const float* H, float* Y,
+                        int nslot, cudaStream_t s) {
   RowGeo rg = row_geo(es.f, es.bits);
+  if (rg.NIT == 1 && all_smem(es.f, es.bits, batch * nslot) <= kAllSmemMax) {
+    const size_t sm = all_smem(es.f, es.bits, batch * nslot);
+    cudaError_t e;
+    if (es.bits == 4) {
+      if ((e = set_smem(k_down_all<4>, sm)) != cudaSuccess) return e;
+      k_down_all<4><<<num_sms(), kAllThreads, sm, s>>>(es, plan, H, batch, Y, nslot);
+    } else {
+      if ((e = set_smem(k_down_all<2>, sm)) != cudaSuccess) return e;
+      k_down_all<2><<<num_sms(), kAllThreads, sm, s>>>(es, plan, H, batch, Y, nslot);
+    }
+    return cudaGetLastError();
+  }
+  size_t sm = qgemv_int16_smem(es.f, es.bits, kTaskTok);
   int nrb = (es.d + kExpWarps * rg.RPP - 1) / (kExpWarps * rg.RPP);
   int grid = expert_grid(max_tasks * nrb);
   cudaError_t e;
