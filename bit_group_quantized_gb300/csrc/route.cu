@@ -15,8 +15,10 @@
 // With a plan pointer, the last CTA also groups the (token, slot) pairs by
 // expert (counting sort, stable by token then slot) into grouped-GEMV tasks of
 // at most 8 tokens, routed experts in ascending order, then the shared expert.
+#include "../../include/bgq.h"
 #include "common.cuh"
 #include "kernels.h"
+#include "topk.cuh"
 
 namespace bgq {
 
@@ -308,9 +310,207 @@ k_route(const uint16_t* __restrict__ router, const uint16_t* __restrict__ sgate,
   if (threadIdx.x == 0) ctrl->route_counter = 0;  // ready for the next launch
 }
 
+// ---------------------------------------------------------------------------
+// Cooperative router: one 512-thread CTA per SM.
+//   1. CTA c computes the logits of its share of the rows for every token
+//      (rows in 1024-column slices, summed in the same order as above and as
+//      the persistent batch-1 kernel, so the logits are bit-identical);
+//   2. after a grid-wide counter, CTA t selects token t's experts with the
+//      block top-K of the persistent kernel (tokens in parallel instead of
+//      one warp each in the last CTA);
+//   3. the last CTA to finish step 2 builds the grouping plan.
+// The counter wait is bounded like every wait in the library.
+// ---------------------------------------------------------------------------
+constexpr int kRcThreads = 512;
+constexpr int kRcWarps = kRcThreads / 32;
+static_assert(kRcWarps == kTopkWarps, "block top-K needs 16 warps");
+constexpr long long kRcTimeoutNs = 2000000000ll;
+
+__device__ __forceinline__ unsigned long long rc_now() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Block barrier, then thread 0 adds 1 to *cnt (release) and waits (acquire)
+// until it reaches target. False for the whole block on abort or timeout
+// (a timeout writes BGQ_ERR_TIMEOUT and raises the abort flag).
+__device__ bool rc_grid_sync(int* cnt, int target, Ctrl* ctrl) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(cnt) : "memory");
+    int ok = 1;
+    const unsigned long long t0 = rc_now();
+    long long it = 0;
+    while (true) {
+      int v;
+      asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+      if (v >= target) break;
+      if (*(volatile int*)&ctrl->misc[0]) {
+        ok = 0;
+        break;
+      }
+      if (++it > (1ll << 26) || (long long)(rc_now() - t0) > kRcTimeoutNs) {
+        atomicExch(&ctrl->status, BGQ_ERR_TIMEOUT);
+        atomicExch(&ctrl->misc[0], 1);
+        ok = 0;
+        break;
+      }
+      if (it > 16) __nanosleep(32);
+    }
+    s_ok = ok;
+  }
+  __syncthreads();
+  return s_ok != 0;
+}
+
+__global__ void __launch_bounds__(kRcThreads, 1)
+k_route_coop(const uint16_t* __restrict__ router, const uint16_t* __restrict__ sgate, const uint16_t* __restrict__ x,
+             int B, int d, int E, int K, float* __restrict__ lg, Ctrl* ctrl, int32_t* __restrict__ idx,
+             float* __restrict__ w, float* __restrict__ gamma, float* __restrict__ logits_out, Plan* plan,
+             int* __restrict__ sel_ws) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);                       // [kRouteTok][d]
+  float* red = reinterpret_cast<float*>(smem + (size_t)kRouteTok * d * 2);  // [warps][kRouteTok]
+  __shared__ int s_idx[kMaxTopK];
+  __shared__ float s_w[kMaxTopK + 1];
+  __shared__ int s_last;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const RouteGeo g = route_geo(d);
+  const int nrows = E + (sgate ? 1 : 0);
+  const int rpp = kRcWarps / g.sk;  // rows per pass
+  const int r0 = (int)((long long)nrows * blockIdx.x / gridDim.x);
+  const int r1 = (int)((long long)nrows * (blockIdx.x + 1) / gridDim.x);
+
+  // 1. logits of rows [r0, r1) for every token
+  for (int rb = r0; rb < r1; rb += rpp) {
+    const int rloc = warp / g.sk, half = warp - rloc * g.sk;
+    const int row = rb + rloc;
+    const bool valid = rloc < rpp && row < r1;
+    const uint16_t* wrow = (row < E) ? router + (size_t)row * d : sgate;
+    const int c0 = half * (d / g.sk);
+    uint4 wv[kRouteMaxVec];
+#pragma unroll
+    for (int i = 0; i < kRouteMaxVec; ++i)
+      wv[i] = (valid && i < g.nvec) ? ldg_stream16(wrow + c0 + (i * 32 + lane) * 8) : make_uint4(0, 0, 0, 0);
+    for (int t0 = 0; t0 < B; t0 += kRouteTok) {
+      const int T = B - t0 < kRouteTok ? B - t0 : kRouteTok;
+      __syncthreads();
+      for (int i = threadIdx.x; i < T * d / 8; i += blockDim.x)
+        reinterpret_cast<uint4*>(xs)[i] = reinterpret_cast<const uint4*>(x + (size_t)t0 * d)[i];
+      __syncthreads();
+      float acc[kRouteTok];
+#pragma unroll
+      for (int t = 0; t < kRouteTok; ++t) acc[t] = 0.f;
+#pragma unroll
+      for (int i = 0; i < kRouteMaxVec; ++i) {
+        if (i < g.nvec) {
+          const float wf[8] = {bf16lo(wv[i].x), bf16hi(wv[i].x), bf16lo(wv[i].y), bf16hi(wv[i].y),
+                               bf16lo(wv[i].z), bf16hi(wv[i].z), bf16lo(wv[i].w), bf16hi(wv[i].w)};
+          const int col = c0 + (i * 32 + lane) * 8;
+#pragma unroll
+          for (int t = 0; t < kRouteTok; ++t) {
+            if (t < T) {
+              const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)t * d + col);
+              float a = acc[t];
+              a = fmaf(wf[0], bf16lo(xv.x), a);
+              a = fmaf(wf[1], bf16hi(xv.x), a);
+              a = fmaf(wf[2], bf16lo(xv.y), a);
+              a = fmaf(wf[3], bf16hi(xv.y), a);
+              a = fmaf(wf[4], bf16lo(xv.z), a);
+              a = fmaf(wf[5], bf16hi(xv.z), a);
+              a = fmaf(wf[6], bf16lo(xv.w), a);
+              a = fmaf(wf[7], bf16hi(xv.w), a);
+              acc[t] = a;
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < kRouteTok; ++t) {
+        const float v = warp_sum(acc[t]);
+        if (lane == 0) red[warp * kRouteTok + t] = v;
+      }
+      __syncthreads();
+      if (valid && half == 0 && lane < T) {
+        float v = 0.f;
+        for (int h = 0; h < g.sk; ++h) v += red[(rloc * g.sk + h) * kRouteTok + lane];
+        lg[(size_t)(t0 + lane) * (E + 1) + row] = v;
+      }
+    }
+  }
+  if (!rc_grid_sync(&ctrl->misc[10], (int)gridDim.x, ctrl)) return;
+
+  // 2. token t's experts, tokens spread over the CTAs
+  float* lgs = reinterpret_cast<float*>(smem);  // E + 1 logits, then the candidates
+  for (int t = blockIdx.x; t < B; t += gridDim.x) {
+    __syncthreads();
+    for (int e = threadIdx.x; e < nrows; e += blockDim.x) {
+      const float v = __ldcg(lg + (size_t)t * (E + 1) + e);
+      lgs[e] = v;
+      if (logits_out && e < E) logits_out[(size_t)t * E + e] = v;
+    }
+    __syncthreads();
+    block_topk(lgs, reinterpret_cast<int*>(lgs + ((E + 4) & ~3)), E, K, sgate != nullptr, s_idx, s_w);
+    if (threadIdx.x < K) {
+      idx[t * K + threadIdx.x] = s_idx[threadIdx.x];
+      w[t * K + threadIdx.x] = s_w[threadIdx.x];
+      sel_ws[t * K + threadIdx.x] = s_idx[threadIdx.x];
+    }
+    if (threadIdx.x == 0 && gamma) gamma[t] = s_w[K];
+  }
+
+  // 3. the last CTA out builds the plan and resets the counters
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int prev = atomicAdd(&ctrl->misc[11], 1);
+    s_last = prev == (int)gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (plan) {
+    int* s_cnt = reinterpret_cast<int*>(smem);  // 4*E ints + scan scratch
+    build_plan(sel_ws, B, K, E, plan, s_cnt, s_cnt + 4 * E);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    ctrl->misc[10] = 0;
+    ctrl->misc[11] = 0;
+    __threadfence();
+  }
+}
+
+static size_t route_coop_smem(int d, int E) {
+  size_t sm = (size_t)kRouteTok * d * 2 + kRcWarps * kRouteTok * sizeof(float);
+  const size_t sm_topk = ((size_t)((E + 4) & ~3) + 2 * kTopkWarps * 8) * sizeof(float);
+  const size_t sm_plan = (size_t)(4 * E + 40) * sizeof(int);
+  if (sm_topk > sm) sm = sm_topk;
+  if (sm_plan > sm) sm = sm_plan;
+  return sm;
+}
+
 cudaError_t launch_route(const uint16_t* router, const uint16_t* sgate, const uint16_t* x, int batch, int d, int E,
                          int K, float* logits_ws, Ctrl* ctrl, int32_t* idx, float* w, float* gamma,
                          float* logits_out, Plan* plan, cudaStream_t s) {
+  // selected experts scratch for the plan: right after the logits
+  int* sel = reinterpret_cast<int*>(logits_ws + (size_t)batch * (E + 1));
+  if (E <= kTopkWarps * 64) {
+    const size_t smc = route_coop_smem(d, E);
+    cudaError_t e = cudaFuncSetAttribute(k_route_coop, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smc);
+    int per_sm = 0;
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_route_coop, kRcThreads, smc);
+    if (e != cudaSuccess) return e;
+    if (per_sm >= 1) {
+      void* args[] = {(void*)&router, (void*)&sgate, (void*)&x,     (void*)&batch, (void*)&d,
+                      (void*)&E,      (void*)&K,     (void*)&logits_ws, (void*)&ctrl, (void*)&idx,
+                      (void*)&w,      (void*)&gamma, (void*)&logits_out, (void*)&plan, (void*)&sel};
+      return cudaLaunchCooperativeKernel((void*)k_route_coop, dim3(num_sms()), dim3(kRcThreads), args, smc, s);
+    }
+  }
   RouteGeo g = route_geo(d);
   int nrows = E + (sgate ? 1 : 0);
   int grid = (nrows + g.rows_cta - 1) / g.rows_cta;
@@ -321,10 +521,8 @@ cudaError_t launch_route(const uint16_t* router, const uint16_t* sgate, const ui
     cudaError_t e = cudaFuncSetAttribute(k_route, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
   }
-  // selected experts scratch for the plan: right after the logits
-  int* sel_ws = reinterpret_cast<int*>(logits_ws + (size_t)batch * (E + 1));
   k_route<<<grid, kRouteThreads, sm, s>>>(router, sgate, x, batch, d, E, K, logits_ws, ctrl, idx, w, gamma,
-                                          logits_out, plan, sel_ws);
+                                          logits_out, plan, sel);
   return cudaGetLastError();
 }
 
