@@ -62,6 +62,7 @@ struct LayerWs {
   float* gamma;
   float* H;  // [B][K+1][f]
   float* Y;  // [B][K+1][d]
+  unsigned char* stage;  // inputs staged in global memory when too many for shared memory
   // batch-1 persistent kernel scratch
   float* fh;        // [d] residual stream
   float* fpart;     // [2][1024] per-CTA sums of squares
@@ -81,6 +82,10 @@ LayerWs carve_layer(void* ws, int B, int d, int f, int E, int K) {
   L.gamma = c.take<float>((size_t)B * 4);
   L.H = c.take<float>((size_t)B * (K + 1) * f * 4);
   L.Y = c.take<float>((size_t)B * (K + 1) * d * 4);
+  {
+    const size_t sx = staged_tokens_bytes(d, 4, B), sh = staged_tokens_bytes(f, 4, B * (K + 1));
+    L.stage = c.take<unsigned char>(sx > sh ? sx : sh);  // 4-bit staging is the larger
+  }
   L.fh = c.take<float>((size_t)d * 4);
   L.fpart = c.take<float>(2 * 1024 * 4);
   L.fidx = c.take<int32_t>(16 * 4);
@@ -230,7 +235,9 @@ int32_t moe_route_topk(const uint16_t* router, const uint16_t* shared_gate, cons
 size_t moe_expert_workspace_bytes(const bgq_expert* e, int32_t batch) {
   if (!e || batch < 1) return 0;
   const int d = e->gate.cols, f = e->gate.rows;
-  return sizeof(Ctrl) + up256(plan_bytes(batch, 0)) + up256((size_t)batch * f * 4) + up256((size_t)batch * d * 4);
+  const size_t sx = staged_tokens_bytes(d, 4, batch), sh = staged_tokens_bytes(f, 4, batch);
+  return sizeof(Ctrl) + up256(plan_bytes(batch, 0)) + up256((size_t)batch * f * 4) + up256((size_t)batch * d * 4) +
+         up256(sx > sh ? sx : sh);
 }
 
 int32_t moe_expert_swiglu(const bgq_expert* e, const uint16_t* x, int32_t batch, uint16_t* y, float* y_f32,
@@ -250,6 +257,8 @@ int32_t moe_expert_swiglu(const bgq_expert* e, const uint16_t* x, int32_t batch,
   Plan* plan = c.take<Plan>(plan_bytes(batch, 0));
   float* H = c.take<float>((size_t)batch * f * 4);
   float* Y = c.take<float>((size_t)batch * d * 4);
+  const size_t sx = staged_tokens_bytes(d, 4, batch), sh = staged_tokens_bytes(f, 4, batch);
+  unsigned char* stage = c.take<unsigned char>(sx > sh ? sx : sh);
   ExpertSet es{};
   es.shared = ExpertRef{e->gate.q, e->gate.sb, e->up.q, e->up.sb, e->down.q, e->down.sb};
   es.d = d;
@@ -258,9 +267,9 @@ int32_t moe_expert_swiglu(const bgq_expert* e, const uint16_t* x, int32_t batch,
   cudaStream_t s = st(stream);
   const int ntasks = (batch + kTaskTok - 1) / kTaskTok;
   if (launch_plan_single(plan, batch, s) != cudaSuccess) return BGQ_ERR_CUDA;
-  if (launch_gateup(es, plan, ntasks, batch, x, H, 1, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  if (launch_gateup(es, plan, ntasks, batch, x, H, 1, stage, s) != cudaSuccess) return BGQ_ERR_CUDA;
   if (launch_gateup_tc(es, plan, batch, 0, x, H, 1, ctrl, s) != cudaSuccess) return BGQ_ERR_CUDA;
-  if (launch_down(es, plan, ntasks, batch, H, Y, 1, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  if (launch_down(es, plan, ntasks, batch, H, Y, 1, stage, s) != cudaSuccess) return BGQ_ERR_CUDA;
   if (launch_down_tc(es, plan, batch, 0, H, Y, 1, ctrl, s) != cudaSuccess) return BGQ_ERR_CUDA;
   return cuda_status(launch_combine(Y, nullptr, nullptr, batch, 0, d, y, y_f32, s));
 }
@@ -283,9 +292,9 @@ static int32_t layer_forward_impl(const bgq_moe_layer* L, const uint16_t* x, int
   const ExpertSet es = expert_set(L);
   const int max_tasks = plan_max_tasks(batch, K);
   // experts with < 16 tokens: grouped GEMV; with >= 16: tensor-core GEMM
-  if (launch_gateup(es, W.plan, max_tasks, batch, x, W.H, K + 1, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  if (launch_gateup(es, W.plan, max_tasks, batch, x, W.H, K + 1, W.stage, s) != cudaSuccess) return BGQ_ERR_CUDA;
   if (launch_gateup_tc(es, W.plan, batch, K, x, W.H, K + 1, W.ctrl, s) != cudaSuccess) return BGQ_ERR_CUDA;
-  if (launch_down(es, W.plan, max_tasks, batch, W.H, W.Y, K + 1, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  if (launch_down(es, W.plan, max_tasks, batch, W.H, W.Y, K + 1, W.stage, s) != cudaSuccess) return BGQ_ERR_CUDA;
   if (launch_down_tc(es, W.plan, batch, K, W.H, W.Y, K + 1, W.ctrl, s) != cudaSuccess) return BGQ_ERR_CUDA;
   return cuda_status(launch_combine(W.Y, w, gamma, batch, K, L->d_model, out, out_f32, s));
 }

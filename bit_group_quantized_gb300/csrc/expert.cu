@@ -245,20 +245,25 @@ __device__ __forceinline__ void load_gateup(const ExpertSet& es, const Plan* pla
 template <int BITS>
 __global__ void __launch_bounds__(kAllThreads, 1)
 k_gateup_all(ExpertSet es, const Plan* __restrict__ plan, const uint16_t* __restrict__ x, int B,
-             float* __restrict__ H, int nslot) {
+             float* __restrict__ H, int nslot, XStage gst) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int d = es.d, f = es.f;
   const RowGeo rg = row_geo(d, BITS);  // LPR == 32, NIT <= kMaxNitE (checked by the launcher)
-  XStage st;
-  st.chunks = reinterpret_cast<uint4*>(smem);
-  st.partinfo = reinterpret_cast<float2*>(smem + (size_t)B * d * 2);
+  // inputs staged here, or (too many tokens for shared memory) read from the
+  // copy k_stage_tokens made in global memory (L1/L2 resident)
+  const bool local = gst.chunks == nullptr;
+  XStage st = gst;
+  if (local) {
+    st.chunks = reinterpret_cast<uint4*>(smem);
+    st.partinfo = reinterpret_cast<float2*>(smem + (size_t)B * d * 2);
+  }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const RowSpan rs = cta_rows(f);
   const int nr = rs.e - rs.b;
   const int total = plan->ntasks * nr;
   GateUpRows cur, nxt;
   if (warp < total) load_gateup<BITS>(es, plan, warp, nr, rs.b, rg, lane, cur);  // in flight during staging
-  stage_x_int16<BITS>(StridedSrc<uint16_t>{x, d}, B, d, st, nullptr);
+  if (local) stage_x_int16<BITS>(StridedSrc<uint16_t>{x, d}, B, d, st, nullptr);
   for (int item = warp; item < total; item += kAllWarps) {
     if (item + kAllWarps < total) load_gateup<BITS>(es, plan, item + kAllWarps, nr, rs.b, rg, lane, nxt);
     const Task& tk = plan_tasks(plan)[item / nr];
@@ -322,14 +327,17 @@ __device__ __forceinline__ void load_down(const ExpertSet& es, const Plan* plan,
 template <int BITS>
 __global__ void __launch_bounds__(kAllThreads, 1)
 k_down_all(ExpertSet es, const Plan* __restrict__ plan, const float* __restrict__ H, int B,
-           float* __restrict__ Y, int nslot) {
+           float* __restrict__ Y, int nslot, XStage gst) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int d = es.d, f = es.f;
   const RowGeo rg = row_geo(f, BITS);  // NIT == 1 (checked by the launcher)
   const int T = B * nslot;             // staged vector (tok, slot) at index tok * nslot + slot
-  XStage st;
-  st.chunks = reinterpret_cast<uint4*>(smem);
-  st.partinfo = reinterpret_cast<float2*>(smem + (size_t)T * f * 2);
+  const bool local = gst.chunks == nullptr;  // else: staged in global memory (see k_gateup_all)
+  XStage st = gst;
+  if (local) {
+    st.chunks = reinterpret_cast<uint4*>(smem);
+    st.partinfo = reinterpret_cast<float2*>(smem + (size_t)T * f * 2);
+  }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int lp = lane % rg.LPR, rsub = lane / rg.LPR;
   const RowSpan rs = cta_rows(d);
@@ -339,7 +347,7 @@ k_down_all(ExpertSet es, const Plan* __restrict__ plan, const float* __restrict_
   const int total = plan->ntasks * nch;
   DownRows cur, nxt;
   if (warp < total) load_down<BITS>(es, plan, down_item(warp, nch, nrg), rs.b, nrows, rg, lp, rsub, cur);
-  stage_x_int16<BITS>(StridedSrc<float>{H, f}, T, f, st, nullptr);
+  if (local) stage_x_int16<BITS>(StridedSrc<float>{H, f}, T, f, st, nullptr);
   for (int i = warp; i < total; i += kAllWarps) {
     if (i + kAllWarps < total)
       load_down<BITS>(es, plan, down_item(i + kAllWarps, nch, nrg), rs.b, nrows, rg, lp, rsub, nxt);
@@ -375,12 +383,50 @@ k_down_all(ExpertSet es, const Plan* __restrict__ plan, const float* __restrict_
   }
 }
 
-// Shared memory of the small-batch kernels: T staged vectors of `cols` values.
+// T staged vectors of `cols` values: bytes (shared or global memory).
 static size_t all_smem(int cols, int bits, int T) {
   const RowGeo rg = row_geo(cols, bits);
   return (size_t)T * cols * 2 + (size_t)T * rg.P * 8;
 }
 constexpr size_t kAllSmemMax = 200 * 1024;
+
+size_t staged_tokens_bytes(int cols, int bits, int T) { return all_smem(cols, bits, T); }
+
+// Stages T vectors of `cols` values into global memory (same layout and
+// values as the shared-memory staging), one thread per code word.
+template <int BITS, typename Src>
+__global__ void k_stage_tokens(const Src src, int T, int cols, XStage st) {
+  using G = Geo<BITS>;
+  const RowGeo rg = row_geo(cols, BITS);
+  const int words = cols * BITS / 32;
+  const int tw = blockIdx.x * blockDim.x + threadIdx.x;  // whole warps run: groups never straddle one
+  const bool active = tw < T * words;
+  const int t = active ? tw / words : 0, w = active ? tw - t * words : 0;
+  float v[G::kPer];
+#pragma unroll
+  for (int i = 0; i < G::kPer; i += 8) {
+    if (active) {
+      src.load8(t, w * G::kPer + i, v + i);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[i + j] = 0.f;
+    }
+  }
+  stage_word<BITS>(v, active, t, w, rg, __ffs(rg.LPR) - 1, st);
+}
+
+static XStage global_stage(unsigned char* buf, int cols, int T) {
+  XStage g;
+  g.chunks = reinterpret_cast<uint4*>(buf);
+  g.partinfo = reinterpret_cast<float2*>(buf + (size_t)T * cols * 2);
+  return g;
+}
+template <int BITS, typename Src>
+static cudaError_t stage_tokens(const Src src, int T, int cols, XStage st, cudaStream_t s) {
+  const int n = T * (cols * BITS / 32);
+  k_stage_tokens<BITS><<<(n + 255) / 256, 256, 0, s>>>(src, T, cols, st);
+  return cudaGetLastError();
+}
 
 template <typename K>
 static cudaError_t set_smem(K kern, size_t sm) {
@@ -394,17 +440,27 @@ static int expert_grid(int max_items) {
 }
 
 cudaError_t launch_gateup(const ExpertSet& es, const Plan* plan, int max_tasks, int batch, const uint16_t* x, float* H,
-                          int nslot, cudaStream_t s) {
+                          int nslot, unsigned char* stage_ws, cudaStream_t s) {
   RowGeo rg = row_geo(es.d, es.bits);
-  if (rg.LPR == 32 && rg.NIT <= kMaxNitE && all_smem(es.d, es.bits, batch) <= kAllSmemMax) {
-    const size_t sm = all_smem(es.d, es.bits, batch);
+  const bool fits = all_smem(es.d, es.bits, batch) <= kAllSmemMax;
+  if (rg.LPR == 32 && rg.NIT <= kMaxNitE && (fits || stage_ws)) {
+    XStage gst{};
+    size_t sm = 0;
     cudaError_t e;
+    if (fits) {
+      sm = all_smem(es.d, es.bits, batch);
+    } else {
+      gst = global_stage(stage_ws, es.d, batch);
+      e = es.bits == 4 ? stage_tokens<4>(StridedSrc<uint16_t>{x, es.d}, batch, es.d, gst, s)
+                       : stage_tokens<2>(StridedSrc<uint16_t>{x, es.d}, batch, es.d, gst, s);
+      if (e != cudaSuccess) return e;
+    }
     if (es.bits == 4) {
       if ((e = set_smem(k_gateup_all<4>, sm)) != cudaSuccess) return e;
-      k_gateup_all<4><<<num_sms(), kAllThreads, sm, s>>>(es, plan, x, batch, H, nslot);
+      k_gateup_all<4><<<num_sms(), kAllThreads, sm, s>>>(es, plan, x, batch, H, nslot, gst);
     } else {
       if ((e = set_smem(k_gateup_all<2>, sm)) != cudaSuccess) return e;
-      k_gateup_all<2><<<num_sms(), kAllThreads, sm, s>>>(es, plan, x, batch, H, nslot);
+      k_gateup_all<2><<<num_sms(), kAllThreads, sm, s>>>(es, plan, x, batch, H, nslot, gst);
     }
     return cudaGetLastError();
   }
@@ -423,17 +479,28 @@ cudaError_t launch_gateup(const ExpertSet& es, const Plan* plan, int max_tasks, 
 }
 
 cudaError_t launch_down(const ExpertSet& es, const Plan* plan, int max_tasks, int batch, const float* H, float* Y,
-                        int nslot, cudaStream_t s) {
+                        int nslot, unsigned char* stage_ws, cudaStream_t s) {
   RowGeo rg = row_geo(es.f, es.bits);
-  if (rg.NIT == 1 && all_smem(es.f, es.bits, batch * nslot) <= kAllSmemMax) {
-    const size_t sm = all_smem(es.f, es.bits, batch * nslot);
+  const int T = batch * nslot;
+  const bool fits = all_smem(es.f, es.bits, T) <= kAllSmemMax;
+  if (rg.NIT == 1 && (fits || stage_ws)) {
+    XStage gst{};
+    size_t sm = 0;
     cudaError_t e;
+    if (fits) {
+      sm = all_smem(es.f, es.bits, T);
+    } else {
+      gst = global_stage(stage_ws, es.f, T);
+      e = es.bits == 4 ? stage_tokens<4>(StridedSrc<float>{H, es.f}, T, es.f, gst, s)
+                       : stage_tokens<2>(StridedSrc<float>{H, es.f}, T, es.f, gst, s);
+      if (e != cudaSuccess) return e;
+    }
     if (es.bits == 4) {
       if ((e = set_smem(k_down_all<4>, sm)) != cudaSuccess) return e;
-      k_down_all<4><<<num_sms(), kAllThreads, sm, s>>>(es, plan, H, batch, Y, nslot);
+      k_down_all<4><<<num_sms(), kAllThreads, sm, s>>>(es, plan, H, batch, Y, nslot, gst);
     } else {
       if ((e = set_smem(k_down_all<2>, sm)) != cudaSuccess) return e;
-      k_down_all<2><<<num_sms(), kAllThreads, sm, s>>>(es, plan, H, batch, Y, nslot);
+      k_down_all<2><<<num_sms(), kAllThreads, sm, s>>>(es, plan, H, batch, Y, nslot, gst);
     }
     return cudaGetLastError();
   }

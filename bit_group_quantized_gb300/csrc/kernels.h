@@ -118,12 +118,16 @@ cudaError_t launch_down_tc(const ExpertSet& es, const Plan* plan, int B, int K, 
                            Ctrl* ctrl, cudaStream_t s);
 
 // Grouped gate/up + SiLU*mul: H[(tok*nslot + slot)*f + row].
-// batch: tokens of x (all of them are staged at once when they fit in shared memory).
+// batch: tokens of x, staged all at once in shared memory when they fit, else
+// into stage_ws (staged_tokens_bytes(d, bits, batch) bytes of global memory;
+// null: the per-task kernels instead).
 cudaError_t launch_gateup(const ExpertSet& es, const Plan* plan, int max_tasks, int batch, const uint16_t* x, float* H,
-                          int nslot, cudaStream_t s);
-// Grouped down projection: Y[(tok*nslot + slot)*d + row]; H holds batch*nslot vectors of f.
+                          int nslot, unsigned char* stage_ws, cudaStream_t s);
+// Grouped down projection: Y[(tok*nslot + slot)*d + row]; H holds batch*nslot
+// vectors of f (stage_ws: staged_tokens_bytes(f, bits, batch*nslot) bytes).
 cudaError_t launch_down(const ExpertSet& es, const Plan* plan, int max_tasks, int batch, const float* H, float* Y,
-                        int nslot, cudaStream_t s);
+                        int nslot, unsigned char* stage_ws, cudaStream_t s);
+size_t staged_tokens_bytes(int cols, int bits, int T);
 // out[t][r] = sum_{k<K} w[t][k] Y[t][k][r] + gamma[t] Y[t][K][r]  (K may be 0; gamma NULL => 1).
 cudaError_t launch_combine(const float* Y, const float* w, const float* gamma, int batch, int K, int d,
                            uint16_t* out, float* out_f32, cudaStream_t s);

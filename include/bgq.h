@@ -188,7 +188,7 @@ int32_t moe_layer_forward(const bgq_moe_layer* L, const uint16_t* x, int32_t bat
  * not create them).
  * Same arguments, kernels and results as moe_layer_forward; the scratch memory
  * is a 4 MiB array inside the library (held on every GPU that loads the
- * library until the process exits), enough for batch <= 39 at d_model 4096,
+ * library until the process exits), enough for batch <= 35 at d_model 4096,
  * d_ff 1024, 512 experts, top-4. A call whose moe_layer_workspace_bytes(L,
  * batch) exceeds 4 MiB returns BGQ_ERR_WORKSPACE and launches nothing.
  * The first call on each device looks up the array's device address
