@@ -66,6 +66,19 @@ __device__ bool tc_mbar_wait(uint64_t* m, uint32_t parity, long long limit_ns) {
   return true;
 }
 __device__ __forceinline__ void tc_fence_proxy() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// Asynchronous global -> shared copies (16 bytes through L2 only, 4 bytes), grouped per K step.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc_smem(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(tc_smem(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -209,14 +222,22 @@ __device__ __forceinline__ ExpertRef tc_resolve(const ExpertSet& es, int e) {
 }
 
 // Shared memory of one CTA: [mbar x2][tmem slot] then two stages of
-// NA weight tiles (16 KB each) and one activation tile (Npad*128 bytes).
+// NA weight tiles (16 KB each) and one activation tile (Npad*128 bytes), then
+// the ring of raw codes: kTcD K steps in flight, per step and row NA code
+// slices (qb bytes each), then per step and row NA scale/bias words.
+constexpr int kTcD = 8;  // K steps of raw codes in flight per thread (hides HBM latency)
 struct TcSmem {
   uint64_t* mbar;
   uint32_t* tslot;
   unsigned char* stage[2];
+  unsigned char* ringq;
+  uint32_t* rings;
   int a_bytes, b_off;
 };
-__device__ __forceinline__ TcSmem tc_carve(unsigned char* smem, int na, int npad) {
+__host__ __device__ inline size_t tc_ring_bytes(int na, int bits) {
+  return (size_t)kTcD * kTcM * na * (kTcBK * bits / 8 + 4);
+}
+__device__ __forceinline__ TcSmem tc_carve(unsigned char* smem, int na, int npad, int bits) {
   TcSmem S;
   S.mbar = reinterpret_cast<uint64_t*>(smem);
   S.tslot = reinterpret_cast<uint32_t*>(smem + 16);
@@ -225,9 +246,13 @@ __device__ __forceinline__ TcSmem tc_carve(unsigned char* smem, int na, int npad
   const int stage_bytes = S.b_off + npad * kTcBK * 2;
   S.stage[0] = smem + 1024;
   S.stage[1] = smem + 1024 + stage_bytes;
+  S.ringq = smem + 1024 + 2 * stage_bytes;
+  S.rings = reinterpret_cast<uint32_t*>(S.ringq + (size_t)kTcD * kTcM * na * (kTcBK * bits / 8));
   return S;
 }
-size_t tc_smem_bytes(int na, int npad) { return 1024 + 2 * ((size_t)na * kTcM * kTcBK * 2 + (size_t)npad * kTcBK * 2); }
+size_t tc_smem_bytes(int na, int npad, int bits) {
+  return 1024 + 2 * ((size_t)na * kTcM * kTcBK * 2 + (size_t)npad * kTcBK * 2) + tc_ring_bytes(na, bits);
+}
 
 __device__ __forceinline__ void tc_fail(Ctrl* ctrl) { atomicExch(&ctrl->status, BGQ_ERR_TIMEOUT); }
 
@@ -247,11 +272,31 @@ k_gateup_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const uin
   const int npad = (bt.ntok + 15) & ~15;
   const int tid = threadIdx.x, warp = tid >> 5;
   const int m0 = blockIdx.x * kTcM;
-  TcSmem S = tc_carve(smem, 2, npad);
+  TcSmem S = tc_carve(smem, 2, npad, BITS);
   const ExpertRef ex = tc_resolve(es, bt.expert);
   const int wpr = d * BITS / 32, gpr = d / kGroup;
   uint32_t ncols = 32;
   while ((int)ncols < 2 * npad) ncols <<= 1;
+  constexpr int qb = kTcBK * BITS / 8;  // code bytes of one row and K step
+  const int rme = m0 + tid;             // the row this thread copies and dequantises
+  // raw codes and scale/bias of step kb for row rme, gate and up, into ring slot kb % kTcD
+  auto issue = [&](int kb, int nk_) {
+    if (kb < nk_ && rme < f) {
+      const int slot = kb % kTcD;
+      unsigned char* dq = S.ringq + ((size_t)(slot * kTcM + tid) * 2) * qb;
+      const uint32_t* g = ex.gate_q + (size_t)rme * wpr + kb * (kTcBK * BITS / 32);
+      const uint32_t* u = ex.up_q + (size_t)rme * wpr + kb * (kTcBK * BITS / 32);
+#pragma unroll
+      for (int o = 0; o < qb; o += 16) {
+        cp_async16(dq + o, g + o / 4);
+        cp_async16(dq + qb + o, u + o / 4);
+      }
+      uint32_t* ds = S.rings + (slot * kTcM + tid) * 2;
+      cp_async4(ds, reinterpret_cast<const uint32_t*>(ex.gate_sb) + (size_t)rme * gpr + kb);
+      cp_async4(ds + 1, reinterpret_cast<const uint32_t*>(ex.up_sb) + (size_t)rme * gpr + kb);
+    }
+    cp_async_commit();
+  };
 
   if (tid == 0) {
     tc_mbar_init(&S.mbar[0]);
@@ -266,24 +311,25 @@ k_gateup_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const uin
   const uint32_t idesc = tc_idesc(npad);
   const int nk = d / kTcBK;
   bool ok = true;
+  for (int kb = 0; kb < kTcD - 1; ++kb) issue(kb, nk);
 
   for (int kb = 0; kb < nk; ++kb) {
     const int s = kb & 1;
     unsigned char* st = S.stage[s];
+    issue(kb + kTcD - 1, nk);
+    cp_async_wait<kTcD - 1>();  // this thread's copies of step kb have landed
     if (kb >= 2 && !tc_mbar_wait(&S.mbar[s], (uint32_t)((kb / 2 - 1) & 1), kTcTimeoutNs)) {
       ok = false;
       break;
     }
     // weights: thread t dequantises row m0 + t of gate and of up
     {
-      const int r = m0 + tid;
-      if (r < f) {
-        const uint32_t* gq = ex.gate_q + (size_t)r * wpr + kb * (kTcBK * BITS / 32);
-        const uint32_t* uq = ex.up_q + (size_t)r * wpr + kb * (kTcBK * BITS / 32);
-        const uint32_t gs = reinterpret_cast<const uint32_t*>(ex.gate_sb)[(size_t)r * gpr + kb];
-        const uint32_t us = reinterpret_cast<const uint32_t*>(ex.up_sb)[(size_t)r * gpr + kb];
-        dequant_row<BITS>(gq, gs, st, tid);
-        dequant_row<BITS>(uq, us, st + S.a_bytes, tid);
+      if (rme < f) {
+        const int slot = kb % kTcD;
+        const unsigned char* dq = S.ringq + ((size_t)(slot * kTcM + tid) * 2) * qb;
+        const uint32_t* ds = S.rings + (slot * kTcM + tid) * 2;
+        dequant_row<BITS>(reinterpret_cast<const uint32_t*>(dq), ds[0], st, tid);
+        dequant_row<BITS>(reinterpret_cast<const uint32_t*>(dq + qb), ds[1], st + S.a_bytes, tid);
       } else {
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
@@ -319,6 +365,7 @@ k_gateup_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const uin
       tc_commit(&S.mbar[s]);
     }
   }
+  cp_async_wait_all();
   // the last commit covers every MMA
   if (ok) ok = tc_mbar_wait(&S.mbar[(nk - 1) & 1], (uint32_t)(((nk - 1) / 2) & 1), kTcTimeoutNs);
   if (ok) {
@@ -363,11 +410,24 @@ k_down_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const float
   const int npad = (bt.ntok + 15) & ~15;
   const int tid = threadIdx.x, warp = tid >> 5;
   const int m0 = blockIdx.x * kTcM;
-  TcSmem S = tc_carve(smem, 1, npad);
+  TcSmem S = tc_carve(smem, 1, npad, BITS);
   const ExpertRef ex = tc_resolve(es, bt.expert);
   const int wpr = f * BITS / 32, gpr = f / kGroup;
   uint32_t ncols = 32;
   while ((int)ncols < npad) ncols <<= 1;
+  constexpr int qb = kTcBK * BITS / 8;
+  const int rme = m0 + tid;
+  auto issue = [&](int kb, int nk_) {
+    if (kb < nk_ && rme < d) {
+      const int slot = kb % kTcD;
+      unsigned char* dq = S.ringq + (size_t)(slot * kTcM + tid) * qb;
+      const uint32_t* q = ex.down_q + (size_t)rme * wpr + kb * (kTcBK * BITS / 32);
+#pragma unroll
+      for (int o = 0; o < qb; o += 16) cp_async16(dq + o, q + o / 4);
+      cp_async4(S.rings + slot * kTcM + tid, reinterpret_cast<const uint32_t*>(ex.down_sb) + (size_t)rme * gpr + kb);
+    }
+    cp_async_commit();
+  };
 
   if (tid == 0) {
     tc_mbar_init(&S.mbar[0]);
@@ -382,20 +442,22 @@ k_down_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const float
   const uint32_t idesc = tc_idesc(npad);
   const int nk = f / kTcBK;
   bool ok = true;
+  for (int kb = 0; kb < kTcD - 1; ++kb) issue(kb, nk);
 
   for (int kb = 0; kb < nk; ++kb) {
     const int s = kb & 1;
     unsigned char* st = S.stage[s];
+    issue(kb + kTcD - 1, nk);
+    cp_async_wait<kTcD - 1>();
     if (kb >= 2 && !tc_mbar_wait(&S.mbar[s], (uint32_t)((kb / 2 - 1) & 1), kTcTimeoutNs)) {
       ok = false;
       break;
     }
     {
-      const int r = m0 + tid;
-      if (r < d) {
-        const uint32_t* dq = ex.down_q + (size_t)r * wpr + kb * (kTcBK * BITS / 32);
-        const uint32_t ds = reinterpret_cast<const uint32_t*>(ex.down_sb)[(size_t)r * gpr + kb];
-        dequant_row<BITS>(dq, ds, st, tid);
+      if (rme < d) {
+        const int slot = kb % kTcD;
+        dequant_row<BITS>(reinterpret_cast<const uint32_t*>(S.ringq + (size_t)(slot * kTcM + tid) * qb),
+                          S.rings[slot * kTcM + tid], st, tid);
       } else {
 #pragma unroll
         for (int c = 0; c < 8; ++c)
@@ -431,6 +493,7 @@ k_down_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const float
       tc_commit(&S.mbar[s]);
     }
   }
+  cp_async_wait_all();
   if (ok) ok = tc_mbar_wait(&S.mbar[(nk - 1) & 1], (uint32_t)(((nk - 1) / 2) & 1), kTcTimeoutNs);
   if (ok) {
     tc_fence_after();
@@ -465,7 +528,7 @@ cudaError_t launch_gateup_tc(const ExpertSet& es, const Plan* plan, int B, int K
                              int nslot, Ctrl* ctrl, cudaStream_t s) {
   if (B < kBigTok) return cudaSuccess;  // no task can have 16 tokens
   const int npad = tc_npad_max(B);
-  const size_t sm = tc_smem_bytes(2, npad);
+  const size_t sm = tc_smem_bytes(2, npad, es.bits);
   dim3 grid((es.f + kTcM - 1) / kTcM, plan_max_big(B, K));
   void* kern = es.bits == 4 ? (void*)k_gateup_tc<4> : (void*)k_gateup_tc<2>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
@@ -481,7 +544,7 @@ cudaError_t launch_down_tc(const ExpertSet& es, const Plan* plan, int B, int K, 
                            Ctrl* ctrl, cudaStream_t s) {
   if (B < kBigTok) return cudaSuccess;
   const int npad = tc_npad_max(B);
-  const size_t sm = tc_smem_bytes(1, npad);
+  const size_t sm = tc_smem_bytes(1, npad, es.bits);
   dim3 grid((es.d + kTcM - 1) / kTcM, plan_max_big(B, K));
   void* kern = es.bits == 4 ? (void*)k_down_tc<4> : (void*)k_down_tc<2>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
