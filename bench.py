@@ -9,7 +9,7 @@ router, softmax/top-4, SwiGLU experts, shared expert, combine, residual).
 Seeded synthetic weights and activations (no trained model exists here).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload stack4|stack2|layer|gemv] [--layers L] [--batch B]
+                  [--workload stack4|stack2|layer|gemv|host] [--layers L] [--batch B]
 
 Prints one JSON line. With N > 1 (torchrun) every rank runs its own decode
 stream on its own GPU (replicas; no data-path collective); the slowest
@@ -214,6 +214,9 @@ def workload_name(args) -> str:
     if args.workload == "layer":
         return (f"moe_layer: 512 routed + 1 shared experts, d_model 4096, d_ff 1024, top-4, 4-bit, batch {args.batch}"
                 f", ring of {args.ring} distinct layers")
+    if args.workload == "host":
+        return (f"moe_layer with the 512 routed experts in pinned host memory (router and shared expert in HBM), "
+                f"d_model 4096, d_ff 1024, top-4, 4-bit, batch {args.batch}, ring of 16 inputs")
     return f"q4_gemv: 1024x4096 4-bit, group 64, batch 1, variant {args.variant}, ring of {args.ring} matrices"
 
 
@@ -448,6 +451,56 @@ def run_layer(args):
     return 0
 
 
+def run_host(args):
+    """One MoE layer whose routed-expert pool (3.6 GB) lives in pinned host
+    memory, read over the CPU-GPU link (NVLink-C2C on a GB300 node) by the
+    grouped kernels; router and shared expert stay in HBM. A ring of 16 inputs
+    selects different experts per call (16 x ~28 MB exceeds L2)."""
+    import torch
+
+    from bit_group_quantized_gb300 import lib, synth
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    lib.load()
+    B, R = args.batch, 16
+    shape = synth.PoolShape(D_MODEL, D_FF, N_EXPERTS, 4)
+    t = synth.layer_tensors(args.seed + 300, 0, shape, device=dev)
+    pool_q = t["pool_q"][:N_EXPERTS].to("cpu").pin_memory()
+    pool_sb = t["pool_sb"][:N_EXPERTS].to("cpu").pin_memory()
+    shared_q, shared_sb = t["pool_q"][N_EXPERTS].clone(), t["pool_sb"][N_EXPERTS].clone()
+    router, gate = t["router"], t["shared_gate"]
+    del t
+    torch.cuda.empty_cache()
+    layer = lib.MoELayer(D_MODEL, D_FF, N_EXPERTS, TOP_K, 4, router, gate, pool_q, pool_sb, shared_q, shared_sb)
+    xs = [synth.activations(args.seed + 300, r, B, D_MODEL, device=dev) for r in range(R)]
+    outs = [torch.empty((B, D_MODEL), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    ws = lib.workspace(lib.moe_layer_workspace_bytes(layer, B), dev)
+    distinct = [len(set(lib.moe_layer_forward(layer, xs[r], ws=ws, want_route=True)[2].flatten().tolist()))
+                for r in range(R)]
+    stream = torch.cuda.Stream(device=dev)
+
+    def body():
+        for r in range(R):
+            lib.moe_layer_forward(layer, xs[r], ws=ws, out=outs[r], stream=stream)
+
+    n_rep = max(1, args.steps // R)
+    clocks = ClockSampler(0)
+    ms = _timed_graph(torch, stream, body, n_rep, args.warmup) / R
+    clock = clocks.stop()
+    dmean = sum(distinct) / len(distinct)
+    host_bytes = dmean * shape.expert_bytes
+    print(json.dumps({
+        "metric": METRIC, "value": round(B * 1000.0 / ms, 2), "unit": "tokens/s", "n_gpus": 1,
+        "steps": n_rep * R, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u4 codes; dp4a, f32 accumulate", "data": "synthetic",
+        "config": {"workload": workload_name(args), "us_per_layer": round(ms * 1000, 3),
+                   "distinct_experts_mean": dmean, "host_bytes_per_layer": int(host_bytes),
+                   "host_read_gbs": round(host_bytes / (ms * 1e-3) / 1e9, 1)},
+        "roofline": None, "clocks": clock}), flush=True)
+    return 0
+
+
 def run_gemv(args):
     """q4_gemv (1024x4096, batch 1) per step, cycling through `ring` distinct matrices."""
     import torch
@@ -495,7 +548,7 @@ def main():
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="stack4", choices=["stack4", "stack2", "layer", "gemv"])
+    ap.add_argument("--workload", default="stack4", choices=["stack4", "stack2", "layer", "gemv", "host"])
     ap.add_argument("--variant", type=int, default=0, help="gemv: 0 integer (production), 1 standard, "
                                                             "2 reordered (the page's fma form), 3 hoisted fp32")
     ap.add_argument("--ring", type=int, default=8, help="layer/gemv: distinct weight copies cycled through")
@@ -513,6 +566,8 @@ def main():
         return run_layer(args)
     if args.workload == "gemv":
         return run_gemv(args)
+    if args.workload == "host":
+        return run_host(args)
     return run_ours(args)
 
 

@@ -3,6 +3,7 @@
 // Every entry point validates its arguments before it enqueues anything,
 // carves the caller's workspace into the regions its kernels need, and
 // launches on the caller's stream. Nothing here allocates or synchronises.
+#include <climits>
 #include <stdint.h>
 #include <string.h>
 
@@ -130,6 +131,35 @@ ExpertSet expert_set(const bgq_moe_layer* L) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? BGQ_OK : BGQ_ERR_CUDA; }
 
+// Where weights live. Device memory is read by every kernel; pinned host
+// memory mapped into the device address space (Grace memory over the CPU-GPU
+// link) is read by the kernels that use plain loads only: the router, the
+// grouped GEMVs and the combine, never the bulk copies of the persistent
+// kernel or the tensor-core path.
+enum class Where { kDevice, kHost, kBad };
+Where where_is(const void* p) {
+  if (!p) return Where::kDevice;
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return Where::kBad;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return Where::kDevice;
+  if (a.type == cudaMemoryTypeHost && a.devicePointer == p) return Where::kHost;
+  return Where::kBad;
+}
+Where layer_where(const bgq_moe_layer* L) {
+  const void* ps[] = {L->router, L->shared_gate, L->expert_q, L->expert_sb, L->shared_q, L->shared_sb};
+  Where w = Where::kDevice;
+  for (const void* p : ps) {
+    const Where k = where_is(p);
+    if (k == Where::kBad) return Where::kBad;
+    if (k == Where::kHost) w = Where::kHost;
+  }
+  return w;
+}
+int big_min_for(Where w) { return w == Where::kHost ? INT_MAX : kBigTok; }
+
 constexpr long long kFusedTimeoutNs = 2000000000ll;  // bounded waits inside the persistent kernel
 
 // The persistent kernel streams weight rows with 16-byte bulk copies.
@@ -229,7 +259,7 @@ int32_t moe_route_topk(const uint16_t* router, const uint16_t* shared_gate, cons
   Ctrl* ctrl = c.take<Ctrl>(sizeof(Ctrl));
   float* lg = c.take<float>((size_t)batch * (n_experts + 1) * 4 + (size_t)batch * top_k * 4);
   return cuda_status(launch_route(router, shared_gate, x, batch, d_model, n_experts, top_k, lg, ctrl, idx, w, gamma,
-                                  logits, nullptr, st(stream)));
+                                  logits, nullptr, kBigTok, st(stream)));
 }
 
 size_t moe_expert_workspace_bytes(const bgq_expert* e, int32_t batch) {
@@ -266,11 +296,19 @@ int32_t moe_expert_swiglu(const bgq_expert* e, const uint16_t* x, int32_t batch,
   es.bits = bits;
   cudaStream_t s = st(stream);
   const int ntasks = (batch + kTaskTok - 1) / kTaskTok;
-  if (launch_plan_single(plan, batch, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  Where where = Where::kDevice;
+  for (const void* p : {(const void*)e->gate.q, (const void*)e->gate.sb, (const void*)e->up.q, (const void*)e->up.sb,
+                        (const void*)e->down.q, (const void*)e->down.sb}) {
+    const Where k = where_is(p);
+    if (k == Where::kBad) return BGQ_ERR_INVALID_ARG;
+    if (k == Where::kHost) where = Where::kHost;
+  }
+  const int big_min = big_min_for(where);
+  if (launch_plan_single(plan, batch, big_min, s) != cudaSuccess) return BGQ_ERR_CUDA;
   if (launch_gateup(es, plan, ntasks, batch, x, H, 1, stage, s) != cudaSuccess) return BGQ_ERR_CUDA;
-  if (launch_gateup_tc(es, plan, batch, 0, x, H, 1, ctrl, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  if (batch >= big_min && launch_gateup_tc(es, plan, batch, 0, x, H, 1, ctrl, s) != cudaSuccess) return BGQ_ERR_CUDA;
   if (launch_down(es, plan, ntasks, batch, H, Y, 1, stage, s) != cudaSuccess) return BGQ_ERR_CUDA;
-  if (launch_down_tc(es, plan, batch, 0, H, Y, 1, ctrl, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  if (batch >= big_min && launch_down_tc(es, plan, batch, 0, H, Y, 1, ctrl, s) != cudaSuccess) return BGQ_ERR_CUDA;
   return cuda_status(launch_combine(Y, nullptr, nullptr, batch, 0, d, y, y_f32, s));
 }
 
@@ -281,21 +319,23 @@ size_t moe_layer_workspace_bytes(const bgq_moe_layer* L, int32_t max_batch) {
 
 static int32_t layer_forward_impl(const bgq_moe_layer* L, const uint16_t* x, int32_t batch, uint16_t* out,
                                   float* out_f32, int32_t* idx_out, float* w_out, float* gamma_out, const LayerWs& W,
-                                  cudaStream_t s) {
+                                  Where where, cudaStream_t s) {
+  const int big_min = big_min_for(where);
   const int K = L->top_k, E = L->n_experts;
   int32_t* idx = idx_out ? idx_out : W.idx;
   float* w = w_out ? w_out : W.w;
   float* gamma = gamma_out ? gamma_out : W.gamma;
   if (launch_route(L->router, L->shared_gate, x, batch, L->d_model, E, K, W.logits, W.ctrl, idx, w, gamma, nullptr,
-                   W.plan, s) != cudaSuccess)
+                   W.plan, big_min, s) != cudaSuccess)
     return BGQ_ERR_CUDA;
   const ExpertSet es = expert_set(L);
   const int max_tasks = plan_max_tasks(batch, K);
   // experts with < 16 tokens: grouped GEMV; with >= 16: tensor-core GEMM
   if (launch_gateup(es, W.plan, max_tasks, batch, x, W.H, K + 1, W.stage, s) != cudaSuccess) return BGQ_ERR_CUDA;
-  if (launch_gateup_tc(es, W.plan, batch, K, x, W.H, K + 1, W.ctrl, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  const bool tc = batch >= big_min;
+  if (tc && launch_gateup_tc(es, W.plan, batch, K, x, W.H, K + 1, W.ctrl, s) != cudaSuccess) return BGQ_ERR_CUDA;
   if (launch_down(es, W.plan, max_tasks, batch, W.H, W.Y, K + 1, W.stage, s) != cudaSuccess) return BGQ_ERR_CUDA;
-  if (launch_down_tc(es, W.plan, batch, K, W.H, W.Y, K + 1, W.ctrl, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  if (tc && launch_down_tc(es, W.plan, batch, K, W.H, W.Y, K + 1, W.ctrl, s) != cudaSuccess) return BGQ_ERR_CUDA;
   return cuda_status(launch_combine(W.Y, w, gamma, batch, K, L->d_model, out, out_f32, s));
 }
 
@@ -307,8 +347,10 @@ int32_t moe_layer_forward(const bgq_moe_layer* L, const uint16_t* x, int32_t bat
   if ((out && !al(out, 16)) || (out_f32 && !al(out_f32, 16))) return BGQ_ERR_INVALID_ARG;
   if (batch < 1 || batch > kMaxBatch) return BGQ_ERR_INVALID_ARG;
   if (!ws || !al(ws, 256) || ws_bytes < moe_layer_workspace_bytes(L, batch)) return BGQ_ERR_WORKSPACE;
+  const Where where = layer_where(L);
+  if (where == Where::kBad) return BGQ_ERR_INVALID_ARG;
   LayerWs W = carve_layer(ws, batch, L->d_model, L->d_ff, L->n_experts, L->top_k);
-  if (batch == 1 && use_fused(L)) {
+  if (batch == 1 && where == Where::kDevice && use_fused(L)) {
     static_assert(sizeof(FusedParams) < 32000, "kernel parameter space");
     FusedParams P{};
     fill_fused_common(P, L, W);
@@ -324,7 +366,7 @@ int32_t moe_layer_forward(const bgq_moe_layer* L, const uint16_t* x, int32_t bat
     P.layers[0] = fused_layer(L, nullptr);
     return cuda_status(launch_fused(P, L->bits, st(stream)));
   }
-  return layer_forward_impl(L, x, batch, out, out_f32, idx_out, w_out, gamma_out, W, st(stream));
+  return layer_forward_impl(L, x, batch, out, out_f32, idx_out, w_out, gamma_out, W, where, st(stream));
 }
 
 int32_t bgq_rmsnorm(const float* h, const uint16_t* rho, int32_t batch, int32_t d, float eps, uint16_t* a,
@@ -389,8 +431,16 @@ static int32_t stack_decode_impl(const bgq_moe_layer* layers, const uint16_t* co
   if (!(eps >= 0.f) || L0->d_model % 256) return BGQ_ERR_INVALID_ARG;
   if (!ws || !al(ws, 256) || ws_bytes < moe_stack_workspace_bytes(layers, n_layers)) return BGQ_ERR_WORKSPACE;
   const int d = L0->d_model, K = L0->top_k;
+  Where wl[kMaxLayers];
+  bool all_device = true;
+  for (int l = 0; l < n_layers; ++l) {
+    wl[l] = layer_where(&layers[l]);
+    if (wl[l] == Where::kBad || where_is(rho[l]) == Where::kBad) return BGQ_ERR_INVALID_ARG;
+    all_device = all_device && wl[l] == Where::kDevice && where_is(rho[l]) == Where::kDevice;
+  }
   LayerWs W = carve_layer(ws, 1, d, L0->d_ff, L0->n_experts, K);
-  if (use_fused(L0)) {
+  if (trace && !(all_device && use_fused(L0))) return BGQ_ERR_UNSUPPORTED;  // phase timestamps: persistent kernel only
+  if (all_device && use_fused(L0)) {
     FusedParams P{};
     fill_fused_common(P, L0, W);
     P.n_layers = n_layers;
@@ -413,7 +463,7 @@ static int32_t stack_decode_impl(const bgq_moe_layer* layers, const uint16_t* co
   for (int l = 0; l < n_layers; ++l) {
     if (launch_rmsnorm(h, rho[l], 1, d, eps, a, s) != cudaSuccess) return BGQ_ERR_CUDA;
     int r = layer_forward_impl(&layers[l], a, 1, nullptr, o, idx_out ? idx_out + (size_t)l * K : nullptr, nullptr,
-                               nullptr, W, s);
+                               nullptr, W, wl[l], s);
     if (r) return r;
     if (launch_residual_add(h, o, d, s) != cudaSuccess) return BGQ_ERR_CUDA;
   }

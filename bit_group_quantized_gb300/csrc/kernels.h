@@ -102,13 +102,14 @@ size_t qgemv_int16_smem(int cols, int bits, int T);
 cudaError_t launch_qgemv(const QMat& W, const uint16_t* x, int batch, uint16_t* y, float* yf, int variant,
                          cudaStream_t s);
 
-// Router + softmax + top-K (+ optional grouping plan).
+// Router + softmax + top-K (+ optional grouping plan). Experts with at least
+// big_min tokens become tensor-core tasks (kBigTok; INT_MAX: none).
 cudaError_t launch_route(const uint16_t* router, const uint16_t* sgate, const uint16_t* x, int batch, int d,
                          int E, int K, float* logits_ws, Ctrl* ctrl, int32_t* idx, float* w, float* gamma,
-                         float* logits_out, Plan* plan, cudaStream_t s);
+                         float* logits_out, Plan* plan, int big_min, cudaStream_t s);
 
 // Builds the plan of one explicit expert over `batch` tokens (slot 0).
-cudaError_t launch_plan_single(Plan* plan, int batch, cudaStream_t s);
+cudaError_t launch_plan_single(Plan* plan, int batch, int big_min, cudaStream_t s);
 
 // Tensor-core (tcgen05) gate/up + SiLU*mul and down projection for the plan's
 // big tasks (experts with >= kBigTok tokens). B, K: the plan's batch and top_k.

@@ -145,7 +145,7 @@ __device__ void block_exclusive_scan(int* a, int n, int* tmp /* >= 33 ints */) {
   __syncthreads();
 }
 
-__device__ void build_plan(const int* sel, int B, int K, int E, Plan* plan, int* s_cnt, int* s_tmp) {
+__device__ void build_plan(const int* sel, int B, int K, int E, int big_min, Plan* plan, int* s_cnt, int* s_tmp) {
   const int npairs = B * K;
   Task* tasks = plan_tasks(plan);
   BigTask* big = plan_big(plan, B, K);
@@ -160,7 +160,7 @@ __device__ void build_plan(const int* sel, int B, int K, int E, Plan* plan, int*
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     const int c = s_cnt[e];
-    const bool bigc = c >= kBigTok;
+    const bool bigc = c >= big_min;
     s_first[e] = bigc ? 0 : (c + kTaskTok - 1) / kTaskTok;
     s_pfirst[e] = bigc ? c : 0;
     s_bidx[e] = bigc ? 1 : 0;
@@ -176,7 +176,7 @@ __device__ void build_plan(const int* sel, int B, int K, int E, Plan* plan, int*
     const int e = sel[i];
     int r = 0;
     for (int j = 0; j < i; ++j) r += (sel[j] == e);
-    if (s_cnt[e] >= kBigTok) {
+    if (s_cnt[e] >= big_min) {
       ptok[s_pfirst[e] + r] = i / K;
       pslot[s_pfirst[e] + r] = i % K;
       if (r == 0) big[s_bidx[e]] = BigTask{e, s_cnt[e], s_pfirst[e], 0};
@@ -194,7 +194,7 @@ __device__ void build_plan(const int* sel, int B, int K, int E, Plan* plan, int*
   }
   // the shared expert takes every token (slot K)
   int nshared = 0, nbig = nbigr;
-  if (B >= kBigTok) {
+  if (B >= big_min) {
     for (int t = threadIdx.x; t < B; t += blockDim.x) {
       ptok[nbigpairs + t] = t;
       pslot[nbigpairs + t] = K;
@@ -223,7 +223,7 @@ __device__ void build_plan(const int* sel, int B, int K, int E, Plan* plan, int*
 __global__ void __launch_bounds__(kRouteThreads)
 k_route(const uint16_t* __restrict__ router, const uint16_t* __restrict__ sgate, const uint16_t* __restrict__ x, int B,
         int d, int E, int K, float* __restrict__ lg, Ctrl* ctrl, int32_t* __restrict__ idx, float* __restrict__ w,
-        float* __restrict__ gamma, float* __restrict__ logits_out, Plan* plan, int* __restrict__ sel_ws) {
+        float* __restrict__ gamma, float* __restrict__ logits_out, Plan* plan, int big_min, int* __restrict__ sel_ws) {
   extern __shared__ __align__(16) unsigned char smem[];
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem);                       // [kRouteTok][d]
   float* red = reinterpret_cast<float*>(smem + (size_t)kRouteTok * d * 2);  // [warps][kRouteTok]
@@ -305,7 +305,7 @@ k_route(const uint16_t* __restrict__ router, const uint16_t* __restrict__ sgate,
     __syncthreads();
     __threadfence_block();
     int* s_cnt = reinterpret_cast<int*>(smem);  // reuse: 4*E ints + scan scratch
-    build_plan(sel_ws, B, K, E, plan, s_cnt, s_cnt + 4 * E);
+    build_plan(sel_ws, B, K, E, big_min, plan, s_cnt, s_cnt + 4 * E);
   }
   if (threadIdx.x == 0) ctrl->route_counter = 0;  // ready for the next launch
 }
@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(kRcThreads, 1)
 k_route_coop(const uint16_t* __restrict__ router, const uint16_t* __restrict__ sgate, const uint16_t* __restrict__ x,
              int B, int d, int E, int K, float* __restrict__ lg, Ctrl* ctrl, int32_t* __restrict__ idx,
              float* __restrict__ w, float* __restrict__ gamma, float* __restrict__ logits_out, Plan* plan,
-             int* __restrict__ sel_ws) {
+             int big_min, int* __restrict__ sel_ws) {
   extern __shared__ __align__(16) unsigned char smem[];
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem);                       // [kRouteTok][d]
   float* red = reinterpret_cast<float*>(smem + (size_t)kRouteTok * d * 2);  // [warps][kRouteTok]
@@ -473,7 +473,7 @@ k_route_coop(const uint16_t* __restrict__ router, const uint16_t* __restrict__ s
   __threadfence();
   if (plan) {
     int* s_cnt = reinterpret_cast<int*>(smem);  // 4*E ints + scan scratch
-    build_plan(sel_ws, B, K, E, plan, s_cnt, s_cnt + 4 * E);
+    build_plan(sel_ws, B, K, E, big_min, plan, s_cnt, s_cnt + 4 * E);
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -494,7 +494,7 @@ static size_t route_coop_smem(int d, int E) {
 
 cudaError_t launch_route(const uint16_t* router, const uint16_t* sgate, const uint16_t* x, int batch, int d, int E,
                          int K, float* logits_ws, Ctrl* ctrl, int32_t* idx, float* w, float* gamma,
-                         float* logits_out, Plan* plan, cudaStream_t s) {
+                         float* logits_out, Plan* plan, int big_min, cudaStream_t s) {
   // selected experts scratch for the plan: right after the logits
   int* sel = reinterpret_cast<int*>(logits_ws + (size_t)batch * (E + 1));
   if (E <= kTopkWarps * 64) {
@@ -507,7 +507,7 @@ cudaError_t launch_route(const uint16_t* router, const uint16_t* sgate, const ui
     if (per_sm >= 1) {
       void* args[] = {(void*)&router, (void*)&sgate, (void*)&x,     (void*)&batch, (void*)&d,
                       (void*)&E,      (void*)&K,     (void*)&logits_ws, (void*)&ctrl, (void*)&idx,
-                      (void*)&w,      (void*)&gamma, (void*)&logits_out, (void*)&plan, (void*)&sel};
+                      (void*)&w,      (void*)&gamma, (void*)&logits_out, (void*)&plan, (void*)&big_min, (void*)&sel};
       return cudaLaunchCooperativeKernel((void*)k_route_coop, dim3(num_sms()), dim3(kRcThreads), args, smc, s);
     }
   }
@@ -522,14 +522,14 @@ cudaError_t launch_route(const uint16_t* router, const uint16_t* sgate, const ui
     if (e != cudaSuccess) return e;
   }
   k_route<<<grid, kRouteThreads, sm, s>>>(router, sgate, x, batch, d, E, K, logits_ws, ctrl, idx, w, gamma,
-                                          logits_out, plan, sel);
+                                          logits_out, plan, big_min, sel);
   return cudaGetLastError();
 }
 
 // Plan of one explicit expert over B tokens (slot 0): one tensor-core task for
-// B >= kBigTok, else grouped-GEMV tasks of up to 8 tokens. Plan sized for (B, 0).
-__global__ void k_plan_single(Plan* plan, int B) {
-  if (B >= kBigTok) {
+// B >= big_min, else grouped-GEMV tasks of up to 8 tokens. Plan sized for (B, 0).
+__global__ void k_plan_single(Plan* plan, int B, int big_min) {
+  if (B >= big_min) {
     BigTask* big = plan_big(plan, B, 0);
     int* ptok = plan_ptok(plan, B, 0);
     int* pslot = plan_pslot(plan, B, 0);
@@ -561,8 +561,8 @@ __global__ void k_plan_single(Plan* plan, int B) {
   }
 }
 
-cudaError_t launch_plan_single(Plan* plan, int batch, cudaStream_t s) {
-  k_plan_single<<<1, 64, 0, s>>>(plan, batch);
+cudaError_t launch_plan_single(Plan* plan, int batch, int big_min, cudaStream_t s) {
+  k_plan_single<<<1, 64, 0, s>>>(plan, batch, big_min);
   return cudaGetLastError();
 }
 

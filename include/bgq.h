@@ -36,6 +36,16 @@
  *     once before first use (the kernels leave their counters at zero).
  *   - bf16 values are passed as their uint16 bit patterns.
  *   - Calls sharing one workspace must not run concurrently.
+ *   - Weights of moe_layer_forward, moe_stack_decode and moe_expert_swiglu
+ *     (router, shared gate, expert pools, RMSNorm weights) may also live in
+ *     pinned host memory mapped into the device address space (e.g. Grace
+ *     memory on a GB300 node, read over the CPU-GPU link): the Flash-MoE
+ *     page's idea of keeping the experts outside GPU memory and streaming
+ *     only the selected ones (section "架构设计：SSD当显存用"). Such layers
+ *     run on the kernels that read weights with plain loads (router, grouped
+ *     GEMVs, combine): every expert row is read once per call, directly from
+ *     host memory. Pointers the CUDA runtime does not know (unregistered
+ *     pageable memory) are rejected with BGQ_ERR_INVALID_ARG.
  */
 #ifndef BGQ_H
 #define BGQ_H
