@@ -12,7 +12,9 @@
 //
 // Tile: 128 weight rows (M) x Npad tokens (N = the task's tokens rounded up
 // to 16), K in steps of 64 (one quantisation group). Two shared-memory stages:
-// while the tensor core multiplies one stage, the 128 threads fill the other.
+// while the tensor core multiplies one stage, 256 threads (two per weight row)
+// fill the other; raw codes, scale/bias and activations of the next K steps
+// are in flight in a cp.async ring meanwhile.
 // Operands use the canonical no-swizzle K-major layout: 8x16-byte core
 // matrices, the next core matrix along K 128 bytes on (LBO), the next 8 rows
 // 1024 bytes on (SBO). Within each 16-column block the columns are stored in
@@ -30,7 +32,7 @@
 
 namespace bgq {
 
-constexpr int kTcThreads = 128;
+constexpr int kTcThreads = 256;  // two threads per weight row (half a K step each)
 constexpr int kTcM = 128;
 constexpr int kTcBK = 64;
 constexpr long long kTcTimeoutNs = 1000000000ll;
@@ -69,6 +71,9 @@ __device__ __forceinline__ void tc_fence_proxy() { asm volatile("fence.proxy.asy
 // Asynchronous global -> shared copies (16 bytes through L2 only, 4 bytes), grouped per K step.
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc_smem(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(tc_smem(dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(tc_smem(dst)), "l"(src) : "memory");
@@ -133,7 +138,7 @@ __device__ __forceinline__ int tc_off(int r, int kb, int s) {
   return (r >> 3) * 1024 + (kb * 2 + (s >> 3)) * 128 + (r & 7) * 16 + (s & 7) * 2;
 }
 // Slot of column k (0..15) inside its 16-column block, matching the order in
-// which dequant_row() writes codes (4-bit: pairs (j, j+4) per 8 columns;
+// which dequant_half() writes codes (4-bit: pairs (j, j+4) per 8 columns;
 // 2-bit: pairs (j, j+8) per 16 columns).
 template <int BITS>
 __device__ __forceinline__ int tc_slot(int k) {
@@ -145,45 +150,43 @@ __device__ __forceinline__ int tc_slot(int k) {
   }
 }
 
-// Dequantise one row's 64 codes (group g) to fp16 into the tile.
+// Dequantise half h (columns 32h..32h+31) of one row's 64 codes to fp16 into
+// the tile; qh points at that half's code words (4 at 4 bits, 2 at 2 bits).
 template <int BITS>
-__device__ __forceinline__ void dequant_row(const uint32_t* qrow, uint32_t sbw, unsigned char* tile, int r) {
+__device__ __forceinline__ void dequant_half(const uint32_t* qh, uint32_t sbw, unsigned char* tile, int r, int h) {
   const __half2 s2 = __float2half2_rn(bf16lo(sbw));
   const __half2 b2 = __float2half2_rn(bf16hi(sbw));
   const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f);
-  constexpr int kWords = 64 * BITS / 32;  // 8 (4-bit) or 4 (2-bit)
-  uint32_t w[kWords];
+  uint32_t w[4];
   if (BITS == 4) {
-    const uint4 a = *reinterpret_cast<const uint4*>(qrow), b = *reinterpret_cast<const uint4*>(qrow + 4);
+    const uint4 a = *reinterpret_cast<const uint4*>(qh);
     w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
-    w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
   } else {
-    const uint4 a = *reinterpret_cast<const uint4*>(qrow);
-    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+    const uint2 a = *reinterpret_cast<const uint2*>(qh);
+    w[0] = a.x; w[1] = a.y; w[2] = 0; w[3] = 0;
   }
-  // each 16-byte chunk (8 slots) = 4 half2 pairs
-  constexpr int kChunks = 8;  // 64 columns = 8 chunks of 8
 #pragma unroll
-  for (int c = 0; c < kChunks; ++c) {
+  for (int cc = 0; cc < 4; ++cc) {
+    const int c = 4 * h + cc;  // chunk of the row
     uint32_t o[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       uint32_t v;
       if (BITS == 4) {
-        v = (w[c] >> (4 * j)) & 0x000F000Fu;  // codes j and j+4 of word c
+        v = (w[cc] >> (4 * j)) & 0x000F000Fu;  // codes j and j+4 of word c
       } else {
-        const int wi = c >> 1, base = (c & 1) * 4;  // chunk c: half (c&1) of word c/2
-        v = (w[wi] >> (2 * (base + j))) & 0x00030003u;  // codes base+j and base+j+8
+        const int base = (cc & 1) * 4;                    // chunk c: half (c&1) of word c/2
+        v = (w[cc >> 1] >> (2 * (base + j))) & 0x00030003u;  // codes base+j and base+j+8
       }
-      const uint32_t m = v | 0x64006400u;                                // fp16 1024 + code
-      __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&m), k1024);  // exact code values
-      h = __hfma2(h, s2, b2);                                      // q*s + b, one rounding
-      o[j] = *reinterpret_cast<uint32_t*>(&h);
+      const uint32_t m = v | 0x64006400u;
+      __half2 hh = __hsub2(*reinterpret_cast<const __half2*>(&m), k1024);
+      hh = __hfma2(hh, s2, b2);
+      o[j] = *reinterpret_cast<uint32_t*>(&hh);
     }
-    // chunk c covers columns 8c..8c+7: block kb = c/2, slots (c%2)*8 ..
     *reinterpret_cast<uint4*>(tile + tc_off(r, c >> 1, (c & 1) * 8)) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
+
 
 // Write 16 activation values (columns 16*kb .. +15 of token row n) into the
 // tile in tc_slot order.
@@ -223,21 +226,22 @@ __device__ __forceinline__ ExpertRef tc_resolve(const ExpertSet& es, int e) {
 
 // Shared memory of one CTA: [mbar x2][tmem slot] then two stages of
 // NA weight tiles (16 KB each) and one activation tile (Npad*128 bytes), then
-// the ring of raw codes: kTcD K steps in flight, per step and row NA code
-// slices (qb bytes each), then per step and row NA scale/bias words.
-constexpr int kTcD = 8;  // K steps of raw codes in flight per thread (hides HBM latency)
+// the rings of data in flight for D K steps: per step and row NA code slices
+// (qb bytes each), per step, row and half NA scale/bias words, per step the task's
+// raw activations (Npad x 4 items of 16 values, ab bytes per item).
 struct TcSmem {
   uint64_t* mbar;
   uint32_t* tslot;
   unsigned char* stage[2];
   unsigned char* ringq;
   uint32_t* rings;
+  unsigned char* ringa;
   int a_bytes, b_off;
 };
-__host__ __device__ inline size_t tc_ring_bytes(int na, int bits) {
-  return (size_t)kTcD * kTcM * na * (kTcBK * bits / 8 + 4);
+__host__ __device__ inline size_t tc_ring_bytes(int na, int bits, int npad, int ab, int D) {
+  return (size_t)D * ((size_t)kTcM * na * (kTcBK * bits / 8 + 2 * 4) + (size_t)npad * 4 * ab);
 }
-__device__ __forceinline__ TcSmem tc_carve(unsigned char* smem, int na, int npad, int bits) {
+__device__ __forceinline__ TcSmem tc_carve(unsigned char* smem, int na, int npad, int bits, int D) {
   TcSmem S;
   S.mbar = reinterpret_cast<uint64_t*>(smem);
   S.tslot = reinterpret_cast<uint32_t*>(smem + 16);
@@ -247,11 +251,12 @@ __device__ __forceinline__ TcSmem tc_carve(unsigned char* smem, int na, int npad
   S.stage[0] = smem + 1024;
   S.stage[1] = smem + 1024 + stage_bytes;
   S.ringq = smem + 1024 + 2 * stage_bytes;
-  S.rings = reinterpret_cast<uint32_t*>(S.ringq + (size_t)kTcD * kTcM * na * (kTcBK * bits / 8));
+  S.rings = reinterpret_cast<uint32_t*>(S.ringq + (size_t)D * kTcM * na * (kTcBK * bits / 8));
+  S.ringa = reinterpret_cast<unsigned char*>(S.rings + (size_t)D * kTcM * na * 2);
   return S;
 }
-size_t tc_smem_bytes(int na, int npad, int bits) {
-  return 1024 + 2 * ((size_t)na * kTcM * kTcBK * 2 + (size_t)npad * kTcBK * 2) + tc_ring_bytes(na, bits);
+size_t tc_smem_bytes(int na, int npad, int bits, int ab, int D) {
+  return 1024 + 2 * ((size_t)na * kTcM * kTcBK * 2 + (size_t)npad * kTcBK * 2) + tc_ring_bytes(na, bits, npad, ab, D);
 }
 
 __device__ __forceinline__ void tc_fail(Ctrl* ctrl) { atomicExch(&ctrl->status, BGQ_ERR_TIMEOUT); }
@@ -259,7 +264,7 @@ __device__ __forceinline__ void tc_fail(Ctrl* ctrl) { atomicExch(&ctrl->status, 
 // ---------------------------------------------------------------------------
 // gate/up + SiLU*mul: blockIdx.x = tile of 128 rows of d_ff, blockIdx.y = big task.
 // ---------------------------------------------------------------------------
-template <int BITS>
+template <int BITS, int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
 k_gateup_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const uint16_t* __restrict__ x,
             float* __restrict__ H, int nslot, Ctrl* ctrl) {
@@ -272,26 +277,43 @@ k_gateup_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const uin
   const int npad = (bt.ntok + 15) & ~15;
   const int tid = threadIdx.x, warp = tid >> 5;
   const int m0 = blockIdx.x * kTcM;
-  TcSmem S = tc_carve(smem, 2, npad, BITS);
+  TcSmem S = tc_carve(smem, 2, npad, BITS, D);
   const ExpertRef ex = tc_resolve(es, bt.expert);
   const int wpr = d * BITS / 32, gpr = d / kGroup;
   uint32_t ncols = 32;
   while ((int)ncols < 2 * npad) ncols <<= 1;
   constexpr int qb = kTcBK * BITS / 8;  // code bytes of one row and K step
-  const int rme = m0 + tid;             // the row this thread copies and dequantises
-  // raw codes and scale/bias of step kb for row rme, gate and up, into ring slot kb % kTcD
+  constexpr int ab = 32;                // bytes of one activation item (16 bf16)
+  const int rr = tid & (kTcM - 1), hf = tid >> 7;  // tile row and half K step of this thread
+  const int rme = m0 + rr;                          // the row this thread copies and dequantises
+  // Step kb into ring slot kb % D: raw codes (this thread's half) and scale/bias of row rme (gate
+  // and up) and this thread's activation items; one commit group per step.
   auto issue = [&](int kb, int nk_) {
-    if (kb < nk_ && rme < f) {
-      const int slot = kb % kTcD;
-      unsigned char* dq = S.ringq + ((size_t)(slot * kTcM + tid) * 2) * qb;
-      const uint32_t* g = ex.gate_q + (size_t)rme * wpr + kb * (kTcBK * BITS / 32);
-      const uint32_t* u = ex.up_q + (size_t)rme * wpr + kb * (kTcBK * BITS / 32);
-#pragma unroll
-      for (int o = 0; o < qb; o += 16) {
-        cp_async16(dq + o, g + o / 4);
-        cp_async16(dq + qb + o, u + o / 4);
+    if (kb < nk_) {
+      const int slot = kb % D;
+      for (int i = tid; i < npad * 4; i += kTcThreads) {
+        const int n = i >> 2, blk = i & 3;
+        if (n < bt.ntok) {
+          const uint16_t* src = x + (size_t)ptok[n] * d + kb * kTcBK + blk * 16;
+          unsigned char* dst = S.ringa + ((size_t)slot * npad * 4 + i) * ab;
+          cp_async16(dst, src);
+          cp_async16(dst + 16, src + 8);
+        }
       }
-      uint32_t* ds = S.rings + (slot * kTcM + tid) * 2;
+    }
+    if (kb < nk_ && rme < f) {
+      const int slot = kb % D;
+      unsigned char* dq = S.ringq + ((size_t)(slot * kTcM + rr) * 2) * qb + hf * (qb / 2);
+      const uint32_t* g = ex.gate_q + (size_t)rme * wpr + kb * (kTcBK * BITS / 32) + hf * (qb / 8);
+      const uint32_t* u = ex.up_q + (size_t)rme * wpr + kb * (kTcBK * BITS / 32) + hf * (qb / 8);
+      if (qb / 2 == 16) {
+        cp_async16(dq, g);
+        cp_async16(dq + qb, u);
+      } else {
+        cp_async8(dq, g);
+        cp_async8(dq + qb, u);
+      }
+      uint32_t* ds = S.rings + ((slot * kTcM + rr) * 2 + hf) * 2;  // each half keeps its own copy
       cp_async4(ds, reinterpret_cast<const uint32_t*>(ex.gate_sb) + (size_t)rme * gpr + kb);
       cp_async4(ds + 1, reinterpret_cast<const uint32_t*>(ex.up_sb) + (size_t)rme * gpr + kb);
     }
@@ -311,41 +333,41 @@ k_gateup_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const uin
   const uint32_t idesc = tc_idesc(npad);
   const int nk = d / kTcBK;
   bool ok = true;
-  for (int kb = 0; kb < kTcD - 1; ++kb) issue(kb, nk);
+  for (int kb = 0; kb < D - 1; ++kb) issue(kb, nk);
 
   for (int kb = 0; kb < nk; ++kb) {
     const int s = kb & 1;
     unsigned char* st = S.stage[s];
-    issue(kb + kTcD - 1, nk);
-    cp_async_wait<kTcD - 1>();  // this thread's copies of step kb have landed
+    issue(kb + D - 1, nk);
+    cp_async_wait<D - 1>();  // this thread's copies of step kb have landed
     if (kb >= 2 && !tc_mbar_wait(&S.mbar[s], (uint32_t)((kb / 2 - 1) & 1), kTcTimeoutNs)) {
       ok = false;
       break;
     }
-    // weights: thread t dequantises row m0 + t of gate and of up
+    // weights: this thread dequantises its half of row rme of gate and of up
     {
       if (rme < f) {
-        const int slot = kb % kTcD;
-        const unsigned char* dq = S.ringq + ((size_t)(slot * kTcM + tid) * 2) * qb;
-        const uint32_t* ds = S.rings + (slot * kTcM + tid) * 2;
-        dequant_row<BITS>(reinterpret_cast<const uint32_t*>(dq), ds[0], st, tid);
-        dequant_row<BITS>(reinterpret_cast<const uint32_t*>(dq + qb), ds[1], st + S.a_bytes, tid);
+        const int slot = kb % D;
+        const unsigned char* dq = S.ringq + ((size_t)(slot * kTcM + rr) * 2) * qb + hf * (qb / 2);
+        const uint32_t* ds = S.rings + ((slot * kTcM + rr) * 2 + hf) * 2;
+        dequant_half<BITS>(reinterpret_cast<const uint32_t*>(dq), ds[0], st, rr, hf);
+        dequant_half<BITS>(reinterpret_cast<const uint32_t*>(dq + qb), ds[1], st + S.a_bytes, rr, hf);
       } else {
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          *reinterpret_cast<uint4*>(st + tc_off(tid, c >> 1, (c & 1) * 8)) = make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(st + S.a_bytes + tc_off(tid, c >> 1, (c & 1) * 8)) = make_uint4(0, 0, 0, 0);
+        for (int c = 4 * hf; c < 4 * hf + 4; ++c) {
+          *reinterpret_cast<uint4*>(st + tc_off(rr, c >> 1, (c & 1) * 8)) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(st + S.a_bytes + tc_off(rr, c >> 1, (c & 1) * 8)) = make_uint4(0, 0, 0, 0);
         }
       }
     }
-    // activations: (token n, 16-column block) per thread
+    // activations: (token n, 16-column block) per thread, from the ring
     for (int i = tid; i < npad * 4; i += kTcThreads) {
       const int n = i >> 2, blk = i & 3;
       float v[16];
       if (n < bt.ntok) {
-        const uint16_t* xp = x + (size_t)ptok[n] * d + kb * kTcBK + blk * 16;
+        const unsigned char* xp = S.ringa + ((size_t)(kb % D) * npad * 4 + i) * ab;
         unpack_bf16x8(*reinterpret_cast<const uint4*>(xp), v);
-        unpack_bf16x8(*reinterpret_cast<const uint4*>(xp + 8), v + 8);
+        unpack_bf16x8(*reinterpret_cast<const uint4*>(xp + 16), v + 8);
       } else {
 #pragma unroll
         for (int k = 0; k < 16; ++k) v[k] = 0.f;
@@ -368,7 +390,7 @@ k_gateup_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const uin
   cp_async_wait_all();
   // the last commit covers every MMA
   if (ok) ok = tc_mbar_wait(&S.mbar[(nk - 1) & 1], (uint32_t)(((nk - 1) / 2) & 1), kTcTimeoutNs);
-  if (ok) {
+  if (ok && warp < 4) {  // warp w reads tensor-memory lanes 32w..32w+31
     tc_fence_after();
     const int row = m0 + warp * 32 + (tid & 31);
     for (int c0 = 0; c0 < npad; c0 += 8) {
@@ -384,7 +406,7 @@ k_gateup_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const uin
         }
       }
     }
-  } else {
+  } else if (!ok) {
     if (tid == 0) tc_fail(ctrl);
     // give the tensor core a last bounded chance to finish before the memory is freed
     tc_mbar_wait(&S.mbar[0], 0, kTcTimeoutNs / 4);
@@ -397,7 +419,7 @@ k_gateup_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const uin
 // ---------------------------------------------------------------------------
 // down projection: blockIdx.x = tile of 128 rows of d_model, blockIdx.y = big task.
 // ---------------------------------------------------------------------------
-template <int BITS>
+template <int BITS, int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
 k_down_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const float* __restrict__ H,
           float* __restrict__ Y, int nslot, Ctrl* ctrl) {
@@ -410,21 +432,38 @@ k_down_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const float
   const int npad = (bt.ntok + 15) & ~15;
   const int tid = threadIdx.x, warp = tid >> 5;
   const int m0 = blockIdx.x * kTcM;
-  TcSmem S = tc_carve(smem, 1, npad, BITS);
+  TcSmem S = tc_carve(smem, 1, npad, BITS, D);
   const ExpertRef ex = tc_resolve(es, bt.expert);
   const int wpr = f * BITS / 32, gpr = f / kGroup;
   uint32_t ncols = 32;
   while ((int)ncols < npad) ncols <<= 1;
   constexpr int qb = kTcBK * BITS / 8;
-  const int rme = m0 + tid;
+  constexpr int ab = 64;  // bytes of one activation item (16 fp32)
+  const int rr = tid & (kTcM - 1), hf = tid >> 7;  // tile row and half K step of this thread
+  const int rme = m0 + rr;
   auto issue = [&](int kb, int nk_) {
-    if (kb < nk_ && rme < d) {
-      const int slot = kb % kTcD;
-      unsigned char* dq = S.ringq + (size_t)(slot * kTcM + tid) * qb;
-      const uint32_t* q = ex.down_q + (size_t)rme * wpr + kb * (kTcBK * BITS / 32);
+    if (kb < nk_) {
+      const int slot = kb % D;
+      for (int i = tid; i < npad * 4; i += kTcThreads) {
+        const int n = i >> 2, blk = i & 3;
+        if (n < bt.ntok) {
+          const float* src = H + ((size_t)ptok[n] * nslot + pslot[n]) * f + kb * kTcBK + blk * 16;
+          unsigned char* dst = S.ringa + ((size_t)slot * npad * 4 + i) * ab;
 #pragma unroll
-      for (int o = 0; o < qb; o += 16) cp_async16(dq + o, q + o / 4);
-      cp_async4(S.rings + slot * kTcM + tid, reinterpret_cast<const uint32_t*>(ex.down_sb) + (size_t)rme * gpr + kb);
+          for (int o = 0; o < 4; ++o) cp_async16(dst + 16 * o, src + 4 * o);
+        }
+      }
+    }
+    if (kb < nk_ && rme < d) {
+      const int slot = kb % D;
+      unsigned char* dq = S.ringq + (size_t)(slot * kTcM + rr) * qb + hf * (qb / 2);
+      const uint32_t* q = ex.down_q + (size_t)rme * wpr + kb * (kTcBK * BITS / 32) + hf * (qb / 8);
+      if (qb / 2 == 16)
+        cp_async16(dq, q);
+      else
+        cp_async8(dq, q);
+      cp_async4(S.rings + (slot * kTcM + rr) * 2 + hf,
+                reinterpret_cast<const uint32_t*>(ex.down_sb) + (size_t)rme * gpr + kb);
     }
     cp_async_commit();
   };
@@ -442,33 +481,34 @@ k_down_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const float
   const uint32_t idesc = tc_idesc(npad);
   const int nk = f / kTcBK;
   bool ok = true;
-  for (int kb = 0; kb < kTcD - 1; ++kb) issue(kb, nk);
+  for (int kb = 0; kb < D - 1; ++kb) issue(kb, nk);
 
   for (int kb = 0; kb < nk; ++kb) {
     const int s = kb & 1;
     unsigned char* st = S.stage[s];
-    issue(kb + kTcD - 1, nk);
-    cp_async_wait<kTcD - 1>();
+    issue(kb + D - 1, nk);
+    cp_async_wait<D - 1>();
     if (kb >= 2 && !tc_mbar_wait(&S.mbar[s], (uint32_t)((kb / 2 - 1) & 1), kTcTimeoutNs)) {
       ok = false;
       break;
     }
     {
       if (rme < d) {
-        const int slot = kb % kTcD;
-        dequant_row<BITS>(reinterpret_cast<const uint32_t*>(S.ringq + (size_t)(slot * kTcM + tid) * qb),
-                          S.rings[slot * kTcM + tid], st, tid);
+        const int slot = kb % D;
+        dequant_half<BITS>(
+            reinterpret_cast<const uint32_t*>(S.ringq + (size_t)(slot * kTcM + rr) * qb + hf * (qb / 2)),
+            S.rings[(slot * kTcM + rr) * 2 + hf], st, rr, hf);
       } else {
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(st + tc_off(tid, c >> 1, (c & 1) * 8)) = make_uint4(0, 0, 0, 0);
+        for (int c = 4 * hf; c < 4 * hf + 4; ++c)
+          *reinterpret_cast<uint4*>(st + tc_off(rr, c >> 1, (c & 1) * 8)) = make_uint4(0, 0, 0, 0);
       }
     }
     for (int i = tid; i < npad * 4; i += kTcThreads) {
       const int n = i >> 2, blk = i & 3;
       float v[16];
       if (n < bt.ntok) {
-        const float* hp = H + ((size_t)ptok[n] * nslot + pslot[n]) * f + kb * kTcBK + blk * 16;
+        const float* hp = reinterpret_cast<const float*>(S.ringa + ((size_t)(kb % D) * npad * 4 + i) * ab);
 #pragma unroll
         for (int k = 0; k < 16; k += 4) {
           const float4 a = *reinterpret_cast<const float4*>(hp + k);
@@ -495,7 +535,7 @@ k_down_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const float
   }
   cp_async_wait_all();
   if (ok) ok = tc_mbar_wait(&S.mbar[(nk - 1) & 1], (uint32_t)(((nk - 1) / 2) & 1), kTcTimeoutNs);
-  if (ok) {
+  if (ok && warp < 4) {  // warp w reads tensor-memory lanes 32w..32w+31
     tc_fence_after();
     const int row = m0 + warp * 32 + (tid & 31);
     for (int c0 = 0; c0 < npad; c0 += 8) {
@@ -509,7 +549,7 @@ k_down_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const float
         }
       }
     }
-  } else {
+  } else if (!ok) {
     if (tid == 0) tc_fail(ctrl);
     tc_mbar_wait(&S.mbar[0], 0, kTcTimeoutNs / 4);
   }
@@ -524,36 +564,60 @@ static int tc_npad_max(int B) {
   return (n + 15) & ~15;
 }
 
+// Ring depth by the task width (shared memory: the rings grow with Npad).
+static int tc_depth(int npad, bool down) {
+  if (npad <= 64) return 8;
+  if (npad <= 128) return 4;
+  return down ? 1 : 2;
+}
+
+template <int BITS, int D>
+static cudaError_t gateup_tc_d(const ExpertSet& es, const Plan* plan, int B, int K, const uint16_t* x, float* H,
+                               int nslot, Ctrl* ctrl, int npad, cudaStream_t s) {
+  const size_t sm = tc_smem_bytes(2, npad, BITS, 32, D);
+  cudaError_t e = cudaFuncSetAttribute(k_gateup_tc<BITS, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  dim3 grid((es.f + kTcM - 1) / kTcM, plan_max_big(B, K));
+  k_gateup_tc<BITS, D><<<grid, kTcThreads, sm, s>>>(es, plan, B, K, x, H, nslot, ctrl);
+  return cudaGetLastError();
+}
+template <int BITS, int D>
+static cudaError_t down_tc_d(const ExpertSet& es, const Plan* plan, int B, int K, const float* H, float* Y,
+                             int nslot, Ctrl* ctrl, int npad, cudaStream_t s) {
+  const size_t sm = tc_smem_bytes(1, npad, BITS, 64, D);
+  cudaError_t e = cudaFuncSetAttribute(k_down_tc<BITS, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  dim3 grid((es.d + kTcM - 1) / kTcM, plan_max_big(B, K));
+  k_down_tc<BITS, D><<<grid, kTcThreads, sm, s>>>(es, plan, B, K, H, Y, nslot, ctrl);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gateup_tc(const ExpertSet& es, const Plan* plan, int B, int K, const uint16_t* x, float* H,
                              int nslot, Ctrl* ctrl, cudaStream_t s) {
   if (B < kBigTok) return cudaSuccess;  // no task can have 16 tokens
   const int npad = tc_npad_max(B);
-  const size_t sm = tc_smem_bytes(2, npad, es.bits);
-  dim3 grid((es.f + kTcM - 1) / kTcM, plan_max_big(B, K));
-  void* kern = es.bits == 4 ? (void*)k_gateup_tc<4> : (void*)k_gateup_tc<2>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-  if (e != cudaSuccess) return e;
+  const int D = tc_depth(npad, false);
   if (es.bits == 4)
-    k_gateup_tc<4><<<grid, kTcThreads, sm, s>>>(es, plan, B, K, x, H, nslot, ctrl);
-  else
-    k_gateup_tc<2><<<grid, kTcThreads, sm, s>>>(es, plan, B, K, x, H, nslot, ctrl);
-  return cudaGetLastError();
+    return D == 8 ? gateup_tc_d<4, 8>(es, plan, B, K, x, H, nslot, ctrl, npad, s)
+                  : D == 4 ? gateup_tc_d<4, 4>(es, plan, B, K, x, H, nslot, ctrl, npad, s)
+                           : gateup_tc_d<4, 2>(es, plan, B, K, x, H, nslot, ctrl, npad, s);
+  return D == 8 ? gateup_tc_d<2, 8>(es, plan, B, K, x, H, nslot, ctrl, npad, s)
+                : D == 4 ? gateup_tc_d<2, 4>(es, plan, B, K, x, H, nslot, ctrl, npad, s)
+                         : gateup_tc_d<2, 2>(es, plan, B, K, x, H, nslot, ctrl, npad, s);
 }
 
 cudaError_t launch_down_tc(const ExpertSet& es, const Plan* plan, int B, int K, const float* H, float* Y, int nslot,
                            Ctrl* ctrl, cudaStream_t s) {
   if (B < kBigTok) return cudaSuccess;
   const int npad = tc_npad_max(B);
-  const size_t sm = tc_smem_bytes(1, npad, es.bits);
-  dim3 grid((es.d + kTcM - 1) / kTcM, plan_max_big(B, K));
-  void* kern = es.bits == 4 ? (void*)k_down_tc<4> : (void*)k_down_tc<2>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-  if (e != cudaSuccess) return e;
+  const int D = tc_depth(npad, true);
   if (es.bits == 4)
-    k_down_tc<4><<<grid, kTcThreads, sm, s>>>(es, plan, B, K, H, Y, nslot, ctrl);
-  else
-    k_down_tc<2><<<grid, kTcThreads, sm, s>>>(es, plan, B, K, H, Y, nslot, ctrl);
-  return cudaGetLastError();
+    return D == 8 ? down_tc_d<4, 8>(es, plan, B, K, H, Y, nslot, ctrl, npad, s)
+                  : D == 4 ? down_tc_d<4, 4>(es, plan, B, K, H, Y, nslot, ctrl, npad, s)
+                           : down_tc_d<4, 1>(es, plan, B, K, H, Y, nslot, ctrl, npad, s);
+  return D == 8 ? down_tc_d<2, 8>(es, plan, B, K, H, Y, nslot, ctrl, npad, s)
+                : D == 4 ? down_tc_d<2, 4>(es, plan, B, K, H, Y, nslot, ctrl, npad, s)
+                         : down_tc_d<2, 1>(es, plan, B, K, H, Y, nslot, ctrl, npad, s);
 }
 
 }  // namespace bgq
