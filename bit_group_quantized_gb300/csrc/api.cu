@@ -158,7 +158,12 @@ Where layer_where(const bgq_moe_layer* L) {
   }
   return w;
 }
-int big_min_for(Where w) { return w == Where::kHost ? INT_MAX : kBigTok; }
+// Tokens an expert needs in a layer call before it runs on tensor cores.
+// Measured on GB300 (one layer, 4096/1024/512/top-4): with the shared
+// expert's 16 tokens on tensor cores batch 16 took 272 us, on the grouped
+// GEMVs 185 us; at 64 tokens both paths take the same time.
+constexpr int kLayerTcMinTokens = 64;
+int big_min_for(Where w) { return w == Where::kHost ? INT_MAX : kLayerTcMinTokens; }
 
 constexpr long long kFusedTimeoutNs = 2000000000ll;  // bounded waits inside the persistent kernel
 
@@ -303,7 +308,7 @@ int32_t moe_expert_swiglu(const bgq_expert* e, const uint16_t* x, int32_t batch,
     if (k == Where::kBad) return BGQ_ERR_INVALID_ARG;
     if (k == Where::kHost) where = Where::kHost;
   }
-  const int big_min = big_min_for(where);
+  const int big_min = where == Where::kHost ? INT_MAX : kBigTok;  // an explicit expert: tensor cores from 16 tokens
   if (launch_plan_single(plan, batch, big_min, s) != cudaSuccess) return BGQ_ERR_CUDA;
   if (launch_gateup(es, plan, ntasks, batch, x, H, 1, stage, s) != cudaSuccess) return BGQ_ERR_CUDA;
   if (batch >= big_min && launch_gateup_tc(es, plan, batch, 0, x, H, 1, ctrl, s) != cudaSuccess) return BGQ_ERR_CUDA;

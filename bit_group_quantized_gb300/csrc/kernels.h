@@ -34,7 +34,7 @@ struct ExpertSet {
 };
 
 constexpr int kTaskTok = 8;  // tokens per task (grouped GEMV width)
-constexpr int kBigTok = 16;  // an expert with at least this many tokens goes to the tensor-core path
+constexpr int kBigTok = 16;  // smallest tensor-core task (an explicit expert; a layer call uses 64, api.cu)
 
 // One grouped-GEMV task: expert `expert` applied to up to 8 tokens; token i's
 // result goes to slot slot[i] of token tok[i].

@@ -1,7 +1,9 @@
 // umma.cu — tensor-core (tcgen05) grouped GEMM for experts with many tokens.
 //
-// When a batch routes kBigTok (16) or more tokens to one expert (always true for
-// the shared expert at batch >= 16), the expert's three matrices are a dense
+// When a batch routes enough tokens to one expert (16 for an explicit expert,
+// 64 in a layer call, where the grouped GEMVs measured faster below that;
+// always true for the shared expert at batch >= 64), the expert's three
+// matrices are a dense
 // contraction: rows x K weights against K x tokens activations. Here the
 // weights are dequantised (w = q*scale + bias, Flash-MoE page, "FMA Dequant")
 // to fp16 in shared memory, the tokens' inputs are converted to fp16 next to

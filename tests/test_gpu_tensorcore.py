@@ -41,11 +41,11 @@ def test_expert_tensorcore_deterministic(cuda_device):
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
-@pytest.mark.parametrize("bits,B", [(4, 48), (2, 20)])
+@pytest.mark.parametrize("bits,B", [(4, 80), (2, 64)])
 def test_skewed_routing_sends_every_token_to_four_experts(cuda_device, bits, B):
     """Router rows 0..3 aligned with a component shared by all tokens: every
     token selects experts 0, 1, 2, 3, so the four routed experts (and the
-    shared one) run on the tensor-core path."""
+    shared one) get >= 64 tokens each and run on the tensor-core path."""
     E, d, f, K = 64, 1024, 512, 4
     shape = synth.PoolShape(d, f, E, bits)
     L, t = build_layer(17, 0, shape, K, cuda_device)
