@@ -440,8 +440,9 @@ static int32_t stack_decode_impl(const bgq_moe_layer* layers, const uint16_t* co
   bool all_device = true;
   for (int l = 0; l < n_layers; ++l) {
     wl[l] = layer_where(&layers[l]);
-    if (wl[l] == Where::kBad || where_is(rho[l]) == Where::kBad) return BGQ_ERR_INVALID_ARG;
-    all_device = all_device && wl[l] == Where::kDevice && where_is(rho[l]) == Where::kDevice;
+    const Where wr = where_is(rho[l]);
+    if (wl[l] == Where::kBad || wr == Where::kBad) return BGQ_ERR_INVALID_ARG;
+    all_device = all_device && wl[l] == Where::kDevice && wr == Where::kDevice;
   }
   LayerWs W = carve_layer(ws, 1, d, L0->d_ff, L0->n_experts, K);
   if (trace && !(all_device && use_fused(L0))) return BGQ_ERR_UNSUPPORTED;  // phase timestamps: persistent kernel only
