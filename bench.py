@@ -220,6 +220,25 @@ def workload_name(args) -> str:
     return f"q4_gemv: 1024x4096 4-bit, group 64, batch 1, variant {args.variant}, ring of {args.ring} matrices"
 
 
+# ------------------------------------------------------------------ ranks
+def slowest_rank(value: float, world: int, device) -> float:
+    """The largest of every rank's value (a time): the job is as slow as its
+    slowest replica. Identity for one rank."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tokens_per_s(world: int, ms_per_step: float) -> float:
+    """Every rank decodes one token per step (replicas, weak scaling)."""
+    return world * 1000.0 / ms_per_step
+
+
 # ------------------------------------------------------------------ GPU arm
 def run_ours(args):
     import torch
@@ -298,11 +317,7 @@ def run_ours(args):
     clock = clocks.stop()
     if world > 1:
         dist.barrier()
-    ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = slowest_rank(e0.elapsed_time(e1) / args.steps, world, dev)
 
     # ---- end to end through the public API with host buffers
     xh = torch.empty(D_MODEL, dtype=torch.bfloat16, pin_memory=True)
@@ -320,11 +335,7 @@ def run_ours(args):
             oh.copy_(x_out, non_blocking=True)
             stream.synchronize()
             xh.copy_(oh)
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = slowest_rank((time.perf_counter() - t0) / e2e_steps, world, dev)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -345,7 +356,7 @@ def run_ours(args):
         fused = lib.load().moe_stack_trace_entries(stack.c_layers, n_layers) > 0
         launches = 1 if fused else 1 + 6 * n_layers + 1
         line = {
-            "metric": METRIC, "value": round(world * 1000.0 / ms, 2), "unit": "tokens/s", "n_gpus": world,
+            "metric": METRIC, "value": round(whole_job_tokens_per_s(world, ms), 2), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "u4 codes x s16 fixed-point x (dp4a), f32 accumulate" if bits == 4
             else "u2 codes x s16 fixed-point x (dp4a), f32 accumulate",
