@@ -250,6 +250,80 @@ __device__ void stage_x_int16(const Src src, int T, int cols, XStage st, int* gs
   __syncthreads();
 }
 
+// The same staging with two consecutive code words per thread: half the
+// threads, so T * words <= 2 * blockDim.x takes a single pass. A group's words
+// sit on kGW/2 consecutive lanes and a part's 4 words on 2, so the group
+// maximum, the shifts and the part sums, hence every staged byte, equal
+// stage_x_int16's. All threads of the block must call; ends with __syncthreads().
+template <int BITS, typename Src>
+__device__ __forceinline__ void stage_x_int16_pairs(const Src src, int T, int cols, XStage st) {
+  using G = Geo<BITS>;
+  constexpr int kGL = kGroup / G::kPer / 2;  // lanes per group
+  const RowGeo rg = row_geo(cols, BITS);
+  const int lpr_shift = __ffs(rg.LPR) - 1;
+  const int hw = cols * BITS / 64;  // word pairs per input (cols is a multiple of 64)
+  const int total = T * hw;
+  const float inv_hw = 1.f / (float)hw;  // exact floor below, as in stage_x_int16
+  for (int base = 0; base < total; base += blockDim.x) {
+    const int i = base + threadIdx.x;
+    const bool active = i < total;
+    const int t = active ? (int)(((float)i + 0.5f) * inv_hw) : 0;
+    const int w0 = active ? 2 * (i - t * hw) : 0;
+    float v[2 * G::kPer];
+#pragma unroll
+    for (int k = 0; k < 2 * G::kPer; k += 8) {
+      if (active) {
+        src.load8(t, w0 * G::kPer + k, v + k);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[k + j] = 0.f;
+      }
+    }
+    float m = 0.f;
+#pragma unroll
+    for (int k = 0; k < 2 * G::kPer; ++k) m = fmaxf(m, fabsf(v[k]));
+#pragma unroll
+    for (int o = kGL / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+    int sh = 0;
+    if (m > 0.f) {
+      const int e = (int)((__float_as_uint(m) >> 23) & 0xff) - 127;
+      sh = 14 - e;
+      sh = sh > 126 ? 126 : (sh < -126 ? -126 : sh);
+    }
+    const float sc = exp2i(sh);
+    int xsum = 0;
+    const int p = w0 >> 2;
+    const int it = p >> lpr_shift, lp = p & (rg.LPR - 1);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      int X[G::kPer];
+#pragma unroll
+      for (int k = 0; k < G::kPer; ++k) {
+        const int q = __float_as_int(fmaf(v[h * G::kPer + k], sc, 12582912.f)) - 0x4B400000;
+        X[k] = min(q, 32767);
+        xsum += X[k];
+      }
+      uint32_t lo[G::kNvec], hi[G::kNvec];
+#pragma unroll
+      for (int j = 0; j < G::kNvec; ++j)
+        pack_lohi(X[j], X[j + G::kNvec], X[j + 2 * G::kNvec], X[j + 3 * G::kNvec], lo[j], hi[j]);
+      if (active) {
+        const int c = (w0 + h) & 3;
+        uint4* dst = st.chunks + ((((t * rg.NIT + it) * 4 + c) * G::kNch) << lpr_shift) + lp;
+#pragma unroll
+        for (int ch = 0; ch < G::kNch; ++ch)
+          dst[ch << lpr_shift] = make_uint4(lo[2 * ch], hi[2 * ch], lo[2 * ch + 1], hi[2 * ch + 1]);
+      }
+    }
+    xsum += __shfl_xor_sync(kFull, xsum, 1);  // the part's other word pair
+    if (active && (w0 & 3) == 0) {
+      const float inv = exp2i(-sh);
+      st.partinfo[t * rg.P + p] = make_float2(inv, (float)xsum * inv);
+    }
+  }
+  __syncthreads();
+}
+
 // Integer dot product of one part (4 code words) with its staged input chunks
 // xc[c*NCH + ch] and part info pi. Returns s*2^-sh*sum(q*X) + b*2^-sh*sum(X)
 // added to acc.

@@ -335,7 +335,7 @@ __device__ __forceinline__ float router_dot(const uint16_t* wrow, const uint16_t
 
 // x staging from fp32 values in shared memory (the layer input).
 template <int BITS>
-__device__ __noinline__ void stage_f32(const float* src, int ld, int T, int cols, const XStage st) {
+__device__ __forceinline__ void stage_f32(const float* src, int ld, int T, int cols, const XStage st) {
   stage_x_int16<BITS>(StridedSrc<float>{src, ld}, T, cols, st, nullptr);
 }
 // Thread 0 stamps event ev of layer l (no-op without a trace buffer).
@@ -850,7 +850,7 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
             if (i0 + j * kFThreads < n4) hks[i0 + j * kFThreads] = v[j];
         }
         __syncthreads();
-        stage_f32<BITS>(reinterpret_cast<const float*>(hks), f, K + 1, f, sth);
+        stage_x_int16_pairs<BITS>(StridedSrc<float>{reinterpret_cast<const float*>(hks), f}, K + 1, f, sth);
       }
       stamp(P, l, 13);
       mbar_wait(S.mC, par, ctrl, P.timeout_ns);
