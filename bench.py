@@ -58,6 +58,9 @@ def layer_algorithmic_bytes(bits: int) -> int:
     return layer_weight_bytes(bits) + D_MODEL * 2 + D_MODEL * 2 + D_MODEL * 4 * 2
 
 
+KERNEL_SOURCES = ("fused.cu", "common.cuh", "topk.cuh", "fused.h")  # what k_fused_decode is built from
+
+
 def profiled_traffic(n_layers: int):
     """DRAM bytes of one k_fused_decode launch, from the committed 1-layer ncu
     capture scaled by the number of layers (each layer reads the same bytes);
@@ -74,7 +77,7 @@ def profiled_traffic(n_layers: int):
             fields[k] = v.strip()
     csrc = os.path.join(ROOT, "bit_group_quantized_gb300", "csrc")
     h = hashlib.sha256()
-    for f in ("fused.cu", "common.cuh"):
+    for f in KERNEL_SOURCES:
         h.update(open(os.path.join(csrc, f), "rb").read())
     if fields.get("kernel_sources_sha256_16") != h.hexdigest()[:16] or "traffic_bytes_per_layer" not in fields:
         return None
