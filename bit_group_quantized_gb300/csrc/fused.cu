@@ -175,6 +175,9 @@ __host__ __device__ inline FGeo fgeo(int nC, int d, int f, int E, int K, int bit
   const int c_bytes = (K + 1) * rows_c * (f * bits / 8 + (f / kGroup) * 4) + (K + 1) * rows_c * 4 + 32 +
                       (K + 1) * f * 4;
   if (g.bufB < c_bytes) g.bufB = c_bytes;
+  // the selection's logits and scratch live in bufB before phase B's copies
+  const int sel_bytes = (((E + 4) & ~3) + topk_scratch_ints(E)) * 4;
+  if (g.bufB < sel_bytes) g.bufB = sel_bytes;
   return g;
 }
 
@@ -636,7 +639,8 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
   S.cpar = S.apar + 52;
   int* s_idx = S.apar + 2;                              // [8]   ints 2..9
   float* s_w = reinterpret_cast<float*>(S.apar + 10);  // [9]   ints 10..18
-  float* red = reinterpret_cast<float*>(S.apar + 20);  // [16]  ints 20..35 (< 64)
+  float* red = reinterpret_cast<float*>(S.apar + 20);  // [16]  ints 20..35
+  float* s_l = reinterpret_cast<float*>(S.apar + 36);  // [9]   ints 36..44 (< 52)
   uint16_t* a_s = reinterpret_cast<uint16_t*>(smem + FL.a_s);
   XStage sta;
   sta.chunks = reinterpret_cast<uint4*>(smem + FL.sta_chunks);
@@ -793,17 +797,21 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
       float* lg_s = reinterpret_cast<float*>(S.bufB);  // bufB is free until the B copies
       for (int e = tid; e <= E; e += kFThreads) lg_s[e] = __ldcg(P.logits + e);
       __syncthreads();
-      block_topk(lg_s, reinterpret_cast<int*>(lg_s + ((E + 4) & ~3)), E, K, has_gate, s_idx, s_w);
+      block_topk_select(lg_s, reinterpret_cast<int*>(lg_s + ((E + 4) & ~3)), E, K, has_gate, s_idx, s_l);
       stamp(P, l, 11);
-      if (blockIdx.x == 0 && tid < K) {
-        if (P.idx_out) P.idx_out[l * K + tid] = s_idx[tid];
-        if (P.w_out) P.w_out[l * K + tid] = s_w[tid];
-      }
-      if (blockIdx.x == 0 && tid == 0 && P.gamma_out) P.gamma_out[l] = s_w[K];
     }
 
     // ---------------- B: the selected experts' gate/up units (in bufB)
     if (warp == kFWarps - 1) issue_B(P, g, l, S, s_idx);  // the last warp: its phase-B units (if any) come last
+    if (warp == 0) {  // the routing weights (used by the combine) while phase B's copies start
+      block_topk_weights(s_l, K, has_gate, s_w);
+      __syncwarp();
+      if (blockIdx.x == 0 && lane < K) {
+        if (P.idx_out) P.idx_out[l * K + lane] = s_idx[lane];
+        if (P.w_out) P.w_out[l * K + lane] = s_w[lane];
+      }
+      if (blockIdx.x == 0 && lane == 0 && P.gamma_out) P.gamma_out[l] = s_w[K];
+    }
     {
       // The shared expert's gate/up units (phase A's data, in bufA) do not
       // gate the selection, so they run here, while phase B's rows stream in;

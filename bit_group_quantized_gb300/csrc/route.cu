@@ -375,6 +375,7 @@ k_route_coop(const uint16_t* __restrict__ router, const uint16_t* __restrict__ s
   float* red = reinterpret_cast<float*>(smem + (size_t)kRouteTok * d * 2);  // [warps][kRouteTok]
   __shared__ int s_idx[kMaxTopK];
   __shared__ float s_w[kMaxTopK + 1];
+  __shared__ float s_l[kMaxTopK + 1];
   __shared__ int s_last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const RouteGeo g = route_geo(d);
@@ -452,7 +453,7 @@ k_route_coop(const uint16_t* __restrict__ router, const uint16_t* __restrict__ s
       if (logits_out && e < E) logits_out[(size_t)t * E + e] = v;
     }
     __syncthreads();
-    block_topk(lgs, reinterpret_cast<int*>(lgs + ((E + 4) & ~3)), E, K, sgate != nullptr, s_idx, s_w);
+    block_topk(lgs, reinterpret_cast<int*>(lgs + ((E + 4) & ~3)), E, K, sgate != nullptr, s_idx, s_l, s_w);
     if (threadIdx.x < K) {
       idx[t * K + threadIdx.x] = s_idx[threadIdx.x];
       w[t * K + threadIdx.x] = s_w[threadIdx.x];
@@ -485,7 +486,7 @@ k_route_coop(const uint16_t* __restrict__ router, const uint16_t* __restrict__ s
 
 static size_t route_coop_smem(int d, int E) {
   size_t sm = (size_t)kRouteTok * d * 2 + kRcWarps * kRouteTok * sizeof(float);
-  const size_t sm_topk = ((size_t)((E + 4) & ~3) + 2 * kTopkWarps * 8) * sizeof(float);
+  const size_t sm_topk = ((size_t)((E + 4) & ~3) + topk_scratch_ints(E)) * sizeof(float);
   const size_t sm_plan = (size_t)(4 * E + 40) * sizeof(int);
   if (sm_topk > sm) sm = sm_topk;
   if (sm_plan > sm) sm = sm_plan;

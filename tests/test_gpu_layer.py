@@ -153,6 +153,29 @@ def test_layer_expert_permutation(cuda_device):
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
 
 
+@pytest.mark.parametrize("B", [1, 4])
+def test_layer_all_equal_logits_pick_lowest_indices(cuda_device, B):
+    """A zero router makes all 512 logits equal: the top-4 are experts 0..3
+    (ties to the lower index, the oracle's stable top-K), each weighted 1/4.
+    Every logit is then a candidate of the block top-K (its path for more
+    than 32 candidates): batch 1 runs the persistent kernel, batch 4 the
+    cooperative router."""
+    shape = synth.PoolShape(1024, 256, 512, 4)
+    L, t = build_layer(41, 0, shape, 4, cuda_device)
+    t["router"].zero_()
+    x = synth.activations(41, 1, B, shape.d, device=cuda_device)
+    out, _, idx, w, _ = lib.moe_layer_forward(L, x, want_route=True)
+    torch.cuda.synchronize()
+    assert idx.cpu().tolist() == [[0, 1, 2, 3]] * B
+    assert torch.all(w == 0.25)
+    src = ExpertSource(41, 0, shape)
+    xd = f64(x)
+    for tok in range(B):
+        ref, oi, _, _, _ = oracle_layer_token(t, src, shape, 4, xd[tok])
+        assert oi.tolist() == [0, 1, 2, 3]
+        assert_bf16_output(f64(out)[tok], ref, tok, own_tol=own_tol_for(B))
+
+
 # ------------------------------------------------------------------ stack
 def stack_case(dev, seed, n_layers, shape, K):
     built = [build_layer(seed, l, shape, K, dev) for l in range(n_layers)]
