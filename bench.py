@@ -219,7 +219,9 @@ def workload_name(args) -> str:
                 f", ring of {args.ring} distinct layers")
     if args.workload == "host":
         return (f"moe_layer with the 512 routed experts in pinned host memory (router and shared expert in HBM), "
-                f"d_model 4096, d_ff 1024, top-4, 4-bit, batch {args.batch}, ring of 16 inputs")
+                f"d_model 4096, d_ff 1024, top-4, 4-bit, batch {args.batch}, ring of 16 inputs, "
+                + ("selected experts copied into HBM slots, then computed" if args.fetch == "copy"
+                   else "selected experts read directly while computing"))
     return f"q4_gemv: 1024x4096 4-bit, group 64, batch 1, variant {args.variant}, ring of {args.ring} matrices"
 
 
@@ -467,9 +469,12 @@ def run_layer(args):
 
 def run_host(args):
     """One MoE layer whose routed-expert pool (3.6 GB) lives in pinned host
-    memory, read over the CPU-GPU link (NVLink-C2C on a GB300 node) by the
-    grouped kernels; router and shared expert stay in HBM. A ring of 16 inputs
-    selects different experts per call (16 x ~28 MB exceeds L2)."""
+    memory (NVLink-C2C on a GB300 node); router and shared expert stay in HBM.
+    --fetch direct: the grouped kernels read the selected experts straight from
+    host memory while computing (fetch overlapped with compute); --fetch copy:
+    moe_layer_forward_streamed copies them into HBM slots first, then computes
+    (serial fetch, as the pages do). A ring of 16 inputs selects different
+    experts per call (16 x ~28 MB exceeds L2)."""
     import torch
 
     from bit_group_quantized_gb300 import lib, synth
@@ -490,13 +495,18 @@ def run_host(args):
     xs = [synth.activations(args.seed + 300, r, B, D_MODEL, device=dev) for r in range(R)]
     outs = [torch.empty((B, D_MODEL), dtype=torch.bfloat16, device=dev) for _ in range(R)]
     ws = lib.workspace(lib.moe_layer_workspace_bytes(layer, B), dev)
+    copy = args.fetch == "copy"
+    slots = torch.empty(lib.moe_stream_slots_bytes(layer, B), dtype=torch.uint8, device=dev) if copy else None
     distinct = [len(set(lib.moe_layer_forward(layer, xs[r], ws=ws, want_route=True)[2].flatten().tolist()))
                 for r in range(R)]
     stream = torch.cuda.Stream(device=dev)
 
     def body():
         for r in range(R):
-            lib.moe_layer_forward(layer, xs[r], ws=ws, out=outs[r], stream=stream)
+            if copy:
+                lib.moe_layer_forward_streamed(layer, xs[r], slots=slots, ws=ws, out=outs[r], stream=stream)
+            else:
+                lib.moe_layer_forward(layer, xs[r], ws=ws, out=outs[r], stream=stream)
 
     n_rep = max(1, args.steps // R)
     clocks = ClockSampler(0)
@@ -509,7 +519,7 @@ def run_host(args):
         "steps": n_rep * R, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u4 codes; dp4a, f32 accumulate", "data": "synthetic",
         "config": {"workload": workload_name(args), "us_per_layer": round(ms * 1000, 3),
-                   "distinct_experts_mean": dmean, "host_bytes_per_layer": int(host_bytes),
+                   "fetch": args.fetch, "distinct_experts_mean": dmean, "host_bytes_per_layer": int(host_bytes),
                    "host_read_gbs": round(host_bytes / (ms * 1e-3) / 1e9, 1)},
         "roofline": None, "clocks": clock}), flush=True)
     return 0
@@ -568,6 +578,8 @@ def main():
     ap.add_argument("--ring", type=int, default=8, help="layer/gemv: distinct weight copies cycled through")
     ap.add_argument("--layers", type=int, default=24)
     ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--fetch", default="direct", choices=["direct", "copy"],
+                    help="host: read host-resident experts directly (direct) or copy them into HBM first (copy)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -374,6 +374,47 @@ int32_t moe_layer_forward(const bgq_moe_layer* L, const uint16_t* x, int32_t bat
   return layer_forward_impl(L, x, batch, out, out_f32, idx_out, w_out, gamma_out, W, where, st(stream));
 }
 
+size_t moe_stream_slots_bytes(const bgq_moe_layer* L, int32_t batch) {
+  if (!L || batch < 1 || L->top_k < 1 || L->n_experts < 1 || L->d_model <= 0 || L->d_ff <= 0) return 0;
+  if (L->bits != 4 && L->bits != 2) return 0;
+  const long long pairs = (long long)batch * L->top_k;
+  const int max_slots = (int)(pairs < L->n_experts ? pairs : L->n_experts);
+  return (size_t)slot_geo(L->d_model, L->d_ff, L->bits, max_slots).total;
+}
+
+int32_t moe_layer_forward_streamed(const bgq_moe_layer* L, const uint16_t* x, int32_t batch, uint16_t* out,
+                                   float* out_f32, int32_t* idx_out, float* w_out, float* gamma_out, void* slots,
+                                   size_t slots_bytes, void* ws, size_t ws_bytes, void* stream) {
+  int r = check_layer(L);
+  if (r) return r;
+  if (!x || !al(x, 16) || (!out && !out_f32)) return BGQ_ERR_INVALID_ARG;
+  if ((out && !al(out, 16)) || (out_f32 && !al(out_f32, 16))) return BGQ_ERR_INVALID_ARG;
+  if (batch < 1 || batch > kMaxBatch) return BGQ_ERR_INVALID_ARG;
+  if (!ws || !al(ws, 256) || ws_bytes < moe_layer_workspace_bytes(L, batch)) return BGQ_ERR_WORKSPACE;
+  if (!slots || !al(slots, 256) || slots_bytes < moe_stream_slots_bytes(L, batch)) return BGQ_ERR_WORKSPACE;
+  if (layer_where(L) == Where::kBad || where_is(slots) != Where::kDevice) return BGQ_ERR_INVALID_ARG;
+  const LayerWs W = carve_layer(ws, batch, L->d_model, L->d_ff, L->n_experts, L->top_k);
+  const cudaStream_t s = st(stream);
+  const int K = L->top_k, E = L->n_experts;
+  int32_t* idx = idx_out ? idx_out : W.idx;
+  float* w = w_out ? w_out : W.w;
+  float* gamma = gamma_out ? gamma_out : W.gamma;
+  // routing and the grouping plan (grouped GEMVs only: no tensor-core tasks)
+  if (launch_route(L->router, L->shared_gate, x, batch, L->d_model, E, K, W.logits, W.ctrl, idx, w, gamma, nullptr,
+                   W.plan, INT_MAX, s) != cudaSuccess)
+    return BGQ_ERR_CUDA;
+  // fetch: the selected experts into the slots, then compute on the slots
+  const ExpertSet pool = expert_set(L);
+  const long long pairs = (long long)batch * K;
+  const SlotGeo g = slot_geo(L->d_model, L->d_ff, L->bits, (int)(pairs < E ? pairs : E));
+  if (launch_slot_copy(W.plan, E, pool, g, slots, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  const ExpertSet es = slot_expert_set(pool, g, slots);
+  const int max_tasks = plan_max_tasks(batch, K);
+  if (launch_gateup(es, W.plan, max_tasks, batch, x, W.H, K + 1, W.stage, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  if (launch_down(es, W.plan, max_tasks, batch, W.H, W.Y, K + 1, W.stage, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  return cuda_status(launch_combine(W.Y, w, gamma, batch, K, L->d_model, out, out_f32, s));
+}
+
 int32_t bgq_rmsnorm(const float* h, const uint16_t* rho, int32_t batch, int32_t d, float eps, uint16_t* a,
                     void* stream) {
   if (!h || !a || !al(h, 16) || !al(a, 16) || (rho && !al(rho, 16))) return BGQ_ERR_INVALID_ARG;

@@ -138,6 +138,22 @@ cudaError_t launch_rmsnorm(const float* h, const uint16_t* rho, int batch, int d
 cudaError_t launch_residual_add(float* h, const float* delta, long long n, cudaStream_t s);
 cudaError_t launch_widen(const uint16_t* x, float* h, int n, cudaStream_t s);
 
+// Experts copied per layer into HBM slots (stream.cu). Slot buffer layout:
+// header (int count, then the expert of each slot), the slots' codes, then
+// their scale/bias rows, every region 256-byte aligned.
+struct SlotGeo {
+  int max_slots;
+  long long q_bytes, sb_bytes;  // one expert's codes / scale-bias bytes (gate, up, down)
+  long long slot_q, slot_sb;    // slot strides (bytes)
+  long long hdr, total;         // header bytes, whole buffer bytes
+};
+SlotGeo slot_geo(int d, int f, int bits, int max_slots);
+// Turn the plan's experts into slot numbers and copy the selected experts of
+// `pool` into the slots (two kernels on s).
+cudaError_t launch_slot_copy(Plan* plan, int E, const ExpertSet& pool, const SlotGeo& g, void* slots, cudaStream_t s);
+// The slots as an expert set (shared expert as in `pool`).
+ExpertSet slot_expert_set(const ExpertSet& pool, const SlotGeo& g, void* slots);
+
 int num_sms();
 
 }  // namespace bgq

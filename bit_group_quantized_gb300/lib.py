@@ -62,6 +62,9 @@ _SIGS = {
     "moe_layer_workspace_bytes": (_S, [C.POINTER(bgq_moe_layer), _I]),
     "moe_layer_forward": (_I, [C.POINTER(bgq_moe_layer), _P, _I, _P, _P, _P, _P, _P, _P, _S, _P]),
     "moe_layer_forward_noalloc": (_I, [C.POINTER(bgq_moe_layer), _P, _I, _P, _P, _P, _P, _P, _P]),
+    "moe_stream_slots_bytes": (_S, [C.POINTER(bgq_moe_layer), _I]),
+    "moe_layer_forward_streamed": (_I, [C.POINTER(bgq_moe_layer), _P, _I, _P, _P, _P, _P, _P, _P, _S, _P, _S,
+                                        _P]),
     "bgq_rmsnorm": (_I, [_P, _P, _I, _I, C.c_float, _P, _P]),
     "bgq_residual_add": (_I, [_P, _P, C.c_int64, _P]),
     "moe_stack_workspace_bytes": (_S, [C.POINTER(bgq_moe_layer), _I]),
@@ -254,6 +257,39 @@ def moe_layer_forward_noalloc(layer: MoELayer, x: torch.Tensor, out=None, out_f3
     s = layer.struct()
     _check(load().moe_layer_forward_noalloc(C.byref(s), _ptr(x), B, _ptr(out), _ptr(out_f32), _ptr(idx), _ptr(w),
                                             _ptr(gamma), _stream(stream)), "moe_layer_forward_noalloc")
+    return out, out_f32, idx, w, gamma
+
+
+def moe_stream_slots_bytes(layer: MoELayer, batch: int) -> int:
+    s = layer.struct()
+    return load().moe_stream_slots_bytes(C.byref(s), batch)
+
+
+def moe_layer_forward_streamed(layer: MoELayer, x: torch.Tensor, slots=None, ws=None, out=None, out_f32=None,
+                               want_out=True, want_f32=False, want_route=False, stream=None):
+    """moe_layer_forward with the selected experts copied into device `slots`
+    first (a uint8 tensor of moe_stream_slots_bytes(layer, batch) bytes), then
+    computed there."""
+    lib = load()
+    B, d = x.shape
+    dev = x.device
+    s = layer.struct()
+    if out is None and want_out:
+        out = torch.empty((B, d), dtype=torch.bfloat16, device=dev)
+    if out_f32 is None and want_f32:
+        out_f32 = torch.empty((B, d), dtype=torch.float32, device=dev)
+    idx = w = gamma = None
+    if want_route:
+        idx = torch.empty((B, layer.top_k), dtype=torch.int32, device=dev)
+        w = torch.empty((B, layer.top_k), dtype=torch.float32, device=dev)
+        gamma = torch.empty((B,), dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = workspace(lib.moe_layer_workspace_bytes(C.byref(s), B), dev)
+    if slots is None:
+        slots = torch.empty(lib.moe_stream_slots_bytes(C.byref(s), B), dtype=torch.uint8, device=dev)
+    _check(lib.moe_layer_forward_streamed(C.byref(s), _ptr(x), B, _ptr(out), _ptr(out_f32), _ptr(idx), _ptr(w),
+                                          _ptr(gamma), _ptr(slots), slots.numel(), _ptr(ws), ws.numel(),
+                                          _stream(stream)), "moe_layer_forward_streamed")
     return out, out_f32, idx, w, gamma
 
 

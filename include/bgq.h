@@ -211,6 +211,26 @@ int32_t moe_layer_forward(const bgq_moe_layer* L, const uint16_t* x, int32_t bat
 int32_t moe_layer_forward_noalloc(const bgq_moe_layer* L, const uint16_t* x, int32_t batch, uint16_t* out,
                                   float* out_f32, int32_t* idx_out, float* w_out, float* gamma_out, void* stream);
 
+/* moe_layer_forward with the selected experts fetched first (Flash-MoE page,
+ * section "架构设计：SSD当显存用": the pool stays outside GPU memory; after
+ * routing, each layer reads only its selected experts into fixed buffers and
+ * runs the expert kernels on those, fetch and compute one after the other).
+ * Here the routed pool is normally in pinned host memory (see above) and the
+ * buffers are `slots`, device memory of moe_stream_slots_bytes(L, batch)
+ * bytes, 256-byte aligned, caller-owned: a header, then min(batch * top_k,
+ * n_experts) expert slots of the pool's codes and scale/bias rows (gate, up,
+ * down). Every distinct selected expert is copied once per call, then the
+ * grouped expert kernels read the slots. The same layer through
+ * moe_layer_forward reads the host-resident experts directly while computing
+ * (fetch overlapped with compute); both give bit-identical results for
+ * batches below 16 tokens per expert. Other arguments as moe_layer_forward.
+ * Errors: as moe_layer_forward; slots NULL, misaligned or too small =>
+ * BGQ_ERR_WORKSPACE; slots not device memory => BGQ_ERR_INVALID_ARG. */
+size_t moe_stream_slots_bytes(const bgq_moe_layer* L, int32_t batch);
+int32_t moe_layer_forward_streamed(const bgq_moe_layer* L, const uint16_t* x, int32_t batch, uint16_t* out,
+                                   float* out_f32, int32_t* idx_out, float* w_out, float* gamma_out, void* slots,
+                                   size_t slots_bytes, void* ws, size_t ws_bytes, void* stream);
+
 /* a[b] = bf16( h[b] / sqrt(mean(h[b]^2) + eps) * rho ) — the RMSNorm placed
  * before each layer of a decode stack (Flash-MoE page, "架构设计": "norm").
  * h: fp32 [batch][d]; rho (nullable => 1): bf16 [d]; a: bf16 [batch][d].

@@ -145,3 +145,26 @@ def test_stack_validation(lib):
         lib.ERR_WORKSPACE
     assert L.bgq_rmsnorm(FAKE, None, 1, 100, 1e-6, FAKE, None) == lib.ERR_INVALID_ARG
     assert L.bgq_read_device_status(None, None) == lib.ERR_INVALID_ARG
+
+
+def test_streamed_slot_bytes_and_validation(lib):
+    """moe_stream_slots_bytes: a 256-byte-aligned header (count + one int per
+    slot), then min(batch*K, E) slots of one expert's gate/up/down codes and
+    scale/bias rows; the streamed forward rejects missing, short or misaligned
+    slot buffers before touching anything."""
+    L = lib.load()
+    Ls = layer_struct(lib)
+    q = 3 * 4096 * 1024 * 4 // 8           # codes of gate, up, down (4-bit)
+    sb = 3 * (4096 * 1024 // 64) * 2 * 2    # one bf16 (scale, bias) pair per group of 64
+    assert L.moe_stream_slots_bytes(C.byref(Ls), 1) == 256 + 4 * (q + sb)
+    assert L.moe_stream_slots_bytes(C.byref(Ls), 3) == 256 + 12 * (q + sb)
+    assert L.moe_stream_slots_bytes(C.byref(Ls), 200) == 2304 + 512 * (q + sb)  # capped at E slots
+    L2 = layer_struct(lib, bits=2)
+    assert L.moe_stream_slots_bytes(C.byref(L2), 1) == 256 + 4 * (q // 2 + sb)
+    need = L.moe_layer_workspace_bytes(C.byref(Ls), 1)
+    slots = L.moe_stream_slots_bytes(C.byref(Ls), 1)
+    call = lambda sl, n: L.moe_layer_forward_streamed(C.byref(Ls), FAKE, 1, FAKE, None, None, None, None, sl, n,
+                                                      FAKE, need, None)
+    assert call(None, slots) == lib.ERR_WORKSPACE
+    assert call(FAKE, slots - 256) == lib.ERR_WORKSPACE
+    assert call(FAKE + 16, slots) == lib.ERR_WORKSPACE

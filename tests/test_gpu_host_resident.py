@@ -81,3 +81,50 @@ def test_pageable_host_weights_are_rejected(cuda_device):
     with pytest.raises(lib.BGQError) as ei:
         lib.moe_layer_forward(bad, x)
     assert ei.value.status == lib.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("E,d,f,bits,B,move_router", [
+    (16, 1024, 256, 4, 1, False),
+    (16, 1024, 256, 4, 5, True),
+    (8, 512, 256, 2, 3, False),
+    (512, 4096, 1024, 4, 4, False),  # the benchmark layer
+])
+def test_streamed_layer_equals_device_layer(cuda_device, E, d, f, bits, B, move_router):
+    """Experts copied into device slots before computing give the same bits as
+    the device-resident layer, and the slot header lists exactly the distinct
+    selected experts, ascending."""
+    shape = synth.PoolShape(d, f, E, bits)
+    L, t = build_layer(24, 0, shape, 4, cuda_device)
+    t["router"].copy_((t["router"].float() * np.sqrt(4096 / d)).to(torch.bfloat16))
+    Hl, keep = host_copy(L, t, shape, 4, move_router)
+    x = synth.activations(24, 1, B, d, device=cuda_device)
+    slots = torch.empty(lib.moe_stream_slots_bytes(Hl, B), dtype=torch.uint8, device=cuda_device)
+    a = lib.moe_layer_forward(L, x, want_f32=True, want_route=True)
+    b = lib.moe_layer_forward_streamed(Hl, x, slots=slots, want_f32=True, want_route=True)
+    torch.cuda.synchronize()
+    assert torch.equal(a[2], b[2])
+    assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16))
+    assert torch.equal(a[1], b[1])
+    hdr = slots[:256].view(torch.int32).cpu()
+    distinct = sorted(set(b[2].cpu().flatten().tolist()))
+    assert int(hdr[0]) == len(distinct)
+    assert hdr[1:1 + len(distinct)].tolist() == distinct
+
+
+def test_streamed_layer_matches_oracle_at_batch_20(cuda_device):
+    shape = synth.PoolShape(1024, 512, 16, 4)
+    L, t = build_layer(25, 0, shape, 4, cuda_device)
+    t["router"].copy_((t["router"].float() * np.sqrt(4096 / 1024)).to(torch.bfloat16))
+    Hl, keep = host_copy(L, t, shape, 4, move_router=True)
+    B = 20
+    x = synth.activations(25, 1, B, shape.d, device=cuda_device)
+    out, _, idx, _, _ = lib.moe_layer_forward_streamed(Hl, x, want_route=True)
+    torch.cuda.synchronize()
+    src = ExpertSource(25, 0, shape)
+    xd = f64(x)
+    for tok in (0, 9, 19):
+        gi = idx[tok].cpu().numpy()
+        ref, oi, _, _, logits = oracle_layer_token(t, src, shape, 4, xd[tok], gi)
+        if topk_gap(logits, 4) > TIE_GAP:
+            assert gi.tolist() == oi.tolist()
+        assert_bf16_output(f64(out)[tok], ref, tok, own_tol=own_tol_for(1))
