@@ -54,6 +54,11 @@ struct Carver {
   }
 };
 
+// A layer call sends an expert to the tensor cores from 64 tokens (the
+// grouped GEMVs are faster below that on this GPU; an explicit expert call
+// uses kBigTok).
+constexpr int kLayerTcMinTokens = 64;
+
 struct LayerWs {
   Ctrl* ctrl;
   float* logits;  // [B][E+1] then B*K ints of selected experts
@@ -69,6 +74,7 @@ struct LayerWs {
   float* fpart;     // [2][1024] per-CTA sums of squares
   int32_t* fidx;    // [16]
   float* fw;        // [16]
+  unsigned char* tcs;  // split-K scratch of the tensor-core kernels (batches that can use them)
   size_t bytes;
 };
 
@@ -91,6 +97,7 @@ LayerWs carve_layer(void* ws, int B, int d, int f, int E, int K) {
   L.fpart = c.take<float>(2 * 1024 * 4);
   L.fidx = c.take<int32_t>(16 * 4);
   L.fw = c.take<float>(16 * 4);
+  L.tcs = B >= kLayerTcMinTokens ? c.take<unsigned char>(tc_split_bytes(d, f, B, K)) : nullptr;
   L.bytes = c.off;
   return L;
 }
@@ -162,7 +169,6 @@ Where layer_where(const bgq_moe_layer* L) {
 // Measured on GB300 (one layer, 4096/1024/512/top-4): with the shared
 // expert's 16 tokens on tensor cores batch 16 took 272 us, on the grouped
 // GEMVs 185 us; at 64 tokens both paths take the same time.
-constexpr int kLayerTcMinTokens = 64;
 int big_min_for(Where w) { return w == Where::kHost ? INT_MAX : kLayerTcMinTokens; }
 
 constexpr long long kFusedTimeoutNs = 2000000000ll;  // bounded waits inside the persistent kernel
@@ -272,7 +278,7 @@ size_t moe_expert_workspace_bytes(const bgq_expert* e, int32_t batch) {
   const int d = e->gate.cols, f = e->gate.rows;
   const size_t sx = staged_tokens_bytes(d, 4, batch), sh = staged_tokens_bytes(f, 4, batch);
   return sizeof(Ctrl) + up256(plan_bytes(batch, 0)) + up256((size_t)batch * f * 4) + up256((size_t)batch * d * 4) +
-         up256(sx > sh ? sx : sh);
+         up256(sx > sh ? sx : sh) + (batch >= kBigTok ? up256(tc_split_bytes(d, f, batch, 0)) : 0);
 }
 
 int32_t moe_expert_swiglu(const bgq_expert* e, const uint16_t* x, int32_t batch, uint16_t* y, float* y_f32,
@@ -294,6 +300,8 @@ int32_t moe_expert_swiglu(const bgq_expert* e, const uint16_t* x, int32_t batch,
   float* Y = c.take<float>((size_t)batch * d * 4);
   const size_t sx = staged_tokens_bytes(d, 4, batch), sh = staged_tokens_bytes(f, 4, batch);
   unsigned char* stage = c.take<unsigned char>(sx > sh ? sx : sh);
+  const TcSplit sp = batch >= kBigTok ? tc_split_carve(c.take<unsigned char>(tc_split_bytes(d, f, batch, 0)), d, f, batch, 0)
+                                      : TcSplit{nullptr, nullptr};
   ExpertSet es{};
   es.shared = ExpertRef{e->gate.q, e->gate.sb, e->up.q, e->up.sb, e->down.q, e->down.sb};
   es.d = d;
@@ -311,9 +319,9 @@ int32_t moe_expert_swiglu(const bgq_expert* e, const uint16_t* x, int32_t batch,
   const int big_min = where == Where::kHost ? INT_MAX : kBigTok;  // an explicit expert: tensor cores from 16 tokens
   if (launch_plan_single(plan, batch, big_min, s) != cudaSuccess) return BGQ_ERR_CUDA;
   if (launch_gateup(es, plan, ntasks, batch, x, H, 1, stage, s) != cudaSuccess) return BGQ_ERR_CUDA;
-  if (batch >= big_min && launch_gateup_tc(es, plan, batch, 0, x, H, 1, ctrl, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  if (batch >= big_min && launch_gateup_tc(es, plan, batch, 0, x, H, 1, ctrl, sp, s) != cudaSuccess) return BGQ_ERR_CUDA;
   if (launch_down(es, plan, ntasks, batch, H, Y, 1, stage, s) != cudaSuccess) return BGQ_ERR_CUDA;
-  if (batch >= big_min && launch_down_tc(es, plan, batch, 0, H, Y, 1, ctrl, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  if (batch >= big_min && launch_down_tc(es, plan, batch, 0, H, Y, 1, ctrl, sp, s) != cudaSuccess) return BGQ_ERR_CUDA;
   return cuda_status(launch_combine(Y, nullptr, nullptr, batch, 0, d, y, y_f32, s));
 }
 
@@ -338,9 +346,10 @@ static int32_t layer_forward_impl(const bgq_moe_layer* L, const uint16_t* x, int
   // experts with < 16 tokens: grouped GEMV; with >= 16: tensor-core GEMM
   if (launch_gateup(es, W.plan, max_tasks, batch, x, W.H, K + 1, W.stage, s) != cudaSuccess) return BGQ_ERR_CUDA;
   const bool tc = batch >= big_min;
-  if (tc && launch_gateup_tc(es, W.plan, batch, K, x, W.H, K + 1, W.ctrl, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  const TcSplit sp = W.tcs ? tc_split_carve(W.tcs, L->d_model, L->d_ff, batch, K) : TcSplit{nullptr, nullptr};
+  if (tc && launch_gateup_tc(es, W.plan, batch, K, x, W.H, K + 1, W.ctrl, sp, s) != cudaSuccess) return BGQ_ERR_CUDA;
   if (launch_down(es, W.plan, max_tasks, batch, W.H, W.Y, K + 1, W.stage, s) != cudaSuccess) return BGQ_ERR_CUDA;
-  if (tc && launch_down_tc(es, W.plan, batch, K, W.H, W.Y, K + 1, W.ctrl, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  if (tc && launch_down_tc(es, W.plan, batch, K, W.H, W.Y, K + 1, W.ctrl, sp, s) != cudaSuccess) return BGQ_ERR_CUDA;
   return cuda_status(launch_combine(W.Y, w, gamma, batch, K, L->d_model, out, out_f32, s));
 }
 

@@ -263,13 +263,31 @@ size_t tc_smem_bytes(int na, int npad, int bits, int ab, int D) {
 
 __device__ __forceinline__ void tc_fail(Ctrl* ctrl) { atomicExch(&ctrl->status, BGQ_ERR_TIMEOUT); }
 
+// Split K: every CTA of a tile publishes its partial sums, then counts itself
+// in *cnt; true (for the whole block) in the last one, which resets *cnt for
+// the next launch. Nothing waits, so a failed CTA cannot hang the others.
+__device__ bool tc_last_of_tile(int* cnt, int nsplit) {
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int prev = atomicAdd(cnt, 1);
+    s_last = prev == nsplit - 1;
+    if (s_last) *cnt = 0;
+  }
+  __syncthreads();
+  if (s_last) __threadfence();
+  return s_last != 0;
+}
+
 // ---------------------------------------------------------------------------
-// gate/up + SiLU*mul: blockIdx.x = tile of 128 rows of d_ff, blockIdx.y = big task.
+// gate/up + SiLU*mul: blockIdx.x = tile of 128 rows of d_ff x nsplit K ranges,
+// blockIdx.y = big task.
 // ---------------------------------------------------------------------------
 template <int BITS, int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
 k_gateup_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const uint16_t* __restrict__ x,
-            float* __restrict__ H, int nslot, Ctrl* ctrl) {
+            float* __restrict__ H, int nslot, Ctrl* ctrl, TcSplit sp, int nsplit) {
   extern __shared__ __align__(1024) unsigned char smem[];
   if ((int)blockIdx.y >= plan->nbig) return;
   const BigTask bt = plan_big(plan, B, K)[blockIdx.y];
@@ -278,7 +296,8 @@ k_gateup_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const uin
   const int d = es.d, f = es.f;
   const int npad = (bt.ntok + 15) & ~15;
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int m0 = blockIdx.x * kTcM;
+  const int tile = blockIdx.x / nsplit, split = blockIdx.x - tile * nsplit;
+  const int m0 = tile * kTcM;
   TcSmem S = tc_carve(smem, 2, npad, BITS, D);
   const ExpertRef ex = tc_resolve(es, bt.expert);
   const int wpr = d * BITS / 32, gpr = d / kGroup;
@@ -333,16 +352,18 @@ k_gateup_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const uin
   tc_fence_after();
   const uint32_t tbase = *S.tslot;
   const uint32_t idesc = tc_idesc(npad);
-  const int nk = d / kTcBK;
+  const int nkt = d / kTcBK;  // K steps of the whole row; this CTA takes [kb0, nk)
+  const int kb0 = nkt * split / nsplit, nk = nkt * (split + 1) / nsplit;
   bool ok = true;
-  for (int kb = 0; kb < D - 1; ++kb) issue(kb, nk);
+  for (int kb = kb0; kb < kb0 + D - 1; ++kb) issue(kb, nk);
 
-  for (int kb = 0; kb < nk; ++kb) {
-    const int s = kb & 1;
+  for (int kb = kb0; kb < nk; ++kb) {
+    const int j = kb - kb0;  // local step: stage and mbarrier phase
+    const int s = j & 1;
     unsigned char* st = S.stage[s];
     issue(kb + D - 1, nk);
     cp_async_wait<D - 1>();  // this thread's copies of step kb have landed
-    if (kb >= 2 && !tc_mbar_wait(&S.mbar[s], (uint32_t)((kb / 2 - 1) & 1), kTcTimeoutNs)) {
+    if (j >= 2 && !tc_mbar_wait(&S.mbar[s], (uint32_t)((j / 2 - 1) & 1), kTcTimeoutNs)) {
       ok = false;
       break;
     }
@@ -381,17 +402,19 @@ k_gateup_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const uin
     if (tid == 0) {
       tc_fence_after();
 #pragma unroll
-      for (int j = 0; j < kTcBK / 16; ++j) {
-        const uint64_t bd = tc_desc(st + S.b_off + j * 256);
-        tc_mma(tbase, tc_desc(st + j * 256), bd, idesc, (kb | j) ? 1u : 0u);
-        tc_mma(tbase + npad, tc_desc(st + S.a_bytes + j * 256), bd, idesc, (kb | j) ? 1u : 0u);
+      for (int jj = 0; jj < kTcBK / 16; ++jj) {
+        const uint64_t bd = tc_desc(st + S.b_off + jj * 256);
+        tc_mma(tbase, tc_desc(st + jj * 256), bd, idesc, (j | jj) ? 1u : 0u);
+        tc_mma(tbase + npad, tc_desc(st + S.a_bytes + jj * 256), bd, idesc, (j | jj) ? 1u : 0u);
       }
       tc_commit(&S.mbar[s]);
     }
   }
   cp_async_wait_all();
   // the last commit covers every MMA
-  if (ok) ok = tc_mbar_wait(&S.mbar[(nk - 1) & 1], (uint32_t)(((nk - 1) / 2) & 1), kTcTimeoutNs);
+  const int nl = nk - kb0;
+  if (ok) ok = tc_mbar_wait(&S.mbar[(nl - 1) & 1], (uint32_t)(((nl - 1) / 2) & 1), kTcTimeoutNs);
+  const size_t pc = (size_t)plan_max_pairs(B, K);
   if (ok && warp < 4) {  // warp w reads tensor-memory lanes 32w..32w+31
     tc_fence_after();
     const int row = m0 + warp * 32 + (tid & 31);
@@ -404,7 +427,14 @@ k_gateup_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const uin
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int n = c0 + i;
-          if (n < bt.ntok) H[((size_t)ptok[n] * nslot + pslot[n]) * f + row] = g[i] / (1.f + expf(-g[i])) * u[i];
+          if (n >= bt.ntok) continue;
+          if (nsplit == 1) {
+            H[((size_t)ptok[n] * nslot + pslot[n]) * f + row] = g[i] / (1.f + expf(-g[i])) * u[i];
+          } else {  // partial sums of this K range: [split][pair][gate, up][row]
+            float* pp = sp.part + (((size_t)split * pc + bt.first + n) * 2) * f + row;
+            pp[0] = g[i];
+            pp[f] = u[i];
+          }
         }
       }
     }
@@ -416,15 +446,30 @@ k_gateup_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const uin
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_free(tbase, ncols);
+  if (nsplit > 1 && tc_last_of_tile(sp.cnt + (size_t)blockIdx.y * gridDim.x / nsplit + tile, nsplit)) {
+    // the tile's last CTA: partial sums in split order, then SiLU(gate) * up
+    for (int i = tid; i < kTcM * bt.ntok; i += kTcThreads) {
+      const int n = i / kTcM, row = m0 + (i - n * kTcM);
+      if (row >= f) continue;
+      const float* pp = sp.part + ((size_t)bt.first + n) * 2 * f + row;
+      float g = 0.f, u = 0.f;
+      for (int q = 0; q < nsplit; ++q) {
+        g += __ldcg(pp + (size_t)q * pc * 2 * f);
+        u += __ldcg(pp + (size_t)q * pc * 2 * f + f);
+      }
+      H[((size_t)ptok[n] * nslot + pslot[n]) * f + row] = g / (1.f + expf(-g)) * u;
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
-// down projection: blockIdx.x = tile of 128 rows of d_model, blockIdx.y = big task.
+// down projection: blockIdx.x = tile of 128 rows of d_model x nsplit K ranges,
+// blockIdx.y = big task.
 // ---------------------------------------------------------------------------
 template <int BITS, int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
 k_down_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const float* __restrict__ H,
-          float* __restrict__ Y, int nslot, Ctrl* ctrl) {
+          float* __restrict__ Y, int nslot, Ctrl* ctrl, TcSplit sp, int nsplit) {
   extern __shared__ __align__(1024) unsigned char smem[];
   if ((int)blockIdx.y >= plan->nbig) return;
   const BigTask bt = plan_big(plan, B, K)[blockIdx.y];
@@ -433,7 +478,8 @@ k_down_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const float
   const int d = es.d, f = es.f;
   const int npad = (bt.ntok + 15) & ~15;
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int m0 = blockIdx.x * kTcM;
+  const int tile = blockIdx.x / nsplit, split = blockIdx.x - tile * nsplit;
+  const int m0 = tile * kTcM;
   TcSmem S = tc_carve(smem, 1, npad, BITS, D);
   const ExpertRef ex = tc_resolve(es, bt.expert);
   const int wpr = f * BITS / 32, gpr = f / kGroup;
@@ -481,16 +527,18 @@ k_down_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const float
   tc_fence_after();
   const uint32_t tbase = *S.tslot;
   const uint32_t idesc = tc_idesc(npad);
-  const int nk = f / kTcBK;
+  const int nkt = f / kTcBK;  // K steps of the whole row; this CTA takes [kb0, nk)
+  const int kb0 = nkt * split / nsplit, nk = nkt * (split + 1) / nsplit;
   bool ok = true;
-  for (int kb = 0; kb < D - 1; ++kb) issue(kb, nk);
+  for (int kb = kb0; kb < kb0 + D - 1; ++kb) issue(kb, nk);
 
-  for (int kb = 0; kb < nk; ++kb) {
-    const int s = kb & 1;
+  for (int kb = kb0; kb < nk; ++kb) {
+    const int j = kb - kb0;  // local step: stage and mbarrier phase
+    const int s = j & 1;
     unsigned char* st = S.stage[s];
     issue(kb + D - 1, nk);
     cp_async_wait<D - 1>();
-    if (kb >= 2 && !tc_mbar_wait(&S.mbar[s], (uint32_t)((kb / 2 - 1) & 1), kTcTimeoutNs)) {
+    if (j >= 2 && !tc_mbar_wait(&S.mbar[s], (uint32_t)((j / 2 - 1) & 1), kTcTimeoutNs)) {
       ok = false;
       break;
     }
@@ -530,13 +578,15 @@ k_down_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const float
     if (tid == 0) {
       tc_fence_after();
 #pragma unroll
-      for (int j = 0; j < kTcBK / 16; ++j)
-        tc_mma(tbase, tc_desc(st + j * 256), tc_desc(st + S.b_off + j * 256), idesc, (kb | j) ? 1u : 0u);
+      for (int jj = 0; jj < kTcBK / 16; ++jj)
+        tc_mma(tbase, tc_desc(st + jj * 256), tc_desc(st + S.b_off + jj * 256), idesc, (j | jj) ? 1u : 0u);
       tc_commit(&S.mbar[s]);
     }
   }
   cp_async_wait_all();
-  if (ok) ok = tc_mbar_wait(&S.mbar[(nk - 1) & 1], (uint32_t)(((nk - 1) / 2) & 1), kTcTimeoutNs);
+  const int nl = nk - kb0;
+  if (ok) ok = tc_mbar_wait(&S.mbar[(nl - 1) & 1], (uint32_t)(((nl - 1) / 2) & 1), kTcTimeoutNs);
+  const size_t pc = (size_t)plan_max_pairs(B, K);
   if (ok && warp < 4) {  // warp w reads tensor-memory lanes 32w..32w+31
     tc_fence_after();
     const int row = m0 + warp * 32 + (tid & 31);
@@ -547,7 +597,11 @@ k_down_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const float
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int n = c0 + i;
-          if (n < bt.ntok) Y[((size_t)ptok[n] * nslot + pslot[n]) * d + row] = y[i];
+          if (n >= bt.ntok) continue;
+          if (nsplit == 1)
+            Y[((size_t)ptok[n] * nslot + pslot[n]) * d + row] = y[i];
+          else  // partial sums of this K range: [split][pair][row]
+            sp.part[((size_t)split * pc + bt.first + n) * d + row] = y[i];
         }
       }
     }
@@ -558,6 +612,16 @@ k_down_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const float
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_free(tbase, ncols);
+  if (nsplit > 1 && tc_last_of_tile(sp.cnt + (size_t)blockIdx.y * gridDim.x / nsplit + tile, nsplit)) {
+    for (int i = tid; i < kTcM * bt.ntok; i += kTcThreads) {
+      const int n = i / kTcM, row = m0 + (i - n * kTcM);
+      if (row >= d) continue;
+      const float* pp = sp.part + ((size_t)bt.first + n) * d + row;
+      float y = 0.f;
+      for (int q = 0; q < nsplit; ++q) y += __ldcg(pp + (size_t)q * pc * d);
+      Y[((size_t)ptok[n] * nslot + pslot[n]) * d + row] = y;
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -573,53 +637,82 @@ static int tc_depth(int npad, bool down) {
   return down ? 1 : 2;
 }
 
+// K splits: about eight 64-column steps per CTA for gate/up (d columns), four
+// for down (f columns), at most eight splits.
+static int tc_split_gu(int d) {
+  const int n = d / kTcBK / 8;
+  return n < 1 ? 1 : (n > 8 ? 8 : n);
+}
+static int tc_split_dn(int f) {
+  const int n = f / kTcBK / 4;
+  return n < 1 ? 1 : (n > 8 ? 8 : n);
+}
+static size_t tc_up256(size_t n) { return (n + 255) & ~(size_t)255; }
+
+size_t tc_split_bytes(int d, int f, int B, int K) {
+  const size_t pc = (size_t)plan_max_pairs(B, K);
+  const size_t pg = (size_t)tc_split_gu(d) * pc * 2 * f, pd = (size_t)tc_split_dn(f) * pc * d;
+  const size_t tiles = (size_t)((d > f ? d : f) + kTcM - 1) / kTcM;
+  return tc_up256((pg > pd ? pg : pd) * 4) + tc_up256(tiles * plan_max_big(B, K) * 4);
+}
+TcSplit tc_split_carve(void* p, int d, int f, int B, int K) {
+  const size_t pc = (size_t)plan_max_pairs(B, K);
+  const size_t pg = (size_t)tc_split_gu(d) * pc * 2 * f, pd = (size_t)tc_split_dn(f) * pc * d;
+  TcSplit sp;
+  sp.part = static_cast<float*>(p);
+  sp.cnt = reinterpret_cast<int*>(static_cast<unsigned char*>(p) + tc_up256((pg > pd ? pg : pd) * 4));
+  return sp;
+}
+
 template <int BITS, int D>
 static cudaError_t gateup_tc_d(const ExpertSet& es, const Plan* plan, int B, int K, const uint16_t* x, float* H,
-                               int nslot, Ctrl* ctrl, int npad, cudaStream_t s) {
+                               int nslot, Ctrl* ctrl, const TcSplit& sp, int npad, cudaStream_t s) {
   const size_t sm = tc_smem_bytes(2, npad, BITS, 32, D);
   cudaError_t e = cudaFuncSetAttribute(k_gateup_tc<BITS, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
-  dim3 grid((es.f + kTcM - 1) / kTcM, plan_max_big(B, K));
-  k_gateup_tc<BITS, D><<<grid, kTcThreads, sm, s>>>(es, plan, B, K, x, H, nslot, ctrl);
+  const int ns = sp.part ? tc_split_gu(es.d) : 1;
+  dim3 grid((es.f + kTcM - 1) / kTcM * ns, plan_max_big(B, K));
+  k_gateup_tc<BITS, D><<<grid, kTcThreads, sm, s>>>(es, plan, B, K, x, H, nslot, ctrl, sp, ns);
   return cudaGetLastError();
 }
 template <int BITS, int D>
 static cudaError_t down_tc_d(const ExpertSet& es, const Plan* plan, int B, int K, const float* H, float* Y,
-                             int nslot, Ctrl* ctrl, int npad, cudaStream_t s) {
+                             int nslot, Ctrl* ctrl, const TcSplit& sp, int npad, cudaStream_t s) {
   const size_t sm = tc_smem_bytes(1, npad, BITS, 64, D);
   cudaError_t e = cudaFuncSetAttribute(k_down_tc<BITS, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
-  dim3 grid((es.d + kTcM - 1) / kTcM, plan_max_big(B, K));
-  k_down_tc<BITS, D><<<grid, kTcThreads, sm, s>>>(es, plan, B, K, H, Y, nslot, ctrl);
+  const int ns = sp.part ? tc_split_dn(es.f) : 1;
+  dim3 grid((es.d + kTcM - 1) / kTcM * ns, plan_max_big(B, K));
+  k_down_tc<BITS, D><<<grid, kTcThreads, sm, s>>>(es, plan, B, K, H, Y, nslot, ctrl, sp, ns);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gateup_tc(const ExpertSet& es, const Plan* plan, int B, int K, const uint16_t* x, float* H,
-                             int nslot, Ctrl* ctrl, cudaStream_t s) {
+                             int nslot, Ctrl* ctrl, const TcSplit& sp, cudaStream_t s) {
   if (B < kBigTok) return cudaSuccess;  // no task can have 16 tokens
   const int npad = tc_npad_max(B);
   const int D = tc_depth(npad, false);
   if (es.bits == 4)
-    return D == 8 ? gateup_tc_d<4, 8>(es, plan, B, K, x, H, nslot, ctrl, npad, s)
-                  : D == 4 ? gateup_tc_d<4, 4>(es, plan, B, K, x, H, nslot, ctrl, npad, s)
-                           : gateup_tc_d<4, 2>(es, plan, B, K, x, H, nslot, ctrl, npad, s);
-  return D == 8 ? gateup_tc_d<2, 8>(es, plan, B, K, x, H, nslot, ctrl, npad, s)
-                : D == 4 ? gateup_tc_d<2, 4>(es, plan, B, K, x, H, nslot, ctrl, npad, s)
-                         : gateup_tc_d<2, 2>(es, plan, B, K, x, H, nslot, ctrl, npad, s);
+    return D == 8 ? gateup_tc_d<4, 8>(es, plan, B, K, x, H, nslot, ctrl, sp, npad, s)
+                  : D == 4 ? gateup_tc_d<4, 4>(es, plan, B, K, x, H, nslot, ctrl, sp, npad, s)
+                           : gateup_tc_d<4, 2>(es, plan, B, K, x, H, nslot, ctrl, sp, npad, s);
+  return D == 8 ? gateup_tc_d<2, 8>(es, plan, B, K, x, H, nslot, ctrl, sp, npad, s)
+                : D == 4 ? gateup_tc_d<2, 4>(es, plan, B, K, x, H, nslot, ctrl, sp, npad, s)
+                         : gateup_tc_d<2, 2>(es, plan, B, K, x, H, nslot, ctrl, sp, npad, s);
 }
 
 cudaError_t launch_down_tc(const ExpertSet& es, const Plan* plan, int B, int K, const float* H, float* Y, int nslot,
-                           Ctrl* ctrl, cudaStream_t s) {
+                           Ctrl* ctrl, const TcSplit& sp, cudaStream_t s) {
   if (B < kBigTok) return cudaSuccess;
   const int npad = tc_npad_max(B);
   const int D = tc_depth(npad, true);
   if (es.bits == 4)
-    return D == 8 ? down_tc_d<4, 8>(es, plan, B, K, H, Y, nslot, ctrl, npad, s)
-                  : D == 4 ? down_tc_d<4, 4>(es, plan, B, K, H, Y, nslot, ctrl, npad, s)
-                           : down_tc_d<4, 1>(es, plan, B, K, H, Y, nslot, ctrl, npad, s);
-  return D == 8 ? down_tc_d<2, 8>(es, plan, B, K, H, Y, nslot, ctrl, npad, s)
-                : D == 4 ? down_tc_d<2, 4>(es, plan, B, K, H, Y, nslot, ctrl, npad, s)
-                         : down_tc_d<2, 1>(es, plan, B, K, H, Y, nslot, ctrl, npad, s);
+    return D == 8 ? down_tc_d<4, 8>(es, plan, B, K, H, Y, nslot, ctrl, sp, npad, s)
+                  : D == 4 ? down_tc_d<4, 4>(es, plan, B, K, H, Y, nslot, ctrl, sp, npad, s)
+                           : down_tc_d<4, 1>(es, plan, B, K, H, Y, nslot, ctrl, sp, npad, s);
+  return D == 8 ? down_tc_d<2, 8>(es, plan, B, K, H, Y, nslot, ctrl, sp, npad, s)
+                : D == 4 ? down_tc_d<2, 4>(es, plan, B, K, H, Y, nslot, ctrl, sp, npad, s)
+                         : down_tc_d<2, 1>(es, plan, B, K, H, Y, nslot, ctrl, sp, npad, s);
 }
 
 }  // namespace bgq
