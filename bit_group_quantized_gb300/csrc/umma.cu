@@ -263,6 +263,8 @@ size_t tc_smem_bytes(int na, int npad, int bits, int ab, int D) {
 
 __device__ __forceinline__ void tc_fail(Ctrl* ctrl) { atomicExch(&ctrl->status, BGQ_ERR_TIMEOUT); }
 
+constexpr int kTcMaxSplit = 8;  // K splits per tile (partial sums reduced by the tile's last CTA)
+
 // Split K: every CTA of a tile publishes its partial sums, then counts itself
 // in *cnt; true (for the whole block) in the last one, which resets *cnt for
 // the next launch. Nothing waits, so a failed CTA cannot hang the others.
@@ -447,17 +449,33 @@ k_gateup_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const uin
   __syncthreads();
   if (warp == 0) tmem_free(tbase, ncols);
   if (nsplit > 1 && tc_last_of_tile(sp.cnt + (size_t)blockIdx.y * gridDim.x / nsplit + tile, nsplit)) {
-    // the tile's last CTA: partial sums in split order, then SiLU(gate) * up
-    for (int i = tid; i < kTcM * bt.ntok; i += kTcThreads) {
-      const int n = i / kTcM, row = m0 + (i - n * kTcM);
-      if (row >= f) continue;
-      const float* pp = sp.part + ((size_t)bt.first + n) * 2 * f + row;
-      float g = 0.f, u = 0.f;
-      for (int q = 0; q < nsplit; ++q) {
-        g += __ldcg(pp + (size_t)q * pc * 2 * f);
-        u += __ldcg(pp + (size_t)q * pc * 2 * f + f);
-      }
-      H[((size_t)ptok[n] * nslot + pslot[n]) * f + row] = g / (1.f + expf(-g)) * u;
+    // the tile's last CTA: partial sums in split order, then SiLU(gate) * up;
+    // four consecutive rows per thread, every split's loads in flight at once
+    for (int i = tid; i < (kTcM / 4) * bt.ntok; i += kTcThreads) {
+      const int n = i / (kTcM / 4), row = m0 + 4 * (i - n * (kTcM / 4));
+      if (row >= f) continue;  // f is a multiple of 64
+      const float4* pp = reinterpret_cast<const float4*>(sp.part + ((size_t)bt.first + n) * 2 * f + row);
+      const size_t qs = pc * 2 * f / 4, us = f / 4;
+      float4 gq[kTcMaxSplit], uq[kTcMaxSplit];
+#pragma unroll
+      for (int q = 0; q < kTcMaxSplit; ++q)
+        if (q < nsplit) {
+          gq[q] = __ldcg(pp + q * qs);
+          uq[q] = __ldcg(pp + q * qs + us);
+        }
+      float4 g = gq[0], u = uq[0];
+#pragma unroll
+      for (int q = 1; q < kTcMaxSplit; ++q)
+        if (q < nsplit) {
+          g.x += gq[q].x; g.y += gq[q].y; g.z += gq[q].z; g.w += gq[q].w;
+          u.x += uq[q].x; u.y += uq[q].y; u.z += uq[q].z; u.w += uq[q].w;
+        }
+      float4 h;
+      h.x = g.x / (1.f + expf(-g.x)) * u.x;
+      h.y = g.y / (1.f + expf(-g.y)) * u.y;
+      h.z = g.z / (1.f + expf(-g.z)) * u.z;
+      h.w = g.w / (1.f + expf(-g.w)) * u.w;
+      *reinterpret_cast<float4*>(H + ((size_t)ptok[n] * nslot + pslot[n]) * f + row) = h;
     }
   }
 }
@@ -613,13 +631,22 @@ k_down_tc(ExpertSet es, const Plan* __restrict__ plan, int B, int K, const float
   __syncthreads();
   if (warp == 0) tmem_free(tbase, ncols);
   if (nsplit > 1 && tc_last_of_tile(sp.cnt + (size_t)blockIdx.y * gridDim.x / nsplit + tile, nsplit)) {
-    for (int i = tid; i < kTcM * bt.ntok; i += kTcThreads) {
-      const int n = i / kTcM, row = m0 + (i - n * kTcM);
-      if (row >= d) continue;
-      const float* pp = sp.part + ((size_t)bt.first + n) * d + row;
-      float y = 0.f;
-      for (int q = 0; q < nsplit; ++q) y += __ldcg(pp + (size_t)q * pc * d);
-      Y[((size_t)ptok[n] * nslot + pslot[n]) * d + row] = y;
+    for (int i = tid; i < (kTcM / 4) * bt.ntok; i += kTcThreads) {
+      const int n = i / (kTcM / 4), row = m0 + 4 * (i - n * (kTcM / 4));
+      if (row >= d) continue;  // d is a multiple of 64
+      const float4* pp = reinterpret_cast<const float4*>(sp.part + ((size_t)bt.first + n) * d + row);
+      const size_t qs = pc * d / 4;
+      float4 yq[kTcMaxSplit];
+#pragma unroll
+      for (int q = 0; q < kTcMaxSplit; ++q)
+        if (q < nsplit) yq[q] = __ldcg(pp + q * qs);
+      float4 y = yq[0];
+#pragma unroll
+      for (int q = 1; q < kTcMaxSplit; ++q)
+        if (q < nsplit) {
+          y.x += yq[q].x; y.y += yq[q].y; y.z += yq[q].z; y.w += yq[q].w;
+        }
+      *reinterpret_cast<float4*>(Y + ((size_t)ptok[n] * nslot + pslot[n]) * d + row) = y;
     }
   }
 }
@@ -641,11 +668,11 @@ static int tc_depth(int npad, bool down) {
 // for down (f columns), at most eight splits.
 static int tc_split_gu(int d) {
   const int n = d / kTcBK / 8;
-  return n < 1 ? 1 : (n > 8 ? 8 : n);
+  return n < 1 ? 1 : (n > kTcMaxSplit ? kTcMaxSplit : n);
 }
 static int tc_split_dn(int f) {
   const int n = f / kTcBK / 4;
-  return n < 1 ? 1 : (n > 8 ? 8 : n);
+  return n < 1 ? 1 : (n > kTcMaxSplit ? kTcMaxSplit : n);
 }
 static size_t tc_up256(size_t n) { return (n + 255) & ~(size_t)255; }
 
