@@ -320,9 +320,9 @@ int32_t moe_expert_swiglu(const bgq_expert* e, const uint16_t* x, int32_t batch,
   if (launch_plan_single(plan, batch, big_min, s) != cudaSuccess) return BGQ_ERR_CUDA;
   if (launch_gateup(es, plan, ntasks, batch, x, H, 1, stage, s) != cudaSuccess) return BGQ_ERR_CUDA;
   if (batch >= big_min && launch_gateup_tc(es, plan, batch, 0, x, H, 1, ctrl, sp, s) != cudaSuccess) return BGQ_ERR_CUDA;
-  if (launch_down(es, plan, ntasks, batch, H, Y, 1, stage, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  // tensor-core tasks first: the grouped down kernel writes the outputs (y = the one slot)
   if (batch >= big_min && launch_down_tc(es, plan, batch, 0, H, Y, 1, ctrl, sp, s) != cudaSuccess) return BGQ_ERR_CUDA;
-  return cuda_status(launch_combine(Y, nullptr, nullptr, batch, 0, d, y, y_f32, s));
+  return cuda_status(launch_down(es, plan, ntasks, batch, H, Y, 1, stage, Combine{nullptr, nullptr, 0, y, y_f32}, s));
 }
 
 size_t moe_layer_workspace_bytes(const bgq_moe_layer* L, int32_t max_batch) {
@@ -348,9 +348,10 @@ static int32_t layer_forward_impl(const bgq_moe_layer* L, const uint16_t* x, int
   const bool tc = batch >= big_min;
   const TcSplit sp = W.tcs ? tc_split_carve(W.tcs, L->d_model, L->d_ff, batch, K) : TcSplit{nullptr, nullptr};
   if (tc && launch_gateup_tc(es, W.plan, batch, K, x, W.H, K + 1, W.ctrl, sp, s) != cudaSuccess) return BGQ_ERR_CUDA;
-  if (launch_down(es, W.plan, max_tasks, batch, W.H, W.Y, K + 1, W.stage, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  // tensor-core tasks first: the grouped down kernel ends with the weighted combine
   if (tc && launch_down_tc(es, W.plan, batch, K, W.H, W.Y, K + 1, W.ctrl, sp, s) != cudaSuccess) return BGQ_ERR_CUDA;
-  return cuda_status(launch_combine(W.Y, w, gamma, batch, K, L->d_model, out, out_f32, s));
+  return cuda_status(
+      launch_down(es, W.plan, max_tasks, batch, W.H, W.Y, K + 1, W.stage, Combine{w, gamma, K, out, out_f32}, s));
 }
 
 int32_t moe_layer_forward(const bgq_moe_layer* L, const uint16_t* x, int32_t batch, uint16_t* out, float* out_f32,
@@ -420,8 +421,8 @@ int32_t moe_layer_forward_streamed(const bgq_moe_layer* L, const uint16_t* x, in
   const ExpertSet es = slot_expert_set(pool, g, slots);
   const int max_tasks = plan_max_tasks(batch, K);
   if (launch_gateup(es, W.plan, max_tasks, batch, x, W.H, K + 1, W.stage, s) != cudaSuccess) return BGQ_ERR_CUDA;
-  if (launch_down(es, W.plan, max_tasks, batch, W.H, W.Y, K + 1, W.stage, s) != cudaSuccess) return BGQ_ERR_CUDA;
-  return cuda_status(launch_combine(W.Y, w, gamma, batch, K, L->d_model, out, out_f32, s));
+  return cuda_status(
+      launch_down(es, W.plan, max_tasks, batch, W.H, W.Y, K + 1, W.stage, Combine{w, gamma, K, out, out_f32}, s));
 }
 
 int32_t bgq_rmsnorm(const float* h, const uint16_t* rho, int32_t batch, int32_t d, float eps, uint16_t* a,

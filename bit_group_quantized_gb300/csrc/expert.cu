@@ -263,7 +263,7 @@ k_gateup_all(ExpertSet es, const Plan* __restrict__ plan, const uint16_t* __rest
   const int total = plan->ntasks * nr;
   GateUpRows cur, nxt;
   if (warp < total) load_gateup<BITS>(es, plan, warp, nr, rs.b, rg, lane, cur);  // in flight during staging
-  if (local) stage_x_int16<BITS>(StridedSrc<uint16_t>{x, d}, B, d, st, nullptr);
+  if (local) stage_x_int16_pairs<BITS>(StridedSrc<uint16_t>{x, d}, B, d, st);  // two code words per thread
   for (int item = warp; item < total; item += kAllWarps) {
     if (item + kAllWarps < total) load_gateup<BITS>(es, plan, item + kAllWarps, nr, rs.b, rg, lane, nxt);
     const Task& tk = plan_tasks(plan)[item / nr];
@@ -327,7 +327,7 @@ __device__ __forceinline__ void load_down(const ExpertSet& es, const Plan* plan,
 template <int BITS>
 __global__ void __launch_bounds__(kAllThreads, 1)
 k_down_all(ExpertSet es, const Plan* __restrict__ plan, const float* __restrict__ H, int B,
-           float* __restrict__ Y, int nslot, XStage gst) {
+           float* __restrict__ Y, int nslot, XStage gst, Combine cb) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int d = es.d, f = es.f;
   const RowGeo rg = row_geo(f, BITS);  // NIT == 1 (checked by the launcher)
@@ -347,7 +347,7 @@ k_down_all(ExpertSet es, const Plan* __restrict__ plan, const float* __restrict_
   const int total = plan->ntasks * nch;
   DownRows cur, nxt;
   if (warp < total) load_down<BITS>(es, plan, down_item(warp, nch, nrg), rs.b, nrows, rg, lp, rsub, cur);
-  if (local) stage_x_int16<BITS>(StridedSrc<float>{H, f}, T, f, st, nullptr);
+  if (local) stage_x_int16_pairs<BITS>(StridedSrc<float>{H, f}, T, f, st);
   for (int i = warp; i < total; i += kAllWarps) {
     if (i + kAllWarps < total)
       load_down<BITS>(es, plan, down_item(i + kAllWarps, nch, nrg), rs.b, nrows, rg, lp, rsub, nxt);
@@ -380,6 +380,22 @@ k_down_all(ExpertSet es, const Plan* __restrict__ plan, const float* __restrict_
       }
     }
     cur = nxt;
+  }
+  if (cb.out || cb.out_f32) {
+    // This CTA now holds every (token, slot) output of its rows (the
+    // tensor-core tasks' ran before this kernel): the weighted combine of
+    // k_combine, same order (k = 0..K-1, then the shared expert).
+    __syncthreads();
+    for (int i = threadIdx.x; i < B * nrows; i += blockDim.x) {
+      const int t = i / nrows, r = rs.b + (i - t * nrows);
+      const float* yt = Y + (size_t)t * nslot * d + r;
+      float acc = 0.f;
+      for (int k = 0; k < cb.K; ++k) acc = fmaf(cb.w[t * cb.K + k], yt[(size_t)k * d], acc);
+      const float g = cb.gamma ? cb.gamma[t] : 1.f;
+      acc = fmaf(g, yt[(size_t)cb.K * d], acc);
+      if (cb.out) cb.out[(size_t)t * d + r] = f2bf(acc);
+      if (cb.out_f32) cb.out_f32[(size_t)t * d + r] = acc;
+    }
   }
 }
 
@@ -479,7 +495,7 @@ cudaError_t launch_gateup(const ExpertSet& es, const Plan* plan, int max_tasks, 
 }
 
 cudaError_t launch_down(const ExpertSet& es, const Plan* plan, int max_tasks, int batch, const float* H, float* Y,
-                        int nslot, unsigned char* stage_ws, cudaStream_t s) {
+                        int nslot, unsigned char* stage_ws, const Combine& cb, cudaStream_t s) {
   RowGeo rg = row_geo(es.f, es.bits);
   const int T = batch * nslot;
   const bool fits = all_smem(es.f, es.bits, T) <= kAllSmemMax;
@@ -497,10 +513,10 @@ cudaError_t launch_down(const ExpertSet& es, const Plan* plan, int max_tasks, in
     }
     if (es.bits == 4) {
       if ((e = set_smem(k_down_all<4>, sm)) != cudaSuccess) return e;
-      k_down_all<4><<<num_sms(), kAllThreads, sm, s>>>(es, plan, H, batch, Y, nslot, gst);
+      k_down_all<4><<<num_sms(), kAllThreads, sm, s>>>(es, plan, H, batch, Y, nslot, gst, cb);
     } else {
       if ((e = set_smem(k_down_all<2>, sm)) != cudaSuccess) return e;
-      k_down_all<2><<<num_sms(), kAllThreads, sm, s>>>(es, plan, H, batch, Y, nslot, gst);
+      k_down_all<2><<<num_sms(), kAllThreads, sm, s>>>(es, plan, H, batch, Y, nslot, gst, cb);
     }
     return cudaGetLastError();
   }
@@ -515,7 +531,10 @@ cudaError_t launch_down(const ExpertSet& es, const Plan* plan, int max_tasks, in
     if ((e = set_smem(k_down<2>, sm)) != cudaSuccess) return e;
     k_down<2><<<grid, kExpThreads, sm, s>>>(es, plan, H, Y, nslot);
   }
-  return cudaGetLastError();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (cb.out || cb.out_f32)  // the per-task kernel leaves the combine to its own launch
+    return launch_combine(Y, cb.w, cb.gamma, batch, cb.K, es.d, cb.out, cb.out_f32, s);
+  return cudaSuccess;
 }
 
 // ---------------------------------------------------------------------------

@@ -133,10 +133,21 @@ cudaError_t launch_down_tc(const ExpertSet& es, const Plan* plan, int B, int K, 
 // null: the per-task kernels instead).
 cudaError_t launch_gateup(const ExpertSet& es, const Plan* plan, int max_tasks, int batch, const uint16_t* x, float* H,
                           int nslot, unsigned char* stage_ws, cudaStream_t s);
+// Weighted combine of the K + 1 slots per token (launch_combine's formula),
+// done by launch_down when out or out_f32 is set. w: [batch][K] (K may be 0),
+// gamma nullable (1).
+struct Combine {
+  const float* w;
+  const float* gamma;
+  int K;
+  uint16_t* out;
+  float* out_f32;
+};
 // Grouped down projection: Y[(tok*nslot + slot)*d + row]; H holds batch*nslot
 // vectors of f (stage_ws: staged_tokens_bytes(f, bits, batch*nslot) bytes).
+// Every tensor-core task's Y must be written before (the combine reads them).
 cudaError_t launch_down(const ExpertSet& es, const Plan* plan, int max_tasks, int batch, const float* H, float* Y,
-                        int nslot, unsigned char* stage_ws, cudaStream_t s);
+                        int nslot, unsigned char* stage_ws, const Combine& cb, cudaStream_t s);
 size_t staged_tokens_bytes(int cols, int bits, int T);
 // out[t][r] = sum_{k<K} w[t][k] Y[t][k][r] + gamma[t] Y[t][K][r]  (K may be 0; gamma NULL => 1).
 cudaError_t launch_combine(const float* Y, const float* w, const float* gamma, int batch, int K, int d,
