@@ -108,55 +108,95 @@ __device__ void topk_one_token(const float* __restrict__ lg, int E, int K, float
   }
 }
 
-// Block-wide exclusive scan of n <= 4*blockDim ints in shared memory (in place).
-__device__ void block_exclusive_scan(int* a, int n, int* tmp /* >= 33 ints */) {
+// Block-wide exclusive scan of three int arrays a0, a1, a2 of n entries in
+// shared memory, in place, in one pass (each thread takes a contiguous run of
+// ceil(n / blockDim) entries); the three totals go to tot[0..2]. wt: 96 ints.
+__device__ void block_exclusive_scan3(int* a0, int* a1, int* a2, int n, int* wt, int* tot) {
   const int per = (n + blockDim.x - 1) / blockDim.x;
   const int lo = threadIdx.x * per;
-  int local = 0;
+  int l0 = 0, l1 = 0, l2 = 0;
   for (int i = 0; i < per; ++i)
-    if (lo + i < n) local += a[lo + i];
-  // scan of per-thread totals
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = local;
-  for (int o = 1; o < 32; o <<= 1) {
-    int v = __shfl_up_sync(kFull, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) tmp[warp] = incl;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int run = 0;
-    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) {
-      int v = tmp[i];
-      tmp[i] = run;
-      run += v;
-    }
-    tmp[32] = run;
-  }
-  __syncthreads();
-  int run = tmp[warp] + incl - local;
-  for (int i = 0; i < per; ++i) {
     if (lo + i < n) {
-      int v = a[lo + i];
-      a[lo + i] = run;
-      run += v;
+      l0 += a0[lo + i];
+      l1 += a1[lo + i];
+      l2 += a2[lo + i];
+    }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  int c0 = l0, c1 = l1, c2 = l2;  // inclusive within the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v0 = __shfl_up_sync(kFull, c0, o), v1 = __shfl_up_sync(kFull, c1, o), v2 = __shfl_up_sync(kFull, c2, o);
+    if (lane >= o) {
+      c0 += v0;
+      c1 += v1;
+      c2 += v2;
     }
   }
+  if (lane == 31) {
+    wt[warp] = c0;
+    wt[32 + warp] = c1;
+    wt[64 + warp] = c2;
+  }
+  __syncthreads();
+  if (warp == 0) {  // exclusive scan of the warp totals
+    const int t0 = lane < nw ? wt[lane] : 0, t1 = lane < nw ? wt[32 + lane] : 0, t2 = lane < nw ? wt[64 + lane] : 0;
+    int i0 = t0, i1 = t1, i2 = t2;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v0 = __shfl_up_sync(kFull, i0, o), v1 = __shfl_up_sync(kFull, i1, o), v2 = __shfl_up_sync(kFull, i2, o);
+      if (lane >= o) {
+        i0 += v0;
+        i1 += v1;
+        i2 += v2;
+      }
+    }
+    wt[lane] = i0 - t0;
+    wt[32 + lane] = i1 - t1;
+    wt[64 + lane] = i2 - t2;
+    if (lane == 31) {
+      tot[0] = i0;
+      tot[1] = i1;
+      tot[2] = i2;
+    }
+  }
+  __syncthreads();
+  int r0 = wt[warp] + c0 - l0, r1 = wt[32 + warp] + c1 - l1, r2 = wt[64 + warp] + c2 - l2;
+  for (int i = 0; i < per; ++i)
+    if (lo + i < n) {
+      const int v0 = a0[lo + i], v1 = a1[lo + i], v2 = a2[lo + i];
+      a0[lo + i] = r0;
+      a1[lo + i] = r1;
+      a2[lo + i] = r2;
+      r0 += v0;
+      r1 += v1;
+      r2 += v2;
+    }
   __syncthreads();
 }
 
-__device__ void build_plan(const int* sel, int B, int K, int E, int big_min, Plan* plan, int* s_cnt, int* s_tmp) {
+// Shared-memory ints build_plan needs for B tokens, top-K and E experts.
+__host__ __device__ inline int plan_scratch_ints(int B, int K, int E) { return 4 * E + 104 + B * K; }
+
+// The grouping plan from the selections sel[B*K] (token-major): routed
+// experts with fewer than big_min tokens become grouped-GEMV tasks of at most
+// kTaskTok tokens (stable: token order, then slot), the others tensor-core
+// tasks; then the shared expert (every token, slot K). `s_cnt`:
+// plan_scratch_ints(B, K, E) ints of shared memory.
+__device__ void build_plan(const int* sel, int B, int K, int E, int big_min, Plan* plan, int* s_cnt) {
   const int npairs = B * K;
   Task* tasks = plan_tasks(plan);
   BigTask* big = plan_big(plan, B, K);
   int* ptok = plan_ptok(plan, B, K);
   int* pslot = plan_pslot(plan, B, K);
-  int* s_first = s_cnt + E;    // task index of each small expert's first chunk
+  int* s_first = s_cnt + E;       // task index of each small expert's first chunk
   int* s_pfirst = s_cnt + 2 * E;  // pair offset of each big expert
   int* s_bidx = s_cnt + 3 * E;    // big-task index of each big expert
+  int* wt = s_cnt + 4 * E;        // [96] scan scratch, then [3] totals
+  int* s_sel = wt + 104;          // [npairs] the selections, staged once
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+  for (int i = threadIdx.x; i < npairs; i += blockDim.x) s_sel[i] = __ldcg(sel + i);
   __syncthreads();
-  for (int i = threadIdx.x; i < npairs; i += blockDim.x) atomicAdd(&s_cnt[sel[i]], 1);
+  for (int i = threadIdx.x; i < npairs; i += blockDim.x) atomicAdd(&s_cnt[s_sel[i]], 1);
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     const int c = s_cnt[e];
@@ -166,16 +206,12 @@ __device__ void build_plan(const int* sel, int B, int K, int E, int big_min, Pla
     s_bidx[e] = bigc ? 1 : 0;
   }
   __syncthreads();
-  block_exclusive_scan(s_first, E, s_tmp);
-  const int nsmall = s_tmp[32];
-  block_exclusive_scan(s_pfirst, E, s_tmp);
-  const int nbigpairs = s_tmp[32];
-  block_exclusive_scan(s_bidx, E, s_tmp);
-  const int nbigr = s_tmp[32];
+  block_exclusive_scan3(s_first, s_pfirst, s_bidx, E, wt, wt + 96);
+  const int nsmall = wt[96], nbigpairs = wt[97], nbigr = wt[98];
   for (int i = threadIdx.x; i < npairs; i += blockDim.x) {
-    const int e = sel[i];
-    int r = 0;
-    for (int j = 0; j < i; ++j) r += (sel[j] == e);
+    const int e = s_sel[i];
+    int r = 0;  // earlier pairs of the same expert
+    for (int j = 0; j < i; ++j) r += (s_sel[j] == e);
     if (s_cnt[e] >= big_min) {
       ptok[s_pfirst[e] + r] = i / K;
       pslot[s_pfirst[e] + r] = i % K;
@@ -304,8 +340,8 @@ k_route(const uint16_t* __restrict__ router, const uint16_t* __restrict__ sgate,
   if (plan) {
     __syncthreads();
     __threadfence_block();
-    int* s_cnt = reinterpret_cast<int*>(smem);  // reuse: 4*E ints + scan scratch
-    build_plan(sel_ws, B, K, E, big_min, plan, s_cnt, s_cnt + 4 * E);
+    int* s_cnt = reinterpret_cast<int*>(smem);  // reuse: plan_scratch_ints(B, K, E) ints
+    build_plan(sel_ws, B, K, E, big_min, plan, s_cnt);
   }
   if (threadIdx.x == 0) ctrl->route_counter = 0;  // ready for the next launch
 }
@@ -473,8 +509,8 @@ k_route_coop(const uint16_t* __restrict__ router, const uint16_t* __restrict__ s
   if (!s_last) return;
   __threadfence();
   if (plan) {
-    int* s_cnt = reinterpret_cast<int*>(smem);  // 4*E ints + scan scratch
-    build_plan(sel_ws, B, K, E, big_min, plan, s_cnt, s_cnt + 4 * E);
+    int* s_cnt = reinterpret_cast<int*>(smem);  // plan_scratch_ints(B, K, E) ints
+    build_plan(sel_ws, B, K, E, big_min, plan, s_cnt);
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -484,10 +520,10 @@ k_route_coop(const uint16_t* __restrict__ router, const uint16_t* __restrict__ s
   }
 }
 
-static size_t route_coop_smem(int d, int E) {
+static size_t route_coop_smem(int d, int E, int B, int K) {
   size_t sm = (size_t)kRouteTok * d * 2 + kRcWarps * kRouteTok * sizeof(float);
   const size_t sm_topk = ((size_t)((E + 4) & ~3) + topk_scratch_ints(E)) * sizeof(float);
-  const size_t sm_plan = (size_t)(4 * E + 40) * sizeof(int);
+  const size_t sm_plan = (size_t)plan_scratch_ints(B, K, E) * sizeof(int);
   if (sm_topk > sm) sm = sm_topk;
   if (sm_plan > sm) sm = sm_plan;
   return sm;
@@ -499,7 +535,7 @@ cudaError_t launch_route(const uint16_t* router, const uint16_t* sgate, const ui
   // selected experts scratch for the plan: right after the logits
   int* sel = reinterpret_cast<int*>(logits_ws + (size_t)batch * (E + 1));
   if (E <= kTopkWarps * 64) {
-    const size_t smc = route_coop_smem(d, E);
+    const size_t smc = route_coop_smem(d, E, batch, K);
     cudaError_t e = cudaFuncSetAttribute(k_route_coop, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smc);
     int per_sm = 0;
     if (e == cudaSuccess)
@@ -516,7 +552,7 @@ cudaError_t launch_route(const uint16_t* router, const uint16_t* sgate, const ui
   int nrows = E + (sgate ? 1 : 0);
   int grid = (nrows + g.rows_cta - 1) / g.rows_cta;
   size_t sm = (size_t)kRouteTok * d * 2 + kRouteWarps * kRouteTok * sizeof(float);
-  size_t sm_plan = (size_t)(4 * E + 40) * sizeof(int);
+  size_t sm_plan = (size_t)plan_scratch_ints(batch, K, E) * sizeof(int);
   if (sm_plan > sm) sm = sm_plan;
   if (sm > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(k_route, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
