@@ -68,6 +68,14 @@ def oracle_layer_token(t, src, shape, K, x_tok, gpu_idx=None):
     (16, 1024, 256, 4, 4, 1),
     (8, 2048, 512, 2, 2, 1),
     (64, 1024, 512, 8, 4, 1),
+    # limits and degenerate cases: 1024 experts with top-8 (the largest the
+    # kernels take), every expert selected (E == K), a single expert (K == 1)
+    (1024, 256, 128, 8, 4, 3),
+    (1024, 1024, 256, 8, 4, 1),
+    (4, 256, 128, 4, 4, 2),
+    (4, 1024, 256, 4, 4, 1),
+    (16, 512, 256, 1, 4, 9),
+    (16, 1024, 256, 1, 4, 1),
 ])
 def test_small_layer_matches_oracle(cuda_device, E, d, f, K, bits, B):
     shape = synth.PoolShape(d, f, E, bits)
@@ -96,7 +104,8 @@ def full_layer(cuda_device):
     return shape, L, t
 
 
-@pytest.mark.parametrize("B,sample", [(1, [0]), (4, [0, 3]), (16, [0, 9, 15]), (64, [0, 31, 63])])
+@pytest.mark.parametrize("B,sample", [(1, [0]), (4, [0, 3]), (16, [0, 9, 15]), (64, [0, 31, 63]),
+                                      (256, [0, 130, 255])])  # the largest batch: the shared expert's 256 tokens on tensor cores
 def test_full_layer_matches_oracle_on_sampled_tokens(cuda_device, full_layer, B, sample):
     shape, L, t = full_layer
     x = synth.activations(0, 100 + B, B, shape.d, device=cuda_device)
