@@ -76,6 +76,9 @@ def oracle_layer_token(t, src, shape, K, x_tok, gpu_idx=None):
     (4, 1024, 256, 4, 4, 1),
     (16, 512, 256, 1, 4, 9),
     (16, 1024, 256, 1, 4, 1),
+    # down rows of 2048 columns at 4 bits: the per-task down kernel, then a
+    # separate combine launch
+    (8, 512, 2048, 2, 4, 3),
 ])
 def test_small_layer_matches_oracle(cuda_device, E, d, f, K, bits, B):
     shape = synth.PoolShape(d, f, E, bits)
