@@ -61,6 +61,7 @@ constexpr int kLayerTcMinTokens = 64;
 
 struct LayerWs {
   Ctrl* ctrl;
+  int* tccnt;     // tensor-core split-K counters (zero between calls; fixed place for any batch)
   float* logits;  // [B][E+1] then B*K ints of selected experts
   Plan* plan;
   int32_t* idx;
@@ -74,7 +75,7 @@ struct LayerWs {
   float* fpart;     // [2][1024] per-CTA sums of squares
   int32_t* fidx;    // [16]
   float* fw;        // [16]
-  unsigned char* tcs;  // split-K scratch of the tensor-core kernels (batches that can use them)
+  float* tcs;  // split-K partial sums of the tensor-core kernels (batches that can use them)
   size_t bytes;
 };
 
@@ -82,6 +83,7 @@ LayerWs carve_layer(void* ws, int B, int d, int f, int E, int K) {
   Carver c(ws);
   LayerWs L;
   L.ctrl = c.take<Ctrl>(sizeof(Ctrl));
+  L.tccnt = c.take<int>(tc_split_cnt_bytes(d, f, K));  // right after the control block, whatever B is
   L.logits = c.take<float>((size_t)B * (E + 1) * 4 + (size_t)B * K * 4);
   L.plan = c.take<Plan>(plan_bytes(B, K));
   L.idx = c.take<int32_t>((size_t)B * K * 4);
@@ -97,7 +99,7 @@ LayerWs carve_layer(void* ws, int B, int d, int f, int E, int K) {
   L.fpart = c.take<float>(2 * 1024 * 4);
   L.fidx = c.take<int32_t>(16 * 4);
   L.fw = c.take<float>(16 * 4);
-  L.tcs = B >= kLayerTcMinTokens ? c.take<unsigned char>(tc_split_bytes(d, f, B, K)) : nullptr;
+  L.tcs = B >= kLayerTcMinTokens ? c.take<float>(tc_split_part_bytes(d, f, B, K)) : nullptr;
   L.bytes = c.off;
   return L;
 }
@@ -277,8 +279,9 @@ size_t moe_expert_workspace_bytes(const bgq_expert* e, int32_t batch) {
   if (!e || batch < 1) return 0;
   const int d = e->gate.cols, f = e->gate.rows;
   const size_t sx = staged_tokens_bytes(d, 4, batch), sh = staged_tokens_bytes(f, 4, batch);
-  return sizeof(Ctrl) + up256(plan_bytes(batch, 0)) + up256((size_t)batch * f * 4) + up256((size_t)batch * d * 4) +
-         up256(sx > sh ? sx : sh) + (batch >= kBigTok ? up256(tc_split_bytes(d, f, batch, 0)) : 0);
+  return sizeof(Ctrl) + tc_split_cnt_bytes(d, f, 0) + up256(plan_bytes(batch, 0)) + up256((size_t)batch * f * 4) +
+         up256((size_t)batch * d * 4) + up256(sx > sh ? sx : sh) +
+         (batch >= kBigTok ? tc_split_part_bytes(d, f, batch, 0) : 0);
 }
 
 int32_t moe_expert_swiglu(const bgq_expert* e, const uint16_t* x, int32_t batch, uint16_t* y, float* y_f32,
@@ -295,13 +298,13 @@ int32_t moe_expert_swiglu(const bgq_expert* e, const uint16_t* x, int32_t batch,
   if (!ws || !al(ws, 256) || ws_bytes < moe_expert_workspace_bytes(e, batch)) return BGQ_ERR_WORKSPACE;
   Carver c(ws);
   Ctrl* ctrl = c.take<Ctrl>(sizeof(Ctrl));
+  int* tccnt = c.take<int>(tc_split_cnt_bytes(d, f, 0));  // fixed place: zero between calls of any batch
   Plan* plan = c.take<Plan>(plan_bytes(batch, 0));
   float* H = c.take<float>((size_t)batch * f * 4);
   float* Y = c.take<float>((size_t)batch * d * 4);
   const size_t sx = staged_tokens_bytes(d, 4, batch), sh = staged_tokens_bytes(f, 4, batch);
   unsigned char* stage = c.take<unsigned char>(sx > sh ? sx : sh);
-  const TcSplit sp = batch >= kBigTok ? tc_split_carve(c.take<unsigned char>(tc_split_bytes(d, f, batch, 0)), d, f, batch, 0)
-                                      : TcSplit{nullptr, nullptr};
+  const TcSplit sp{batch >= kBigTok ? c.take<float>(tc_split_part_bytes(d, f, batch, 0)) : nullptr, tccnt};
   ExpertSet es{};
   es.shared = ExpertRef{e->gate.q, e->gate.sb, e->up.q, e->up.sb, e->down.q, e->down.sb};
   es.d = d;
@@ -346,7 +349,7 @@ static int32_t layer_forward_impl(const bgq_moe_layer* L, const uint16_t* x, int
   // experts with < 16 tokens: grouped GEMV; with >= 16: tensor-core GEMM
   if (launch_gateup(es, W.plan, max_tasks, batch, x, W.H, K + 1, W.stage, s) != cudaSuccess) return BGQ_ERR_CUDA;
   const bool tc = batch >= big_min;
-  const TcSplit sp = W.tcs ? tc_split_carve(W.tcs, L->d_model, L->d_ff, batch, K) : TcSplit{nullptr, nullptr};
+  const TcSplit sp{W.tcs, W.tccnt};
   if (tc && launch_gateup_tc(es, W.plan, batch, K, x, W.H, K + 1, W.ctrl, sp, s) != cudaSuccess) return BGQ_ERR_CUDA;
   // tensor-core tasks first: the grouped down kernel ends with the weighted combine
   if (tc && launch_down_tc(es, W.plan, batch, K, W.H, W.Y, K + 1, W.ctrl, sp, s) != cudaSuccess) return BGQ_ERR_CUDA;

@@ -114,14 +114,16 @@ cudaError_t launch_plan_single(Plan* plan, int batch, int big_min, cudaStream_t 
 // Tensor-core (tcgen05) gate/up + SiLU*mul and down projection for the plan's
 // big tasks (experts with >= kBigTok tokens). B, K: the plan's batch and top_k.
 // K is split over several CTAs per 128-row tile; their fp32 partial sums go
-// to `part` and the tile's last CTA (counter in `cnt`, left at zero) adds them
-// in split order. tc_split_bytes: the scratch for a plan of (B, K).
+// to `part` (tc_split_part_bytes for a plan of (B, K); written before read)
+// and the tile's last CTA adds them in split order, found with the counters
+// `cnt` (tc_split_cnt_bytes, enough for any batch; zero before a call and
+// left zero, so callers keep them at a fixed place of a reused workspace).
 struct TcSplit {
   float* part;
   int* cnt;
 };
-size_t tc_split_bytes(int d, int f, int B, int K);
-TcSplit tc_split_carve(void* p, int d, int f, int B, int K);
+size_t tc_split_part_bytes(int d, int f, int B, int K);
+size_t tc_split_cnt_bytes(int d, int f, int K);
 cudaError_t launch_gateup_tc(const ExpertSet& es, const Plan* plan, int B, int K, const uint16_t* x, float* H,
                              int nslot, Ctrl* ctrl, const TcSplit& sp, cudaStream_t s);
 cudaError_t launch_down_tc(const ExpertSet& es, const Plan* plan, int B, int K, const float* H, float* Y, int nslot,

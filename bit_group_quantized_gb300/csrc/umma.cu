@@ -676,19 +676,15 @@ static int tc_split_dn(int f) {
 }
 static size_t tc_up256(size_t n) { return (n + 255) & ~(size_t)255; }
 
-size_t tc_split_bytes(int d, int f, int B, int K) {
+size_t tc_split_part_bytes(int d, int f, int B, int K) {
   const size_t pc = (size_t)plan_max_pairs(B, K);
   const size_t pg = (size_t)tc_split_gu(d) * pc * 2 * f, pd = (size_t)tc_split_dn(f) * pc * d;
-  const size_t tiles = (size_t)((d > f ? d : f) + kTcM - 1) / kTcM;
-  return tc_up256((pg > pd ? pg : pd) * 4) + tc_up256(tiles * plan_max_big(B, K) * 4);
+  return tc_up256((pg > pd ? pg : pd) * 4);
 }
-TcSplit tc_split_carve(void* p, int d, int f, int B, int K) {
-  const size_t pc = (size_t)plan_max_pairs(B, K);
-  const size_t pg = (size_t)tc_split_gu(d) * pc * 2 * f, pd = (size_t)tc_split_dn(f) * pc * d;
-  TcSplit sp;
-  sp.part = static_cast<float*>(p);
-  sp.cnt = reinterpret_cast<int*>(static_cast<unsigned char*>(p) + tc_up256((pg > pd ? pg : pd) * 4));
-  return sp;
+constexpr int kTcCntBatch = 256;  // the largest batch of any call
+size_t tc_split_cnt_bytes(int d, int f, int K) {
+  const size_t tiles = (size_t)((d > f ? d : f) + kTcM - 1) / kTcM;
+  return tc_up256(tiles * plan_max_big(kTcCntBatch, K) * 4);
 }
 
 template <int BITS, int D>

@@ -138,6 +138,21 @@ def test_layer_batch_equals_single_bitwise(cuda_device, full_layer):
         assert torch.equal(ob[tok].view(torch.int16), o1[0].view(torch.int16)), tok
 
 
+def test_layer_workspace_reused_across_batches(cuda_device, full_layer):
+    """One workspace sized for the largest batch serves calls of several batch
+    sizes (the tensor-core path's split-K counters must be zero at every call,
+    whatever the previous call's layout) and gives the bits of a fresh one."""
+    shape, L, t = full_layer
+    ws = lib.workspace(lib.moe_layer_workspace_bytes(L, 100), cuda_device)
+    for B in (100, 64, 1, 100, 64):
+        x = synth.activations(0, 700 + B, B, shape.d, device=cuda_device)
+        a = lib.moe_layer_forward(L, x, ws=ws)[0].clone()
+        b = lib.moe_layer_forward(L, x)[0]
+        torch.cuda.synchronize()
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), B
+    assert lib.read_device_status(ws) == lib.OK
+
+
 def test_layer_deterministic(cuda_device, full_layer):
     shape, L, t = full_layer
     x = synth.activations(0, 901, 16, shape.d, device=cuda_device)
