@@ -28,8 +28,8 @@ CPU and GPU agree bit for bit):
 * uniform u in [0, 1):  (v >> 8) * 2**-24
 * approximately normal n:  Irwin-Hall sum of twelve 16-bit uniforms minus 6
   (twelve halves of six draws), range [-6, 6], unit variance.
-* packed code words: the raw 32-bit draw. Every 4-bit (or 2-bit) field of a
-  uniform 32-bit word is itself uniform on 0..15 (0..3).
+* packed code words: the raw 32-bit draw. Every 8-, 4- or 2-bit field of a
+  uniform 32-bit word is itself uniform on 0..255 (0..15, 0..3).
 
 Value distributions (the workload's recipe; the second parameter of N(.,.)
 is read as a standard deviation, the usual convention for weight inits):
@@ -157,16 +157,21 @@ def words_per_row(cols: int, bits: int) -> int:
     return cols * bits // 32
 
 
-def qmatrix(seed: int, rows: int, cols: int, bits: int = 4, device="cpu", tag: int = 0):
-    """A standalone packed matrix: (q int32 [rows][cols*bits/32], sb bf16 [rows][cols/64][2])."""
-    assert cols % GROUP == 0 and bits in (2, 4)
+def qmatrix(seed: int, rows: int, cols: int, bits: int = 4, device="cpu", tag: int = 0, group: int = GROUP):
+    """A standalone packed matrix: (q int32 [rows][cols*bits/32], sb bf16 [rows][cols/group][2]).
+
+    bits 2, 4 or 8; group 64, or cols for one (scale, bias) pair per row (the
+    per-row 8-bit format). At 8 bits the bias is -128*s + noise, the affine
+    form of symmetric signed int8.
+    """
+    assert cols % GROUP == 0 and bits in (2, 4, 8) and group in (GROUP, cols)
     wpr = words_per_row(cols, bits)
     kq = stream_keys(seed, TAG_MATRIX_Q, tag)
     q = _as_int32_bits(draws(kq, 0, rows * wpr, device)).view(rows, wpr)
     ks = stream_keys(seed, TAG_MATRIX_SCALE, tag)
     kn = stream_keys(seed, TAG_MATRIX_BIASNOISE, tag)
-    sb = _scale_bias(ks, kn, 0, rows * (cols // GROUP), bits, device)
-    return q, sb.view(rows, cols // GROUP, 2)
+    sb = _scale_bias(ks, kn, 0, rows * (cols // group), bits, device)
+    return q, sb.view(rows, cols // group, 2)
 
 
 # ---------------------------------------------------------------- expert pools

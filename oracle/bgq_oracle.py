@@ -20,6 +20,10 @@ Sources (web pages; the method is described on the first):
          "架构设计：SSD当显存用" (per-token pipeline: routing, softmax + topK,
          expert forward + combine + norm), "FMA Dequant：一条指令省12%"
          (w = nibble*scale + bias and its fma reordering), "2-bit vs 4-bit".
+  [H3]   "Redis 之父下场手写推理引擎：antirez 用约 24000 行原生代码驯服视频生成模型"
+         (text-matrix.pages.dev/posts/tech/antirez-h3-metal/): the paragraph
+         on --use-int8-row-fc2 (int8 MLP weights with a scale per group; FC2
+         with one scale per row).
 Where the page is silent the workload definition fixes the value (group 64,
 bf16 scale and bias, LSB-first packing, renormalised top-K weights, lowest
 index wins ties, a sigmoid-gated shared expert, RMSNorm before each layer).
@@ -81,7 +85,8 @@ def unpack_codes(q_words, bits: int) -> np.ndarray:
 
     READING (the page says only that weights are 4-bit nibbles): the codes
     are stored least-significant-first, element k of a row in word
-    k // (32/bits) at bit offset bits * (k % (32/bits)).
+    k // (32/bits) at bit offset bits * (k % (32/bits)). bits is 2, 4 or 8
+    (8: four bytes per word, byte 0 first).
     """
     w = np.asarray(_np(q_words)).astype(np.int64) & 0xFFFFFFFF
     per = 32 // bits
@@ -91,22 +96,25 @@ def unpack_codes(q_words, bits: int) -> np.ndarray:
     return q.reshape(w.shape[0], w.shape[1] * per)
 
 
-def dequant(q_words, sb, bits: int) -> np.ndarray:
-    """w[n, k] = q[n, k] * s[n, g] + b[n, g], g = k // 64.
+def dequant(q_words, sb, bits: int, group: int = GROUP) -> np.ndarray:
+    """w[n, k] = q[n, k] * s[n, g] + b[n, g], g = k // group.
 
     [FM] "FMA Dequant": each weight is ``nibble * scale + bias``. scale and
     bias are bf16, one pair per group of 64 consecutive columns of a row.
+    [H3] (the --use-int8-row-fc2 paragraph): int8 weights with one scale per
+    group, or, for FC2, a single scale per row. READING: the same affine form
+    at 8 bits (codes 0..255); the per-row format is ``group`` = row length.
     """
     q = unpack_codes(q_words, bits).astype(np.float64)
-    sbv = bf16_to_f64(sb).reshape(q.shape[0], q.shape[1] // GROUP, 2)
-    s = np.repeat(sbv[:, :, 0], GROUP, axis=1)
-    b = np.repeat(sbv[:, :, 1], GROUP, axis=1)
+    sbv = bf16_to_f64(sb).reshape(q.shape[0], q.shape[1] // group, 2)
+    s = np.repeat(sbv[:, :, 0], group, axis=1)
+    b = np.repeat(sbv[:, :, 1], group, axis=1)
     return q * s + b
 
 
-def gemv(q_words, sb, bits: int, x) -> np.ndarray:
+def gemv(q_words, sb, bits: int, x, group: int = GROUP) -> np.ndarray:
     """y = W x with W dequantised in float64 (x: [cols] or [batch][cols])."""
-    W = dequant(q_words, sb, bits)
+    W = dequant(q_words, sb, bits, group)
     x = np.asarray(x, dtype=np.float64)
     return x @ W.T if x.ndim == 2 else W @ x
 

@@ -92,6 +92,91 @@ def test_hand_cases():
     check_hand_cases()
 
 
+# ------------------------------------------- A'. 8-bit hand cases (int8 MLP / QKV / FC2 format)
+def load_hand_cases8():
+    text = open(os.path.join(GOLDEN, "hand_gemv8.txt"), encoding="utf-8").read()
+    cases = []
+    for block in re.split(r"\n(?=case )", text):
+        lines = [l for l in block.splitlines() if l and not l.startswith("#")]
+        if not lines or not lines[0].startswith("case "):
+            continue
+        head = lines[0].split()
+        c = {"name": head[1]}
+        for kv in head[2:]:
+            k, v = kv.split("=")
+            c[k] = int(v)
+        for l in lines[1:]:
+            key, val = l.split(" ", 1)
+            c[key] = val.strip()
+        cases.append(c)
+    return cases
+
+
+def hand_case8_arrays(c):
+    cols, group = c["cols"], c["group"]
+    rows = [[int(c[k][2 * i:2 * i + 2], 16) for i in range(cols)] for k in ("q0", "q1")]
+    q = pack_rows(rows, 8)
+    sb = []
+    for key in ("sb0", "sb1"):
+        groups = [tuple(float(v) for v in g.split(",")) for g in c[key].split(";")]
+        assert len(groups) == cols // group
+        sb.append([v for g in groups for v in g])
+    sb = bf16_bits(sb).reshape(2, cols // group, 2)
+    spec = c["x"].split()
+    x = np.zeros(cols)
+    if spec[0] == "all":
+        x[:] = float(spec[1])
+    else:
+        x[int(spec[1])] = 1.0
+    y = np.array([float(v) for v in c["y"].split()])
+    return q, sb, x, y
+
+
+HAND8 = load_hand_cases8()
+
+
+def check_hand_cases8():
+    assert len(HAND8) >= 8
+    for c in HAND8:
+        q, sb, x, y = hand_case8_arrays(c)
+        got = O.gemv(q, sb, 8, x, group=c["group"])
+        assert np.array_equal(got, y), (c["name"], got, y)
+
+
+def test_hand_cases_8bit():
+    check_hand_cases8()
+
+
+def test_eight_bit_equals_four_bit_repack():
+    """4-bit codes (0..15) repacked one per byte give the same oracle result at 8 bits."""
+    q4, sb = synth.qmatrix(23, 6, 256, 4)
+    codes = codes_by_string(q4.numpy(), 4)
+    q8 = pack_rows(codes.tolist(), 8)
+    x = O.round_bf16(np.random.default_rng(4).standard_normal(256))
+    assert np.array_equal(O.gemv(q4.numpy(), sb, 4, x), O.gemv(q8, sb, 8, x))
+
+
+def test_per_row_equals_uniform_groups():
+    """One (scale, bias) per row equals the per-group format with that pair in every group."""
+    q, sb_row = synth.qmatrix(24, 5, 512, 8, group=512)
+    sb_groups = sb_row.repeat(1, 512 // 64, 1)  # [5][8][2], every group the row's pair
+    x = O.round_bf16(np.random.default_rng(5).standard_normal(512))
+    assert np.array_equal(O.gemv(q.numpy(), sb_row, 8, x, group=512), O.gemv(q.numpy(), sb_groups, 8, x))
+
+
+def test_signed_int8_closed_form():
+    """Symmetric int8 c (w = c*s) stored as q = c + 128 with bias -128*s dequantises to c*s exactly."""
+    rng = np.random.default_rng(6)
+    c = rng.integers(-128, 128, size=(3, 128))
+    s = O.round_bf16(rng.uniform(0.001, 0.05, size=(3, 2)))
+    sb = np.stack([s, -128.0 * s], axis=-1)  # -128*s is exact in bf16
+    sbb = bf16_bits(sb)
+    assert np.array_equal(O.bf16_to_f64(sbb), sb)
+    q = pack_rows((c + 128).tolist(), 8)
+    w = O.dequant(q, sbb, 8)
+    assert np.array_equal(w, c * np.repeat(s, 64, axis=1))
+
+
 # --------------------------------------------------------- bf16 rounding
 def check_bf16_rounding():
     cases = {
@@ -143,7 +228,7 @@ def check_column_extraction(bits):
         assert np.array_equal(O.gemv(qn, sb, bits, x), expect), k
 
 
-@pytest.mark.parametrize("bits", [4, 2])
+@pytest.mark.parametrize("bits", [4, 2, 8])
 def test_column_extraction(bits):
     check_column_extraction(bits)
 
@@ -380,10 +465,37 @@ def test_planted_msb_first_unpack_is_caught(monkeypatch):
     _raises(check_hand_cases)
 
 
+def test_planted_msb_first_byte_order_is_caught(monkeypatch):
+    good = O.unpack_codes
+
+    def msb_first(qw, bits):
+        q = good(qw, bits)
+        per = 32 // bits
+        return q.reshape(q.shape[0], -1, per)[:, :, ::-1].reshape(q.shape)
+
+    monkeypatch.setattr(O, "unpack_codes", msb_first)
+    _raises(check_hand_cases8)
+
+
+def test_planted_per_row_as_first_group_is_caught(monkeypatch):
+    good = O.dequant
+
+    def dequant_group64(qw, sb, bits, group=64):
+        # a plausible slip: the per-row pair applied only to the first 64 columns
+        w = good(qw, sb, bits, group)
+        if group != 64:
+            q = O.unpack_codes(qw, bits).astype(np.float64)
+            w[:, 64:] = q[:, 64:]
+        return w
+
+    monkeypatch.setattr(O, "dequant", dequant_group64)
+    _raises(check_hand_cases8)
+
+
 def test_planted_swapped_scale_bias_is_caught(monkeypatch):
     good = O.bf16_to_f64
 
-    def dequant_swapped(qw, sb, bits):
+    def dequant_swapped(qw, sb, bits, group=64):
         q = O.unpack_codes(qw, bits).astype(np.float64)
         sbv = good(sb).reshape(q.shape[0], q.shape[1] // 64, 2)
         s = np.repeat(sbv[:, :, 1], 64, axis=1)
@@ -395,7 +507,7 @@ def test_planted_swapped_scale_bias_is_caught(monkeypatch):
 
 
 def test_planted_dropped_bias_is_caught(monkeypatch):
-    def dequant_nobias(qw, sb, bits):
+    def dequant_nobias(qw, sb, bits, group=64):
         q = O.unpack_codes(qw, bits).astype(np.float64)
         sbv = O.bf16_to_f64(sb).reshape(q.shape[0], q.shape[1] // 64, 2)
         return q * np.repeat(sbv[:, :, 0], 64, axis=1)
@@ -406,7 +518,7 @@ def test_planted_dropped_bias_is_caught(monkeypatch):
 
 
 def test_planted_wrong_group_index_is_caught(monkeypatch):
-    def dequant_modgroup(qw, sb, bits):
+    def dequant_modgroup(qw, sb, bits, group=64):
         q = O.unpack_codes(qw, bits).astype(np.float64)
         sbv = O.bf16_to_f64(sb).reshape(q.shape[0], q.shape[1] // 64, 2)
         g = np.arange(q.shape[1]) % sbv.shape[1]
