@@ -9,7 +9,8 @@ router, softmax/top-4, SwiGLU experts, shared expert, combine, residual).
 Seeded synthetic weights and activations (no trained model exists here).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload stack4|stack2|layer|gemv|host] [--layers L] [--batch B]
+                  [--workload stack4|stack2|layer|gemv|gemv8|host] [--layers L] [--batch B]
+                  [--rows R --cols C --per-row]   (gemv8: the int8 MLP / QKV GEMV)
 
 Prints one JSON line. With N > 1 (torchrun) every rank runs its own decode
 stream on its own GPU (replicas; no data-path collective); the slowest
@@ -222,6 +223,10 @@ def workload_name(args) -> str:
                 f"d_model 4096, d_ff 1024, top-4, 4-bit, batch {args.batch}, ring of 16 inputs, "
                 + ("selected experts copied into HBM slots, then computed" if args.fetch == "copy"
                    else "selected experts read directly while computing"))
+    if args.workload == "gemv8":
+        return (f"q8_gemv: {args.rows}x{args.cols} 8-bit codes, " +
+                ("one bf16 scale+bias per row" if args.per_row else "group 64 bf16 scale+bias") +
+                f", batch {args.batch}, ring of {args.ring} matrices")
     return f"q4_gemv: 1024x4096 4-bit, group 64, batch 1, variant {args.variant}, ring of {args.ring} matrices"
 
 
@@ -566,13 +571,56 @@ def run_gemv(args):
     return 0
 
 
+def run_gemv8(args):
+    """q8_gemv (int8 weights, rows x cols, batch B) per step, cycling through a
+    ring of distinct matrices larger than L2 (4 x 129 MB at least)."""
+    import torch
+
+    from bit_group_quantized_gb300 import lib, synth
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    lib.load()
+    rows, cols, B = args.rows, args.cols, args.batch
+    group = cols if args.per_row else 64
+    gpr = cols // group
+    mat_bytes = rows * cols + rows * gpr * 4
+    R = args.ring = max(args.ring, -(-600_000_000 // mat_bytes))
+    mats = []
+    for r in range(R):
+        q, sb = synth.qmatrix(args.seed + r, rows, cols, 8, device=dev, group=group)
+        mats.append(lib.QMatrix(q, sb, rows, cols, 8, group))
+    xs = [synth.activations(args.seed, 2000 + r, B, cols, device=dev) for r in range(R)]
+    ys = [torch.empty((B, rows), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    stream = torch.cuda.Stream(device=dev)
+
+    def body():
+        for r in range(R):
+            lib.q8_gemv(mats[r], xs[r], y=ys[r], stream=stream)
+
+    n_rep = max(1, args.steps // R)
+    ms = _timed_graph(torch, stream, body, n_rep, args.warmup) / R
+    nbytes = mat_bytes + B * cols * 2 + B * rows * 2
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+    print(json.dumps({
+        "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": 1, "steps": n_rep * R,
+        "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u8 codes x s16 fixed-point x (dp4a), f32 accumulate", "data": "synthetic",
+        "config": {"workload": workload_name(args), "us_per_gemv": round(ms * 1000, 3), "bytes": nbytes,
+                   "l2": f"ring of {R} matrices ({R * mat_bytes / 1e6:.0f} MB) cycled, larger than L2"},
+        "roofline": {"bound": "hbm", "kernel": "k_q8gemv", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gbs / peak, 4), "peak_kind": peak_kind, "traffic": None}}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="stack4", choices=["stack4", "stack2", "layer", "gemv", "host"])
+    ap.add_argument("--workload", default="stack4", choices=["stack4", "stack2", "layer", "gemv", "gemv8", "host"])
     ap.add_argument("--variant", type=int, default=0, help="gemv: 0 integer (production), 1 standard, "
                                                             "2 reordered (the page's fma form), 3 hoisted fp32")
     ap.add_argument("--ring", type=int, default=8, help="layer/gemv: distinct weight copies cycled through")
@@ -580,6 +628,9 @@ def main():
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--fetch", default="direct", choices=["direct", "copy"],
                     help="host: read host-resident experts directly (direct) or copy them into HBM first (copy)")
+    ap.add_argument("--rows", type=int, default=4096, help="gemv8: output rows")
+    ap.add_argument("--cols", type=int, default=4096, help="gemv8: input columns")
+    ap.add_argument("--per-row", action="store_true", help="gemv8: one (scale, bias) per row (the FC2 format)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -592,6 +643,8 @@ def main():
         return run_layer(args)
     if args.workload == "gemv":
         return run_gemv(args)
+    if args.workload == "gemv8":
+        return run_gemv8(args)
     if args.workload == "host":
         return run_host(args)
     return run_ours(args)

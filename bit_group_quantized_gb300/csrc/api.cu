@@ -254,6 +254,18 @@ int32_t bgq_qgemv_variant(const bgq_qmatrix* W, const uint16_t* x, uint16_t* y, 
   return gemv_common(W, x, y, batch, variant, 0, stream);
 }
 
+int32_t q8_gemv(const bgq_qmatrix* W, const uint16_t* x, uint16_t* y, int32_t batch, void* stream) {
+  if (!W || !W->q || !W->sb || !x || !y) return BGQ_ERR_INVALID_ARG;
+  if (W->bits != 8) return BGQ_ERR_INVALID_ARG;
+  if (W->rows <= 0 || W->cols <= 0 || W->cols % kGroup || W->cols > 65536) return BGQ_ERR_INVALID_ARG;
+  if (W->group != kGroup && W->group != W->cols) return BGQ_ERR_UNSUPPORTED;
+  if (!cols_supported(W->cols, 8) || q8gemv_max_tokens(W->cols) < 1) return BGQ_ERR_UNSUPPORTED;
+  if (!al(W->q, 16) || !al(W->sb, 4) || !al(x, 16) || !al(y, 16)) return BGQ_ERR_INVALID_ARG;
+  if (batch < 1 || batch > 64) return BGQ_ERR_INVALID_ARG;
+  const int gpr = W->group == W->cols ? 1 : W->cols / kGroup;
+  return cuda_status(launch_q8gemv(qm(W), gpr, x, batch, y, st(stream)));
+}
+
 size_t moe_route_workspace_bytes(int32_t batch, int32_t n_experts) {
   if (batch < 1 || n_experts < 1) return 0;
   return sizeof(Ctrl) + up256((size_t)batch * (n_experts + 1) * 4 + (size_t)batch * kMaxTopK * 4);

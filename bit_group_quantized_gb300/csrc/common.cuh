@@ -456,4 +456,34 @@ __device__ __forceinline__ float row_reduce8(float (&v)[8], int LPR, int lane) {
   return v[0];
 }
 
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch (sm_90+). A kernel launched with
+// launch_overlapped() may start while the previous kernel on its stream is
+// still running. Before pdl_wait() it reads only data that no earlier kernel
+// writes (the weights); pdl_wait() blocks until every earlier kernel on the
+// stream has completed and its writes are visible; inputs are read and outputs
+// written after that. pdl_trigger() comes right after the wait, so the next
+// kernel starts its prologue only once this one runs: at most one kernel waits
+// on the SMs behind the running one (triggering at the start let a chain of
+// waiting kernels fill the SMs and slowed the running one).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_overlapped(void (*kern)(KArgs...), int grid, int block, size_t smem, cudaStream_t s,
+                                     Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 }  // namespace bgq

@@ -60,6 +60,8 @@ k_qgemv_int16(const uint32_t* __restrict__ q, const uint32_t* __restrict__ sb, i
     }
   }
 
+  pdl_wait();  // x may come from the previous kernel; y may still be read by it
+  pdl_trigger();  // the next kernel may start its prologue now (at most one waits behind this one)
   stage_x_int16<BITS>(StridedSrc<uint16_t>{x, ldx}, T, cols, st, gsh);
 
   float acc[T];
@@ -147,7 +149,8 @@ k_qgemv_float(const uint32_t* __restrict__ q, const uint32_t* __restrict__ sb, i
   const int wpr = cols * BITS / 32, gpr = cols / kGroup;
   const uint32_t* qrow = q + (size_t)(valid ? row : 0) * wpr;
   const uint32_t* sbrow = sb + (size_t)(valid ? row : 0) * gpr;
-
+  pdl_wait();
+  pdl_trigger();
   stage_x_f32<BITS>(x, ldx, T, cols, slots, partsum);
 
   for (int t = 0; t < T; ++t) {
@@ -205,9 +208,8 @@ static cudaError_t launch_int16_t(const QMat& W, const uint16_t* x, int ldx, uin
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
   }
-  kern<<<grid, kGemvThreads, sm, s>>>(W.q, reinterpret_cast<const uint32_t*>(W.sb), W.rows, W.cols, x, ldx, y, yf,
-                                      ldy);
-  return cudaGetLastError();
+  return launch_overlapped(kern, grid, kGemvThreads, sm, s, W.q, reinterpret_cast<const uint32_t*>(W.sb), W.rows,
+                           W.cols, x, ldx, y, yf, ldy);
 }
 
 template <int BITS>
@@ -251,9 +253,8 @@ cudaError_t launch_qgemv(const QMat& W, const uint16_t* x, int batch, uint16_t* 
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
         if (e != cudaSuccess) return e;
       }
-      kern<<<grid, kGemvThreads, sm, s>>>(W.q, reinterpret_cast<const uint32_t*>(W.sb), W.rows, W.cols, xt, W.cols,
-                                          T, yt, W.rows);
-      e = cudaGetLastError();
+      e = launch_overlapped(kern, grid, kGemvThreads, sm, s, W.q, reinterpret_cast<const uint32_t*>(W.sb), W.rows,
+                            W.cols, xt, W.cols, T, yt, W.rows);
     }
     if (e != cudaSuccess) return e;
   }

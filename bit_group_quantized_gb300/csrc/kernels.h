@@ -102,6 +102,11 @@ size_t qgemv_int16_smem(int cols, int bits, int T);
 cudaError_t launch_qgemv(const QMat& W, const uint16_t* x, int batch, uint16_t* y, float* yf, int variant,
                          cudaStream_t s);
 
+// 8-bit GEMV (gemv8.cu). gpr = (scale, bias) pairs per row: cols/64 or 1 (per
+// row). q8gemv_max_tokens: inputs staged per launch for `cols` (0: too wide).
+int q8gemv_max_tokens(int cols);
+cudaError_t launch_q8gemv(const QMat& W, int gpr, const uint16_t* x, int batch, uint16_t* y, cudaStream_t s);
+
 // Router + softmax + top-K (+ optional grouping plan). Experts with at least
 // big_min tokens become tensor-core tasks (kBigTok; INT_MAX: none).
 cudaError_t launch_route(const uint16_t* router, const uint16_t* sgate, const uint16_t* x, int batch, int d,

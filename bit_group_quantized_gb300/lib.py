@@ -55,6 +55,7 @@ _SIGS = {
     "q4_gemv": (_I, [C.POINTER(bgq_qmatrix), _P, _P, _I, _P]),
     "q2_gemv": (_I, [C.POINTER(bgq_qmatrix), _P, _P, _I, _P]),
     "bgq_qgemv_variant": (_I, [C.POINTER(bgq_qmatrix), _P, _P, _I, _I, _P]),
+    "q8_gemv": (_I, [C.POINTER(bgq_qmatrix), _P, _P, _I, _P]),
     "moe_route_workspace_bytes": (_S, [_I, _I]),
     "moe_route_topk": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _S, _P]),
     "moe_expert_workspace_bytes": (_S, [C.POINTER(bgq_expert), _I]),
@@ -120,13 +121,16 @@ def workspace(nbytes: int, device) -> torch.Tensor:
 
 # ------------------------------------------------------------------ matrices
 class QMatrix:
-    """A packed matrix: q int32 [rows][cols*bits/32], sb bf16 [rows][cols/64][2]."""
+    """A packed matrix: q int32 [rows][cols*bits/32], sb bf16 [rows][cols/group][2].
 
-    def __init__(self, q: torch.Tensor, sb: torch.Tensor, rows: int, cols: int, bits: int):
-        self.q, self.sb, self.rows, self.cols, self.bits = q, sb, rows, cols, bits
+    group is 64, or cols for the per-row 8-bit format (one (scale, bias) per row).
+    """
+
+    def __init__(self, q: torch.Tensor, sb: torch.Tensor, rows: int, cols: int, bits: int, group: int = GROUP):
+        self.q, self.sb, self.rows, self.cols, self.bits, self.group = q, sb, rows, cols, bits, group
 
     def struct(self) -> bgq_qmatrix:
-        return bgq_qmatrix(self.q.data_ptr(), self.sb.data_ptr(), self.rows, self.cols, self.bits, GROUP)
+        return bgq_qmatrix(self.q.data_ptr(), self.sb.data_ptr(), self.rows, self.cols, self.bits, self.group)
 
 
 def _gemv(fn, W: QMatrix, x, y, stream, *extra):
@@ -144,6 +148,11 @@ def q4_gemv(W: QMatrix, x: torch.Tensor, y: torch.Tensor | None = None, stream=N
 
 def q2_gemv(W: QMatrix, x: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     return _gemv(load().q2_gemv, W, x, y, stream)
+
+
+def q8_gemv(W: QMatrix, x: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """8-bit GEMV (int8 MLP / QKV weights; per-group or, with W.group == W.cols, per-row scale/bias)."""
+    return _gemv(load().q8_gemv, W, x, y, stream)
 
 
 def qgemv_variant(W: QMatrix, x: torch.Tensor, variant: int, y=None, stream=None) -> torch.Tensor:

@@ -150,6 +150,25 @@ int32_t q2_gemv(const bgq_qmatrix* W, const uint16_t* x, uint16_t* y, int32_t ba
 int32_t bgq_qgemv_variant(const bgq_qmatrix* W, const uint16_t* x, uint16_t* y, int32_t batch,
                           int32_t variant, void* stream);
 
+/* y[b][n] = bf16( sum_k W[n][k] * x[b][k] ), b < batch, fp32 accumulation, for
+ * 8-bit weights: the int8 format of dense MLP and QKV projections.
+ * Source: "Redis 之父下场手写推理引擎：antirez 用约 24000 行原生代码驯服视频生成模型"
+ * (text-matrix.pages.dev), the paragraph on --use-int8-row-fc2: MLP weights are
+ * int8 with one scale per group, and FC2 can instead carry one scale per row.
+ *   W->bits must be 8: codes q in 0..255, four per uint32, code k of a row in
+ *     word k/4 at bit offset 8*(k%4); W[n][k] = q[n][k]*scale + bias.
+ *   W->group = 64: sb is bf16 [rows][cols/64][2], one (scale, bias) per group;
+ *   W->group = W->cols: the per-row format, sb is bf16 [rows][1][2].
+ *   Symmetric signed int8 c (W = c*scale) is stored as q = c + 128 with
+ *   bias = -128*scale (exact in bf16).
+ *   cols: 64, 128, 256 or a multiple of 512, at most 65536.
+ *   x: bf16 [batch][cols], y: bf16 [batch][rows], 1 <= batch <= 64 (inputs
+ *   are staged in groups of up to 8 per launch, fewer for cols > 11264; W is
+ *   read once per group). Alignment: q, x, y 16 bytes; sb 4 bytes.
+ * Errors: BGQ_ERR_INVALID_ARG (NULL, bits != 8, bad sizes, misalignment),
+ * BGQ_ERR_UNSUPPORTED (group neither 64 nor cols, cols shape), BGQ_ERR_CUDA. */
+int32_t q8_gemv(const bgq_qmatrix* W, const uint16_t* x, uint16_t* y, int32_t batch, void* stream);
+
 /* Router of a batch of tokens (Flash-MoE page, "架构设计": routing, then
  * softmax + top-K on the logits).
  *   logits_l[b][e] = router[e] . x[b] (fp32), p = softmax_fp32(l[b]),

@@ -48,6 +48,27 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(lib._SIGS) >= set(names)
 
 
+def test_q8_gemv_validation(lib):
+    L = lib.load()
+    W = qmat(lib, bits=8)
+    assert L.q8_gemv(None, FAKE, FAKE, 1, None) == lib.ERR_INVALID_ARG
+    assert L.q8_gemv(C.byref(W), None, FAKE, 1, None) == lib.ERR_INVALID_ARG
+    assert L.q8_gemv(C.byref(W), FAKE + 2, FAKE, 1, None) == lib.ERR_INVALID_ARG  # misaligned x
+    assert L.q8_gemv(C.byref(W), FAKE, FAKE + 8, 1, None) == lib.ERR_INVALID_ARG  # misaligned y
+    assert L.q8_gemv(C.byref(W), FAKE, FAKE, 0, None) == lib.ERR_INVALID_ARG
+    assert L.q8_gemv(C.byref(W), FAKE, FAKE, 65, None) == lib.ERR_INVALID_ARG
+    assert L.q8_gemv(C.byref(qmat(lib, bits=4)), FAKE, FAKE, 1, None) == lib.ERR_INVALID_ARG  # wrong bits
+    assert L.q4_gemv(C.byref(W), FAKE, FAKE, 1, None) == lib.ERR_INVALID_ARG  # 8-bit only through q8_gemv
+    assert L.bgq_qgemv_variant(C.byref(W), FAKE, FAKE, 1, 1, None) == lib.ERR_INVALID_ARG
+    assert L.q8_gemv(C.byref(qmat(lib, bits=8, group=128)), FAKE, FAKE, 1, None) == lib.ERR_UNSUPPORTED
+    assert L.q8_gemv(C.byref(qmat(lib, bits=8, cols=100)), FAKE, FAKE, 1, None) == lib.ERR_INVALID_ARG
+    assert L.q8_gemv(C.byref(qmat(lib, bits=8, cols=768)), FAKE, FAKE, 1, None) == lib.ERR_UNSUPPORTED
+    assert L.q8_gemv(C.byref(qmat(lib, bits=8, cols=65536 + 512)), FAKE, FAKE, 1, None) == lib.ERR_INVALID_ARG
+    assert L.q8_gemv(C.byref(qmat(lib, bits=8, q=FAKE + 4)), FAKE, FAKE, 1, None) == lib.ERR_INVALID_ARG
+    assert L.q8_gemv(C.byref(qmat(lib, bits=8, sb=FAKE + 2)), FAKE, FAKE, 1, None) == lib.ERR_INVALID_ARG
+    assert L.q8_gemv(C.byref(qmat(lib, bits=8, rows=0)), FAKE, FAKE, 1, None) == lib.ERR_INVALID_ARG
+
+
 def test_status_strings(lib):
     assert lib.status_string(0) == "ok"
     assert "workspace" in lib.status_string(5)
