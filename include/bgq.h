@@ -138,6 +138,14 @@ const char* bgq_status_string(int32_t status);
 /* ABI version of this header (major*100 + minor). */
 int32_t bgq_abi_version(void);
 
+/* Overlapped launch of the GEMVs (q4_gemv, q2_gemv, bgq_qgemv_variant, q8_gemv):
+ * their kernels are launched with programmatic dependent launch, so a GEMV may
+ * start while the kernel before it on the stream is still running. Before it
+ * waits for that kernel it reads only W (q and sb): W must not be written by
+ * the kernels enqueued just before the call on the same stream (weights are
+ * normally written once, long before). x is read and y written only after
+ * every earlier kernel on the stream has completed, as with a plain launch. */
+
 /* y[b][n] = bf16( sum_k W[n][k] * x[b][k] ), b < batch, fp32 accumulation.
  * The standalone GEMV of the format (Flash-MoE page, "FMA Dequant").
  * W->bits must be 4 for q4_gemv and 2 for q2_gemv. x: bf16 [batch][cols],
