@@ -39,6 +39,11 @@ Q8_CASES = [
     (1024, 4096, 4096, 1),  # per-row scale/bias (FC2 format)
     (777, 1024, 1024, 6),  # per-row, ragged
     (128, 128, 128, 1),  # per-row, 8 lanes per row
+    (300, 1536, 64, 3),  # 3 parts per lane: one row per item
+    (50, 2560, 2560, 3),  # 5 parts per lane, per row
+    (5000, 1024, 64, 3),  # streaming kernel: several rows per warp, four rows packed per item
+    (20000, 256, 256, 4),  # streaming kernel: 16 lanes per row, eight row pairs per item; per row
+    (16384, 4096, 64, 2),  # one-shot kernel over several waves
 ]
 
 
