@@ -9,7 +9,7 @@ router, softmax/top-4, SwiGLU experts, shared expert, combine, residual).
 Seeded synthetic weights and activations (no trained model exists here).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload stack4|stack2|layer|gemv|gemv8|host] [--layers L] [--batch B]
+                  [--workload stack4|stack2|layer|expert|gemv|gemv8|host] [--layers L] [--batch B]
                   [--rows R --cols C --per-row]   (gemv8: the int8 MLP / QKV GEMV)
 
 Prints one JSON line. With N > 1 (torchrun) every rank runs its own decode
@@ -223,6 +223,9 @@ def workload_name(args) -> str:
                 f"d_model 4096, d_ff 1024, top-4, 4-bit, batch {args.batch}, ring of 16 inputs, "
                 + ("selected experts copied into HBM slots, then computed" if args.fetch == "copy"
                    else "selected experts read directly while computing"))
+    if args.workload == "expert":
+        return (f"moe_expert_swiglu: one SwiGLU expert (gate/up 1024x4096, down 4096x1024), 4-bit, group 64, "
+                f"batch {args.batch}, ring of {args.ring} experts")
     if args.workload == "gemv8":
         return (f"q8_gemv: {args.rows}x{args.cols} 8-bit codes, " +
                 ("one bf16 scale+bias per row" if args.per_row else "group 64 bf16 scale+bias") +
@@ -571,6 +574,51 @@ def run_gemv(args):
     return 0
 
 
+def run_expert(args):
+    """moe_expert_swiglu (one SwiGLU expert: gate/up 1024x4096, down 4096x1024,
+    4-bit) on B tokens per step, cycling through a ring of distinct experts
+    larger than L2."""
+    import torch
+
+    from bit_group_quantized_gb300 import lib, synth
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    lib.load()
+    shape = synth.PoolShape(4096, 1024, 1, 4)
+    R = args.ring = max(args.ring, -(-600_000_000 // shape.expert_bytes))
+    q, sb = synth.expert_pool_range(args.seed, 0, shape, 0, R, device=dev)
+    experts = []
+    for r in range(R):
+        m = synth.expert_matrices(q[r], sb[r], shape)
+        experts.append(lib.Expert(*[lib.QMatrix(mq, ms, mq.shape[0], ms.shape[1] * 64, 4) for mq, ms in m]))
+    B = args.batch
+    xs = [synth.activations(args.seed, 3000 + r, B, shape.d, device=dev) for r in range(R)]
+    ws = lib.workspace(lib.expert_workspace_bytes(experts[0], B), dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def body():
+        for r in range(R):
+            lib.moe_expert_swiglu(experts[r], xs[r], ws=ws, stream=stream)
+
+    n_rep = max(1, args.steps // R)
+    ms = _timed_graph(torch, stream, body, n_rep, args.warmup) / R
+    nbytes = shape.expert_bytes + B * shape.d * 2 * 2
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+    print(json.dumps({
+        "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": 1, "steps": n_rep * R,
+        "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u4 codes x s16 fixed-point x (dp4a), f32 accumulate", "data": "synthetic",
+        "config": {"workload": workload_name(args), "us_per_expert": round(ms * 1000, 3), "bytes": nbytes,
+                   "tokens_per_s": round(B / (ms * 1e-3), 1),
+                   "l2": f"ring of {R} experts ({R * shape.expert_bytes / 1e6:.0f} MB) cycled, larger than L2"},
+        "roofline": {"bound": "hbm", "kernel": "k_gateup + k_down (one expert)", "achieved": round(gbs, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4), "peak_kind": peak_kind,
+                     "traffic": None}}), flush=True)
+    return 0
+
+
 def run_gemv8(args):
     """q8_gemv (int8 weights, rows x cols, batch B) per step, cycling through a
     ring of distinct matrices larger than L2 (4 x 129 MB at least)."""
@@ -620,7 +668,7 @@ def main():
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="stack4", choices=["stack4", "stack2", "layer", "gemv", "gemv8", "host"])
+    ap.add_argument("--workload", default="stack4", choices=["stack4", "stack2", "layer", "expert", "gemv", "gemv8", "host"])
     ap.add_argument("--variant", type=int, default=0, help="gemv: 0 integer (production), 1 standard, "
                                                             "2 reordered (the page's fma form), 3 hoisted fp32")
     ap.add_argument("--ring", type=int, default=8, help="layer/gemv: distinct weight copies cycled through")
@@ -645,6 +693,8 @@ def main():
         return run_gemv(args)
     if args.workload == "gemv8":
         return run_gemv8(args)
+    if args.workload == "expert":
+        return run_expert(args)
     if args.workload == "host":
         return run_host(args)
     return run_ours(args)

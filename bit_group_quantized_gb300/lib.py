@@ -195,6 +195,11 @@ class Expert:
         return bgq_expert(self.gate.struct(), self.up.struct(), self.down.struct())
 
 
+def expert_workspace_bytes(e: Expert, batch: int) -> int:
+    s = e.struct()
+    return int(load().moe_expert_workspace_bytes(C.byref(s), batch))
+
+
 def moe_expert_swiglu(e: Expert, x: torch.Tensor, ws=None, want_f32=False, stream=None):
     lib = load()
     B = x.shape[0]
