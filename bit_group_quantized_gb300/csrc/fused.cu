@@ -184,7 +184,7 @@ __host__ __device__ inline FGeo fgeo(int nC, int d, int f, int E, int K, int bit
 
 // Shared-memory layout (byte offsets; every region 128-byte aligned).
 struct FLayout {
-  size_t misc, rho, a_s, sta_chunks, sta_pi, gsh_a, sth_chunks, sth_pi, gsh_h, bufA, bufB, total;
+  size_t misc, rho, a_s, sta_chunks, sta_pi, gsh_a, sth_chunks, sth_pi, gsh_h, hres, bufA, bufB, total;
 };
 __host__ __device__ inline size_t fl_take(size_t& o, size_t bytes) {
   size_t r = o;
@@ -204,6 +204,7 @@ __host__ __device__ inline FLayout flayout(const FGeo& g, int d, int f, int K, i
   L.sth_chunks = fl_take(o, (size_t)(K + 1) * f * 2);
   L.sth_pi = fl_take(o, (size_t)(K + 1) * (f * bits / 128) * 8);
   L.gsh_h = fl_take(o, (size_t)(K + 1) * (f / kGroup) * 4);
+  L.hres = fl_take(o, (size_t)((d + g.nC - 1) / g.nC) * 4);  // this CTA's rows of the residual
   L.bufA = fl_take(o, (size_t)g.bufA);
   L.bufB = fl_take(o, (size_t)g.bufB);
   L.total = o;
@@ -348,9 +349,6 @@ __device__ __forceinline__ void stamp(const FusedParams& P, int l, int ev) {
     P.trace[((size_t)l * gridDim.x + blockIdx.x) * kTraceEvents + ev] = globaltimer();
 }
 
-__device__ __forceinline__ float h_in(const FusedParams& P, int l, int k) {
-  return l == 0 ? bf16f(P.x_in[k]) : __ldcg(P.h + k);
-}
 
 // Shared-memory state of the kernel.
 struct FSmem {
@@ -651,6 +649,11 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
   sth.partinfo = reinterpret_cast<float2*>(smem + FL.sth_pi);
   S.bufA = smem + FL.bufA;
   S.bufB = smem + FL.bufB;
+  // Stack mode: this CTA's rows [c_b, c_e) of the residual stream (the input
+  // token before layer 0). The CTA writes the same rows every layer (and
+  // thread t always row c_b + t), so the combine adds to this copy instead of
+  // reading them back from L2 (20.96 -> 20.58 us per layer, 24-layer stack).
+  float* hres = reinterpret_cast<float*>(smem + FL.hres);
   __shared__ float s_r;
 
   if (tid == 0) {
@@ -663,6 +666,11 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
     *S.bpar = -1;
     *S.cpar = -1;
     fence_mbar_init();
+  }
+  if (P.stack) {  // the token's input rows of this CTA: the residual before layer 0
+    int hb, he;
+    fsplit(d, blockIdx.x, g.nC, hb, he);
+    for (int k = hb + tid; k < he; k += kFThreads) hres[k - hb] = bf16f(P.x_in[k]);
   }
   __syncthreads();
   if (warp == 0) issue_A(P, g, 0, S);
@@ -875,8 +883,9 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
         float o = 0.f;
         for (int k = 0; k <= K; ++k) o = fmaf(s_w[k], ys[k * nrows + rl], o);
         if (P.stack) {
-          const float hv = h_in(P, l, row) + o;
+          const float hv = hres[rl] + o;
           P.h[row] = hv;
+          hres[rl] = hv;
           ss = fmaf(hv, hv, ss);
         } else {
           if (P.out) P.out[row] = f2bf(o);
@@ -913,7 +922,7 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
     int b, e;
     fsplit(d, blockIdx.x, g.nC, b, e);
     for (int k = b + tid; k < e; k += kFThreads) {
-      float hv = __ldcg(P.h + k);
+      const float hv = hres[k - b];  // written by this thread in the last layer's combine
       if (P.x_next) P.x_next[k] = f2bf(hv * s_r);
       if (P.h_out) P.h_out[k] = hv;
     }
