@@ -76,6 +76,7 @@ struct LayerWs {
   int32_t* fidx;    // [16]
   float* fw;        // [16]
   float* tcs;  // split-K partial sums of the tensor-core kernels (batches that can use them)
+  unsigned long long* ftag;  // batch-1 persistent kernel: tagged logits [E+1]
   size_t bytes;
 };
 
@@ -83,7 +84,10 @@ LayerWs carve_layer(void* ws, int B, int d, int f, int E, int K) {
   Carver c(ws);
   LayerWs L;
   L.ctrl = c.take<Ctrl>(sizeof(Ctrl));
-  L.tccnt = c.take<int>(tc_split_cnt_bytes(d, f, K));  // right after the control block, whatever B is
+  // the persistent kernel's tagged logits right after the control block: zero
+  // between calls like it (layer_zero_prefix_bytes covers both)
+  L.ftag = c.take<unsigned long long>((size_t)(E + 1) * 8);
+  L.tccnt = c.take<int>(tc_split_cnt_bytes(d, f, K));  // at a place that does not depend on B
   L.logits = c.take<float>((size_t)B * (E + 1) * 4 + (size_t)B * K * 4);
   L.plan = c.take<Plan>(plan_bytes(B, K));
   L.idx = c.take<int32_t>((size_t)B * K * 4);
@@ -193,6 +197,7 @@ void fill_fused_common(FusedParams& P, const bgq_moe_layer* L0, const LayerWs& W
   P.h = W.fh;
   P.hk = W.H;
   P.logits = W.logits;
+  P.ltag = W.ftag;
   P.part_ss = W.fpart;
   P.route_idx = W.fidx;
   P.route_w = W.fw;
@@ -213,6 +218,12 @@ FusedLayer fused_layer(const bgq_moe_layer* L, const uint16_t* rho) {
 }
 
 }  // namespace
+
+namespace bgq {
+// Bytes at the start of a layer workspace that must be zero before a call:
+// the control block and the persistent kernel's tagged logits.
+size_t layer_zero_prefix_bytes(int n_experts) { return sizeof(Ctrl) + up256((size_t)(n_experts + 1) * 8); }
+}  // namespace bgq
 
 extern "C" {
 

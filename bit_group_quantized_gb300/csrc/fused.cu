@@ -62,6 +62,14 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
 __device__ __forceinline__ void st_release(int* p, int v) {
   asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -784,11 +792,12 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
       if (valid && qtr == 0 && lane == 0) {
         float s = 0.f;
         for (int q = 0; q < g.qr; ++q) s += red[warp + q];
-        P.logits[row] = s;
+        // one 64-bit word {value, tag}: a reader that sees the tag sees the
+        // value, so the exchange needs no fence and no counter
+        st_relaxed_u64(P.ltag + row, ((unsigned long long)(l + 1) << 32) | __float_as_uint(s));
       }
     }
     stamp(P, l, 3);
-    cta_arrive(&ctrl->misc[1]);
     {  // Staged integer copy of the input for the gate/up rows, while the
        // logits of the other CTAs arrive: fp32 copy in bufB (free until the
        // selection), then staged.
@@ -800,12 +809,44 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
     stamp(P, l, 12);
 
     // ---------------- selection: every CTA selects from the complete logits
-    if (!cta_wait(&ctrl->misc[1], g.nC * (l + 1), ctrl, P.timeout_ns, S)) return;
-    stamp(P, l, 5);
     {
+      // Each thread polls its logits' words until they carry this layer's tag
+      // (bounded: an abort elsewhere or the time limit ends the wait).
+      // Measured against a counter barrier and a separate read of the logits:
+      // see the comment at the top of the file.
       float* lg_s = reinterpret_cast<float*>(S.bufB);  // bufB is free until the B copies
-      for (int e = tid; e <= E; e += kFThreads) lg_s[e] = __ldcg(P.logits + e);
+      const unsigned tag = (unsigned)l + 1u;  // the words are zero when a launch starts
+      const int nrows = E + (has_gate ? 1 : 0);
+      __shared__ int s_fail;
+      if (tid == 0) s_fail = 0;
       __syncthreads();
+      for (int e = tid; e < nrows; e += kFThreads) {
+        unsigned long long v = ld_relaxed_u64(P.ltag + e);
+        if ((unsigned)(v >> 32) != tag) {
+          const unsigned long long t0 = globaltimer();
+          long long it = 0;
+          while ((unsigned)((v = ld_relaxed_u64(P.ltag + e)) >> 32) != tag) {
+            if ((++it & 31) == 0) {
+              if (aborted(ctrl)) {
+                s_fail = 1;
+                break;
+              }
+              if (it > kMaxSpin || (long long)(globaltimer() - t0) > P.timeout_ns) {
+                raise_timeout(ctrl);
+                s_fail = 1;
+                break;
+              }
+            }
+          }
+        }
+        lg_s[e] = __uint_as_float((unsigned)v);
+      }
+      __syncthreads();
+      if (s_fail) {
+        if (tid == 0) drain_copies(S);
+        return;
+      }
+      stamp(P, l, 5);
       block_topk_select(lg_s, reinterpret_cast<int*>(lg_s + ((E + 4) & ~3)), E, K, has_gate, s_idx, s_l);
       stamp(P, l, 11);
     }
@@ -927,10 +968,18 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
       if (P.h_out) P.h_out[k] = hv;
     }
   }
-  // the last CTA out resets the counters for the next launch
+  // the last CTA out resets the counters and clears the tagged logits for the
+  // next launch (every other CTA has read them by now)
   __syncthreads();
+  __shared__ int s_last;
   int prev = 0;
-  if (tid == 0) prev = atomicAdd(&ctrl->misc[5], 1);
+  if (tid == 0) {
+    prev = atomicAdd(&ctrl->misc[5], 1);
+    s_last = prev == g.nC - 1;
+  }
+  __syncthreads();
+  if (s_last)
+    for (int e = tid; e <= E; e += kFThreads) P.ltag[e] = 0ull;
   if (tid == 0 && prev == g.nC - 1) {
     for (int i = 1; i <= 5; ++i) ctrl->misc[i] = 0;
     __threadfence();

@@ -40,6 +40,7 @@ struct FusedParams {
   float* h;          // [d] residual stream
   float* hk;         // [K+1][f] SwiGLU outputs (slot K: shared expert)
   float* logits;     // [E+1]
+  unsigned long long* ltag;  // [E+1] logits as {value bits, tag} words (tag: launch epoch and layer)
   float* part_ss;    // [2][nCTA] per-CTA sums of h^2
   int32_t* route_idx;  // [K]
   float* route_w;      // [K+1] (K: gamma)

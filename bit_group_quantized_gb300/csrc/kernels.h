@@ -102,6 +102,9 @@ size_t qgemv_int16_smem(int cols, int bits, int T);
 cudaError_t launch_qgemv(const QMat& W, const uint16_t* x, int batch, uint16_t* y, float* yf, int variant,
                          cudaStream_t s);
 
+// Bytes at the start of a layer workspace that must be zero before a call (api.cu).
+size_t layer_zero_prefix_bytes(int n_experts);
+
 // 8-bit GEMV (gemv8.cu). gpr = (scale, bias) pairs per row: cols/64 or 1 (per
 // row). q8gemv_max_tokens: inputs staged per launch for `cols` (0: too wide).
 int q8gemv_max_tokens(int cols);

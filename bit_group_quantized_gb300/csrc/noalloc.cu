@@ -17,12 +17,12 @@
 #include <mutex>
 
 #include "../../include/bgq.h"
+#include "kernels.h"
 
 namespace {
 
 constexpr size_t kStaticScratchBytes = 4u << 20;  // 4 MiB
 constexpr int kMaxDevices = 64;
-constexpr size_t kControlBytes = 256;  // status word and counters, must start at zero
 
 static __device__ __align__(256) unsigned char g_layer_scratch[kStaticScratchBytes];
 
@@ -56,9 +56,12 @@ int32_t moe_layer_forward_noalloc(const bgq_moe_layer* L, const uint16_t* x, int
   void* ws = nullptr;
   int32_t r = scratch_for_current_device(&ws);
   if (r != BGQ_OK) return r;
-  // The array keeps whatever the previous call left; only the control block
-  // has to start at zero (every other region is written before it is read).
-  if (cudaMemsetAsync(ws, 0, kControlBytes, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+  // The array keeps whatever the previous call left; only its first bytes (the
+  // control block: status word and counters, and the batch-1 kernel's tagged
+  // routing logits) have to start at zero (every other region is written
+  // before it is read).
+  if (cudaMemsetAsync(ws, 0, bgq::layer_zero_prefix_bytes(L->n_experts), reinterpret_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
     return BGQ_ERR_CUDA;
   return moe_layer_forward(L, x, batch, out, out_f32, idx_out, w_out, gamma_out, ws, kStaticScratchBytes, stream);
 }

@@ -31,6 +31,8 @@
  *     launches nothing. A failed launch returns BGQ_ERR_CUDA.
  *   - Conditions only the GPU can see (a bounded wait that ran out) are written
  *     to the workspace status word; read it with bgq_read_device_status().
+ *     A workspace whose call ended in BGQ_ERR_TIMEOUT must be zero-filled again
+ *     before it is reused (counters and exchange words are left mid-call).
  *   - Device pointers must be 16-byte aligned (codes, x, outputs) and 4-byte
  *     aligned (scale/bias). Workspaces must be 256-byte aligned and zero-filled
  *     once before first use (the kernels leave their counters at zero).
