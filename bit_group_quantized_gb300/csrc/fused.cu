@@ -7,15 +7,17 @@
 // weights are read exactly once, so a layer is bound by HBM bandwidth and by
 // the latency of its three dependent steps. One cooperative launch with one
 // CTA per SM keeps the token on chip and replaces kernel boundaries by
-// grid-wide counters:
+// grid-wide exchanges:
 //
 //   A  RMSNorm of the residual (stack mode), router rows (bf16) and the shared
-//      expert's gate/up rows; every CTA publishes its logits;
-//   B  after the logits counter, every CTA selects the same top-K experts from
-//      all logits and computes its share of their gate/up rows;
+//      expert's gate/up rows; every CTA publishes its logits as tagged words;
+//   B  once every logit carries the layer's tag, every CTA selects the same
+//      top-K experts from all logits and computes its share of their gate/up
+//      rows;
 //   C  after the SwiGLU counter, every CTA computes its output rows: the down
 //      rows of the K selected experts and of the shared expert, combined in a
-//      fixed order, plus the residual add in stack mode.
+//      fixed order, plus the residual add in stack mode (after the residual
+//      counter of the previous layer).
 //
 // Data movement. Each CTA owns a fixed slice of every phase. Its router rows,
 // shared gate/up rows (phase A), selected-expert gate/up rows (phase B) and
@@ -27,9 +29,16 @@
 // slowed the exchange: 21.3 vs 21.0 us per layer). Consumers start on a unit
 // as soon as its own mbarrier completes.
 //
-// (A variant that exchanged logits, SwiGLU outputs and the residual as
-// 64-bit {value, tag} words polled by every CTA, with no counters, measured
-// 29.5 us per layer against 24.8 us for this design on the 24-layer stack.)
+// Exchanges. The logits (2 KB) go as 64-bit {value, layer + 1} words written
+// with relaxed stores and polled by every thread for its share: a reader that
+// sees the tag sees the value, so no fence and no counter are needed (20.74 ->
+// 19.98 us per layer against a counter barrier plus a separate read; the
+// words are zero at every launch's start, the last CTA out clears them). The
+// SwiGLU outputs (20 KB per CTA) and the residual use counters: a CTA's
+// release reduction after a block barrier, thread 0 polling with acquire
+// loads. (Tagged words for the SwiGLU outputs measured 24.90 against 20.01 us
+// per layer: their polls slowed the last CTAs' phase-B copies; an earlier
+// variant with all three exchanges tagged, 29.5 against 24.8 us.)
 //
 // Every wait is bounded (an iteration count and %globaltimer). On expiry the
 // CTA sets BGQ_ERR_TIMEOUT in the status word and an abort flag that makes
@@ -811,9 +820,8 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
     // ---------------- selection: every CTA selects from the complete logits
     {
       // Each thread polls its logits' words until they carry this layer's tag
-      // (bounded: an abort elsewhere or the time limit ends the wait).
-      // Measured against a counter barrier and a separate read of the logits:
-      // see the comment at the top of the file.
+      // (bounded: an abort elsewhere or the time limit ends the wait; the
+      // exchange is described at the top of the file).
       float* lg_s = reinterpret_cast<float*>(S.bufB);  // bufB is free until the B copies
       const unsigned tag = (unsigned)l + 1u;  // the words are zero when a launch starts
       const int nrows = E + (has_gate ? 1 : 0);
