@@ -232,8 +232,9 @@ int32_t moe_layer_forward(const bgq_moe_layer* L, const uint16_t* x, int32_t bat
  * batch) exceeds 4 MiB returns BGQ_ERR_WORKSPACE and launches nothing.
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before
- * any stream capture. Each call clears the array's 256-byte control block on
- * `stream`, then runs the layer. All calls on a device share the one array,
+ * any stream capture. Each call clears the start of the array on `stream`
+ * (the 256-byte control block and the batch-1 kernel's (n_experts + 1)
+ * tagged logit words, rounded up to 256 bytes), then runs the layer. All calls on a device share the one array,
  * which keeps the last call's contents: calls that can overlap on the GPU (on
  * different streams, or from different host threads) race and must be
  * serialised by the caller. Allocates nothing. */
