@@ -153,6 +153,24 @@ def test_layer_workspace_reused_across_batches(cuda_device, full_layer):
     assert lib.read_device_status(ws) == lib.OK
 
 
+def test_batch1_calls_in_a_row_share_a_workspace(cuda_device, full_layer):
+    """The batch-1 kernel exchanges the routing logits as words tagged with the
+    layer; the last CTA of every launch clears them, so consecutive calls on
+    one workspace (different inputs, same tags) give the bits of fresh
+    workspaces and never read the previous call's logits."""
+    shape, L, t = full_layer
+    ws = lib.workspace(lib.moe_layer_workspace_bytes(L, 1), cuda_device)
+    for call in range(4):
+        x = synth.activations(0, 950 + call, 1, shape.d, device=cuda_device)
+        a, _, ia, _, _ = lib.moe_layer_forward(L, x, ws=ws, want_route=True)
+        a, ia = a.clone(), ia.clone()
+        b, _, ib, _, _ = lib.moe_layer_forward(L, x, want_route=True)
+        torch.cuda.synchronize()
+        assert torch.equal(ia, ib), call
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), call
+    assert lib.read_device_status(ws) == lib.OK
+
+
 def test_layer_deterministic(cuda_device, full_layer):
     shape, L, t = full_layer
     x = synth.activations(0, 901, 16, shape.d, device=cuda_device)
@@ -256,6 +274,26 @@ def test_stack_matches_oracle(cuda_device, n_layers, d, f, E, bits):
     # different values, so the stack's own error may exceed one layer's.
     assert_bf16_output(O.bf16_to_f64(bits16(x_next)), O.rmsnorm(ho, None), "x_next", own_tol=REL_L2_TOL)
     assert rel_l2(O.bf16_to_f64(bits16(x_next)), O.bf16_to_f64(xo)) <= REL_L2_TOL
+
+
+def test_stack_tokens_in_a_row_share_a_workspace(cuda_device):
+    """Decode steps on one workspace (the next token's input is the previous
+    token's output) give the bits of steps on fresh workspaces."""
+    K = 4
+    shape = synth.PoolShape(1024, 256, 16, 4)
+    built, rhos = stack_case(cuda_device, 4, 3, shape, K)
+    st = lib.Stack([b[0] for b in built], rhos)
+    ws = lib.workspace(st.ws_bytes, cuda_device)
+    x = synth.activations(4, 6, 1, shape.d, device=cuda_device)[0].clone()
+    for step in range(3):
+        xa = torch.empty_like(x)
+        xb = torch.empty_like(x)
+        lib.moe_stack_decode(st, x, 1e-6, ws=ws, x_next=xa)
+        lib.moe_stack_decode(st, x, 1e-6, x_next=xb)
+        torch.cuda.synchronize()
+        assert torch.equal(xa.view(torch.int16), xb.view(torch.int16)), step
+        x = xa
+    assert lib.read_device_status(ws) == lib.OK
 
 
 def test_bounded_wait_times_out_cleanly(cuda_device):
