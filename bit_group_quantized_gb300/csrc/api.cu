@@ -77,6 +77,7 @@ struct LayerWs {
   float* fw;        // [16]
   float* tcs;  // split-K partial sums of the tensor-core kernels (batches that can use them)
   unsigned long long* ftag;  // batch-1 persistent kernel: tagged logits [E+1]
+  size_t zero_bytes;  // leading bytes that must be zero when a call starts (ctrl, ftag, tccnt)
   size_t bytes;
 };
 
@@ -88,6 +89,7 @@ LayerWs carve_layer(void* ws, int B, int d, int f, int E, int K) {
   // between calls like it (layer_zero_prefix_bytes covers both)
   L.ftag = c.take<unsigned long long>((size_t)(E + 1) * 8);
   L.tccnt = c.take<int>(tc_split_cnt_bytes(d, f, K));  // at a place that does not depend on B
+  L.zero_bytes = c.off;  // everything above is left at zero by the kernels; the rest is written before read
   L.logits = c.take<float>((size_t)B * (E + 1) * 4 + (size_t)B * K * 4);
   L.plan = c.take<Plan>(plan_bytes(B, K));
   L.idx = c.take<int32_t>((size_t)B * K * 4);
@@ -221,8 +223,29 @@ FusedLayer fused_layer(const bgq_moe_layer* L, const uint16_t* rho) {
 
 namespace bgq {
 // Bytes at the start of a layer workspace that must be zero before a call:
-// the control block and the persistent kernel's tagged logits.
-size_t layer_zero_prefix_bytes(int n_experts) { return sizeof(Ctrl) + up256((size_t)(n_experts + 1) * 8); }
+// the control block, the persistent kernel's tagged logits and the
+// tensor-core split-K counters. Their places depend on the layer's shape but
+// not on the batch.
+size_t layer_zero_prefix_bytes(const bgq_moe_layer* L) {
+  return carve_layer(nullptr, 1, L->d_model, L->d_ff, L->n_experts, L->top_k).zero_bytes;
+}
+
+// moe_layer_forward's argument checks that come before the workspace's, in
+// the same order, so that both layer entry points return the same status for
+// the same bad call before anything is enqueued.
+int layer_call_check(const bgq_moe_layer* L, const uint16_t* x, int batch, const void* out, const void* out_f32) {
+  int r = check_layer(L);
+  if (r) return r;
+  if (!x || !al(x, 16) || (!out && !out_f32)) return BGQ_ERR_INVALID_ARG;
+  if ((out && !al(out, 16)) || (out_f32 && !al(out_f32, 16))) return BGQ_ERR_INVALID_ARG;
+  if (batch < 1 || batch > kMaxBatch) return BGQ_ERR_INVALID_ARG;
+  return BGQ_OK;
+}
+// The last check (after the workspace's): every weight pointer is device
+// memory or pinned host memory mapped into the device address space.
+int layer_location_check(const bgq_moe_layer* L) {
+  return layer_where(L) == Where::kBad ? BGQ_ERR_INVALID_ARG : BGQ_OK;
+}
 }  // namespace bgq
 
 extern "C" {
@@ -382,11 +405,8 @@ static int32_t layer_forward_impl(const bgq_moe_layer* L, const uint16_t* x, int
 
 int32_t moe_layer_forward(const bgq_moe_layer* L, const uint16_t* x, int32_t batch, uint16_t* out, float* out_f32,
                           int32_t* idx_out, float* w_out, float* gamma_out, void* ws, size_t ws_bytes, void* stream) {
-  int r = check_layer(L);
+  int r = bgq::layer_call_check(L, x, batch, out, out_f32);
   if (r) return r;
-  if (!x || !al(x, 16) || (!out && !out_f32)) return BGQ_ERR_INVALID_ARG;
-  if ((out && !al(out, 16)) || (out_f32 && !al(out_f32, 16))) return BGQ_ERR_INVALID_ARG;
-  if (batch < 1 || batch > kMaxBatch) return BGQ_ERR_INVALID_ARG;
   if (!ws || !al(ws, 256) || ws_bytes < moe_layer_workspace_bytes(L, batch)) return BGQ_ERR_WORKSPACE;
   const Where where = layer_where(L);
   if (where == Where::kBad) return BGQ_ERR_INVALID_ARG;

@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+struct bgq_moe_layer;
+
 namespace bgq {
 
 struct QMat {
@@ -102,8 +104,15 @@ size_t qgemv_int16_smem(int cols, int bits, int T);
 cudaError_t launch_qgemv(const QMat& W, const uint16_t* x, int batch, uint16_t* y, float* yf, int variant,
                          cudaStream_t s);
 
-// Bytes at the start of a layer workspace that must be zero before a call (api.cu).
-size_t layer_zero_prefix_bytes(int n_experts);
+// Bytes at the start of a layer workspace that must be zero before a call:
+// control block, tagged logits and split-K counters (api.cu).
+size_t layer_zero_prefix_bytes(const bgq_moe_layer* L);
+// moe_layer_forward's argument checks, split around its workspace check
+// (api.cu): BGQ_OK or the status moe_layer_forward returns for the same
+// arguments. layer_call_check comes first, layer_location_check (weights in
+// device or mapped pinned host memory) after the workspace's.
+int layer_call_check(const bgq_moe_layer* L, const uint16_t* x, int batch, const void* out, const void* out_f32);
+int layer_location_check(const bgq_moe_layer* L);
 
 // 8-bit GEMV (gemv8.cu). gpr = (scale, bias) pairs per row: cols/64 or 1 (per
 // row). q8gemv_max_tokens: inputs staged per launch for `cols` (0: too wide).

@@ -13,7 +13,9 @@
 // GPU that loads the library holds one copy of it until the process exits.
 // Host code cannot use the array's name as a device address, so the first
 // call on each device looks the address up with cudaGetSymbolAddress (with
-// that device current) and keeps it for later calls on that device.
+// that device current) and keeps it for later calls on that device. The kept
+// address belongs to the device's current context: after cudaDeviceReset the
+// entry point must not be used again in the process.
 #include <mutex>
 
 #include "../../include/bgq.h"
@@ -49,18 +51,23 @@ extern "C" {
 
 int32_t moe_layer_forward_noalloc(const bgq_moe_layer* L, const uint16_t* x, int32_t batch, uint16_t* out,
                                   float* out_f32, int32_t* idx_out, float* w_out, float* gamma_out, void* stream) {
-  if (!L) return BGQ_ERR_INVALID_ARG;
-  const size_t need = moe_layer_workspace_bytes(L, batch);
-  if (need == 0) return BGQ_ERR_INVALID_ARG;
-  if (need > kStaticScratchBytes) return BGQ_ERR_WORKSPACE;  // this batch/shape needs more than the fixed array
-  void* ws = nullptr;
-  int32_t r = scratch_for_current_device(&ws);
+  // The same checks, in the same order, as moe_layer_forward (the fixed array
+  // standing in for the workspace), all before anything is enqueued.
+  int32_t r = bgq::layer_call_check(L, x, batch, out, out_f32);
   if (r != BGQ_OK) return r;
-  // The array keeps whatever the previous call left; only its first bytes (the
-  // control block: status word and counters, and the batch-1 kernel's tagged
-  // routing logits) have to start at zero (every other region is written
-  // before it is read).
-  if (cudaMemsetAsync(ws, 0, bgq::layer_zero_prefix_bytes(L->n_experts), reinterpret_cast<cudaStream_t>(stream)) !=
+  if (moe_layer_workspace_bytes(L, batch) > kStaticScratchBytes) return BGQ_ERR_WORKSPACE;
+  r = bgq::layer_location_check(L);
+  if (r != BGQ_OK) return r;
+  void* ws = nullptr;
+  r = scratch_for_current_device(&ws);
+  if (r != BGQ_OK) return r;
+  // The array keeps whatever the previous call (of any layer shape) left. The
+  // leading bytes that the kernels expect at zero (the control block with its
+  // status word and counters, the batch-1 kernel's tagged routing logits and
+  // the tensor-core split-K tile counters) are cleared on every call; every
+  // other region is written before it is read. A call that ended in
+  // BGQ_ERR_TIMEOUT therefore leaves nothing that the next call would read.
+  if (cudaMemsetAsync(ws, 0, bgq::layer_zero_prefix_bytes(L), reinterpret_cast<cudaStream_t>(stream)) !=
       cudaSuccess)
     return BGQ_ERR_CUDA;
   return moe_layer_forward(L, x, batch, out, out_f32, idx_out, w_out, gamma_out, ws, kStaticScratchBytes, stream);

@@ -230,14 +230,22 @@ int32_t moe_layer_forward(const bgq_moe_layer* L, const uint16_t* x, int32_t bat
  * library until the process exits), enough for batch <= 35 at d_model 4096,
  * d_ff 1024, 512 experts, top-4. A call whose moe_layer_workspace_bytes(L,
  * batch) exceeds 4 MiB returns BGQ_ERR_WORKSPACE and launches nothing.
+ * Every argument check of moe_layer_forward runs first, in the same order,
+ * with the same status codes; nothing is enqueued when one fails.
  * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call before
- * any stream capture. Each call clears the start of the array on `stream`
- * (the 256-byte control block and the batch-1 kernel's (n_experts + 1)
- * tagged logit words, rounded up to 256 bytes), then runs the layer. All calls on a device share the one array,
- * which keeps the last call's contents: calls that can overlap on the GPU (on
- * different streams, or from different host threads) race and must be
- * serialised by the caller. Allocates nothing. */
+ * (cudaGetSymbolAddress) with that device current and keeps it; make that
+ * first call before any stream capture, and do not call this entry point again
+ * after cudaDeviceReset in the same process. Each call clears, on `stream`,
+ * the leading bytes of the array that the kernels expect at zero (the
+ * 256-byte control block, the batch-1 kernel's (n_experts + 1) tagged logit
+ * words and the tensor-core split-K tile counters, each rounded up to 256
+ * bytes; their sizes depend on the layer's shape, not on the batch), then runs
+ * the layer. Every other region is written before it is read, so calls of
+ * different layer shapes may follow each other, and a call that ended in
+ * BGQ_ERR_TIMEOUT needs no clean-up before the next one. All calls on a device
+ * share the one array, which keeps the last call's contents: calls that can
+ * overlap on the GPU (on different streams, or from different host threads)
+ * race and must be serialised by the caller. Allocates nothing. */
 int32_t moe_layer_forward_noalloc(const bgq_moe_layer* L, const uint16_t* x, int32_t batch, uint16_t* out,
                                   float* out_f32, int32_t* idx_out, float* w_out, float* gamma_out, void* stream);
 

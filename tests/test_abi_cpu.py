@@ -189,3 +189,45 @@ def test_streamed_slot_bytes_and_validation(lib):
     assert call(None, slots) == lib.ERR_WORKSPACE
     assert call(FAKE, slots - 256) == lib.ERR_WORKSPACE
     assert call(FAKE + 16, slots) == lib.ERR_WORKSPACE
+
+
+def test_noalloc_rejects_what_the_workspace_entry_point_rejects(lib):
+    """moe_layer_forward_noalloc runs moe_layer_forward's argument checks, in
+    the same order, before it clears its scratch array: a bad call returns the
+    same status from both entry points and nothing is enqueued (no CUDA call
+    is reached on these paths, so this runs without a GPU)."""
+    L = lib.load()
+    Ls = layer_struct(lib)
+    big = 1 << 30
+
+    def both(layer, x=FAKE, batch=1, out=FAKE, out_f32=None):
+        a = L.moe_layer_forward(C.byref(layer) if layer is not None else None, x, batch, out, out_f32, None, None,
+                                None, FAKE, big, None)
+        b = L.moe_layer_forward_noalloc(C.byref(layer) if layer is not None else None, x, batch, out, out_f32, None,
+                                        None, None, None)
+        return a, b
+
+    cases = [
+        dict(layer=None),
+        dict(layer=Ls, x=None),
+        dict(layer=Ls, x=FAKE + 2),       # misaligned input
+        dict(layer=Ls, out=None),         # no output at all
+        dict(layer=Ls, out=FAKE + 8),     # misaligned output
+        dict(layer=Ls, out_f32=FAKE + 4),
+        dict(layer=Ls, batch=0),
+        dict(layer=Ls, batch=257),
+        dict(layer=layer_struct(lib, E=2000)),        # beyond the expert limit: unsupported, not "workspace"
+        dict(layer=layer_struct(lib, K=9)),
+        dict(layer=layer_struct(lib, group=32)),
+        dict(layer=layer_struct(lib, bits=3)),
+        dict(layer=layer_struct(lib, d=4000)),
+        dict(layer=layer_struct(lib, qs=100)),
+    ]
+    for c in cases:
+        a, b = both(**c)
+        assert a == b and a in (lib.ERR_INVALID_ARG, lib.ERR_UNSUPPORTED), (c, a, b)
+    assert both(layer_struct(lib, E=2000))[1] == lib.ERR_UNSUPPORTED
+    # a valid call too large for the 4 MiB array (batch 36 at the full shape)
+    assert L.moe_layer_workspace_bytes(C.byref(Ls), 36) > (4 << 20)
+    assert L.moe_layer_forward_noalloc(C.byref(Ls), FAKE, 36, FAKE, None, None, None, None, None) == \
+        lib.ERR_WORKSPACE

@@ -57,3 +57,26 @@ def test_noalloc_rejects_batches_beyond_the_fixed_scratch(cuda_device):
     with pytest.raises(lib.BGQError) as ei:
         lib.moe_layer_forward_noalloc(L, x, out=out)
     assert ei.value.status == lib.ERR_WORKSPACE
+
+
+def test_noalloc_alternating_shapes_reach_the_tensor_core_path(cuda_device):
+    """The fixed array is shared by calls of every layer shape. The regions
+    that must start at zero (control block, tagged logits, tensor-core split-K
+    counters) sit at shape-dependent places, so one shape's logits can land
+    where another shape keeps its counters. Alternate shapes, including a
+    batch-64 call whose shared expert runs on the tensor cores with split K,
+    and compare every call with moe_layer_forward on a fresh zeroed workspace."""
+    K = 4
+    full = layer(cuda_device, 512, 4096, 1024, K, seed=13)   # 4 MiB-class call, batch 35
+    tiny = layer(cuda_device, 8, 256, 128, K, seed=14)       # its logits overlap tc's counters
+    tc = layer(cuda_device, 16, 512, 256, K, seed=15)        # batch 64: the tensor-core path
+    seq = [(full, 4096, 35), (tiny, 256, 20), (tc, 512, 64), (tc, 512, 1), (full, 4096, 1), (tc, 512, 64),
+           (tiny, 256, 3), (tc, 512, 100)]
+    for i, (L, d, B) in enumerate(seq):
+        x = synth.activations(13, 200 + i, B, d, device=cuda_device)
+        ref = lib.moe_layer_forward(L, x, want_out=False, want_f32=True)[1]
+        out_f32 = torch.empty((B, d), dtype=torch.float32, device=cuda_device)
+        lib.moe_layer_forward_noalloc(L, x, out_f32=out_f32)
+        torch.cuda.synchronize()
+        # same kernels, same inputs: the same bits as a fresh workspace
+        assert torch.equal(out_f32, ref), (i, d, B, float((out_f32 - ref).abs().max()))
