@@ -426,6 +426,135 @@ def test_stack_with_zero_experts():
     assert np.array_equal(x1, O.f64_to_bf16_bits(x0d / np.sqrt(np.mean(x0d ** 2) + 1e-6)))
 
 
+# ------------------------------------- the stack's layer input, non-zero experts
+def torch_dense_layer(R, G, mats_of, shared, x, K, force=None):
+    """One layer from torch float64 library routines on the dequantised weights:
+    softmax, a stable descending sort for the top-K, SiLU, dense matmuls."""
+    xt = torch.as_tensor(x, dtype=torch.float64)
+    Rt = torch.from_numpy(O.bf16_to_f64(np.asarray(R.view(torch.int16) if torch.is_tensor(R) else R)))
+    logits = Rt @ xt
+    p = torch.softmax(logits, dim=0)
+    idx = torch.sort(logits, descending=True, stable=True).indices[:K] if force is None else \
+        torch.as_tensor(force, dtype=torch.int64)
+    w = p[idx] / p[idx].sum()
+    Gt = torch.from_numpy(O.bf16_to_f64(np.asarray(G.view(torch.int16) if torch.is_tensor(G) else G)))
+    gamma = torch.sigmoid(Gt @ xt)
+
+    def expert(m):
+        g, u, dn = (torch.from_numpy(O.dequant(mm[0], mm[1], 4)) for mm in m)
+        return dn @ (torch.nn.functional.silu(g @ xt) * (u @ xt))
+
+    out = torch.zeros(Rt.shape[1], dtype=torch.float64)
+    for k in range(K):
+        out += w[k] * expert(mats_of(int(idx[k])))
+    out += gamma * expert(shared)
+    return out, idx.numpy(), w.numpy()
+
+
+def torch_stack_token(layers, x0_bits, K, eps=1e-6):
+    """The decode step from torch routines: a = bf16(rms_norm(h) * rho) before
+    each layer, h += layer(a), next input bf16(rms_norm(h))."""
+    h = torch.from_numpy(O.bf16_to_f64(x0_bits))
+    idxs = []
+    for L in layers:
+        rho = torch.from_numpy(O.bf16_to_f64(L["rho"]))
+        a = torch.nn.functional.rms_norm(h, (h.shape[0],), weight=rho, eps=eps)
+        a = a.to(torch.bfloat16).to(torch.float64)
+        out, idx, _ = torch_dense_layer(L["router"], L["shared_gate"], L["get_expert"], L["shared"], a, K)
+        h = h + out
+        idxs.append(idx)
+    xn = torch.nn.functional.rms_norm(h, (h.shape[0],), eps=eps).to(torch.bfloat16)
+    return xn.view(torch.int16).numpy().astype(np.uint16), h.numpy(), idxs
+
+
+def nonzero_stack(seed, n_layers=3):
+    shape, mats, R, G = tiny_layer(seed)
+    layers = []
+    for l in range(n_layers):
+        Rl = synth.router(seed, l, shape.E, shape.d)
+        Rl = (Rl.float() * 16).to(torch.bfloat16).view(torch.int16).numpy().astype(np.uint16)
+        Gl = synth.shared_gate(seed, l, shape.d).view(torch.int16).numpy().astype(np.uint16)
+        q, sb = synth.expert_pool(seed, l, shape)
+        ml = [[(m[0].numpy(), m[1].view(torch.int16).numpy().astype(np.uint16))
+               for m in synth.expert_matrices(q[e], sb[e], shape)] for e in range(shape.E + 1)]
+        layers.append(dict(router=Rl, shared_gate=Gl,
+                           rho=synth.rho(seed, l, shape.d).view(torch.int16).numpy().astype(np.uint16),
+                           get_expert=(lambda ml: (lambda e: ml[e]))(ml), shared=ml[shape.E]))
+    x0 = synth.activations(seed, 0, 1, shape.d)[0].view(torch.int16).numpy().astype(np.uint16)
+    return layers, x0
+
+
+def check_stack_token_input(seed=34):
+    layers, x0 = nonzero_stack(seed)
+    xo, ho, io = O.stack_token(layers, x0, 4, 2)
+    xt, ht, it = torch_stack_token(layers, x0, 2)
+    assert np.abs(ho).max() > 0.1 and not np.array_equal(ho, O.bf16_to_f64(x0))  # the layers add something
+    assert [list(a) for a in io] == [list(b) for b in it]
+    assert np.allclose(ho, ht, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(xo, xt)
+
+
+def test_stack_token_layer_input():
+    """The stack feeds each layer bf16(rmsnorm(h) * rho), adds the layer's
+    unrounded output to h, and emits bf16(rmsnorm(h)): checked against torch's
+    rms_norm, bf16 cast, softmax, stable sort and SiLU on a 3-layer stack whose
+    experts are not zero (so every layer's input shows in its output)."""
+    check_stack_token_input()
+
+
+def test_planted_layer_fed_residual_is_caught(monkeypatch):
+    good = O.rmsnorm
+    monkeypatch.setattr(O, "rmsnorm", lambda h, rho, eps=1e-6: np.asarray(h, float) if rho is not None
+                        else good(h, rho, eps))
+    _raises(check_stack_token_input)
+
+
+def test_planted_dropped_rho_is_caught(monkeypatch):
+    good = O.rmsnorm
+    monkeypatch.setattr(O, "rmsnorm", lambda h, rho, eps=1e-6: good(h, None, eps))
+    _raises(check_stack_token_input)
+
+
+def test_planted_unrounded_layer_input_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "round_bf16", lambda v: np.asarray(v, dtype=np.float64))
+    _raises(check_stack_token_input)
+
+
+# ------------------------------------------------ the layer on a forced expert set
+def check_forced_set(seed=35):
+    shape, mats, R, G = tiny_layer(seed)
+    x = O.bf16_to_f64(synth.activations(seed, 1, 1, shape.d).view(torch.int16).numpy()[0])
+    Rn = R.view(torch.int16).numpy().astype(np.uint16)
+    Gn = G.view(torch.int16).numpy().astype(np.uint16)
+    natural = O.route(Rn, x, 2, Gn)[2]
+    for force in ([int(natural[1]), int(natural[0])],                    # the same set, other order
+                  [int(O.topk_stable(O.route(Rn, x, 2, Gn)[0], 4)[2]), int(natural[0])],  # 3rd-ranked in
+                  [7, 5]):                                               # any set
+        out, idx, w, gamma = O.moe_layer(Rn, Gn, lambda e: mats[e], mats[shape.E], 4, x, 2, force_idx=force)
+        ref, ridx, rw = torch_dense_layer(Rn, Gn, lambda e: mats[e], mats[shape.E], x, 2, force=force)
+        assert list(idx) == list(force) == list(ridx)
+        assert np.allclose(w, rw, rtol=1e-12) and abs(w.sum() - 1) < 1e-12
+        assert np.allclose(out, ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_layer_on_a_forced_expert_set():
+    """moe_layer(force_idx=S) weights expert S_k by softmax(l)[S_k] renormalised
+    over S alone (torch softmax over all logits, then divided by the sum over S),
+    in the order S gives, plus the gated shared expert."""
+    check_forced_set()
+
+
+def test_planted_forced_set_renormalised_over_natural_top_k_is_caught(monkeypatch):
+    good = O.route
+
+    def route(R, x, K, G=None):
+        logits, p, idx, w, gamma = good(R, x, K, G)
+        return logits, np.where(np.isin(np.arange(len(p)), idx), p, 0.0), idx, w, gamma
+
+    monkeypatch.setattr(O, "route", route)  # probabilities outside the natural top-K lost
+    _raises(check_forced_set)
+
+
 # ------------------------------------------------------- G. size figures
 def test_expert_size_matches_page():
     """[Flash-MoE page, "架构设计"]: each expert is about 6.75 MB at 4-bit.
