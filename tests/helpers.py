@@ -97,3 +97,44 @@ def assert_bf16_output(got_bf16, ref_f64, what="", own_tol=1e-3):
     tol = bf16_ulp(ref) + 1e-3 * np.abs(ref).max()
     bad = np.abs(got - ref) > tol
     assert not bad.any(), (what, np.flatnonzero(bad)[:10], got[bad][:5], ref[bad][:5])
+
+
+def oracle_stack_token(seed, bits, n_layers, x_bits, gpu_idx, d=4096, f=1024, E=512, K=4, eps=1e-6,
+                       torch_threads=2):
+    """One decode token of the synthetic stack (seed, layers 0..n_layers-1)
+    through the fp64 oracle, teacher-forced on the input bits x_bits.
+
+    Regenerates every weight it needs on the host from the seeded generator,
+    so it can run in a worker process with no GPU. Where a layer's K-th and
+    (K+1)-th oracle logits are within TIE_GAP, the layer is evaluated with the
+    GPU's expert set gpu_idx[l] (after checking that set is a valid top-K).
+    Returns (x_next bits, h, per-layer oracle top-K, per-layer gap, per-layer
+    'forced' flags)."""
+    torch.set_num_threads(torch_threads)
+    shape = synth.PoolShape(d, f, E, bits)
+    layers, gaps, nat, forced = [], [], [], []
+    h = O.bf16_to_f64(np.asarray(x_bits, dtype=np.uint16))
+    force = []
+    for l in range(n_layers):
+        R = bits16(synth.router(seed, l, E, d))
+        G = bits16(synth.shared_gate(seed, l, d))
+        rho = bits16(synth.rho(seed, l, d))
+        src = ExpertSource(seed, l, shape)
+        L = dict(router=R, shared_gate=G, rho=rho, get_expert=src, shared=src(E))
+        a = O.round_bf16(O.rmsnorm(h, rho, eps))
+        logits = O.route(R, a, K, G)[0]
+        gap = topk_gap(logits, K)
+        fi = None
+        if gap <= TIE_GAP:
+            check_topk_valid(gpu_idx[l], logits, K)
+            fi = np.asarray(gpu_idx[l], dtype=np.int64)
+        out, idx, _, _ = O.moe_layer(R, G, src, L["shared"], bits, a, K, force_idx=fi)
+        h = h + out
+        gaps.append(gap)
+        nat.append([int(i) for i in O.topk_stable(logits, K)])
+        forced.append(fi is not None)
+        force.append(fi)
+        L["shared"] = None  # keep the worker's memory small: one layer's experts at a time
+        src.cache.clear()
+    x_next = O.f64_to_bf16_bits(O.rmsnorm(h, None, eps))
+    return x_next, h, nat, gaps, forced

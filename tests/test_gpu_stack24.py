@@ -1,0 +1,86 @@
+"""The benchmarked configuration against the fp64 oracle: a decode stack of
+24 MoE layers at the full shape (d_model 4096, d_ff 1024, 512 routed experts
++ 1 shared, top-4), 4-bit and 2-bit, run as consecutive tokens on one
+workspace (each token's input is the previous token's GPU output).
+
+Every token is checked teacher-forced: the oracle takes the GPU's input bits
+for that token and runs all 24 layers itself. Per layer, the GPU's expert set
+must equal the oracle's top-4 wherever the 4th and 5th oracle logits differ
+by more than 1e-3 (elsewhere it must be a valid top-4 within 1e-3, and the
+oracle continues with the GPU's set); the final residual and the next input
+must be within the 2e-3 relative-L2 tolerance.
+
+The oracle runs in a pool of spawned worker processes (one token each) that
+regenerate the weights on the host from the seeded generator."""
+
+import concurrent.futures as cf
+import multiprocessing as mp
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from bit_group_quantized_gb300 import lib, synth
+from oracle import bgq_oracle as O
+from tests.helpers import REL_L2_TOL, TIE_GAP, assert_bf16_output, bits16, f64, oracle_stack_token, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+D, F, E, K, NL = 4096, 1024, 512, 4, 24
+
+
+def gpu_tokens(dev, seed, bits, n_tokens):
+    shape = synth.PoolShape(D, F, E, bits)
+    keep, layers, rhos = [], [], []
+    for l in range(NL):
+        t = synth.layer_tensors(seed, l, shape, device=dev)
+        keep.append(t)
+        layers.append(lib.MoELayer(D, F, E, K, bits, t["router"], t["shared_gate"], t["pool_q"][:E],
+                                   t["pool_sb"][:E], t["pool_q"][E], t["pool_sb"][E]))
+        rhos.append(synth.rho(seed, l, D, device=dev))
+    st = lib.Stack(layers, rhos)
+    ws = lib.workspace(st.ws_bytes, dev)
+    x = synth.activations(seed, 0, 1, D, device=dev)[0].clone()
+    rec = []
+    for _ in range(n_tokens):
+        xn = torch.empty_like(x)
+        h = torch.empty(D, dtype=torch.float32, device=dev)
+        idx = torch.empty((NL, K), dtype=torch.int32, device=dev)
+        lib.moe_stack_decode(st, x, 1e-6, ws=ws, x_next=xn, h_out=h, idx_out=idx)
+        torch.cuda.synchronize()
+        rec.append((bits16(x), bits16(xn), f64(h), idx.cpu().numpy()))
+        x = xn
+    assert lib.read_device_status(ws) == lib.OK
+    del keep, layers, st, ws
+    torch.cuda.empty_cache()
+    return rec
+
+
+@pytest.mark.parametrize("bits,n_tokens", [(4, 8), (2, 2)])
+def test_stack24_consecutive_tokens_match_oracle(cuda_device, bits, n_tokens):
+    seed = 21
+    rec = gpu_tokens(cuda_device, seed, bits, n_tokens)
+    workers = min(n_tokens, max(1, (os.cpu_count() or 2) // 2))
+    old = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS")}
+    os.environ.update(OMP_NUM_THREADS="2", OPENBLAS_NUM_THREADS="2")
+    try:
+        with cf.ProcessPoolExecutor(workers, mp_context=mp.get_context("spawn")) as ex:
+            futs = [ex.submit(oracle_stack_token, seed, bits, NL, xb, gi) for xb, _, _, gi in rec]
+            res = [f.result() for f in futs]
+    finally:
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    for t, ((xb, xn, h, gi), (ox, oh, nat, gaps, forced)) in enumerate(zip(rec, res)):
+        for l in range(NL):
+            if gaps[l] > TIE_GAP:
+                assert gi[l].tolist() == nat[l], (t, l, gi[l], nat[l], gaps[l])
+        assert rel_l2(h, oh) <= REL_L2_TOL, (t, rel_l2(h, oh))
+        assert_bf16_output(O.bf16_to_f64(xn), O.rmsnorm(oh, None), ("x_next", t), own_tol=REL_L2_TOL)
+        assert rel_l2(O.bf16_to_f64(xn), O.bf16_to_f64(ox)) <= REL_L2_TOL, t
+    # consecutive tokens really are a chain: each input is the previous output
+    for t in range(1, n_tokens):
+        assert np.array_equal(rec[t][0], rec[t - 1][1])
