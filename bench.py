@@ -60,29 +60,31 @@ def layer_algorithmic_bytes(bits: int) -> int:
 
 
 KERNEL_SOURCES = ("fused.cu", "common.cuh", "topk.cuh", "fused.h")  # what k_fused_decode is built from
+TRAFFIC_RECORD = os.path.join("profiles", "k_fused_decode_traffic.json")
 
 
-def profiled_traffic(n_layers: int):
-    """DRAM bytes of one k_fused_decode launch, from the committed 1-layer ncu
-    capture scaled by the number of layers (each layer reads the same bytes);
-    None if the kernel sources changed since the capture."""
+def kernel_sources_hash() -> str:
     import hashlib
 
-    prof = os.path.join(ROOT, "profiles", "k_fused_decode_stack1_full.md")
-    if not os.path.exists(prof):
-        return None
-    fields = {}
-    for line in open(prof, encoding="utf-8"):
-        if ":" in line and line.split(":", 1)[0] in ("traffic_bytes_per_layer", "kernel_sources_sha256_16"):
-            k, v = line.split(":", 1)
-            fields[k] = v.strip()
     csrc = os.path.join(ROOT, "bit_group_quantized_gb300", "csrc")
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
         h.update(open(os.path.join(csrc, f), "rb").read())
-    if fields.get("kernel_sources_sha256_16") != h.hexdigest()[:16] or "traffic_bytes_per_layer" not in fields:
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(n_layers: int, bits: int):
+    """DRAM bytes of one k_fused_decode launch: the committed record of a
+    1-layer ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) scaled
+    by the number of layers (each layer reads the same bytes); None if there is
+    no record for this width or the kernel sources changed since the capture."""
+    path = os.path.join(ROOT, TRAFFIC_RECORD)
+    if not os.path.exists(path):
         return None
-    return int(fields["traffic_bytes_per_layer"]) * n_layers
+    rec = json.load(open(path)).get(f"{bits}bit")
+    if not rec or rec.get("kernel_sources_sha256_16") != kernel_sources_hash():
+        return None
+    return int(rec["traffic_bytes_per_layer"]) * n_layers
 
 
 class ClockSampler:
@@ -183,36 +185,55 @@ def cpu_cores() -> int:
 
 
 def run_reference(args):
-    """The oracle as the reference arm: fp64 on the host cores, bounded sample per step."""
+    """The oracle as the reference arm: fp64 on the host cores. Each timed step
+    is a bounded sample of the workload: one of its layers for one token
+    (router, top-4, four routed experts, shared expert, RMSNorm, residual);
+    tokens/s is that layer time extrapolated to the whole stack."""
     rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
     if rank != 0:
         return 0
     bits = 2 if args.workload == "stack2" else 4
     n_layers = args.layers
-    per_step_layers = 1  # each step: one layer of the stack for one token (bounded sample)
     for _ in range(args.warmup):
-        oracle_sample(bits, per_step_layers)
-    times = [oracle_sample(bits, per_step_layers, seed=s + 1) for s in range(args.steps)]
+        oracle_sample(bits, 1)
+    times = [oracle_sample(bits, 1, seed=s + 1) for s in range(args.steps)]
     s_layer = statistics.mean(times)
     tok_s = 1.0 / (s_layer * n_layers)
     cores = cpu_cores()
     line = {
-        "impl": "reference", "metric": METRIC, "value": round(tok_s, 4), "unit": "tokens/s", "n_gpus": 1,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(s_layer * n_layers * 1000, 3),
+        "impl": "reference", "metric": METRIC, "value": round(tok_s, 4), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(s_layer * 1000, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workload_name(args), "us_per_layer": round(s_layer * 1e6, 1)},
+        "config": stack_config(args, bits, world),
+        "detail": {"step": "one layer of the stack for one token (the bounded sample that was timed)",
+                   "us_per_layer": round(s_layer * 1e6, 1),
+                   "extrapolated_ms_per_token": round(s_layer * n_layers * 1000, 3)},
         "cpu_baseline": {"value": round(tok_s, 4), "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": f"each step: 1 of {n_layers} layers for one token (router + 4 experts + shared),"
-                                   " scaled to the full stack"},
+                                   " extrapolated to the full stack"},
         "e2e": {"value": round(tok_s, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
 
 
-def workload_name(args) -> str:
+def stack_config(args, bits: int, world: int) -> dict:
+    """The workload of the decode-stack lines (identical in both arms)."""
+    from bit_group_quantized_gb300 import synth
+
+    shape = synth.PoolShape(D_MODEL, D_FF, N_EXPERTS, bits)
+    return {"workload": workload_name(args, bits), "layers": args.layers, "batch": 1,
+            "bytes_per_layer": layer_algorithmic_bytes(bits),
+            "l2": "inputs larger than L2 (the stack holds %.1f GB of weights)" % (
+                args.layers * shape.expert_bytes * (N_EXPERTS + 1) / 1e9),
+            "parallelism": f"replicas x{world}"}
+
+
+def workload_name(args, bits=None) -> str:
     if args.workload in ("stack4", "stack2"):
-        bits = 4 if args.workload == "stack4" else 2
+        if bits is None:
+            bits = 4 if args.workload == "stack4" else 2
         return (f"moe_decode_stack: {args.layers} layers x (512 routed + 1 shared SwiGLU experts, d_model 4096, "
                 f"d_ff 1024, top-4), {bits}-bit codes, group 64 bf16 scale+bias, batch 1")
     if args.workload == "layer":
@@ -253,11 +274,95 @@ def whole_job_tokens_per_s(world: int, ms_per_step: float) -> float:
 
 
 # ------------------------------------------------------------------ GPU arm
+class DecodeStack:
+    """A resident stack of synthetic layers, its workspace and a decode step
+    (one token through every layer) captured in a CUDA graph."""
+
+    def __init__(self, bits, n_layers, seed, dev, use_graph=True):
+        import torch
+
+        from bit_group_quantized_gb300 import lib, synth
+
+        self.lib, self.torch, self.dev, self.bits, self.n_layers = lib, torch, dev, bits, n_layers
+        shape = synth.PoolShape(D_MODEL, D_FF, N_EXPERTS, bits)
+        layers, rhos, self.keep = [], [], []
+        for l in range(n_layers):
+            t = synth.layer_tensors(seed, l, shape, device=dev)
+            self.keep.append(t)
+            layers.append(lib.MoELayer(D_MODEL, D_FF, N_EXPERTS, TOP_K, bits, t["router"], t["shared_gate"],
+                                       t["pool_q"][:N_EXPERTS], t["pool_sb"][:N_EXPERTS], t["pool_q"][N_EXPERTS],
+                                       t["pool_sb"][N_EXPERTS]))
+            rhos.append(synth.rho(seed, l, D_MODEL, device=dev))
+        self.rhos = rhos
+        self.stack = lib.Stack(layers, rhos)
+        self.ws = lib.workspace(self.stack.ws_bytes, dev)
+        self.x_in = synth.activations(seed, 0, 1, D_MODEL, device=dev)[0].clone()
+        self.x_out = torch.empty_like(self.x_in)
+        self.stream = torch.cuda.Stream(device=dev)
+        torch.cuda.synchronize()
+        self.graph = None
+        with torch.cuda.stream(self.stream):
+            for _ in range(3):
+                self.step()
+            self.stream.synchronize()
+            if use_graph:
+                self.graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(self.graph, stream=self.stream):
+                    self.step()
+        self.fused = lib.load().moe_stack_trace_entries(self.stack.c_layers, n_layers) > 0
+
+    def step(self):
+        self.lib.moe_stack_decode(self.stack, self.x_in, EPS, ws=self.ws, x_next=self.x_out, stream=self.stream)
+        self.x_in.copy_(self.x_out)
+
+    def run(self, n):
+        with self.torch.cuda.stream(self.stream):
+            for _ in range(n):
+                if self.graph is not None:
+                    self.graph.replay()
+                else:
+                    self.step()
+
+    def check_status(self, when):
+        self.stream.synchronize()
+        status = self.lib.read_device_status(self.ws, self.stream)
+        if status != self.lib.OK:
+            raise RuntimeError(f"device status {when}: {self.lib.status_string(status)}")
+
+    def timed(self, steps):
+        """ms per step over `steps` graph replays (CUDA events on the stream)."""
+        torch = self.torch
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(self.stream)
+        self.run(steps)
+        e1.record(self.stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    def free(self):
+        del self.graph, self.stack, self.keep, self.ws, self.rhos
+        self.torch.cuda.synchronize()
+        self.torch.cuda.empty_cache()
+
+
+def stack_roofline(bits, n_layers, ms, fused, traffic_n_layers=None):
+    peak, peak_kind = peaks()
+    achieved = n_layers * layer_algorithmic_bytes(bits) / (ms * 1e-3) / 1e9
+    return {"bound": "hbm",
+            "kernel": ("k_fused_decode (one launch per token, all %d layers)" % n_layers) if fused
+            else "moe_stack_decode step (multi-kernel path)",
+            "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "peak_kind": f"{peak_kind} copy bandwidth (burst)", "frac_of_8tbs": round(achieved / 8000.0, 4),
+            "traffic": profiled_traffic(n_layers, bits) if fused else None,
+            "traffic_source": "ncu dram__bytes_read+write of a 1-layer capture x layers (%s)" % TRAFFIC_RECORD}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
 
-    from bit_group_quantized_gb300 import lib, synth
+    from bit_group_quantized_gb300 import lib
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -270,49 +375,9 @@ def run_ours(args):
 
     bits = 2 if args.workload == "stack2" else 4
     n_layers = args.layers
-    shape = synth.PoolShape(D_MODEL, D_FF, N_EXPERTS, bits)
-    layers, rhos, keep = [], [], []
-    for l in range(n_layers):
-        t = synth.layer_tensors(args.seed + rank, l, shape, device=dev)
-        keep.append(t)
-        layers.append(lib.MoELayer(D_MODEL, D_FF, N_EXPERTS, TOP_K, bits, t["router"], t["shared_gate"],
-                                   t["pool_q"][:N_EXPERTS], t["pool_sb"][:N_EXPERTS], t["pool_q"][N_EXPERTS],
-                                   t["pool_sb"][N_EXPERTS]))
-        rhos.append(synth.rho(args.seed + rank, l, D_MODEL, device=dev))
-    stack = lib.Stack(layers, rhos)
-    ws = lib.workspace(stack.ws_bytes, dev)
-    x_in = synth.activations(args.seed + rank, 0, 1, D_MODEL, device=dev)[0].clone()
-    x_out = torch.empty_like(x_in)
-    stream = torch.cuda.Stream(device=dev)
-    torch.cuda.synchronize()
-
-    def step():
-        lib.moe_stack_decode(stack, x_in, EPS, ws=ws, x_next=x_out, stream=stream)
-        x_in.copy_(x_out)
-
-    graph = None
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            step()
-        stream.synchronize()
-        if not args.no_graph:
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph, stream=stream):
-                step()
-
-    def run(n):
-        with torch.cuda.stream(stream):
-            for _ in range(n):
-                if graph is not None:
-                    graph.replay()
-                else:
-                    step()
-
-    run(args.warmup)
-    stream.synchronize()
-    status = lib.read_device_status(ws, stream)
-    if status != lib.OK:
-        raise RuntimeError(f"device status after warm-up: {lib.status_string(status)}")
+    ds = DecodeStack(bits, n_layers, args.seed + rank, dev, use_graph=not args.no_graph)
+    ds.run(args.warmup)
+    ds.check_status("after warm-up")
 
     # ---- timed region (device time, CUDA events on the launching stream)
     if world > 1:
@@ -320,35 +385,53 @@ def run_ours(args):
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
     time.sleep(0.3)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    run(args.steps)
-    e1.record(stream)
-    e1.synchronize()
+    ms = ds.timed(args.steps)
     torch.cuda.synchronize()
     clock = clocks.stop()
     if world > 1:
         dist.barrier()
-    ms = slowest_rank(e0.elapsed_time(e1) / args.steps, world, dev)
+    ms = slowest_rank(ms, world, dev)
+    ds.check_status("after the timed steps")
 
     # ---- end to end through the public API with host buffers
     xh = torch.empty(D_MODEL, dtype=torch.bfloat16, pin_memory=True)
-    xh.copy_(x_in.cpu())
+    xh.copy_(ds.x_in.cpu())
     oh = torch.empty(D_MODEL, dtype=torch.bfloat16, pin_memory=True)
     e2e_steps = max(1, min(args.steps, 500))
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
+    with torch.cuda.stream(ds.stream):
         for _ in range(e2e_steps):
-            x_in.copy_(xh, non_blocking=True)
-            lib.moe_stack_decode(stack, x_in, EPS, ws=ws, x_next=x_out, stream=stream)
-            oh.copy_(x_out, non_blocking=True)
-            stream.synchronize()
+            ds.x_in.copy_(xh, non_blocking=True)
+            lib.moe_stack_decode(ds.stack, ds.x_in, EPS, ws=ds.ws, x_next=ds.x_out, stream=ds.stream)
+            oh.copy_(ds.x_out, non_blocking=True)
+            ds.stream.synchronize()
             xh.copy_(oh)
     e2e_s = slowest_rank((time.perf_counter() - t0) / e2e_steps, world, dev)
+    fused = ds.fused
+    ds.free()
+
+    # ---- the same stack at 2 bits (the workload's second width), same run
+    other = None
+    if args.workload == "stack4" and not args.no_stack2:
+        d2 = DecodeStack(2, n_layers, args.seed + rank, dev, use_graph=not args.no_graph)
+        d2.run(args.warmup)
+        d2.check_status("after the 2-bit warm-up")
+        if world > 1:
+            dist.barrier()
+        clocks2 = ClockSampler(local)
+        time.sleep(0.3)
+        ms2 = slowest_rank(d2.timed(args.steps), world, dev)
+        clock2 = clocks2.stop()
+        d2.check_status("after the 2-bit timed steps")
+        other = {"workload": workload_name(args, 2), "value": round(whole_job_tokens_per_s(world, ms2), 2),
+                 "unit": "tokens/s", "ms_per_step": round(ms2, 5), "us_per_layer": round(ms2 * 1000 / n_layers, 3),
+                 "steps": args.steps, "dtype": "u2 codes x s24 fixed-point x (dp4a), f32 accumulate",
+                 "roofline": stack_roofline(2, n_layers, ms2, d2.fused), "clocks": clock2,
+                 "gpu_launches": (1 if d2.fused else 1 + 6 * n_layers + 1) * args.steps}
+        d2.free()
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -356,44 +439,34 @@ def run_ours(args):
         s_layer = oracle_sample(bits, n_s, seed=args.seed)
         cpu = {"value": round(1.0 / (s_layer * n_layers), 5), "unit": "tokens/s", "cores": cpu_cores(),
                "kind": "oracle",
-               "sample": f"one token through {n_s} of the {n_layers} layers (fp64 numpy/BLAS), scaled to the stack"}
+               "sample": f"one token through {n_s} of the {n_layers} layers (fp64 numpy/BLAS), "
+                         "extrapolated to the stack"}
 
     if rank == 0:
-        peak, peak_kind = peaks()
         layer_bytes = layer_algorithmic_bytes(bits)
-        step_bytes = n_layers * layer_bytes
         us_layer = ms * 1000 / n_layers
-        achieved = step_bytes / (ms * 1e-3) / 1e9
         # the persistent kernel runs a whole token in one launch; the multi-kernel
         # fallback launches widen + 6 per layer + the final norm
-        fused = lib.load().moe_stack_trace_entries(stack.c_layers, n_layers) > 0
         launches = 1 if fused else 1 + 6 * n_layers + 1
         line = {
             "metric": METRIC, "value": round(whole_job_tokens_per_s(world, ms), 2), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "u4 codes x s16 fixed-point x (dp4a), f32 accumulate" if bits == 4
-            else "u2 codes x s16 fixed-point x (dp4a), f32 accumulate",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": f"u{bits} codes x s24 fixed-point x (dp4a), f32 accumulate",
             "data": "synthetic (seeded counter-based generator; no trained weights)",
-            "config": {"workload": workload_name(args), "us_per_layer": round(us_layer, 3),
-                       "gbs_per_layer": round(achieved, 1), "bytes_per_layer": layer_bytes,
-                       "l2": "inputs larger than L2 (the stack holds %.1f GB of weights)" % (
-                           n_layers * shape.expert_bytes * (N_EXPERTS + 1) / 1e9),
-                       "graph": graph is not None, "parallelism": f"replicas x{world}"},
-            "roofline": {"bound": "hbm",
-                         "kernel": ("k_fused_decode (one launch per token, all %d layers)" % n_layers) if fused
-                         else "moe_stack_decode step (multi-kernel path)",
-                         "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
-                         "frac_of_8tbs": round(achieved / 8000.0, 4),
-                         "traffic": profiled_traffic(n_layers) if (fused and bits == 4) else None,
-                         "traffic_source": "ncu dram__bytes_read+write of a 1-layer capture "
-                                           "(profiles/k_fused_decode_stack1_full.md) x layers"},
+            "config": stack_config(args, bits, world),
+            "detail": {"us_per_layer": round(us_layer, 3),
+                       "gbs_per_layer": round(layer_bytes / (us_layer * 1e-6) / 1e9, 1),
+                       "graph": not args.no_graph},
+            "roofline": stack_roofline(bits, n_layers, ms, fused),
             "e2e": {"value": round(world / e2e_s, 2), "unit": "tokens/s", "h2d_bytes_per_step": D_MODEL * 2,
                     "d2h_bytes_per_step": D_MODEL * 2},
             "gpu_launches": launches * args.steps,
             "clocks": clock,
             "cpu_baseline": cpu,
         }
+        if other is not None:
+            line["stack2"] = other
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -609,7 +682,7 @@ def run_expert(args):
     print(json.dumps({
         "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": 1, "steps": n_rep * R,
         "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "u4 codes x s16 fixed-point x (dp4a), f32 accumulate", "data": "synthetic",
+        "vs_baseline": None, "dtype": "u4 codes x s24 fixed-point x (dp4a), f32 accumulate", "data": "synthetic",
         "config": {"workload": workload_name(args), "us_per_expert": round(ms * 1000, 3), "bytes": nbytes,
                    "tokens_per_s": round(B / (ms * 1e-3), 1),
                    "l2": f"ring of {R} experts ({R * shape.expert_bytes / 1e6:.0f} MB) cycled, larger than L2"},
@@ -654,7 +727,7 @@ def run_gemv8(args):
     print(json.dumps({
         "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": 1, "steps": n_rep * R,
         "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "u8 codes x s16 fixed-point x (dp4a), f32 accumulate", "data": "synthetic",
+        "vs_baseline": None, "dtype": "u8 codes x s24 fixed-point x (dp4a), f32 accumulate", "data": "synthetic",
         "config": {"workload": workload_name(args), "us_per_gemv": round(ms * 1000, 3), "bytes": nbytes,
                    "l2": f"ring of {R} matrices ({R * mat_bytes / 1e6:.0f} MB) cycled, larger than L2"},
         "roofline": {"bound": "hbm", "kernel": "k_q8gemv", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
@@ -682,6 +755,7 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-stack2", action="store_true", help="stack4: skip the 2-bit stack measured after it")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

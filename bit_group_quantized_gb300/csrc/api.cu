@@ -262,7 +262,7 @@ const char* bgq_status_string(int32_t s) {
   }
 }
 
-int32_t bgq_abi_version(void) { return 100; }
+int32_t bgq_abi_version(void) { return 101; }
 
 static int32_t gemv_common(const bgq_qmatrix* W, const uint16_t* x, uint16_t* y, int32_t batch, int32_t variant,
                            int want_bits, void* stream) {
@@ -271,16 +271,16 @@ static int32_t gemv_common(const bgq_qmatrix* W, const uint16_t* x, uint16_t* y,
   if (want_bits && W->bits != want_bits) return BGQ_ERR_INVALID_ARG;
   if (!x || !y || !al(x, 16) || !al(y, 16)) return BGQ_ERR_INVALID_ARG;
   if (batch < 1 || batch > 64) return BGQ_ERR_INVALID_ARG;
-  if (variant < BGQ_DQ_INT16 || variant > BGQ_DQ_HOISTED) return BGQ_ERR_INVALID_ARG;
+  if (variant < BGQ_DQ_INT || variant > BGQ_DQ_HOISTED) return BGQ_ERR_INVALID_ARG;
   return cuda_status(launch_qgemv(qm(W), x, batch, y, nullptr, variant, st(stream)));
 }
 
 int32_t q4_gemv(const bgq_qmatrix* W, const uint16_t* x, uint16_t* y, int32_t batch, void* stream) {
-  return gemv_common(W, x, y, batch, BGQ_DQ_INT16, 4, stream);
+  return gemv_common(W, x, y, batch, BGQ_DQ_INT, 4, stream);
 }
 
 int32_t q2_gemv(const bgq_qmatrix* W, const uint16_t* x, uint16_t* y, int32_t batch, void* stream) {
-  return gemv_common(W, x, y, batch, BGQ_DQ_INT16, 2, stream);
+  return gemv_common(W, x, y, batch, BGQ_DQ_INT, 2, stream);
 }
 
 int32_t bgq_qgemv_variant(const bgq_qmatrix* W, const uint16_t* x, uint16_t* y, int32_t batch, int32_t variant,

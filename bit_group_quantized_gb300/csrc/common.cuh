@@ -68,7 +68,7 @@ template <int BITS>
 struct Geo {
   static constexpr int kPer = 32 / BITS;         // codes per word
   static constexpr int kNvec = kPer / 4;         // byte vectors per word (4 codes each)
-  static constexpr int kNch = kNvec / 2;         // 16-byte x chunks per word (lo+hi of 2 vectors)
+  static constexpr int kNch = kNvec / 2;         // staged x chunks per word (2 byte vectors each)
   static constexpr int kValsPerPart = 128 / BITS;
   static constexpr uint32_t kByteMask = BITS == 4 ? 0x0f0f0f0fu : 0x03030303u;
 };
@@ -98,28 +98,41 @@ __host__ __device__ inline bool cols_supported(int cols, int bits) {
 // ---------------------------------------------------------------------------
 // x staging for the integer (dp4a) dot product.
 //
-// Per group of 64 inputs: sh = 14 - floor(log2(max|x|)), X_k = rint(x_k * 2^sh),
-// so |X_k| < 2^15 and every input within 2^7 of the group maximum is exact.
-// X is split into an unsigned low byte and a signed high byte: X = 256*hi + lo.
+// Per group of 64 inputs: sh = 22 - floor(log2(max|x|)), X_k = rn(x_k * 2^sh),
+// so |X_k| < 2^23: 24-bit fixed point with one power-of-two exponent per
+// group. Every bf16 input within 2^15 of its group's maximum is exact, and
+// an fp32 input keeps 23 bits below the group maximum (an fp32 dot product's
+// own rounding is 2^-24 of its terms). X is split into three bytes,
+// X = 65536*H + 256*M + L (L, M unsigned, H signed), and each code byte
+// vector meets them in three dp4a: 0.75 dp4a per weight and token.
 // For code word w and byte vector j (codes k = w*per + j + nvec*i, i = 0..3)
-// we store (lo bytes, hi bytes) as two uint32; chunk ch of word w holds vectors
-// 2ch, 2ch+1 as {lo0, hi0, lo1, hi1}.
-// Chunk (t, part p, word c, chunk ch) lives at 16-byte slot
+// the L, M and H bytes of those four inputs form three uint32. Chunk ch of
+// word w holds vectors 2ch, 2ch+1: {L0, M0, L1, M1} in the 16-byte array
+// `chunks` and {H0, H1} in the 8-byte array `hib`, both at slot
 //   (((t*NIT + p/LPR)*4 + c)*NCH + ch)*LPR + p%LPR
-// so that for fixed (t, iteration, c, ch) the lanes of a row read consecutive
-// slots (no bank conflicts). Part info (2^-sh, 2^-sh * sum_k X_k) is a float2
-// at [t*P + p].
+// (part p, word c of the part), so that for fixed (t, iteration, c, ch) the
+// lanes of a row read consecutive slots (no bank conflicts). Part info
+// (2^-sh, 2^-sh * sum_k X_k) is a float2 at [t*P + p].
 // ---------------------------------------------------------------------------
-template <int BITS>
-__host__ __device__ constexpr int xstage_bytes_per_token(int cols) {
-  // codes*2 bytes of X (lo+hi) + 8 bytes of part info per part
-  return cols * 2 + (cols * BITS / 128) * 8;
-}
-
 struct XStage {
-  uint4* chunks;    // [T * P * 4 * NCH] 16-byte slots
+  uint4* chunks;    // [T * P * 4 * NCH] 16-byte slots (L, M bytes)
+  uint2* hib;       // [T * P * 4 * NCH] 8-byte slots (H bytes)
   float2* partinfo; // [T * P]
 };
+
+// Bytes of T staged inputs of `cols` values: 3 bytes per value, 8 per part.
+__host__ __device__ inline size_t xstage_bytes(int T, int cols, int bits) {
+  return (size_t)T * cols * 3 + (size_t)T * (cols * bits / 128) * 8;
+}
+// The staging arrays of T inputs of `cols` values, carved from `base` (16-byte aligned).
+__host__ __device__ inline XStage xstage_carve(void* base, int T, int cols) {
+  XStage s;
+  unsigned char* b = static_cast<unsigned char*>(base);
+  s.chunks = reinterpret_cast<uint4*>(b);
+  s.hib = reinterpret_cast<uint2*>(b + (size_t)T * cols * 2);
+  s.partinfo = reinterpret_cast<float2*>(b + (size_t)T * cols * 3);
+  return s;
+}
 
 // Input element loaders.
 __device__ __forceinline__ float load_in(const uint16_t* x, int i) { return bf16f(x[i]); }
@@ -151,12 +164,48 @@ struct GatherSrc {  // token t at base + off[t] (off in shared memory)
   __device__ void load8(int t, int k0, float* v) const { load8_from(base + off[t] + k0, v); }
 };
 
-// Pack the low bytes and the second bytes of four int16-range values.
-__device__ __forceinline__ void pack_lohi(int x0, int x1, int x2, int x3, uint32_t& lo, uint32_t& hi) {
+// The shift sh = 22 - floor(log2 m) of a group whose largest magnitude is m
+// (0 for an all-zero group), kept within [-126, 126] so that 2^sh and 2^-sh
+// are normal floats.
+__device__ __forceinline__ int x24_shift(float m) {
+  if (!(m > 0.f)) return 0;
+  const int e = (int)((__float_as_uint(m) >> 23) & 0xff) - 127;  // floor(log2 m) for normal m
+  const int sh = 22 - e;
+  return sh > 126 ? 126 : (sh < -126 ? -126 : sh);
+}
+// rn(v * 2^sh) for |v * 2^sh| < 2^23 (the product is exact). Rounding can
+// only reach +2^23 (a value within half a unit below it); it is kept at
+// 2^23 - 1. -2^23 is representable as (H, M, L) = (-128, 0, 0).
+__device__ __forceinline__ int x24_fix(float v, float sc) { return min(__float2int_rn(v * sc), 8388607); }
+
+// The L, M and H bytes of four 24-bit values (byte i from x_i).
+__device__ __forceinline__ void pack24(int x0, int x1, int x2, int x3, uint32_t& L, uint32_t& M, uint32_t& H) {
   const uint32_t t01 = __byte_perm((uint32_t)x0, (uint32_t)x1, 0x5140);  // x0.b0 x1.b0 x0.b1 x1.b1
   const uint32_t t23 = __byte_perm((uint32_t)x2, (uint32_t)x3, 0x5140);
-  lo = __byte_perm(t01, t23, 0x5410);
-  hi = __byte_perm(t01, t23, 0x7632);
+  L = __byte_perm(t01, t23, 0x5410);
+  M = __byte_perm(t01, t23, 0x7632);
+  const uint32_t u01 = __byte_perm((uint32_t)x0, (uint32_t)x1, 0x0062);  // x0.b2 x1.b2
+  const uint32_t u23 = __byte_perm((uint32_t)x2, (uint32_t)x3, 0x0062);
+  H = __byte_perm(u01, u23, 0x5410);
+}
+
+// Store the staged bytes of code word w (part p = w/4, word c = w%4) of token t.
+template <int BITS>
+__device__ __forceinline__ void store_word24(const int (&X)[Geo<BITS>::kPer], int t, int w, const RowGeo& rg,
+                                             int lpr_shift, const XStage& st) {
+  using G = Geo<BITS>;
+  uint32_t L[G::kNvec], M[G::kNvec], H[G::kNvec];
+#pragma unroll
+  for (int j = 0; j < G::kNvec; ++j)
+    pack24(X[j], X[j + G::kNvec], X[j + 2 * G::kNvec], X[j + 3 * G::kNvec], L[j], M[j], H[j]);
+  const int p = w >> 2, c = w & 3;
+  const int it = p >> lpr_shift, lp = p & (rg.LPR - 1);
+  const int slot = ((((t * rg.NIT + it) * 4 + c) * G::kNch) << lpr_shift) + lp;
+#pragma unroll
+  for (int ch = 0; ch < G::kNch; ++ch) {
+    st.chunks[slot + (ch << lpr_shift)] = make_uint4(L[2 * ch], M[2 * ch], L[2 * ch + 1], M[2 * ch + 1]);
+    st.hib[slot + (ch << lpr_shift)] = make_uint2(H[2 * ch], H[2 * ch + 1]);
+  }
 }
 
 // Stage code word w of token t from its kPer input values v (inactive
@@ -174,54 +223,32 @@ __device__ __forceinline__ void stage_word(const float (&v)[Geo<BITS>::kPer], bo
   for (int i = 0; i < G::kPer; ++i) m = fmaxf(m, fabsf(v[i]));
 #pragma unroll
   for (int o = kGW / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-  int sh = 0;
-  if (m > 0.f) {
-    const int e = (int)((__float_as_uint(m) >> 23) & 0xff) - 127;  // floor(log2 m) for normal m
-    sh = 14 - e;
-    sh = sh > 126 ? 126 : (sh < -126 ? -126 : sh);
-  }
+  const int sh = x24_shift(m);
   const float sc = exp2i(sh);
   int X[G::kPer];
   int xsum = 0;
 #pragma unroll
   for (int i = 0; i < G::kPer; ++i) {
-    // rint(v*2^sh) by the 1.5*2^23 addition (|v*2^sh| < 2^15, product
-    // exact). Only +2^15 can come out (an fp32 input within an ulp below a
-    // power of two rounds up); -2^15 is representable as (hi, lo) = (-128, 0).
-    const int q = __float_as_int(fmaf(v[i], sc, 12582912.f)) - 0x4B400000;
-    X[i] = min(q, 32767);
+    X[i] = x24_fix(v[i], sc);
     xsum += X[i];
   }
-  uint32_t lo[G::kNvec], hi[G::kNvec];
-#pragma unroll
-  for (int j = 0; j < G::kNvec; ++j)
-    pack_lohi(X[j], X[j + G::kNvec], X[j + 2 * G::kNvec], X[j + 3 * G::kNvec], lo[j], hi[j]);
-  const int p = w >> 2, c = w & 3;
-  const int it = p >> lpr_shift, lp = p & (rg.LPR - 1);
-  if (active) {
-    uint4* dst = st.chunks + ((((t * rg.NIT + it) * 4 + c) * G::kNch) << lpr_shift) + lp;
-#pragma unroll
-    for (int ch = 0; ch < G::kNch; ++ch)
-      dst[ch << lpr_shift] = make_uint4(lo[2 * ch], hi[2 * ch], lo[2 * ch + 1], hi[2 * ch + 1]);
-  }
+  if (active) store_word24<BITS>(X, t, w, rg, lpr_shift, st);
   // part sum over the 4 words of part p (4 consecutive lanes)
   xsum += __shfl_xor_sync(kFull, xsum, 1);
   xsum += __shfl_xor_sync(kFull, xsum, 2);
-  if (active && c == 0) {
+  if (active && (w & 3) == 0) {
     const float inv = exp2i(-sh);
-    st.partinfo[t * rg.P + p] = make_float2(inv, (float)xsum * inv);
+    st.partinfo[t * rg.P + (w >> 2)] = make_float2(inv, (float)xsum * inv);
   }
 }
 
 // Stage T inputs of `cols` values into shared memory, one thread per code
 // word: the 64/kPer consecutive threads of a group find the group maximum with
 // shuffles, so a single pass with no block barrier inside does the job.
-// `gsh` is unused (kept for the call sites' shared-memory layout). All threads
-// of the block must call; ends with __syncthreads().
+// All threads of the block must call; ends with __syncthreads().
 template <int BITS, typename Src>
-__device__ void stage_x_int16(const Src src, int T, int cols, XStage st, int* gsh) {
+__device__ void stage_x24(const Src src, int T, int cols, XStage st) {
   using G = Geo<BITS>;
-  (void)gsh;
   const RowGeo rg = row_geo(cols, BITS);
   const int lpr_shift = __ffs(rg.LPR) - 1;
   const int words = cols * BITS / 32;
@@ -254,16 +281,16 @@ __device__ void stage_x_int16(const Src src, int T, int cols, XStage st, int* gs
 // threads, so T * words <= 2 * blockDim.x takes a single pass. A group's words
 // sit on kGW/2 consecutive lanes and a part's 4 words on 2, so the group
 // maximum, the shifts and the part sums, hence every staged byte, equal
-// stage_x_int16's. All threads of the block must call; ends with __syncthreads().
+// stage_x24's. All threads of the block must call; ends with __syncthreads().
 template <int BITS, typename Src>
-__device__ __forceinline__ void stage_x_int16_pairs(const Src src, int T, int cols, XStage st) {
+__device__ __forceinline__ void stage_x24_pairs(const Src src, int T, int cols, XStage st) {
   using G = Geo<BITS>;
   constexpr int kGL = kGroup / G::kPer / 2;  // lanes per group
   const RowGeo rg = row_geo(cols, BITS);
   const int lpr_shift = __ffs(rg.LPR) - 1;
   const int hw = cols * BITS / 64;  // word pairs per input (cols is a multiple of 64)
   const int total = T * hw;
-  const float inv_hw = 1.f / (float)hw;  // exact floor below, as in stage_x_int16
+  const float inv_hw = 1.f / (float)hw;  // exact floor below, as in stage_x24
   for (int base = 0; base < total; base += blockDim.x) {
     const int i = base + threadIdx.x;
     const bool active = i < total;
@@ -284,111 +311,105 @@ __device__ __forceinline__ void stage_x_int16_pairs(const Src src, int T, int co
     for (int k = 0; k < 2 * G::kPer; ++k) m = fmaxf(m, fabsf(v[k]));
 #pragma unroll
     for (int o = kGL / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-    int sh = 0;
-    if (m > 0.f) {
-      const int e = (int)((__float_as_uint(m) >> 23) & 0xff) - 127;
-      sh = 14 - e;
-      sh = sh > 126 ? 126 : (sh < -126 ? -126 : sh);
-    }
+    const int sh = x24_shift(m);
     const float sc = exp2i(sh);
     int xsum = 0;
-    const int p = w0 >> 2;
-    const int it = p >> lpr_shift, lp = p & (rg.LPR - 1);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       int X[G::kPer];
 #pragma unroll
       for (int k = 0; k < G::kPer; ++k) {
-        const int q = __float_as_int(fmaf(v[h * G::kPer + k], sc, 12582912.f)) - 0x4B400000;
-        X[k] = min(q, 32767);
+        X[k] = x24_fix(v[h * G::kPer + k], sc);
         xsum += X[k];
       }
-      uint32_t lo[G::kNvec], hi[G::kNvec];
-#pragma unroll
-      for (int j = 0; j < G::kNvec; ++j)
-        pack_lohi(X[j], X[j + G::kNvec], X[j + 2 * G::kNvec], X[j + 3 * G::kNvec], lo[j], hi[j]);
-      if (active) {
-        const int c = (w0 + h) & 3;
-        uint4* dst = st.chunks + ((((t * rg.NIT + it) * 4 + c) * G::kNch) << lpr_shift) + lp;
-#pragma unroll
-        for (int ch = 0; ch < G::kNch; ++ch)
-          dst[ch << lpr_shift] = make_uint4(lo[2 * ch], hi[2 * ch], lo[2 * ch + 1], hi[2 * ch + 1]);
-      }
+      if (active) store_word24<BITS>(X, t, w0 + h, rg, lpr_shift, st);
     }
     xsum += __shfl_xor_sync(kFull, xsum, 1);  // the part's other word pair
     if (active && (w0 & 3) == 0) {
       const float inv = exp2i(-sh);
-      st.partinfo[t * rg.P + p] = make_float2(inv, (float)xsum * inv);
+      st.partinfo[t * rg.P + (w0 >> 2)] = make_float2(inv, (float)xsum * inv);
     }
   }
   __syncthreads();
 }
 
-// Integer dot product of one part (4 code words) with its staged input chunks
-// xc[c*NCH + ch] and part info pi. Returns s*2^-sh*sum(q*X) + b*2^-sh*sum(X)
-// added to acc.
+// Integer dot product of one part (4 code words) with its staged input bytes
+// (xc[c*NCH + ch]: L and M bytes, xh[...]: H bytes) and part info pi. Returns
+// s*2^-sh*sum(q*X) + b*2^-sh*sum(X) added to acc.
 template <int BITS>
 __device__ __forceinline__ float part_dot_x(const uint4 qv, uint32_t sbw, const uint4 (&xc)[4 * Geo<BITS>::kNch],
-                                            const float2 pi, float acc) {
+                                            const uint2 (&xh)[4 * Geo<BITS>::kNch], const float2 pi, float acc) {
   using G = Geo<BITS>;
   const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
-  int A;
+  int lo, hi;
   if (BITS == 4) {
     // odd codes stay in the high nibbles (16x their value) and get their own
     // accumulators, divided by 16 at the end (exact: every term is a multiple
     // of 16); saves the shift per word.
+    uint32_t l0 = 0, l1 = 0, m0 = 0, m1 = 0;
     int h0 = 0, h1 = 0;
-    uint32_t l0 = 0, l1 = 0;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const uint4 x = xc[c];
+      const uint2 xhh = xh[c];
       const uint32_t v0 = qw[c] & 0x0f0f0f0fu, v1 = qw[c] & 0xf0f0f0f0u;
       l0 = dp4a_uu(v0, x.x, l0);
-      h0 = dp4a_us(v0, x.y, h0);
+      m0 = dp4a_uu(v0, x.y, m0);
+      h0 = dp4a_us(v0, xhh.x, h0);
       l1 = dp4a_uu(v1, x.z, l1);
-      h1 = dp4a_us(v1, x.w, h1);
+      m1 = dp4a_uu(v1, x.w, m1);
+      h1 = dp4a_us(v1, xhh.y, h1);
     }
-    A = (h0 + (h1 >> 4)) * 256 + (int)(l0 + (l1 >> 4));
+    lo = (int)(l0 + (l1 >> 4)) + (int)(m0 + (m1 >> 4)) * 256;  // < 2^25
+    hi = h0 + (h1 >> 4);
   } else {
-    int acc_h = 0;
-    uint32_t acc_l = 0;
+    uint32_t l = 0, m = 0;
+    int h = 0;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
 #pragma unroll
       for (int ch = 0; ch < G::kNch; ++ch) {
         const uint4 x = xc[c * G::kNch + ch];
-        uint32_t v0 = (qw[c] >> (BITS * (2 * ch))) & G::kByteMask;
-        uint32_t v1 = (qw[c] >> (BITS * (2 * ch + 1))) & G::kByteMask;
-        acc_l = dp4a_uu(v0, x.x, acc_l);
-        acc_h = dp4a_us(v0, x.y, acc_h);
-        acc_l = dp4a_uu(v1, x.z, acc_l);
-        acc_h = dp4a_us(v1, x.w, acc_h);
+        const uint2 xhh = xh[c * G::kNch + ch];
+        const uint32_t v0 = (qw[c] >> (BITS * (2 * ch))) & G::kByteMask;
+        const uint32_t v1 = (qw[c] >> (BITS * (2 * ch + 1))) & G::kByteMask;
+        l = dp4a_uu(v0, x.x, l);
+        m = dp4a_uu(v0, x.y, m);
+        h = dp4a_us(v0, xhh.x, h);
+        l = dp4a_uu(v1, x.z, l);
+        m = dp4a_uu(v1, x.w, m);
+        h = dp4a_us(v1, xhh.y, h);
       }
     }
-    A = acc_h * 256 + (int)acc_l;
+    lo = (int)l + (int)m * 256;
+    hi = h;
   }
-  float s = bf16lo(sbw), b = bf16hi(sbw);
-  return fmaf(s * pi.x, (float)A, fmaf(b, pi.y, acc));
+  const float A = fmaf((float)hi, 65536.f, (float)lo);
+  const float s = bf16lo(sbw), b = bf16hi(sbw);
+  return fmaf(s * pi.x, A, fmaf(b, pi.y, acc));
 }
 
-// The staged input chunks of part p = it*LPR + lp of token t.
+// The staged input bytes of part p = it*LPR + lp of token t.
 template <int BITS>
-__device__ __forceinline__ void load_part_x(const uint4* __restrict__ chunks, int t, int it, int lp, const RowGeo& rg,
-                                            uint4 (&xc)[4 * Geo<BITS>::kNch]) {
-  const uint4* xb = chunks + ((t * rg.NIT + it) * 4 * Geo<BITS>::kNch) * rg.LPR + lp;
+__device__ __forceinline__ void load_part_x(const XStage& st, int t, int it, int lp, const RowGeo& rg,
+                                            uint4 (&xc)[4 * Geo<BITS>::kNch], uint2 (&xh)[4 * Geo<BITS>::kNch]) {
+  const int base = ((t * rg.NIT + it) * 4 * Geo<BITS>::kNch) * rg.LPR + lp;
 #pragma unroll
-  for (int i = 0; i < 4 * Geo<BITS>::kNch; ++i) xc[i] = xb[i * rg.LPR];
+  for (int i = 0; i < 4 * Geo<BITS>::kNch; ++i) {
+    xc[i] = st.chunks[base + i * rg.LPR];
+    xh[i] = st.hib[base + i * rg.LPR];
+  }
 }
 
 // Integer dot product of one part (4 code words) with staged token t.
 // The part is p = it*LPR + lp (iteration it of lane lp of the row).
 template <int BITS>
-__device__ __forceinline__ float part_dot_int16(const uint4 qv, uint32_t sbw, const uint4* __restrict__ chunks,
-                                                const float2* __restrict__ partinfo, int t, int it, int lp,
-                                                const RowGeo& rg, float acc) {
+__device__ __forceinline__ float part_dot24(const uint4 qv, uint32_t sbw, const XStage& st, int t, int it, int lp,
+                                            const RowGeo& rg, float acc) {
   uint4 xc[4 * Geo<BITS>::kNch];
-  load_part_x<BITS>(chunks, t, it, lp, rg, xc);
-  return part_dot_x<BITS>(qv, sbw, xc, partinfo[t * rg.P + it * rg.LPR + lp], acc);
+  uint2 xh[4 * Geo<BITS>::kNch];
+  load_part_x<BITS>(st, t, it, lp, rg, xc, xh);
+  return part_dot_x<BITS>(qv, sbw, xc, xh, st.partinfo[t * rg.P + it * rg.LPR + lp], acc);
 }
 
 // Group index of part p.

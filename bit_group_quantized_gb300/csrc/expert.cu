@@ -62,7 +62,7 @@ __device__ __forceinline__ void dot_round(const uint4 (&qv)[kMaxNitE], const uin
     if (it < rg.NIT) {
 #pragma unroll
       for (int t = 0; t < kTaskTok; ++t)
-        if (t < ntok) acc[t] = part_dot_int16<BITS>(qv[i], sv[i], st.chunks, st.partinfo, t, it, lp, rg, acc[t]);
+        if (t < ntok) acc[t] = part_dot24<BITS>(qv[i], sv[i], st, t, it, lp, rg, acc[t]);
     }
   }
 }
@@ -92,10 +92,7 @@ k_gateup(ExpertSet es, const Plan* __restrict__ plan, const uint16_t* __restrict
   const int nrb = (f + rows_item - 1) / rows_item;
   const int total = plan->ntasks * nrb;
   const ItemRange ir = my_items(total);
-  XStage st;
-  st.chunks = reinterpret_cast<uint4*>(smem);
-  st.partinfo = reinterpret_cast<float2*>(smem + (size_t)kTaskTok * d * 2);
-  int* gsh = reinterpret_cast<int*>(smem + (size_t)kTaskTok * d * 2 + (size_t)kTaskTok * rg.P * 8);
+  const XStage st = xstage_carve(smem, kTaskTok, d);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int rs = lane / rg.LPR, lp = lane - rs * rg.LPR;
   const int wpr = d * BITS / 32, gpr = d / kGroup;
@@ -119,7 +116,7 @@ k_gateup(ExpertSet es, const Plan* __restrict__ plan, const uint16_t* __restrict
       __syncthreads();  // previous item finished reading the staged inputs
       if (threadIdx.x < kTaskTok) s_off[threadIdx.x] = threadIdx.x < ntok ? tk.tok[threadIdx.x] * d : 0;
       __syncthreads();
-      stage_x_int16<BITS>(GatherSrc<uint16_t>{x, s_off}, ntok, d, st, gsh);
+      stage_x24<BITS>(GatherSrc<uint16_t>{x, s_off}, ntok, d, st);
       staged = ti;
     }
     float ga[kTaskTok], ua[kTaskTok];
@@ -157,10 +154,7 @@ k_down(ExpertSet es, const Plan* __restrict__ plan, const float* __restrict__ H,
   const int nrb = (d + rows_item - 1) / rows_item;
   const int total = plan->ntasks * nrb;
   const ItemRange ir = my_items(total);
-  XStage st;
-  st.chunks = reinterpret_cast<uint4*>(smem);
-  st.partinfo = reinterpret_cast<float2*>(smem + (size_t)kTaskTok * f * 2);
-  int* gsh = reinterpret_cast<int*>(smem + (size_t)kTaskTok * f * 2 + (size_t)kTaskTok * rg.P * 8);
+  const XStage st = xstage_carve(smem, kTaskTok, f);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int rs = lane / rg.LPR, lp = lane - rs * rg.LPR;
   const int wpr = f * BITS / 32, gpr = f / kGroup;
@@ -182,7 +176,7 @@ k_down(ExpertSet es, const Plan* __restrict__ plan, const float* __restrict__ H,
       if (threadIdx.x < kTaskTok)
         s_off[threadIdx.x] = threadIdx.x < ntok ? (tk.tok[threadIdx.x] * nslot + tk.slot[threadIdx.x]) * f : 0;
       __syncthreads();
-      stage_x_int16<BITS>(GatherSrc<float>{H, s_off}, ntok, f, st, gsh);
+      stage_x24<BITS>(GatherSrc<float>{H, s_off}, ntok, f, st);
       staged = ti;
     }
     float acc[kTaskTok];
@@ -254,8 +248,7 @@ k_gateup_all(ExpertSet es, const Plan* __restrict__ plan, const uint16_t* __rest
   const bool local = gst.chunks == nullptr;
   XStage st = gst;
   if (local) {
-    st.chunks = reinterpret_cast<uint4*>(smem);
-    st.partinfo = reinterpret_cast<float2*>(smem + (size_t)B * d * 2);
+    st = xstage_carve(smem, B, d);
   }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const RowSpan rs = cta_rows(f);
@@ -263,7 +256,7 @@ k_gateup_all(ExpertSet es, const Plan* __restrict__ plan, const uint16_t* __rest
   const int total = plan->ntasks * nr;
   GateUpRows cur, nxt;
   if (warp < total) load_gateup<BITS>(es, plan, warp, nr, rs.b, rg, lane, cur);  // in flight during staging
-  if (local) stage_x_int16_pairs<BITS>(StridedSrc<uint16_t>{x, d}, B, d, st);  // two code words per thread
+  if (local) stage_x24_pairs<BITS>(StridedSrc<uint16_t>{x, d}, B, d, st);  // two code words per thread
   for (int item = warp; item < total; item += kAllWarps) {
     if (item + kAllWarps < total) load_gateup<BITS>(es, plan, item + kAllWarps, nr, rs.b, rg, lane, nxt);
     const Task& tk = plan_tasks(plan)[item / nr];
@@ -275,10 +268,11 @@ k_gateup_all(ExpertSet es, const Plan* __restrict__ plan, const uint16_t* __rest
       for (int it = 0; it < kMaxNitE; ++it) {
         if (it < rg.NIT) {
           uint4 xc[4 * Geo<BITS>::kNch];
-          load_part_x<BITS>(st.chunks, t, it, lane, rg, xc);
+          uint2 xh[4 * Geo<BITS>::kNch];
+          load_part_x<BITS>(st, t, it, lane, rg, xc, xh);
           const float2 pi = st.partinfo[t * rg.P + it * 32 + lane];
-          ga = part_dot_x<BITS>(cur.g[it], cur.gs[it], xc, pi, ga);
-          ua = part_dot_x<BITS>(cur.u[it], cur.us[it], xc, pi, ua);
+          ga = part_dot_x<BITS>(cur.g[it], cur.gs[it], xc, xh, pi, ga);
+          ua = part_dot_x<BITS>(cur.u[it], cur.us[it], xc, xh, pi, ua);
         }
       }
       ga = warp_sum(ga);
@@ -335,8 +329,7 @@ k_down_all(ExpertSet es, const Plan* __restrict__ plan, const float* __restrict_
   const bool local = gst.chunks == nullptr;  // else: staged in global memory (see k_gateup_all)
   XStage st = gst;
   if (local) {
-    st.chunks = reinterpret_cast<uint4*>(smem);
-    st.partinfo = reinterpret_cast<float2*>(smem + (size_t)T * f * 2);
+    st = xstage_carve(smem, T, f);
   }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int lp = lane % rg.LPR, rsub = lane / rg.LPR;
@@ -347,7 +340,7 @@ k_down_all(ExpertSet es, const Plan* __restrict__ plan, const float* __restrict_
   const int total = plan->ntasks * nch;
   DownRows cur, nxt;
   if (warp < total) load_down<BITS>(es, plan, down_item(warp, nch, nrg), rs.b, nrows, rg, lp, rsub, cur);
-  if (local) stage_x_int16_pairs<BITS>(StridedSrc<float>{H, f}, T, f, st);
+  if (local) stage_x24_pairs<BITS>(StridedSrc<float>{H, f}, T, f, st);
   for (int i = warp; i < total; i += kAllWarps) {
     if (i + kAllWarps < total)
       load_down<BITS>(es, plan, down_item(i + kAllWarps, nch, nrg), rs.b, nrows, rg, lp, rsub, nxt);
@@ -356,11 +349,12 @@ k_down_all(ExpertSet es, const Plan* __restrict__ plan, const float* __restrict_
     for (int j = 0; j < tk.ntok; ++j) {
       const int v = tk.tok[j] * nslot + tk.slot[j];
       uint4 xc[4 * Geo<BITS>::kNch];
-      load_part_x<BITS>(st.chunks, v, 0, lp, rg, xc);
+      uint2 xh[4 * Geo<BITS>::kNch];
+      load_part_x<BITS>(st, v, 0, lp, rg, xc, xh);
       const float2 pi = st.partinfo[v * rg.P + lp];
       float acc[kAllRows];
 #pragma unroll
-      for (int u = 0; u < kAllRows; ++u) acc[u] = part_dot_x<BITS>(cur.q[u], cur.s[u], xc, pi, 0.f);
+      for (int u = 0; u < kAllRows; ++u) acc[u] = part_dot_x<BITS>(cur.q[u], cur.s[u], xc, xh, pi, 0.f);
       float* yv = Y + (size_t)v * d + rs.b;
       if (rg.LPR >= 8) {
         const float y = row_reduce8(acc, rg.LPR, lane);
@@ -400,10 +394,7 @@ k_down_all(ExpertSet es, const Plan* __restrict__ plan, const float* __restrict_
 }
 
 // T staged vectors of `cols` values: bytes (shared or global memory).
-static size_t all_smem(int cols, int bits, int T) {
-  const RowGeo rg = row_geo(cols, bits);
-  return (size_t)T * cols * 2 + (size_t)T * rg.P * 8;
-}
+static size_t all_smem(int cols, int bits, int T) { return xstage_bytes(T, cols, bits); }
 constexpr size_t kAllSmemMax = 200 * 1024;
 
 size_t staged_tokens_bytes(int cols, int bits, int T) { return all_smem(cols, bits, T); }
@@ -431,12 +422,7 @@ __global__ void k_stage_tokens(const Src src, int T, int cols, XStage st) {
   stage_word<BITS>(v, active, t, w, rg, __ffs(rg.LPR) - 1, st);
 }
 
-static XStage global_stage(unsigned char* buf, int cols, int T) {
-  XStage g;
-  g.chunks = reinterpret_cast<uint4*>(buf);
-  g.partinfo = reinterpret_cast<float2*>(buf + (size_t)T * cols * 2);
-  return g;
-}
+static XStage global_stage(unsigned char* buf, int cols, int T) { return xstage_carve(buf, T, cols); }
 template <int BITS, typename Src>
 static cudaError_t stage_tokens(const Src src, int T, int cols, XStage st, cudaStream_t s) {
   const int n = T * (cols * BITS / 32);
@@ -480,7 +466,7 @@ cudaError_t launch_gateup(const ExpertSet& es, const Plan* plan, int max_tasks, 
     }
     return cudaGetLastError();
   }
-  size_t sm = qgemv_int16_smem(es.d, es.bits, kTaskTok);
+  size_t sm = qgemv_int_smem(es.d, es.bits, kTaskTok);
   int nrb = (es.f + kExpWarps * rg.RPP - 1) / (kExpWarps * rg.RPP);
   int grid = expert_grid(max_tasks * nrb);
   cudaError_t e;
@@ -520,7 +506,7 @@ cudaError_t launch_down(const ExpertSet& es, const Plan* plan, int max_tasks, in
     }
     return cudaGetLastError();
   }
-  size_t sm = qgemv_int16_smem(es.f, es.bits, kTaskTok);
+  size_t sm = qgemv_int_smem(es.f, es.bits, kTaskTok);
   int nrb = (es.d + kExpWarps * rg.RPP - 1) / (kExpWarps * rg.RPP);
   int grid = expert_grid(max_tasks * nrb);
   cudaError_t e;

@@ -189,9 +189,9 @@ __host__ __device__ inline FGeo fgeo(int nC, int d, int f, int E, int K, int bit
   g.bufB = g.nBmax * g.unit;
   // phase C reuses bufB for its down rows (K+1 experts x the CTA's rows) and partial results
   const int rows_c = (d + nC - 1) / nC;
-  // ... followed by the SwiGLU outputs gathered as fp32 before staging
-  const int c_bytes = (K + 1) * rows_c * (f * bits / 8 + (f / kGroup) * 4) + (K + 1) * rows_c * 4 + 32 +
-                      (K + 1) * f * 4;
+  // ... followed by the SwiGLU outputs gathered as fp32, then staged
+  const int c_bytes = (K + 1) * rows_c * (f * bits / 8 + (f / kGroup) * 4) + (K + 1) * rows_c * 4 + 48 +
+                      (K + 1) * f * 4 + (int)xstage_bytes(K + 1, f, bits);
   if (g.bufB < c_bytes) g.bufB = c_bytes;
   // the selection's logits and scratch live in bufB before phase B's copies
   const int sel_bytes = (((E + 4) & ~3) + topk_scratch_ints(E)) * 4;
@@ -201,7 +201,7 @@ __host__ __device__ inline FGeo fgeo(int nC, int d, int f, int E, int K, int bit
 
 // Shared-memory layout (byte offsets; every region 128-byte aligned).
 struct FLayout {
-  size_t misc, rho, a_s, sta_chunks, sta_pi, gsh_a, sth_chunks, sth_pi, gsh_h, hres, bufA, bufB, total;
+  size_t misc, rho, a_s, sta, hres, bufA, bufB, total;
 };
 __host__ __device__ inline size_t fl_take(size_t& o, size_t bytes) {
   size_t r = o;
@@ -215,12 +215,7 @@ __host__ __device__ inline FLayout flayout(const FGeo& g, int d, int f, int K, i
   L.misc = fl_take(o, 256);
   L.rho = fl_take(o, (size_t)d * 2);  // apar, bpar, s_idx[8], s_w[9], red[kFWarps]
   L.a_s = fl_take(o, (size_t)d * 2);
-  L.sta_chunks = fl_take(o, (size_t)d * 2);
-  L.sta_pi = fl_take(o, (size_t)(d * bits / 128) * 8);
-  L.gsh_a = fl_take(o, (size_t)(d / kGroup) * 4);
-  L.sth_chunks = fl_take(o, (size_t)(K + 1) * f * 2);
-  L.sth_pi = fl_take(o, (size_t)(K + 1) * (f * bits / 128) * 8);
-  L.gsh_h = fl_take(o, (size_t)(K + 1) * (f / kGroup) * 4);
+  L.sta = fl_take(o, xstage_bytes(1, d, bits));  // the staged layer input (phase B's SwiGLU outputs: in bufB)
   L.hres = fl_take(o, (size_t)((d + g.nC - 1) / g.nC) * 4);  // this CTA's rows of the residual
   L.bufA = fl_take(o, (size_t)g.bufA);
   L.bufB = fl_take(o, (size_t)g.bufB);
@@ -300,12 +295,13 @@ __device__ __noinline__ float units_gateup2(const unsigned char* c0, int n0, int
     const uint4 a = qg0[p], b = qu0[p], c = qg1[p], d = qu1[p];
     const uint32_t sa = sg0[pg], sb = su0[pg], sc = sg1[pg], sd = su1[pg];
     uint4 xc[4 * G::kNch];
-    load_part_x<BITS>(st.chunks, 0, it, lane, rg, xc);
+    uint2 xh[4 * G::kNch];
+    load_part_x<BITS>(st, 0, it, lane, rg, xc, xh);
     const float2 pi = st.partinfo[p];
-    v[0] = part_dot_x<BITS>(a, sa, xc, pi, v[0]);
-    v[1] = part_dot_x<BITS>(b, sb, xc, pi, v[1]);
-    v[2] = part_dot_x<BITS>(c, sc, xc, pi, v[2]);
-    v[3] = part_dot_x<BITS>(d, sd, xc, pi, v[3]);
+    v[0] = part_dot_x<BITS>(a, sa, xc, xh, pi, v[0]);
+    v[1] = part_dot_x<BITS>(b, sb, xc, xh, pi, v[1]);
+    v[2] = part_dot_x<BITS>(c, sc, xc, xh, pi, v[2]);
+    v[3] = part_dot_x<BITS>(d, sd, xc, xh, pi, v[3]);
   }
   // lanes 0-7: gate 0, 8-15: up 0, 16-23: gate 1, 24-31: up 1 (bit-identical to warp_sum)
   const float r = row_reduce4(v, 32, lane);
@@ -358,7 +354,7 @@ __device__ __forceinline__ float router_dot(const uint16_t* wrow, const uint16_t
 // x staging from fp32 values in shared memory (the layer input).
 template <int BITS>
 __device__ __forceinline__ void stage_f32(const float* src, int ld, int T, int cols, const XStage st) {
-  stage_x_int16<BITS>(StridedSrc<float>{src, ld}, T, cols, st, nullptr);
+  stage_x24<BITS>(StridedSrc<float>{src, ld}, T, cols, st);
 }
 // Thread 0 stamps event ev of layer l (no-op without a trace buffer).
 __device__ __forceinline__ void stamp(const FusedParams& P, int l, int ev) {
@@ -528,11 +524,12 @@ __device__ void issue_B(const FusedParams& P, const FGeo& g, int l, const FSmem&
 // q rows of slot k at k*n*wqf, scale/bias rows at (K+1)*n*wqf + k*n*wsf,
 // partial results ys[k][r] after both.
 struct CLayout {
-  int n, wqf, wsf;
+  int n, wqf, wsf, f;
   __device__ size_t q(int k) const { return (size_t)k * n * wqf; }
   __device__ size_t sb(int K, int k) const { return (size_t)(K + 1) * n * wqf + (size_t)k * n * wsf; }
   __device__ size_t ys(int K) const { return ((size_t)(K + 1) * n * (wqf + wsf) + 15) & ~(size_t)15; }
   __device__ size_t hk(int K) const { return (ys(K) + (size_t)(K + 1) * n * 4 + 15) & ~(size_t)15; }
+  __device__ size_t sth(int K) const { return (hk(K) + (size_t)(K + 1) * f * 4 + 15) & ~(size_t)15; }
 };
 
 // Warp 0: issue phase C's copies (the CTA's down rows of the K selected
@@ -587,7 +584,8 @@ __device__ __forceinline__ void down_rows(const unsigned char* buf, const CLayou
     const int k = c / cpk, ci = c - k * cpk;
     const int g0 = nrg * ci / cpk, g1 = nrg * (ci + 1) / cpk;  // at most kCU row groups
     uint4 xc[4 * G::kNch];
-    load_part_x<BITS>(sth.chunks, k, 0, lp, rgf, xc);
+    uint2 xh[4 * G::kNch];
+    load_part_x<BITS>(sth, k, 0, lp, rgf, xc, xh);
     const float2 pi = sth.partinfo[k * rgf.P + lp];
     const int r0 = g0 * rgf.RPP + rs;
     const unsigned char* qb = buf + cl.q(k) + (size_t)r0 * cl.wqf + lp * 16;
@@ -599,7 +597,7 @@ __device__ __forceinline__ void down_rows(const unsigned char* buf, const CLayou
       if (g0 + u < g1 && r0 + u * rgf.RPP < nrows) {
         const uint4 q = *reinterpret_cast<const uint4*>(qb + u * rstep);
         const uint32_t sbw = *reinterpret_cast<const uint32_t*>(sbb + u * sstep);
-        v[u] = part_dot_x<BITS>(q, sbw, xc, pi, 0.f);
+        v[u] = part_dot_x<BITS>(q, sbw, xc, xh, pi, 0.f);
       }
     }
     if (rgf.LPR >= 8) {
@@ -658,12 +656,7 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
   float* red = reinterpret_cast<float*>(S.apar + 20);  // [16]  ints 20..35
   float* s_l = reinterpret_cast<float*>(S.apar + 36);  // [9]   ints 36..44 (< 52)
   uint16_t* a_s = reinterpret_cast<uint16_t*>(smem + FL.a_s);
-  XStage sta;
-  sta.chunks = reinterpret_cast<uint4*>(smem + FL.sta_chunks);
-  sta.partinfo = reinterpret_cast<float2*>(smem + FL.sta_pi);
-  XStage sth;
-  sth.chunks = reinterpret_cast<uint4*>(smem + FL.sth_chunks);
-  sth.partinfo = reinterpret_cast<float2*>(smem + FL.sth_pi);
+  const XStage sta = xstage_carve(smem + FL.sta, 1, d);
   S.bufA = smem + FL.bufA;
   S.bufB = smem + FL.bufB;
   // Stack mode: this CTA's rows [c_b, c_e) of the residual stream (the input
@@ -893,6 +886,8 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
     cl.n = c_e - c_b;
     cl.wqf = f * BITS / 8;
     cl.wsf = (f / kGroup) * 4;
+    cl.f = f;
+    const XStage sth = xstage_carve(S.bufB + cl.sth(K), K + 1, f);  // after the gathered fp32 copy
     cta_arrive(&ctrl->misc[3]);
     if (warp == 0) issue_C<BITS>(P, g, l, S, s_idx, c_b, cl);
 
@@ -915,7 +910,7 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
             if (i0 + j * kFThreads < n4) hks[i0 + j * kFThreads] = v[j];
         }
         __syncthreads();
-        stage_x_int16_pairs<BITS>(StridedSrc<float>{reinterpret_cast<const float*>(hks), f}, K + 1, f, sth);
+        stage_x24_pairs<BITS>(StridedSrc<float>{reinterpret_cast<const float*>(hks), f}, K + 1, f, sth);
       }
       stamp(P, l, 13);
       mbar_wait(S.mC, par, ctrl, P.timeout_ns);

@@ -21,7 +21,26 @@ struct FusedLayer {
   const uint16_t* rho;  // bf16 [d] (stack mode)
 };
 
+// Geometry of one launch, computed on the host (fused.cu, fused_geo): the
+// work split of every phase and the shared-memory layout.
+struct FGeo {
+  int nC;              // CTAs (one per SM)
+  int qr, rpc;         // warps per router row (1024 columns each), router rows per CTA
+  int nRouter;         // CTAs holding router rows
+  int nit_d, wpr, gpr; // rows of d (router, gate, up): parts per lane, code words, groups
+  int unit;            // shared-memory bytes of one gate+up unit (two rows, their scale/bias)
+  int nBmax;           // selected gate/up units per CTA (at most)
+  int s1_nr;           // shared gate/up units per CTA without router rows
+  int s1_rest0, s1_nparts;  // the other CTAs' split of the remaining shared units
+  int rows_c;          // output rows per CTA (at most)
+  int wqf, wsf;        // bytes of one down row's codes / scale-bias pairs
+  int a_bytes;         // phase-A data at the start of region X (router rows + shared units)
+  // shared-memory byte offsets
+  int o_misc, o_as, o_sta, o_hres, o_x, o_y, total;
+};
+
 struct FusedParams {
+  FGeo g;  // filled by launch_fused
   int n_layers, d, f, E, K;
   int stack;  // 1: RMSNorm + residual per layer, x_next output; 0: one layer, out = layer(x)
   float eps;

@@ -7,7 +7,7 @@
 //     sum_k fma(q_k, s*x_k, b*x_k) = s * sum_k q_k x_k + b * sum_k x_k,
 // so one multiply-add per weight remains (sum_k x_k is shared by all rows).
 // The production kernel evaluates sum_k q_k x_k exactly in integers (dp4a on
-// x held as 16-bit fixed point per group), which needs half a dp4a per weight
+// x held as 24-bit fixed point per group), which needs 0.75 dp4a per weight
 // and keeps the GEMV memory-bound on GB300 at 4 and at 2 bits. The other
 // three variants keep the per-weight floating-point forms for comparison.
 //
@@ -27,7 +27,7 @@ constexpr int kMaxNit = 4;  // parts per lane held in registers at once
 
 template <int BITS, int T>
 __global__ void __launch_bounds__(kGemvThreads)
-k_qgemv_int16(const uint32_t* __restrict__ q, const uint32_t* __restrict__ sb, int rows, int cols,
+k_qgemv_int(const uint32_t* __restrict__ q, const uint32_t* __restrict__ sb, int rows, int cols,
               const uint16_t* __restrict__ x, int ldx, uint16_t* __restrict__ y, float* __restrict__ yf, int ldy) {
   extern __shared__ __align__(16) unsigned char smem[];
   const RowGeo rg = row_geo(cols, BITS);
@@ -37,10 +37,7 @@ k_qgemv_int16(const uint32_t* __restrict__ q, const uint32_t* __restrict__ sb, i
   const bool valid = row < rows;
   const int wpr = cols * BITS / 32, gpr = cols / kGroup;
 
-  XStage st;
-  st.chunks = reinterpret_cast<uint4*>(smem);
-  st.partinfo = reinterpret_cast<float2*>(smem + (size_t)T * cols * 2);
-  int* gsh = reinterpret_cast<int*>(smem + (size_t)T * cols * 2 + (size_t)T * rg.P * 8);
+  const XStage st = xstage_carve(smem, T, cols);
 
   const uint32_t* qrow = q + (size_t)(valid ? row : 0) * wpr;
   const uint32_t* sbrow = sb + (size_t)(valid ? row : 0) * gpr;
@@ -62,7 +59,7 @@ k_qgemv_int16(const uint32_t* __restrict__ q, const uint32_t* __restrict__ sb, i
 
   pdl_wait();  // x may come from the previous kernel; y may still be read by it
   pdl_trigger();  // the next kernel may start its prologue now (at most one waits behind this one)
-  stage_x_int16<BITS>(StridedSrc<uint16_t>{x, ldx}, T, cols, st, gsh);
+  stage_x24<BITS>(StridedSrc<uint16_t>{x, ldx}, T, cols, st);
 
   float acc[T];
 #pragma unroll
@@ -85,7 +82,7 @@ k_qgemv_int16(const uint32_t* __restrict__ q, const uint32_t* __restrict__ sb, i
       int it = it0 + i;
       if (it < rg.NIT) {
 #pragma unroll
-        for (int t = 0; t < T; ++t) acc[t] = part_dot_int16<BITS>(qv[i], sv[i], st.chunks, st.partinfo, t, it, lp, rg, acc[t]);
+        for (int t = 0; t < T; ++t) acc[t] = part_dot24<BITS>(qv[i], sv[i], st, t, it, lp, rg, acc[t]);
       }
     }
   }
@@ -191,19 +188,16 @@ k_qgemv_float(const uint32_t* __restrict__ q, const uint32_t* __restrict__ sb, i
 // ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
-size_t qgemv_int16_smem(int cols, int bits, int T) {
-  RowGeo rg = row_geo(cols, bits);
-  return (size_t)T * cols * 2 + (size_t)T * rg.P * 8 + (size_t)T * (cols / kGroup) * sizeof(int);
-}
+size_t qgemv_int_smem(int cols, int bits, int T) { return xstage_bytes(T, cols, bits); }
 
 template <int BITS, int T>
-static cudaError_t launch_int16_t(const QMat& W, const uint16_t* x, int ldx, uint16_t* y, float* yf, int ldy,
+static cudaError_t launch_int_t(const QMat& W, const uint16_t* x, int ldx, uint16_t* y, float* yf, int ldy,
                                   cudaStream_t s) {
   RowGeo rg = row_geo(W.cols, BITS);
   int rows_per_cta = kGemvWarps * rg.RPP;
   int grid = (W.rows + rows_per_cta - 1) / rows_per_cta;
-  size_t sm = qgemv_int16_smem(W.cols, BITS, T);
-  auto kern = k_qgemv_int16<BITS, T>;
+  size_t sm = qgemv_int_smem(W.cols, BITS, T);
+  auto kern = k_qgemv_int<BITS, T>;
   if (sm > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
@@ -213,31 +207,41 @@ static cudaError_t launch_int16_t(const QMat& W, const uint16_t* x, int ldx, uin
 }
 
 template <int BITS>
-static cudaError_t launch_int16_bits(const QMat& W, const uint16_t* x, int ldx, uint16_t* y, float* yf, int ldy,
+static cudaError_t launch_int_bits(const QMat& W, const uint16_t* x, int ldx, uint16_t* y, float* yf, int ldy,
                                      int T, cudaStream_t s) {
   switch (T) {
-    case 1: return launch_int16_t<BITS, 1>(W, x, ldx, y, yf, ldy, s);
-    case 2: return launch_int16_t<BITS, 2>(W, x, ldx, y, yf, ldy, s);
-    case 3: return launch_int16_t<BITS, 3>(W, x, ldx, y, yf, ldy, s);
-    case 4: return launch_int16_t<BITS, 4>(W, x, ldx, y, yf, ldy, s);
-    case 5: return launch_int16_t<BITS, 5>(W, x, ldx, y, yf, ldy, s);
-    case 6: return launch_int16_t<BITS, 6>(W, x, ldx, y, yf, ldy, s);
-    case 7: return launch_int16_t<BITS, 7>(W, x, ldx, y, yf, ldy, s);
-    default: return launch_int16_t<BITS, 8>(W, x, ldx, y, yf, ldy, s);
+    case 1: return launch_int_t<BITS, 1>(W, x, ldx, y, yf, ldy, s);
+    case 2: return launch_int_t<BITS, 2>(W, x, ldx, y, yf, ldy, s);
+    case 3: return launch_int_t<BITS, 3>(W, x, ldx, y, yf, ldy, s);
+    case 4: return launch_int_t<BITS, 4>(W, x, ldx, y, yf, ldy, s);
+    case 5: return launch_int_t<BITS, 5>(W, x, ldx, y, yf, ldy, s);
+    case 6: return launch_int_t<BITS, 6>(W, x, ldx, y, yf, ldy, s);
+    case 7: return launch_int_t<BITS, 7>(W, x, ldx, y, yf, ldy, s);
+    default: return launch_int_t<BITS, 8>(W, x, ldx, y, yf, ldy, s);
   }
+}
+
+// Inputs staged per launch of the integer kernel: up to 8, as many as fit in
+// the 227 KB of shared memory of a CTA.
+static int qgemv_max_tokens(int cols, int bits) {
+  const size_t per = xstage_bytes(1, cols, bits);
+  const int n = (int)((size_t)227 * 1024 / per);
+  return n < 8 ? n : 8;
 }
 
 cudaError_t launch_qgemv(const QMat& W, const uint16_t* x, int batch, uint16_t* y, float* yf, int variant,
                          cudaStream_t s) {
-  for (int t0 = 0; t0 < batch; t0 += 8) {
-    int T = batch - t0 < 8 ? batch - t0 : 8;
+  const int tmax = variant == 0 ? qgemv_max_tokens(W.cols, W.bits) : 8;
+  if (tmax < 1) return cudaErrorInvalidValue;
+  for (int t0 = 0; t0 < batch; t0 += tmax) {
+    int T = batch - t0 < tmax ? batch - t0 : tmax;
     const uint16_t* xt = x + (size_t)t0 * W.cols;
     uint16_t* yt = y ? y + (size_t)t0 * W.rows : nullptr;
     float* yft = yf ? yf + (size_t)t0 * W.rows : nullptr;
     cudaError_t e;
     if (variant == 0) {
-      e = W.bits == 4 ? launch_int16_bits<4>(W, xt, W.cols, yt, yft, W.rows, T, s)
-                      : launch_int16_bits<2>(W, xt, W.cols, yt, yft, W.rows, T, s);
+      e = W.bits == 4 ? launch_int_bits<4>(W, xt, W.cols, yt, yft, W.rows, T, s)
+                      : launch_int_bits<2>(W, xt, W.cols, yt, yft, W.rows, T, s);
     } else {
       RowGeo rg = row_geo(W.cols, W.bits);
       int rows_per_cta = kGemvWarps * rg.RPP;

@@ -14,10 +14,10 @@
 //
 // Dot product: the same group reordering as the 4-bit kernels (Flash-MoE page,
 // "FMA Dequant"): per 16-code part, y += s*2^-sh*sum(q*X) + b*2^-sh*sum(X),
-// with x held as 16-bit fixed point X (one power-of-two exponent 2^-sh per
-// group of 64 inputs) split into an unsigned low and a signed high byte. Codes
-// are whole bytes, so each word of 4 codes needs two dp4a (low, high) and no
-// masking: half a dp4a per weight and token, as at 4 bits.
+// with x held as 24-bit fixed point X (one power-of-two exponent 2^-sh per
+// group of 64 inputs) split into two unsigned bytes and a signed high byte.
+// Codes are whole bytes, so each word of 4 codes needs three dp4a and no
+// masking: 0.75 dp4a per weight and token, as at 4 bits.
 //
 // Work split: 8 warps per CTA; the LPR lanes of a row each read one 16-byte
 // part (16 codes) per iteration, up to 8 parts in flight per lane; partial sums
@@ -40,21 +40,22 @@ constexpr int kG8Warps = kG8Threads / 32;
 constexpr int kG8Nit = 8;  // parts per lane held in registers at once
 constexpr int kG8MaxSmem = 227 * 1024;  // dynamic shared memory per CTA on sm_103a
 
-// Shared-memory bytes for T staged inputs of `cols` values: 2 bytes of X per
-// value (low + high byte) plus (2^-sh, 2^-sh * sum X) per 16-value part.
+// Shared-memory bytes for T staged inputs of `cols` values: 3 bytes of X per
+// value (L, M, H bytes) plus (2^-sh, 2^-sh * sum X) per 16-value part.
 __host__ __device__ inline size_t q8_stage_bytes(int cols, int T) {
-  return (size_t)T * cols * 2 + (size_t)T * (cols / 16) * 8;
+  return (size_t)T * cols * 3 + (size_t)T * (cols / 16) * 8;
 }
 
 // Stage T inputs, one thread per 8 values (two code words). Slot of part p,
 // half j of token t: ((t*NIT + p/LPR)*2 + j)*LPR + p%LPR holds
-// {lo(word 2j), hi(word 2j), lo(word 2j+1), hi(word 2j+1)}, byte i of lo/hi
-// belonging to code i of that word. Each thread first requests up to AHEAD
+// {L(word 2j), M(word 2j), L(word 2j+1), M(word 2j+1)} in `slots` and
+// {H(word 2j), H(word 2j+1)} in `hslots`, byte i of L/M/H belonging to code i
+// of that word. Each thread first requests up to AHEAD
 // of its 16-byte input pieces, then converts them, so one load latency is paid
 // per AHEAD passes. All threads of the block call; ends with __syncthreads().
 template <int AHEAD>
 __device__ void stage_x8(const uint16_t* __restrict__ x, int ldx, int T, int cols, const RowGeo rg,
-                         uint4* __restrict__ slots, float2* __restrict__ partinfo) {
+                         uint4* __restrict__ slots, uint2* __restrict__ hslots, float2* __restrict__ partinfo) {
   const int hpr = cols / 8;  // 8-value halves of a part per token (a multiple of 8)
   const int total = T * hpr;
   // t = floor(i / hpr); with many passes through a float reciprocal, exact
@@ -89,28 +90,25 @@ __device__ void stage_x8(const uint16_t* __restrict__ x, int ldx, int T, int col
       for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(v[k]));
 #pragma unroll
       for (int o = 4; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-      int sh = 0;
-      if (m > 0.f) {
-        const int e = (int)((__float_as_uint(m) >> 23) & 0xff) - 127;  // floor(log2 m)
-        sh = 14 - e;
-        sh = sh > 126 ? 126 : (sh < -126 ? -126 : sh);
-      }
+      const int sh = x24_shift(m);
       const float sc = exp2i(sh);
       int X[8];
       int xsum = 0;
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        // rint(v * 2^sh) with |v * 2^sh| < 2^15 (the product is exact)
-        const int qv = __float_as_int(fmaf(v[k], sc, 12582912.f)) - 0x4B400000;
-        X[k] = min(qv, 32767);
+        X[k] = x24_fix(v[k], sc);
         xsum += X[k];
       }
-      uint32_t lo0, hi0, lo1, hi1;
-      pack_lohi(X[0], X[1], X[2], X[3], lo0, hi0);
-      pack_lohi(X[4], X[5], X[6], X[7], lo1, hi1);
+      uint32_t L0, M0, H0, L1, M1, H1;
+      pack24(X[0], X[1], X[2], X[3], L0, M0, H0);
+      pack24(X[4], X[5], X[6], X[7], L1, M1, H1);
       const int p = h >> 1, j = h & 1;
       const int it = p / rg.LPR, lp = p - it * rg.LPR;
-      if (active) slots[((t * rg.NIT + it) * 2 + j) * rg.LPR + lp] = make_uint4(lo0, hi0, lo1, hi1);
+      if (active) {
+        const int slot = ((t * rg.NIT + it) * 2 + j) * rg.LPR + lp;
+        slots[slot] = make_uint4(L0, M0, L1, M1);
+        hslots[slot] = make_uint2(H0, H1);
+      }
       xsum += __shfl_xor_sync(kFull, xsum, 1);  // the part's other half
       if (active && j == 0) {
         const float inv = exp2i(-sh);
@@ -127,29 +125,38 @@ __device__ void stage_x8(const uint16_t* __restrict__ x, int ldx, int T, int col
 // main stall there), while the single-token kernel stays within 64 registers.
 template <bool SPLIT>
 __device__ __forceinline__ float part_dot8(const uint4 qv, uint32_t sbw, const uint4 x0, const uint4 x1,
-                                           const float2 pi, float acc) {
-  int A;
+                                           const uint2 h0v, const uint2 h1v, const float2 pi, float acc) {
+  int lo, hi;
   if (SPLIT) {
     uint32_t l0 = dp4a_uu(qv.x, x0.x, 0u), l1 = dp4a_uu(qv.y, x0.z, 0u);
-    int h0 = dp4a_us(qv.x, x0.y, 0), h1 = dp4a_us(qv.y, x0.w, 0);
+    uint32_t m0 = dp4a_uu(qv.x, x0.y, 0u), m1 = dp4a_uu(qv.y, x0.w, 0u);
+    int h0 = dp4a_us(qv.x, h0v.x, 0), h1 = dp4a_us(qv.y, h0v.y, 0);
     l0 = dp4a_uu(qv.z, x1.x, l0);
     l1 = dp4a_uu(qv.w, x1.z, l1);
-    h0 = dp4a_us(qv.z, x1.y, h0);
-    h1 = dp4a_us(qv.w, x1.w, h1);
-    A = (h0 + h1) * 256 + (int)(l0 + l1);  // |A| < 16*255*2^15 < 2^31
+    m0 = dp4a_uu(qv.z, x1.y, m0);
+    m1 = dp4a_uu(qv.w, x1.w, m1);
+    h0 = dp4a_us(qv.z, h1v.x, h0);
+    h1 = dp4a_us(qv.w, h1v.y, h1);
+    lo = (int)(l0 + l1) + (int)(m0 + m1) * 256;  // < 16*255*255*257 < 2^31
+    hi = h0 + h1;
   } else {
-    uint32_t l = dp4a_uu(qv.x, x0.x, 0u);
-    int h = dp4a_us(qv.x, x0.y, 0);
+    uint32_t l = dp4a_uu(qv.x, x0.x, 0u), m = dp4a_uu(qv.x, x0.y, 0u);
+    int h = dp4a_us(qv.x, h0v.x, 0);
     l = dp4a_uu(qv.y, x0.z, l);
-    h = dp4a_us(qv.y, x0.w, h);
+    m = dp4a_uu(qv.y, x0.w, m);
+    h = dp4a_us(qv.y, h0v.y, h);
     l = dp4a_uu(qv.z, x1.x, l);
-    h = dp4a_us(qv.z, x1.y, h);
+    m = dp4a_uu(qv.z, x1.y, m);
+    h = dp4a_us(qv.z, h1v.x, h);
     l = dp4a_uu(qv.w, x1.z, l);
-    h = dp4a_us(qv.w, x1.w, h);
-    A = h * 256 + (int)l;
+    m = dp4a_uu(qv.w, x1.w, m);
+    h = dp4a_us(qv.w, h1v.y, h);
+    lo = (int)l + (int)m * 256;
+    hi = h;
   }
+  const float A = fmaf((float)hi, 65536.f, (float)lo);
   const float s = bf16lo(sbw), b = bf16hi(sbw);
-  return fmaf(s * pi.x, (float)A, fmaf(b, pi.y, acc));
+  return fmaf(s * pi.x, A, fmaf(b, pi.y, acc));
 }
 
 // gpr = (scale, bias) pairs per row: cols/64, or 1 for the per-row format.
@@ -160,7 +167,8 @@ k_q8gemv(const uint32_t* __restrict__ q, const uint32_t* __restrict__ sb, int ro
   extern __shared__ __align__(16) unsigned char smem[];
   const RowGeo rg = row_geo(cols, 8);
   uint4* slots = reinterpret_cast<uint4*>(smem);
-  float2* partinfo = reinterpret_cast<float2*>(smem + (size_t)T * cols * 2);
+  uint2* hslots = reinterpret_cast<uint2*>(smem + (size_t)T * cols * 2);
+  float2* partinfo = reinterpret_cast<float2*>(smem + (size_t)T * cols * 3);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int rs = lane / rg.LPR, lp = lane - rs * rg.LPR;
   const int row = (blockIdx.x * kG8Warps + warp) * rg.RPP + rs;
@@ -188,7 +196,7 @@ k_q8gemv(const uint32_t* __restrict__ q, const uint32_t* __restrict__ sb, int ro
 
   pdl_wait();  // x may come from the previous kernel; y may still be read by it
   pdl_trigger();  // the next kernel may start its prologue now (at most one waits behind this one)
-  stage_x8<T <= 2 ? 2 : 4>(x, ldx, T, cols, rg, slots, partinfo);
+  stage_x8<T <= 2 ? 2 : 4>(x, ldx, T, cols, rg, slots, hslots, partinfo);
 
   float acc[T];
 #pragma unroll
@@ -208,11 +216,12 @@ k_q8gemv(const uint32_t* __restrict__ q, const uint32_t* __restrict__ sb, int ro
     for (int i = 0; i < kG8Nit; ++i) {
       const int it = it0 + i;
       if (it < rg.NIT) {
-        const uint4* xs = slots + (size_t)(it * 2) * rg.LPR + lp;
+        const size_t xs = (size_t)(it * 2) * rg.LPR + lp;
 #pragma unroll
         for (int t = 0; t < T; ++t) {
-          const uint4* xt = xs + (size_t)t * rg.NIT * 2 * rg.LPR;
-          acc[t] = part_dot8<(T >= 3)>(qv[i], sv[i], xt[0], xt[rg.LPR], partinfo[t * rg.P + it * rg.LPR + lp], acc[t]);
+          const size_t xt = xs + (size_t)t * rg.NIT * 2 * rg.LPR;
+          acc[t] = part_dot8<(T >= 3)>(qv[i], sv[i], slots[xt], slots[xt + rg.LPR], hslots[xt], hslots[xt + rg.LPR],
+                                       partinfo[t * rg.P + it * rg.LPR + lp], acc[t]);
         }
       }
     }
@@ -269,7 +278,8 @@ struct Q8Item {
 // part its sums are reduced over the row's lanes, stored, and reset.
 template <int T>
 __device__ __forceinline__ void q8_item(const Q8Item& I, int item, const uint4 (&qv)[kG8Nit],
-                                        const uint32_t (&sv)[kG8Nit], const uint4* slots, const float2* partinfo,
+                                        const uint32_t (&sv)[kG8Nit], const uint4* slots, const uint2* hslots,
+                                        const float2* partinfo,
                                         float (&acc)[T], uint16_t* __restrict__ y, int ldy) {
   const RowGeo& rg = I.rg;
 #pragma unroll
@@ -277,11 +287,12 @@ __device__ __forceinline__ void q8_item(const Q8Item& I, int item, const uint4 (
     int j, it;
     I.slot(item, i, j, it);
     if (I.live(j, it)) {
-      const uint4* xs = slots + (size_t)(it * 2) * rg.LPR + I.lp;
+      const size_t xs = (size_t)(it * 2) * rg.LPR + I.lp;
 #pragma unroll
       for (int t = 0; t < T; ++t) {
-        const uint4* xt = xs + (size_t)t * rg.NIT * 2 * rg.LPR;
-        acc[t] = part_dot8<(T >= 3)>(qv[i], sv[i], xt[0], xt[rg.LPR], partinfo[t * rg.P + it * rg.LPR + I.lp], acc[t]);
+        const size_t xt = xs + (size_t)t * rg.NIT * 2 * rg.LPR;
+        acc[t] = part_dot8<(T >= 3)>(qv[i], sv[i], slots[xt], slots[xt + rg.LPR], hslots[xt], hslots[xt + rg.LPR],
+                                     partinfo[t * rg.P + it * rg.LPR + I.lp], acc[t]);
       }
       if (it == rg.NIT - 1) {  // warp-uniform
         const int row = I.row_of(j);
@@ -313,7 +324,8 @@ k_q8gemv_stream(const uint32_t* __restrict__ q, const uint32_t* __restrict__ sb,
   Q8Item I;
   I.rg = row_geo(cols, 8);
   uint4* slots = reinterpret_cast<uint4*>(smem);
-  float2* partinfo = reinterpret_cast<float2*>(smem + (size_t)T * cols * 2);
+  uint2* hslots = reinterpret_cast<uint2*>(smem + (size_t)T * cols * 2);
+  float2* partinfo = reinterpret_cast<float2*>(smem + (size_t)T * cols * 3);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   I.rs = lane / I.rg.LPR;
   I.lp = lane - I.rs * I.rg.LPR;
@@ -340,16 +352,16 @@ k_q8gemv_stream(const uint32_t* __restrict__ q, const uint32_t* __restrict__ sb,
 
   pdl_wait();  // x may come from the previous kernel; y may still be read by it
   pdl_trigger();  // the next kernel may start its prologue now (at most one waits behind this one)
-  stage_x8<T <= 2 ? 2 : 4>(x, ldx, T, cols, I.rg, slots, partinfo);
+  stage_x8<T <= 2 ? 2 : 4>(x, ldx, T, cols, I.rg, slots, hslots, partinfo);
 
   float acc[T];
 #pragma unroll
   for (int t = 0; t < T; ++t) acc[t] = 0.f;
   for (int item = 0; item < nitems; item += 2) {
-    q8_item<T>(I, item, qa, sa, slots, partinfo, acc, y, ldy);
+    q8_item<T>(I, item, qa, sa, slots, hslots, partinfo, acc, y, ldy);
     if (item + 2 < nitems) I.load(item + 2, qa, sa);
     if (item + 1 < nitems) {
-      q8_item<T>(I, item + 1, qb, sbv, slots, partinfo, acc, y, ldy);
+      q8_item<T>(I, item + 1, qb, sbv, slots, hslots, partinfo, acc, y, ldy);
       if (item + 3 < nitems) I.load(item + 3, qb, sbv);
     }
   }

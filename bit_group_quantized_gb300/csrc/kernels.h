@@ -100,7 +100,7 @@ struct Ctrl {
 };
 static_assert(sizeof(Ctrl) == 256, "control block is 256 bytes");
 
-size_t qgemv_int16_smem(int cols, int bits, int T);
+size_t qgemv_int_smem(int cols, int bits, int T);
 cudaError_t launch_qgemv(const QMat& W, const uint16_t* x, int batch, uint16_t* y, float* yf, int variant,
                          cudaStream_t s);
 

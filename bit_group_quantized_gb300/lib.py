@@ -18,7 +18,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libbgq.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE = range(6)
-DQ_INT16, DQ_STANDARD, DQ_REORDERED, DQ_HOISTED = range(4)
+DQ_INT, DQ_STANDARD, DQ_REORDERED, DQ_HOISTED = range(4)
 GROUP = 64
 
 
@@ -114,9 +114,29 @@ def _stream(stream):
     return C.c_void_p(stream.cuda_stream)
 
 
+_alloc = None
+
+
+def set_allocator(fn) -> None:
+    """Route the buffers this binding creates (outputs not passed in, and
+    workspaces) through fn(shape, dtype, device, zero) -> tensor, e.g. a
+    caller's pool; None restores plain torch allocation. fn must return a
+    contiguous tensor of that shape and dtype, 256-byte aligned, zero-filled
+    when zero is True."""
+    global _alloc
+    _alloc = fn
+
+
+def alloc(shape, dtype, device, zero=False) -> torch.Tensor:
+    """A buffer from the installed allocator (see set_allocator), else torch."""
+    if _alloc is not None:
+        return _alloc(tuple(shape), dtype, device, zero)
+    return (torch.zeros if zero else torch.empty)(tuple(shape), dtype=dtype, device=device)
+
+
 def workspace(nbytes: int, device) -> torch.Tensor:
     """A zero-filled workspace (torch allocations are at least 256-byte aligned)."""
-    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    return alloc((max(int(nbytes), 256),), torch.uint8, device, zero=True)
 
 
 # ------------------------------------------------------------------ matrices
@@ -136,7 +156,7 @@ class QMatrix:
 def _gemv(fn, W: QMatrix, x, y, stream, *extra):
     x2 = x.reshape(-1, W.cols)
     if y is None:
-        y = torch.empty((x2.shape[0], W.rows), dtype=torch.bfloat16, device=x.device)
+        y = alloc((x2.shape[0], W.rows), torch.bfloat16, x.device)
     s = W.struct()
     _check(fn(C.byref(s), _ptr(x2), _ptr(y), x2.shape[0], *extra, _stream(stream)), fn.__name__)
     return y
@@ -159,7 +179,7 @@ def qgemv_variant(W: QMatrix, x: torch.Tensor, variant: int, y=None, stream=None
     lib = load()
     x2 = x.reshape(-1, W.cols)
     if y is None:
-        y = torch.empty((x2.shape[0], W.rows), dtype=torch.bfloat16, device=x.device)
+        y = alloc((x2.shape[0], W.rows), torch.bfloat16, x.device)
     s = W.struct()
     _check(lib.bgq_qgemv_variant(C.byref(s), _ptr(x2), _ptr(y), x2.shape[0], variant, _stream(stream)),
            "bgq_qgemv_variant")
@@ -172,10 +192,10 @@ def moe_route_topk(router, shared_gate, x, top_k, ws=None, want_logits=False, st
     B, d = x.shape
     E = router.shape[0]
     dev = x.device
-    idx = torch.empty((B, top_k), dtype=torch.int32, device=dev)
-    w = torch.empty((B, top_k), dtype=torch.float32, device=dev)
-    gamma = torch.empty((B,), dtype=torch.float32, device=dev)
-    logits = torch.empty((B, E), dtype=torch.float32, device=dev) if want_logits else None
+    idx = alloc((B, top_k), torch.int32, dev)
+    w = alloc((B, top_k), torch.float32, dev)
+    gamma = alloc((B,), torch.float32, dev)
+    logits = alloc((B, E), torch.float32, dev) if want_logits else None
     need = lib.moe_route_workspace_bytes(B, E)
     if ws is None:
         ws = workspace(need, dev)
@@ -205,8 +225,8 @@ def moe_expert_swiglu(e: Expert, x: torch.Tensor, ws=None, want_f32=False, strea
     B = x.shape[0]
     d = e.gate.cols
     s = e.struct()
-    y = torch.empty((B, d), dtype=torch.bfloat16, device=x.device)
-    yf = torch.empty((B, d), dtype=torch.float32, device=x.device) if want_f32 else None
+    y = alloc((B, d), torch.bfloat16, x.device)
+    yf = alloc((B, d), torch.float32, x.device) if want_f32 else None
     need = lib.moe_expert_workspace_bytes(C.byref(s), B)
     if ws is None:
         ws = workspace(need, x.device)
@@ -247,14 +267,14 @@ def moe_layer_forward(layer: MoELayer, x: torch.Tensor, ws=None, out=None, out_f
     dev = x.device
     s = layer.struct()
     if out is None and want_out:
-        out = torch.empty((B, d), dtype=torch.bfloat16, device=dev)
+        out = alloc((B, d), torch.bfloat16, dev)
     if out_f32 is None and want_f32:
-        out_f32 = torch.empty((B, d), dtype=torch.float32, device=dev)
+        out_f32 = alloc((B, d), torch.float32, dev)
     idx = w = gamma = None
     if want_route:
-        idx = torch.empty((B, layer.top_k), dtype=torch.int32, device=dev)
-        w = torch.empty((B, layer.top_k), dtype=torch.float32, device=dev)
-        gamma = torch.empty((B,), dtype=torch.float32, device=dev)
+        idx = alloc((B, layer.top_k), torch.int32, dev)
+        w = alloc((B, layer.top_k), torch.float32, dev)
+        gamma = alloc((B,), torch.float32, dev)
     if ws is None:
         ws = workspace(lib.moe_layer_workspace_bytes(C.byref(s), B), dev)
     _check(lib.moe_layer_forward(C.byref(s), _ptr(x), B, _ptr(out), _ptr(out_f32), _ptr(idx), _ptr(w),
@@ -289,18 +309,18 @@ def moe_layer_forward_streamed(layer: MoELayer, x: torch.Tensor, slots=None, ws=
     dev = x.device
     s = layer.struct()
     if out is None and want_out:
-        out = torch.empty((B, d), dtype=torch.bfloat16, device=dev)
+        out = alloc((B, d), torch.bfloat16, dev)
     if out_f32 is None and want_f32:
-        out_f32 = torch.empty((B, d), dtype=torch.float32, device=dev)
+        out_f32 = alloc((B, d), torch.float32, dev)
     idx = w = gamma = None
     if want_route:
-        idx = torch.empty((B, layer.top_k), dtype=torch.int32, device=dev)
-        w = torch.empty((B, layer.top_k), dtype=torch.float32, device=dev)
-        gamma = torch.empty((B,), dtype=torch.float32, device=dev)
+        idx = alloc((B, layer.top_k), torch.int32, dev)
+        w = alloc((B, layer.top_k), torch.float32, dev)
+        gamma = alloc((B,), torch.float32, dev)
     if ws is None:
         ws = workspace(lib.moe_layer_workspace_bytes(C.byref(s), B), dev)
     if slots is None:
-        slots = torch.empty(lib.moe_stream_slots_bytes(C.byref(s), B), dtype=torch.uint8, device=dev)
+        slots = alloc((lib.moe_stream_slots_bytes(C.byref(s), B),), torch.uint8, dev)
     _check(lib.moe_layer_forward_streamed(C.byref(s), _ptr(x), B, _ptr(out), _ptr(out_f32), _ptr(idx), _ptr(w),
                                           _ptr(gamma), _ptr(slots), slots.numel(), _ptr(ws), ws.numel(),
                                           _stream(stream)), "moe_layer_forward_streamed")
@@ -310,7 +330,7 @@ def moe_layer_forward_streamed(layer: MoELayer, x: torch.Tensor, slots=None, ws=
 def bgq_rmsnorm(h: torch.Tensor, rho, eps: float, a=None, stream=None):
     B, d = h.shape
     if a is None:
-        a = torch.empty((B, d), dtype=torch.bfloat16, device=h.device)
+        a = alloc((B, d), torch.bfloat16, h.device)
     _check(load().bgq_rmsnorm(_ptr(h), _ptr(rho), B, d, eps, _ptr(a), _stream(stream)), "bgq_rmsnorm")
     return a
 
@@ -360,7 +380,7 @@ def moe_stack_decode_traced(stack: Stack, x: torch.Tensor, eps: float = 1e-6, ws
     ent = lib.moe_stack_trace_entries(stack.c_layers, n)
     if ent == 0:
         raise BGQError(ERR_UNSUPPORTED, "moe_stack_trace_entries")
-    trace = torch.zeros(ent, dtype=torch.int64, device=x.device)
+    trace = alloc((ent,), torch.int64, x.device, zero=True)
     if ws is None:
         ws = workspace(stack.ws_bytes, x.device)
     _check(lib.moe_stack_decode_traced(stack.c_layers, stack.c_rho, n, eps, _ptr(x), _ptr(x_next), _ptr(h_out),

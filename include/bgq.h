@@ -70,14 +70,16 @@ enum {
 };
 
 /* Dequantisation variants of the GEMV (bgq_qgemv_variant).
- * BGQ_DQ_INT16     production: per group, y += s*sum(q*x) + b*sum(x), the inner
- *                  sum in exact integer arithmetic on x held as 16-bit fixed point
- *                  with one power-of-two exponent per group of 64 (dp4a).
+ * BGQ_DQ_INT       production: per group, y += s*sum(q*x) + b*sum(x), the inner
+ *                  sum in exact integer arithmetic on x held as 24-bit fixed point
+ *                  with one power-of-two exponent per group of 64 (dp4a): every
+ *                  bf16 input within 2^15 of its group's largest magnitude is
+ *                  exact, an fp32 input keeps 23 bits below it.
  * BGQ_DQ_STANDARD  per weight: acc += (q*s + b) * x        (the page's "standard").
  * BGQ_DQ_REORDERED per weight: acc += fma(q, s*x, b*x)     (the page's reordering).
  * BGQ_DQ_HOISTED   per group:  y += s*sum(q*x) + b*sum(x), fp32 FMAs per weight
  *                  (the reordering summed over a group, where s and b are constant). */
-enum { BGQ_DQ_INT16 = 0, BGQ_DQ_STANDARD = 1, BGQ_DQ_REORDERED = 2, BGQ_DQ_HOISTED = 3 };
+enum { BGQ_DQ_INT = 0, BGQ_DQ_STANDARD = 1, BGQ_DQ_REORDERED = 2, BGQ_DQ_HOISTED = 3 };
 
 /* One group-quantized matrix W [rows x cols] (host struct, device arrays).
  *   q  : codes, uint32 [rows][cols*bits/32]; column k of a row is in word
@@ -137,7 +139,7 @@ typedef struct bgq_moe_layer {
 /* Human-readable name of a status code (static string). */
 const char* bgq_status_string(int32_t status);
 
-/* ABI version of this header (major*100 + minor). */
+/* ABI version of this header (major*100 + minor): 101. */
 int32_t bgq_abi_version(void);
 
 /* Overlapped launch of the GEMVs (q4_gemv, q2_gemv, bgq_qgemv_variant, q8_gemv):
@@ -151,7 +153,7 @@ int32_t bgq_abi_version(void);
 /* y[b][n] = bf16( sum_k W[n][k] * x[b][k] ), b < batch, fp32 accumulation.
  * The standalone GEMV of the format (Flash-MoE page, "FMA Dequant").
  * W->bits must be 4 for q4_gemv and 2 for q2_gemv. x: bf16 [batch][cols],
- * y: bf16 [batch][rows]. 1 <= batch <= 64. Production variant BGQ_DQ_INT16. */
+ * y: bf16 [batch][rows]. 1 <= batch <= 64. Production variant BGQ_DQ_INT. */
 int32_t q4_gemv(const bgq_qmatrix* W, const uint16_t* x, uint16_t* y, int32_t batch, void* stream);
 int32_t q2_gemv(const bgq_qmatrix* W, const uint16_t* x, uint16_t* y, int32_t batch, void* stream);
 
@@ -173,7 +175,7 @@ int32_t bgq_qgemv_variant(const bgq_qmatrix* W, const uint16_t* x, uint16_t* y, 
  *   bias = -128*scale (exact in bf16).
  *   cols: 64, 128, 256 or a multiple of 512, at most 65536.
  *   x: bf16 [batch][cols], y: bf16 [batch][rows], 1 <= batch <= 64 (inputs
- *   are staged in groups of up to 8 per launch, fewer for cols > 11264; W is
+ *   are staged in groups of up to 8 per launch, fewer for cols > 8192; W is
  *   read once per group). Alignment: q, x, y 16 bytes; sb 4 bytes.
  * Errors: BGQ_ERR_INVALID_ARG (NULL, bits != 8, bad sizes, misalignment),
  * BGQ_ERR_UNSUPPORTED (group neither 64 nor cols, cols shape), BGQ_ERR_CUDA. */
@@ -227,7 +229,7 @@ int32_t moe_layer_forward(const bgq_moe_layer* L, const uint16_t* x, int32_t bat
  * not create them).
  * Same arguments, kernels and results as moe_layer_forward; the scratch memory
  * is a 4 MiB array inside the library (held on every GPU that loads the
- * library until the process exits), enough for batch <= 35 at d_model 4096,
+ * library until the process exits), enough for batch <= 33 at d_model 4096,
  * d_ff 1024, 512 experts, top-4. A call whose moe_layer_workspace_bytes(L,
  * batch) exceeds 4 MiB returns BGQ_ERR_WORKSPACE and launches nothing.
  * Every argument check of moe_layer_forward runs first, in the same order,

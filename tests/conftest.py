@@ -20,3 +20,28 @@ def cuda_device():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     return torch.device("cuda:0")
+
+
+@pytest.fixture(autouse=True)
+def guard_canaries(request):
+    """GPU tests: every buffer the binding creates (outputs, workspaces) sits
+    between guard regions of a known byte, checked when the test ends."""
+    if request.node.get_closest_marker("gpu") is None:
+        yield None
+        return
+    import torch
+
+    if not torch.cuda.is_available():
+        yield None
+        return
+    from bit_group_quantized_gb300 import lib
+    from tests.helpers import GuardedAllocator
+
+    g = GuardedAllocator()
+    lib.set_allocator(g)
+    try:
+        yield g
+        torch.cuda.synchronize()
+        g.check()
+    finally:
+        lib.set_allocator(None)

@@ -138,3 +138,45 @@ def oracle_stack_token(seed, bits, n_layers, x_bits, gpu_idx, d=4096, f=1024, E=
         src.cache.clear()
     x_next = O.f64_to_bf16_bits(O.rmsnorm(h, None, eps))
     return x_next, h, nat, gaps, forced
+
+
+# ------------------------------------------------------------------ guard canaries
+GUARD_BYTES = 4096  # a multiple of 256: the guarded buffer keeps torch's alignment
+GUARD_FILL = 0xA5
+
+
+class GuardedAllocator:
+    """Buffers with guard regions in front of and behind them, filled with a
+    known byte, for the outputs and workspaces the binding creates
+    (lib.set_allocator) and for the ones tests create with `empty`. check()
+    finds any byte of any guard that a kernel overwrote: the bounds check used
+    in place of a sanitizer."""
+
+    def __init__(self):
+        self.bufs = []
+
+    def __call__(self, shape, dtype, device, zero=False):
+        return self.empty(shape, dtype, device, zero)
+
+    def empty(self, shape, dtype, device, zero=False):
+        n = 1
+        for s in shape:
+            n *= int(s)
+        esize = torch.empty((), dtype=dtype).element_size()
+        nbytes = max(n * esize, 1)
+        body = (nbytes + 255) // 256 * 256
+        raw = torch.full((2 * GUARD_BYTES + body,), GUARD_FILL, dtype=torch.uint8, device=device)
+        inner = raw[GUARD_BYTES:GUARD_BYTES + n * esize]
+        if zero:
+            inner.zero_()
+        self.bufs.append((raw, GUARD_BYTES + n * esize))
+        return inner.view(dtype).view(tuple(int(s) for s in shape))
+
+    def check(self):
+        for raw, end in self.bufs:
+            front = raw[:GUARD_BYTES]
+            back = raw[end:]
+            bad_f = int((front != GUARD_FILL).sum())
+            bad_b = int((back != GUARD_FILL).sum())
+            assert bad_f == 0 and bad_b == 0, f"guard bytes overwritten: {bad_f} in front, {bad_b} behind"
+        return len(self.bufs)

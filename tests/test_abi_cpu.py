@@ -72,7 +72,7 @@ def test_q8_gemv_validation(lib):
 def test_status_strings(lib):
     assert lib.status_string(0) == "ok"
     assert "workspace" in lib.status_string(5)
-    assert lib.load().bgq_abi_version() == 100
+    assert lib.load().bgq_abi_version() == 101
 
 
 FAKE = 0x10000000  # 256-byte aligned, never dereferenced: validation fails first

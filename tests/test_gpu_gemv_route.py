@@ -34,6 +34,10 @@ GEMV_CASES = [
     (515, 2048, 2, 4),
     (4096, 1024, 2, 1),  # 16 lanes per row at 2 bits
     (64, 64, 2, 1),  # 1 part per row
+    (4096, 4096, 4, 1),  # a square 4-bit projection (attention-like)
+    (4096, 4096, 4, 9),  # ... at a batch that takes two launches
+    (4096, 8192, 4, 8),  # wide rows: the staged inputs fill most of shared memory
+    (256, 16384, 2, 3),  # wider still: fewer inputs per launch
 ]
 
 
@@ -161,3 +165,28 @@ def test_route_no_gate_and_other_k(cuda_device):
                 assert idx[t].cpu().tolist() == oi.tolist()
                 assert np.allclose(w[t].cpu().numpy(), ow, rtol=1e-5, atol=1e-6)
             assert float(gamma[t]) == 1.0
+
+
+@pytest.mark.parametrize("B,d", [(1, 4096), (3, 4096), (16, 1024), (257, 256)])
+def test_rmsnorm_matches_oracle(cuda_device, B, d):
+    """bgq_rmsnorm: a[b] = bf16(h[b] / sqrt(mean(h[b]^2) + eps) * rho), per row."""
+    h = synth.activations(9, d + B, B, d, device=cuda_device).float() * 3.0 - 0.5
+    rho = synth.rho(9, 0, d, device=cuda_device)
+    a = lib.bgq_rmsnorm(h, rho, 1e-6)
+    a1 = lib.bgq_rmsnorm(h, None, 1e-6)
+    torch.cuda.synchronize()
+    for b in range(B):
+        ref = O.rmsnorm(f64(h)[b], bits16(rho), 1e-6)
+        assert_bf16_output(f64(a)[b], ref, b)
+        assert_bf16_output(f64(a1)[b], O.rmsnorm(f64(h)[b], None, 1e-6), b)
+
+
+@pytest.mark.parametrize("n", [1, 4096, 3 * 4096 + 7])
+def test_residual_add(cuda_device, n):
+    """bgq_residual_add: h += delta elementwise in fp32 (exact: one rounding each)."""
+    h = torch.randn(n, generator=torch.Generator().manual_seed(n)).to(cuda_device)
+    delta = torch.randn(n, generator=torch.Generator().manual_seed(n + 1)).to(cuda_device)
+    ref = h.cpu() + delta.cpu()
+    lib.bgq_residual_add(h, delta)
+    torch.cuda.synchronize()
+    assert torch.equal(h.cpu(), ref)

@@ -98,7 +98,7 @@ def test_streamed_layer_equals_device_layer(cuda_device, E, d, f, bits, B, move_
     t["router"].copy_((t["router"].float() * np.sqrt(4096 / d)).to(torch.bfloat16))
     Hl, keep = host_copy(L, t, shape, 4, move_router)
     x = synth.activations(24, 1, B, d, device=cuda_device)
-    slots = torch.empty(lib.moe_stream_slots_bytes(Hl, B), dtype=torch.uint8, device=cuda_device)
+    slots = lib.alloc((lib.moe_stream_slots_bytes(Hl, B),), torch.uint8, cuda_device)
     a = lib.moe_layer_forward(L, x, want_f32=True, want_route=True)
     b = lib.moe_layer_forward_streamed(Hl, x, slots=slots, want_f32=True, want_route=True)
     torch.cuda.synchronize()

@@ -262,9 +262,9 @@ def test_stack_matches_oracle(cuda_device, n_layers, d, f, E, bits):
             t["router"].copy_((t["router"].float() * np.sqrt(4096 / d)).to(torch.bfloat16))
     st = lib.Stack([b[0] for b in built], rhos)
     x = synth.activations(3, 5, 1, d, device=cuda_device)[0]
-    x_next = torch.empty_like(x)
-    h = torch.empty(d, dtype=torch.float32, device=cuda_device)
-    idx = torch.empty((n_layers, K), dtype=torch.int32, device=cuda_device)
+    x_next = lib.alloc(x.shape, x.dtype, x.device)
+    h = lib.alloc((d,), torch.float32, cuda_device)
+    idx = lib.alloc((n_layers, K), torch.int32, cuda_device)
     lib.moe_stack_decode(st, x, 1e-6, x_next=x_next, h_out=h, idx_out=idx)
     torch.cuda.synchronize()
     xo, ho, oidx = oracle_stack(3, built, rhos, shape, K, bits16(x), idx.cpu().numpy())
@@ -286,8 +286,8 @@ def test_stack_tokens_in_a_row_share_a_workspace(cuda_device):
     ws = lib.workspace(st.ws_bytes, cuda_device)
     x = synth.activations(4, 6, 1, shape.d, device=cuda_device)[0].clone()
     for step in range(3):
-        xa = torch.empty_like(x)
-        xb = torch.empty_like(x)
+        xa = lib.alloc(x.shape, x.dtype, x.device)
+        xb = lib.alloc(x.shape, x.dtype, x.device)
         lib.moe_stack_decode(st, x, 1e-6, ws=ws, x_next=xa)
         lib.moe_stack_decode(st, x, 1e-6, x_next=xb)
         torch.cuda.synchronize()

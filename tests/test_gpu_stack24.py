@@ -44,9 +44,9 @@ def gpu_tokens(dev, seed, bits, n_tokens):
     x = synth.activations(seed, 0, 1, D, device=dev)[0].clone()
     rec = []
     for _ in range(n_tokens):
-        xn = torch.empty_like(x)
-        h = torch.empty(D, dtype=torch.float32, device=dev)
-        idx = torch.empty((NL, K), dtype=torch.int32, device=dev)
+        xn = lib.alloc(x.shape, x.dtype, x.device)
+        h = lib.alloc((D,), torch.float32, dev)
+        idx = lib.alloc((NL, K), torch.int32, dev)
         lib.moe_stack_decode(st, x, 1e-6, ws=ws, x_next=xn, h_out=h, idx_out=idx)
         torch.cuda.synchronize()
         rec.append((bits16(x), bits16(xn), f64(h), idx.cpu().numpy()))

@@ -33,7 +33,7 @@ def cols_supported(cols):
 
 def max_tokens(cols):
     T = 8
-    while T > 0 and T * cols * 2 + T * (cols // 16) * 8 > MAX_SMEM:
+    while T > 0 and T * cols * 3 + T * (cols // 16) * 8 > MAX_SMEM:
         T -= 1
     return T
 
@@ -136,14 +136,14 @@ def test_q8_work_split_covers_the_matrix_once(rows, cols, group):
     check_stream(rows, cols, gpr)
 
 
-@pytest.mark.parametrize("cols", [64, 128, 256, 512, 1024, 1536, 4096, 11264, 11776, 65536])
+@pytest.mark.parametrize("cols", [64, 128, 256, 512, 1024, 1536, 4096, 8192, 8704, 11264, 11776, 65536])
 def test_q8_staging_slots_written_once(cols):
     T = max_tokens(cols)
     assert T >= 1
     check_staging(T, cols)
-    if cols <= 11264:
+    if cols <= 8192:
         assert T == 8
-    assert T * cols * 2 + T * (cols // 16) * 8 <= MAX_SMEM
+    assert T * cols * 3 + T * (cols // 16) * 8 <= MAX_SMEM
 
 
 def test_q8_token_index_by_reciprocal_is_exact():

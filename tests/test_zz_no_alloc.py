@@ -33,11 +33,11 @@ def test_noalloc_matches_workspace_entry_point(cuda_device, E, d, f, B):
     for call in range(2):  # two calls in a row share the fixed scratch array
         x = synth.activations(11, 50 + call, B, d, device=cuda_device)
         ref, ref_f32, ref_idx, ref_w, ref_g = lib.moe_layer_forward(L, x, want_f32=True, want_route=True)
-        out = torch.empty((B, d), dtype=torch.bfloat16, device=cuda_device)
-        out_f32 = torch.empty((B, d), dtype=torch.float32, device=cuda_device)
-        idx = torch.empty((B, K), dtype=torch.int32, device=cuda_device)
-        w = torch.empty((B, K), dtype=torch.float32, device=cuda_device)
-        g = torch.empty((B,), dtype=torch.float32, device=cuda_device)
+        out = lib.alloc((B, d), torch.bfloat16, cuda_device)
+        out_f32 = lib.alloc((B, d), torch.float32, cuda_device)
+        idx = lib.alloc((B, K), torch.int32, cuda_device)
+        w = lib.alloc((B, K), torch.float32, cuda_device)
+        g = lib.alloc((B,), torch.float32, cuda_device)
         lib.moe_layer_forward_noalloc(L, x, out=out, out_f32=out_f32, idx=idx, w=w, gamma=g)
         torch.cuda.synchronize()
         assert torch.equal(idx, ref_idx)
@@ -53,7 +53,7 @@ def test_noalloc_rejects_batches_beyond_the_fixed_scratch(cuda_device):
     s = L.struct()
     too_big = next(b for b in range(1, 257) if lib.load().moe_layer_workspace_bytes(C.byref(s), b) > (4 << 20))
     x = synth.activations(12, 0, too_big, 1024, device=cuda_device)
-    out = torch.empty((too_big, 1024), dtype=torch.bfloat16, device=cuda_device)
+    out = lib.alloc((too_big, 1024), torch.bfloat16, cuda_device)
     with pytest.raises(lib.BGQError) as ei:
         lib.moe_layer_forward_noalloc(L, x, out=out)
     assert ei.value.status == lib.ERR_WORKSPACE
@@ -67,15 +67,15 @@ def test_noalloc_alternating_shapes_reach_the_tensor_core_path(cuda_device):
     batch-64 call whose shared expert runs on the tensor cores with split K,
     and compare every call with moe_layer_forward on a fresh zeroed workspace."""
     K = 4
-    full = layer(cuda_device, 512, 4096, 1024, K, seed=13)   # 4 MiB-class call, batch 35
+    full = layer(cuda_device, 512, 4096, 1024, K, seed=13)   # 4 MiB-class call, batch 33
     tiny = layer(cuda_device, 8, 256, 128, K, seed=14)       # its logits overlap tc's counters
     tc = layer(cuda_device, 16, 512, 256, K, seed=15)        # batch 64: the tensor-core path
-    seq = [(full, 4096, 35), (tiny, 256, 20), (tc, 512, 64), (tc, 512, 1), (full, 4096, 1), (tc, 512, 64),
+    seq = [(full, 4096, 33), (tiny, 256, 20), (tc, 512, 64), (tc, 512, 1), (full, 4096, 1), (tc, 512, 64),
            (tiny, 256, 3), (tc, 512, 100)]
     for i, (L, d, B) in enumerate(seq):
         x = synth.activations(13, 200 + i, B, d, device=cuda_device)
         ref = lib.moe_layer_forward(L, x, want_out=False, want_f32=True)[1]
-        out_f32 = torch.empty((B, d), dtype=torch.float32, device=cuda_device)
+        out_f32 = lib.alloc((B, d), torch.float32, cuda_device)
         lib.moe_layer_forward_noalloc(L, x, out_f32=out_f32)
         torch.cuda.synchronize()
         # same kernels, same inputs: the same bits as a fresh workspace
