@@ -54,10 +54,9 @@ struct Carver {
   }
 };
 
-// A layer call sends an expert to the tensor cores from 64 tokens (the
-// grouped GEMVs are faster below that on this GPU; an explicit expert call
-// uses kBigTok).
-constexpr int kLayerTcMinTokens = 64;
+// A layer call sends an expert to the tensor cores from kLayerTcMinTokens
+// tokens (an explicit expert call from kBigTok).
+constexpr int kLayerTcMinTokens = 16;
 
 struct LayerWs {
   Ctrl* ctrl;
@@ -76,6 +75,7 @@ struct LayerWs {
   int32_t* fidx;    // [16]
   float* fw;        // [16]
   float* tcs;  // split-K partial sums of the tensor-core kernels (batches that can use them)
+  unsigned char* tca;  // their staged activations
   unsigned long long* ftag;  // batch-1 persistent kernel: tagged logits [E+1]
   size_t zero_bytes;  // leading bytes that must be zero when a call starts (ctrl, ftag, tccnt)
   size_t bytes;
@@ -106,6 +106,7 @@ LayerWs carve_layer(void* ws, int B, int d, int f, int E, int K) {
   L.fidx = c.take<int32_t>(16 * 4);
   L.fw = c.take<float>(16 * 4);
   L.tcs = B >= kLayerTcMinTokens ? c.take<float>(tc_split_part_bytes(d, f, B, K)) : nullptr;
+  L.tca = B >= kLayerTcMinTokens ? c.take<unsigned char>(tc_act_bytes(d, f, B, K)) : nullptr;
   L.bytes = c.off;
   return L;
 }
@@ -173,11 +174,12 @@ Where layer_where(const bgq_moe_layer* L) {
   }
   return w;
 }
-// Tokens an expert needs in a layer call before it runs on tensor cores.
-// Measured on GB300 (one layer, 4096/1024/512/top-4): with the shared
-// expert's 16 tokens on tensor cores batch 16 took 272 us, on the grouped
-// GEMVs 185 us; at 64 tokens both paths take the same time.
-int big_min_for(Where w) { return w == Where::kHost ? INT_MAX : kLayerTcMinTokens; }
+// Tokens an expert needs in a layer call before it runs on tensor cores
+// (never for host-resident pools, nor for pools whose rows the tensor maps
+// cannot address).
+int big_min_for(Where w, const ExpertSet& es) {
+  return w == Where::kHost || !tc_layer_ok(es) ? INT_MAX : kLayerTcMinTokens;
+}
 
 constexpr long long kFusedTimeoutNs = 2000000000ll;  // bounded waits inside the persistent kernel
 
@@ -327,7 +329,7 @@ size_t moe_expert_workspace_bytes(const bgq_expert* e, int32_t batch) {
   const size_t sx = staged_tokens_bytes(d, 4, batch), sh = staged_tokens_bytes(f, 4, batch);
   return sizeof(Ctrl) + tc_split_cnt_bytes(d, f, 0) + up256(plan_bytes(batch, 0)) + up256((size_t)batch * f * 4) +
          up256((size_t)batch * d * 4) + up256(sx > sh ? sx : sh) +
-         (batch >= kBigTok ? tc_split_part_bytes(d, f, batch, 0) : 0);
+         (batch >= kBigTok ? tc_split_part_bytes(d, f, batch, 0) + tc_act_bytes(d, f, batch, 0) : 0);
 }
 
 int32_t moe_expert_swiglu(const bgq_expert* e, const uint16_t* x, int32_t batch, uint16_t* y, float* y_f32,
@@ -350,7 +352,9 @@ int32_t moe_expert_swiglu(const bgq_expert* e, const uint16_t* x, int32_t batch,
   float* Y = c.take<float>((size_t)batch * d * 4);
   const size_t sx = staged_tokens_bytes(d, 4, batch), sh = staged_tokens_bytes(f, 4, batch);
   unsigned char* stage = c.take<unsigned char>(sx > sh ? sx : sh);
-  const TcSplit sp{batch >= kBigTok ? c.take<float>(tc_split_part_bytes(d, f, batch, 0)) : nullptr, tccnt};
+  float* tcp = batch >= kBigTok ? c.take<float>(tc_split_part_bytes(d, f, batch, 0)) : nullptr;
+  unsigned char* tca = batch >= kBigTok ? c.take<unsigned char>(tc_act_bytes(d, f, batch, 0)) : nullptr;
+  const TcSplit sp{tcp, tccnt, tca};
   ExpertSet es{};
   es.shared = ExpertRef{e->gate.q, e->gate.sb, e->up.q, e->up.sb, e->down.q, e->down.sb};
   es.d = d;
@@ -365,7 +369,7 @@ int32_t moe_expert_swiglu(const bgq_expert* e, const uint16_t* x, int32_t batch,
     if (k == Where::kBad) return BGQ_ERR_INVALID_ARG;
     if (k == Where::kHost) where = Where::kHost;
   }
-  const int big_min = where == Where::kHost ? INT_MAX : kBigTok;  // an explicit expert: tensor cores from 16 tokens
+  const int big_min = where == Where::kHost || !tc_layer_ok(es) ? INT_MAX : kBigTok;  // tensor cores from 16 tokens
   if (launch_plan_single(plan, batch, big_min, s) != cudaSuccess) return BGQ_ERR_CUDA;
   if (launch_gateup(es, plan, ntasks, batch, x, H, 1, stage, s) != cudaSuccess) return BGQ_ERR_CUDA;
   if (batch >= big_min && launch_gateup_tc(es, plan, batch, 0, x, H, 1, ctrl, sp, s) != cudaSuccess) return BGQ_ERR_CUDA;
@@ -382,7 +386,8 @@ size_t moe_layer_workspace_bytes(const bgq_moe_layer* L, int32_t max_batch) {
 static int32_t layer_forward_impl(const bgq_moe_layer* L, const uint16_t* x, int32_t batch, uint16_t* out,
                                   float* out_f32, int32_t* idx_out, float* w_out, float* gamma_out, const LayerWs& W,
                                   Where where, cudaStream_t s) {
-  const int big_min = big_min_for(where);
+  const ExpertSet es = expert_set(L);
+  const int big_min = big_min_for(where, es);
   const int K = L->top_k, E = L->n_experts;
   int32_t* idx = idx_out ? idx_out : W.idx;
   float* w = w_out ? w_out : W.w;
@@ -390,12 +395,11 @@ static int32_t layer_forward_impl(const bgq_moe_layer* L, const uint16_t* x, int
   if (launch_route(L->router, L->shared_gate, x, batch, L->d_model, E, K, W.logits, W.ctrl, idx, w, gamma, nullptr,
                    W.plan, big_min, s) != cudaSuccess)
     return BGQ_ERR_CUDA;
-  const ExpertSet es = expert_set(L);
   const int max_tasks = plan_max_tasks(batch, K);
-  // experts with < 16 tokens: grouped GEMV; with >= 16: tensor-core GEMM
+  // experts with fewer than big_min tokens: grouped GEMV; the others: tensor-core GEMM
   if (launch_gateup(es, W.plan, max_tasks, batch, x, W.H, K + 1, W.stage, s) != cudaSuccess) return BGQ_ERR_CUDA;
   const bool tc = batch >= big_min;
-  const TcSplit sp{W.tcs, W.tccnt};
+  const TcSplit sp{W.tcs, W.tccnt, W.tca};
   if (tc && launch_gateup_tc(es, W.plan, batch, K, x, W.H, K + 1, W.ctrl, sp, s) != cudaSuccess) return BGQ_ERR_CUDA;
   // tensor-core tasks first: the grouped down kernel ends with the weighted combine
   if (tc && launch_down_tc(es, W.plan, batch, K, W.H, W.Y, K + 1, W.ctrl, sp, s) != cudaSuccess) return BGQ_ERR_CUDA;

@@ -34,9 +34,10 @@ struct FGeo {
   int s1_rest0, s1_nparts;  // the other CTAs' split of the remaining shared units
   int rows_c;          // output rows per CTA (at most)
   int wqf, wsf;        // bytes of one down row's codes / scale-bias pairs
-  int a_bytes;         // phase-A data at the start of region X (router rows + shared units)
+  int a_bytes;         // region A: phase-A data (router rows + shared units)
+  int b_bytes;         // region B: selected gate/up units, then phase C's down rows and staged inputs
   // shared-memory byte offsets
-  int o_misc, o_as, o_sta, o_hres, o_x, o_y, total;
+  int o_misc, o_as, o_sta, o_hres, o_a, o_b, total;
 };
 
 struct FusedParams {

@@ -48,7 +48,8 @@ struct Task {
 };
 
 // One tensor-core task: expert `expert` (-1: shared) applied to ntok tokens,
-// listed at ptok[first..first+ntok) with their slots at pslot[...].
+// listed at ptok[first..first+ntok) with their slots at pslot[...]; its
+// activations are staged at rows [pad, pad + ntok rounded up to 16).
 struct BigTask {
   int expert;
   int ntok;
@@ -138,8 +139,14 @@ cudaError_t launch_plan_single(Plan* plan, int batch, int big_min, cudaStream_t 
 struct TcSplit {
   float* part;
   int* cnt;
+  unsigned char* act;  // staged fp16 activations and their per-row scales (tc_act_bytes)
 };
 size_t tc_split_part_bytes(int d, int f, int B, int K);
+// Staged activations of a plan of (B, K) (written before read).
+size_t tc_act_bytes(int d, int f, int B, int K);
+// Whether the pools of `es` can feed the tensor-core path (tensor-map
+// alignment of the codes and scale/bias rows); host-side check.
+bool tc_layer_ok(const ExpertSet& es);
 size_t tc_split_cnt_bytes(int d, int f, int K);
 cudaError_t launch_gateup_tc(const ExpertSet& es, const Plan* plan, int B, int K, const uint16_t* x, float* H,
                              int nslot, Ctrl* ctrl, const TcSplit& sp, cudaStream_t s);

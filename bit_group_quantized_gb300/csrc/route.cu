@@ -254,6 +254,16 @@ __device__ void build_plan(const int* sel, int B, int K, int E, int big_min, Pla
     plan->ntasks = nsmall + nshared;
     plan->nbig = nbig;
   }
+  // each tensor-core task's first row in the staged activations: the sum of
+  // the earlier tasks' token counts rounded up to 16
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int rows = 0;
+    for (int t = 0; t < nbig; ++t) {
+      big[t].pad = rows;
+      rows += (big[t].ntok + 15) & ~15;
+    }
+  }
 }
 
 __global__ void __launch_bounds__(kRouteThreads)

@@ -30,6 +30,28 @@ __device__ __forceinline__ int redux_min(int v) {
   return r;
 }
 
+// Warp-wide selection among n > 32 candidates (keys ck, indices ci in shared
+// memory): K rounds of max, lowest index among equal keys, remove. Lane k
+// returns the k-th selected index. Rare (ties over many logits), so it is
+// kept out of line.
+static __device__ __noinline__ int topk_many_candidates(int* ck, const int* ci, int n, int K, int lane) {
+  int sel = 0;
+  for (int k = 0; k < K; ++k) {
+    int lb = INT_MIN;
+    for (int c = lane; c < n; c += 32) lb = max(lb, ck[c]);
+    const int best = redux_max(lb);
+    int li = INT_MAX;
+    for (int c = lane; c < n; c += 32)
+      if (ck[c] == best) li = min(li, ci[c]);
+    const int bi = redux_min(li);
+    for (int c = lane; c < n; c += 32)
+      if (ci[c] == bi) ck[c] = INT_MIN;
+    __syncwarp();
+    if (lane == k) sel = bi;
+  }
+  return sel;
+}
+
 // Scratch ints block_topk_select needs for E logits.
 __host__ __device__ constexpr int topk_scratch_ints(int E) { return 32 + 2 * E; }
 
@@ -99,19 +121,7 @@ static __device__ void block_topk_select(const float* lg, int* scratch, int E, i
         if (lane == k) sel = bi;
       }
     } else {
-      for (int k = 0; k < K; ++k) {
-        int lb = INT_MIN;
-        for (int c = lane; c < n; c += 32) lb = max(lb, ck[c]);
-        const int best = redux_max(lb);
-        int li = INT_MAX;
-        for (int c = lane; c < n; c += 32)
-          if (ck[c] == best) li = min(li, ci[c]);
-        const int bi = redux_min(li);
-        for (int c = lane; c < n; c += 32)
-          if (ci[c] == bi) ck[c] = INT_MIN;
-        __syncwarp();
-        if (lane == k) sel = bi;
-      }
+      sel = topk_many_candidates(ck, ci, n, K, lane);
     }
     if (lane < K) {
       s_idx[lane] = sel;

@@ -367,8 +367,8 @@ def wait_selftest(ws: torch.Tensor, timeout_ns: int, stream=None) -> None:
 
 
 TRACE_EVENTS = ("layer_start", "prev_layer_done", "input_normalised", "router_done", "shared_gateup_done",
-                "logits_visible", "selected_gateup_done", "swiglu_visible", "down_combine_done", "down_chunks_landed",
-                "down_dots_done", "selected", "input_staged", "swiglu_staged", "down_rows_done", "unused15")
+                "logits_visible", "selected_gateup_done", "swiglu_visible", "down_combine_done", "down_rows_landed",
+                "down_dots_done", "selected", "input_staged", "swiglu_staged", "first_chunk_landed", "last_chunk_landed")
 
 
 def moe_stack_decode_traced(stack: Stack, x: torch.Tensor, eps: float = 1e-6, ws=None, x_next=None, h_out=None,

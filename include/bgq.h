@@ -298,12 +298,13 @@ int32_t moe_stack_decode(const bgq_moe_layer* layers, const uint16_t* const* rho
 /* moe_stack_decode that also records when each phase of each layer starts on
  * each SM (the device-side counterpart of a per-layer --timing report).
  * trace: device uint64 [n_layers][n_sm][16] of %globaltimer values (ns),
- * moe_stack_trace_entries(layers, n_layers) entries, 16-byte aligned. Events:
- * 0 layer start, 1 previous layer complete (grid-wide), 2 input staged,
- * 3 router rows done, 4 shared gate/up done, 5 all logits visible,
- * 11 experts selected, 6 selected gate/up done, 7 all SwiGLU outputs visible,
- * 13 SwiGLU outputs staged, 14 down rows done, 8 down+combine done;
- * 9, 10, 12, 15 unused.
+ * moe_stack_trace_entries(layers, n_layers) entries, 16-byte aligned. Events,
+ * in the order they happen: 0 layer start, 1 previous layer complete
+ * (grid-wide), 2 input normalised, 3 router rows done, 12 input staged,
+ * 4 shared gate/up done, 5 all logits visible, 11 experts selected,
+ * 6 selected gate/up done, 7 all SwiGLU outputs visible, 13 SwiGLU outputs
+ * staged, 9 down rows landed, 10 down rows done, 8 combine done; 14 and 15:
+ * the first and the last chunk of the selected gate/up rows landed.
  * Available when the layers take the persistent batch-1 kernel (otherwise
  * moe_stack_trace_entries returns 0 and the call BGQ_ERR_UNSUPPORTED). */
 size_t moe_stack_trace_entries(const bgq_moe_layer* layers, int32_t n_layers);

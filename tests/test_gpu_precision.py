@@ -18,7 +18,7 @@ import torch
 
 from bit_group_quantized_gb300 import lib, synth
 from oracle import bgq_oracle as O
-from tests.helpers import ExpertSource, assert_bf16_output, bits16, f64, rel_l2
+from tests.helpers import TC_OWN_TOL, ExpertSource, assert_bf16_output, bits16, f64, rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -165,3 +165,28 @@ def test_layer_with_outlier_inputs(cuda_device, B, bits):
         ref, oi, _, _ = O.moe_layer(Rb, Gb, src, src(E), bits, xt, K)
         assert idx[tok].cpu().tolist() == oi.tolist()
         assert_bf16_output(f64(out)[tok], ref, tok)
+
+
+@pytest.mark.parametrize("B", [16, 40])
+def test_tensorcore_operands_beyond_fp16_range(cuda_device, B):
+    """The tensor-core path multiplies fp16 operands; each token's inputs are
+    scaled by a power of two before the conversion and scaled back after, so
+    inputs beyond fp16's range (|x| ~ 1e5 > 65504), tiny inputs (~1e-7) and
+    SwiGLU outputs far beyond 65504 keep the usual tolerance."""
+    d, f, bits = 4096, 1024, 4
+    ex, mats = expert_with_h_outliers(65, d, f, bits, cuda_device, dead=False)
+    x = synth.activations(65, 9, B, d, device=cuda_device).float()
+    x[0] *= 4.0e4   # |x| beyond 65504
+    x[1] *= 1.0e-7  # tiny
+    x[2, ::64] *= 1.0e4  # outliers beyond fp16's range in every group
+    x = x.to(torch.bfloat16)
+    assert float(x.float().abs().max()) > 65504
+    y, yf = lib.moe_expert_swiglu(ex, x, want_f32=True)
+    torch.cuda.synchronize()
+    xd = f64(x)
+    h0 = O.silu(O.gemv(*mats[0], bits, xd[0])) * O.gemv(*mats[1], bits, xd[0])
+    assert np.abs(h0).max() > 65504  # the SwiGLU outputs overflow fp16 unscaled
+    for t in sorted({0, 1, 2, 3, B - 1}):
+        ref = O.expert_swiglu(*mats, bits, xd[t])
+        assert np.all(np.isfinite(f64(yf)[t]))
+        assert_bf16_output(f64(y)[t], ref, t, own_tol=TC_OWN_TOL)
