@@ -55,12 +55,14 @@ struct Carver {
 };
 
 // A layer call sends an expert to the tensor cores from kLayerTcMinTokens
-// tokens (an explicit expert call from kBigTok).
-constexpr int kLayerTcMinTokens = 16;
+// tokens: below that the grouped GEMVs finish the whole layer sooner (d_model
+// 4096, d_ff 1024, top-4: even at batch 32, GEMVs ahead at 16, tensor cores
+// ahead from 64). An explicit expert call uses them from kBigTok, where they
+// are ahead at every batch.
+constexpr int kLayerTcMinTokens = 32;
 
 struct LayerWs {
   Ctrl* ctrl;
-  int* tccnt;     // tensor-core split-K counters (zero between calls; fixed place for any batch)
   float* logits;  // [B][E+1] then B*K ints of selected experts
   Plan* plan;
   int32_t* idx;
@@ -74,10 +76,9 @@ struct LayerWs {
   float* fpart;     // [2][1024] per-CTA sums of squares
   int32_t* fidx;    // [16]
   float* fw;        // [16]
-  float* tcs;  // split-K partial sums of the tensor-core kernels (batches that can use them)
-  unsigned char* tca;  // their staged activations
+  unsigned char* tca;  // staged activations of the tensor-core kernels (batches that can use them)
   unsigned long long* ftag;  // batch-1 persistent kernel: tagged logits [E+1]
-  size_t zero_bytes;  // leading bytes that must be zero when a call starts (ctrl, ftag, tccnt)
+  size_t zero_bytes;  // leading bytes that must be zero when a call starts (ctrl, ftag)
   size_t bytes;
 };
 
@@ -88,7 +89,6 @@ LayerWs carve_layer(void* ws, int B, int d, int f, int E, int K) {
   // the persistent kernel's tagged logits right after the control block: zero
   // between calls like it (layer_zero_prefix_bytes covers both)
   L.ftag = c.take<unsigned long long>((size_t)(E + 1) * 8);
-  L.tccnt = c.take<int>(tc_split_cnt_bytes(d, f, K));  // at a place that does not depend on B
   L.zero_bytes = c.off;  // everything above is left at zero by the kernels; the rest is written before read
   L.logits = c.take<float>((size_t)B * (E + 1) * 4 + (size_t)B * K * 4);
   L.plan = c.take<Plan>(plan_bytes(B, K));
@@ -105,7 +105,6 @@ LayerWs carve_layer(void* ws, int B, int d, int f, int E, int K) {
   L.fpart = c.take<float>(2 * 1024 * 4);
   L.fidx = c.take<int32_t>(16 * 4);
   L.fw = c.take<float>(16 * 4);
-  L.tcs = B >= kLayerTcMinTokens ? c.take<float>(tc_split_part_bytes(d, f, B, K)) : nullptr;
   L.tca = B >= kLayerTcMinTokens ? c.take<unsigned char>(tc_act_bytes(d, f, B, K)) : nullptr;
   L.bytes = c.off;
   return L;
@@ -327,9 +326,9 @@ size_t moe_expert_workspace_bytes(const bgq_expert* e, int32_t batch) {
   if (!e || batch < 1) return 0;
   const int d = e->gate.cols, f = e->gate.rows;
   const size_t sx = staged_tokens_bytes(d, 4, batch), sh = staged_tokens_bytes(f, 4, batch);
-  return sizeof(Ctrl) + tc_split_cnt_bytes(d, f, 0) + up256(plan_bytes(batch, 0)) + up256((size_t)batch * f * 4) +
+  return sizeof(Ctrl) + up256(plan_bytes(batch, 0)) + up256((size_t)batch * f * 4) +
          up256((size_t)batch * d * 4) + up256(sx > sh ? sx : sh) +
-         (batch >= kBigTok ? tc_split_part_bytes(d, f, batch, 0) + tc_act_bytes(d, f, batch, 0) : 0);
+         (batch >= kBigTok ? tc_act_bytes(d, f, batch, 0) : 0);
 }
 
 int32_t moe_expert_swiglu(const bgq_expert* e, const uint16_t* x, int32_t batch, uint16_t* y, float* y_f32,
@@ -346,15 +345,12 @@ int32_t moe_expert_swiglu(const bgq_expert* e, const uint16_t* x, int32_t batch,
   if (!ws || !al(ws, 256) || ws_bytes < moe_expert_workspace_bytes(e, batch)) return BGQ_ERR_WORKSPACE;
   Carver c(ws);
   Ctrl* ctrl = c.take<Ctrl>(sizeof(Ctrl));
-  int* tccnt = c.take<int>(tc_split_cnt_bytes(d, f, 0));  // fixed place: zero between calls of any batch
   Plan* plan = c.take<Plan>(plan_bytes(batch, 0));
   float* H = c.take<float>((size_t)batch * f * 4);
   float* Y = c.take<float>((size_t)batch * d * 4);
   const size_t sx = staged_tokens_bytes(d, 4, batch), sh = staged_tokens_bytes(f, 4, batch);
   unsigned char* stage = c.take<unsigned char>(sx > sh ? sx : sh);
-  float* tcp = batch >= kBigTok ? c.take<float>(tc_split_part_bytes(d, f, batch, 0)) : nullptr;
   unsigned char* tca = batch >= kBigTok ? c.take<unsigned char>(tc_act_bytes(d, f, batch, 0)) : nullptr;
-  const TcSplit sp{tcp, tccnt, tca};
   ExpertSet es{};
   es.shared = ExpertRef{e->gate.q, e->gate.sb, e->up.q, e->up.sb, e->down.q, e->down.sb};
   es.d = d;
@@ -371,10 +367,12 @@ int32_t moe_expert_swiglu(const bgq_expert* e, const uint16_t* x, int32_t batch,
   }
   const int big_min = where == Where::kHost || !tc_layer_ok(es) ? INT_MAX : kBigTok;  // tensor cores from 16 tokens
   if (launch_plan_single(plan, batch, big_min, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  if (batch >= big_min) {  // one tensor-core task holds every token: no grouped-GEMV work
+    if (launch_gateup_tc(es, plan, batch, 0, x, H, 1, ctrl, tca, s) != cudaSuccess) return BGQ_ERR_CUDA;
+    if (launch_down_tc(es, plan, batch, 0, H, Y, 1, ctrl, tca, s) != cudaSuccess) return BGQ_ERR_CUDA;
+    return cuda_status(launch_combine(Y, nullptr, nullptr, batch, 0, d, y, y_f32, s));
+  }
   if (launch_gateup(es, plan, ntasks, batch, x, H, 1, stage, s) != cudaSuccess) return BGQ_ERR_CUDA;
-  if (batch >= big_min && launch_gateup_tc(es, plan, batch, 0, x, H, 1, ctrl, sp, s) != cudaSuccess) return BGQ_ERR_CUDA;
-  // tensor-core tasks first: the grouped down kernel writes the outputs (y = the one slot)
-  if (batch >= big_min && launch_down_tc(es, plan, batch, 0, H, Y, 1, ctrl, sp, s) != cudaSuccess) return BGQ_ERR_CUDA;
   return cuda_status(launch_down(es, plan, ntasks, batch, H, Y, 1, stage, Combine{nullptr, nullptr, 0, y, y_f32}, s));
 }
 
@@ -399,10 +397,9 @@ static int32_t layer_forward_impl(const bgq_moe_layer* L, const uint16_t* x, int
   // experts with fewer than big_min tokens: grouped GEMV; the others: tensor-core GEMM
   if (launch_gateup(es, W.plan, max_tasks, batch, x, W.H, K + 1, W.stage, s) != cudaSuccess) return BGQ_ERR_CUDA;
   const bool tc = batch >= big_min;
-  const TcSplit sp{W.tcs, W.tccnt, W.tca};
-  if (tc && launch_gateup_tc(es, W.plan, batch, K, x, W.H, K + 1, W.ctrl, sp, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  if (tc && launch_gateup_tc(es, W.plan, batch, K, x, W.H, K + 1, W.ctrl, W.tca, s) != cudaSuccess) return BGQ_ERR_CUDA;
   // tensor-core tasks first: the grouped down kernel ends with the weighted combine
-  if (tc && launch_down_tc(es, W.plan, batch, K, W.H, W.Y, K + 1, W.ctrl, sp, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  if (tc && launch_down_tc(es, W.plan, batch, K, W.H, W.Y, K + 1, W.ctrl, W.tca, s) != cudaSuccess) return BGQ_ERR_CUDA;
   return cuda_status(
       launch_down(es, W.plan, max_tasks, batch, W.H, W.Y, K + 1, W.stage, Combine{w, gamma, K, out, out_f32}, s));
 }

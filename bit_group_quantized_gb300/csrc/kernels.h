@@ -36,7 +36,7 @@ struct ExpertSet {
 };
 
 constexpr int kTaskTok = 8;  // tokens per task (grouped GEMV width)
-constexpr int kBigTok = 16;  // smallest tensor-core task (an explicit expert; a layer call uses 64, api.cu)
+constexpr int kBigTok = 16;  // smallest tensor-core task (an explicit expert; a layer call uses 32, api.cu)
 
 // One grouped-GEMV task: expert `expert` applied to up to 8 tokens; token i's
 // result goes to slot slot[i] of token tok[i].
@@ -131,27 +131,18 @@ cudaError_t launch_plan_single(Plan* plan, int batch, int big_min, cudaStream_t 
 
 // Tensor-core (tcgen05) gate/up + SiLU*mul and down projection for the plan's
 // big tasks (experts with >= kBigTok tokens). B, K: the plan's batch and top_k.
-// K is split over several CTAs per 128-row tile; their fp32 partial sums go
-// to `part` (tc_split_part_bytes for a plan of (B, K); written before read)
-// and the tile's last CTA adds them in split order, found with the counters
-// `cnt` (tc_split_cnt_bytes, enough for any batch; zero before a call and
-// left zero, so callers keep them at a fixed place of a reused workspace).
-struct TcSplit {
-  float* part;
-  int* cnt;
-  unsigned char* act;  // staged fp16 activations and their per-row scales (tc_act_bytes)
-};
-size_t tc_split_part_bytes(int d, int f, int B, int K);
-// Staged activations of a plan of (B, K) (written before read).
+// `act` holds the staged fp16 activations and their per-row scales
+// (tc_act_bytes for a plan of (B, K); written before read). K is split over
+// the CTAs of a cluster, whose partial sums meet in distributed shared
+// memory: no other scratch, nothing left behind between calls.
 size_t tc_act_bytes(int d, int f, int B, int K);
 // Whether the pools of `es` can feed the tensor-core path (tensor-map
 // alignment of the codes and scale/bias rows); host-side check.
 bool tc_layer_ok(const ExpertSet& es);
-size_t tc_split_cnt_bytes(int d, int f, int K);
 cudaError_t launch_gateup_tc(const ExpertSet& es, const Plan* plan, int B, int K, const uint16_t* x, float* H,
-                             int nslot, Ctrl* ctrl, const TcSplit& sp, cudaStream_t s);
+                             int nslot, Ctrl* ctrl, unsigned char* act, cudaStream_t s);
 cudaError_t launch_down_tc(const ExpertSet& es, const Plan* plan, int B, int K, const float* H, float* Y, int nslot,
-                           Ctrl* ctrl, const TcSplit& sp, cudaStream_t s);
+                           Ctrl* ctrl, unsigned char* act, cudaStream_t s);
 
 // Grouped gate/up + SiLU*mul: H[(tok*nslot + slot)*f + row].
 // batch: tokens of x, staged all at once in shared memory when they fit, else

@@ -19,19 +19,25 @@
 //  * k_tc_gemm streams each CTA's K range through a ring of 3-4 stages: the
 //    weight codes and scale/bias rows arrive by TMA (cp.async.bulk.tensor on
 //    3-D tensor maps of the expert pool, [expert][row][bytes]), the
-//    activation tiles by bulk copy; the CTA's 256 threads dequantise a step
-//    into one of two A tiles while the tensor core multiplies the previous
-//    one; one thread issues the MMAs and commits them to mbarriers that free
-//    the stage and the A tile.
+//    activation tiles by bulk copy. The warps are specialised: one thread
+//    copies, eight warps dequantise a step into one of 2-3 A tiles, one
+//    thread issues the MMAs and commits them to mbarriers that free the stage
+//    and the A tile, so copies, dequantisation and MMAs of successive steps
+//    overlap.
 // Within each 16-column block the columns are stored in the order the code
 // extraction produces them (tc_slot); the activation tiles use the same order,
 // so every dot product is unchanged.
 //
-// K is split over several CTAs per 128-row tile; the tile's last CTA adds the
-// fp32 partial sums in split order (deterministic). Every wait is bounded
-// (on expiry: BGQ_ERR_TIMEOUT in the status word, a bounded wait for the
-// copies and MMAs in flight, tensor memory freed, return).
+// K is split over the CTAs of a thread-block cluster (one cluster per 128-row
+// tile); the partial sums meet in distributed shared memory and are added in
+// split order (deterministic). Every mbarrier wait is bounded (on expiry:
+// BGQ_ERR_TIMEOUT in the status word, a bounded wait for the copies in
+// flight, tensor memory freed, return); the cluster barriers are taken by
+// every thread of every CTA on every path.
 #include <cuda.h>
+
+#include <mutex>
+#include <vector>
 #include <cuda_fp16.h>
 
 #include "../../include/bgq.h"
@@ -40,7 +46,9 @@
 
 namespace bgq {
 
-constexpr int kTcThreads = 256;  // two threads per weight row (half a K step each)
+constexpr int kTcWarps = 18;  // warp 0: copies, warp 1: MMAs, warps 2-17: dequantisation and epilogue
+constexpr int kTcThreads = kTcWarps * 32;
+constexpr int kTcDq = 512;  // dequantising threads: four per weight row (a quarter K step each)
 constexpr int kTcM = 128;
 constexpr int kTcBK = 64;
 constexpr long long kTcTimeoutNs = 1000000000ll;
@@ -51,8 +59,11 @@ __device__ __forceinline__ unsigned long long tc_time() {
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
   return t;
 }
-__device__ __forceinline__ void tc_mbar_init(uint64_t* m) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem(m)) : "memory");
+__device__ __forceinline__ void tc_mbar_init(uint64_t* m, int count = 1) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(tc_smem(m)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void tc_arrive(uint64_t* m) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc_smem(m)) : "memory");
 }
 __device__ __forceinline__ bool tc_mbar_try(uint64_t* m, uint32_t parity) {
   uint32_t ok;
@@ -65,33 +76,34 @@ __device__ __forceinline__ bool tc_mbar_try(uint64_t* m, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait; false on timeout.
-__device__ bool tc_mbar_wait(uint64_t* m, uint32_t parity, long long limit_ns) {
-  if (tc_mbar_try(m, parity)) return true;
+// The same test, suspending the thread until the phase completes or
+// kTcSuspendNs pass: waiting warps then leave the issue slots to the warps
+// doing the work.
+constexpr uint32_t kTcSuspendNs = 20000;
+__device__ __forceinline__ bool tc_mbar_try_suspend(uint64_t* m, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(tc_smem(m)), "r"(parity), "r"(kTcSuspendNs)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait; false on timeout (the polling loop kept out of line).
+__device__ __noinline__ bool tc_mbar_wait_loop(uint64_t* m, uint32_t parity, long long limit_ns) {
   const unsigned long long t0 = tc_time();
   long long it = 0;
-  while (!tc_mbar_try(m, parity)) {
-    if ((++it & 63) == 0 && ((long long)(tc_time() - t0) > limit_ns || it > (1ll << 28))) return false;
+  while (!tc_mbar_try_suspend(m, parity)) {
+    if ((long long)(tc_time() - t0) > limit_ns || ++it > (1ll << 28)) return false;
   }
   return true;
 }
+__device__ __forceinline__ bool tc_mbar_wait(uint64_t* m, uint32_t parity, long long limit_ns) {
+  return tc_mbar_try(m, parity) || tc_mbar_wait_loop(m, parity, limit_ns);
+}
 __device__ __forceinline__ void tc_fence_proxy() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-// Asynchronous global -> shared copies (16 bytes through L2 only, 4 bytes), grouped per K step.
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc_smem(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(tc_smem(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(tc_smem(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -146,7 +158,7 @@ __device__ __forceinline__ int tc_off(int r, int kb, int s) {
   return (r >> 3) * 1024 + (kb * 2 + (s >> 3)) * 128 + (r & 7) * 16 + (s & 7) * 2;
 }
 // Slot of column k (0..15) inside its 16-column block, matching the order in
-// which dequant_half() writes codes (4-bit: pairs (j, j+4) per 8 columns;
+// which dequant_quarter() writes codes (4-bit: pairs (j, j+4) per 8 columns;
 // 2-bit: pairs (j, j+8) per 16 columns).
 template <int BITS>
 __device__ __forceinline__ int tc_slot(int k) {
@@ -158,80 +170,38 @@ __device__ __forceinline__ int tc_slot(int k) {
   }
 }
 
-// Dequantise half h (columns 32h..32h+31) of one row's 64 codes to fp16 into
-// the tile; qh points at that half's code words (4 at 4 bits, 2 at 2 bits).
+// Dequantise quarter q (columns 16q..16q+15) of one row's 64 codes to fp16
+// into the tile; qq points at that quarter's code words (2 at 4 bits, 1 at 2).
+// fp16 1024 + code comes from placing the code under the exponent of 1024
+// (0x6400); subtracting 1024 and one fused multiply-add give code*scale + bias.
 template <int BITS>
-__device__ __forceinline__ void dequant_half(const uint32_t* qh, uint32_t sbw, unsigned char* tile, int r, int h) {
+__device__ __forceinline__ void dequant_quarter(const uint32_t* qq, uint32_t sbw, unsigned char* tile, int r, int q) {
   const __half2 s2 = __float2half2_rn(bf16lo(sbw));
   const __half2 b2 = __float2half2_rn(bf16hi(sbw));
   const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f);
-  uint32_t w[4];
+  uint32_t w0, w1;
   if (BITS == 4) {
-    const uint4 a = *reinterpret_cast<const uint4*>(qh);
-    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+    const uint2 v = *reinterpret_cast<const uint2*>(qq);
+    w0 = v.x;
+    w1 = v.y;
   } else {
-    const uint2 a = *reinterpret_cast<const uint2*>(qh);
-    w[0] = a.x; w[1] = a.y; w[2] = 0; w[3] = 0;
+    w0 = w1 = *qq;
   }
 #pragma unroll
-  for (int cc = 0; cc < 4; ++cc) {
-    const int c = 4 * h + cc;  // chunk of the row
+  for (int cc = 0; cc < 2; ++cc) {  // chunk 2q + cc of the row: 8 codes
     uint32_t o[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      uint32_t v;
-      if (BITS == 4) {
-        v = (w[cc] >> (4 * j)) & 0x000F000Fu;  // codes j and j+4 of word c
-      } else {
-        const int base = (cc & 1) * 4;                    // chunk c: half (c&1) of word c/2
-        v = (w[cc >> 1] >> (2 * (base + j))) & 0x00030003u;  // codes base+j and base+j+8
-      }
+      // 4-bit: codes j and j+4 of word cc; 2-bit: codes 4cc+j and 4cc+j+8 of the word
+      const uint32_t v = BITS == 4 ? ((cc ? w1 : w0) >> (4 * j)) & 0x000F000Fu : (w0 >> (2 * (4 * cc + j))) & 0x00030003u;
       const uint32_t m = v | 0x64006400u;
       __half2 hh = __hsub2(*reinterpret_cast<const __half2*>(&m), k1024);
       hh = __hfma2(hh, s2, b2);
       o[j] = *reinterpret_cast<uint32_t*>(&hh);
     }
-    *reinterpret_cast<uint4*>(tile + tc_off(r, c >> 1, (c & 1) * 8)) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4*>(tile + tc_off(r, q, cc * 8)) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
-
-
-// Write 16 activation values (columns 16*kb .. +15 of token row n) into the
-// tile in tc_slot order.
-template <int BITS>
-__device__ __forceinline__ void put_act16(unsigned char* tile, int n, int kb, const float (&v)[16]) {
-  __half h[16];
-#pragma unroll
-  for (int k = 0; k < 16; ++k) h[tc_slot<BITS>(k)] = __float2half_rn(v[k]);
-  uint4 c0, c1;
-  c0.x = (uint32_t)__half_as_ushort(h[0]) | ((uint32_t)__half_as_ushort(h[1]) << 16);
-  c0.y = (uint32_t)__half_as_ushort(h[2]) | ((uint32_t)__half_as_ushort(h[3]) << 16);
-  c0.z = (uint32_t)__half_as_ushort(h[4]) | ((uint32_t)__half_as_ushort(h[5]) << 16);
-  c0.w = (uint32_t)__half_as_ushort(h[6]) | ((uint32_t)__half_as_ushort(h[7]) << 16);
-  c1.x = (uint32_t)__half_as_ushort(h[8]) | ((uint32_t)__half_as_ushort(h[9]) << 16);
-  c1.y = (uint32_t)__half_as_ushort(h[10]) | ((uint32_t)__half_as_ushort(h[11]) << 16);
-  c1.z = (uint32_t)__half_as_ushort(h[12]) | ((uint32_t)__half_as_ushort(h[13]) << 16);
-  c1.w = (uint32_t)__half_as_ushort(h[14]) | ((uint32_t)__half_as_ushort(h[15]) << 16);
-  *reinterpret_cast<uint4*>(tile + tc_off(n, kb, 0)) = c0;
-  *reinterpret_cast<uint4*>(tile + tc_off(n, kb, 8)) = c1;
-}
-
-__device__ __forceinline__ ExpertRef tc_resolve(const ExpertSet& es, int e) {
-  if (e < 0) return es.shared;
-  ExpertRef r;
-  const long long mw = (long long)es.d * es.f * es.bits / 32;
-  const long long mg = (long long)es.d * es.f / kGroup * 2;
-  const uint32_t* q = es.pool_q + (long long)e * es.q_stride;
-  const uint16_t* sb = es.pool_sb + (long long)e * es.sb_stride;
-  r.gate_q = q;
-  r.up_q = q + mw;
-  r.down_q = q + 2 * mw;
-  r.gate_sb = sb;
-  r.up_sb = sb + mg;
-  r.down_sb = sb + 2 * mg;
-  return r;
-}
-
 
 // ---------------------------------------------------------------------------
 // Copies
@@ -256,24 +226,25 @@ __device__ __forceinline__ void tc_tma3(void* dst, const CUtensorMap* map, int x
 
 __device__ __forceinline__ void tc_fail(Ctrl* ctrl) { atomicExch(&ctrl->status, BGQ_ERR_TIMEOUT); }
 
-constexpr int kTcMaxSplit = 8;  // K splits per tile (partial sums reduced by the tile's last CTA)
+constexpr int kTcMaxSplit = 8;   // K splits per tile: the CTAs of one cluster
 constexpr int kTcMaxStages = 4;
+constexpr int kTcChunk = 64;     // token columns per epilogue pass
 
-// Split K: every CTA of a tile publishes its partial sums, then counts itself
-// in *cnt; true (for the whole block) in the last one, which resets *cnt for
-// the next launch. Nothing waits, so a failed CTA cannot hang the others.
-__device__ bool tc_last_of_tile(int* cnt, int nsplit) {
-  __shared__ int s_last;
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const int prev = atomicAdd(cnt, 1);
-    s_last = prev == nsplit - 1;
-    if (s_last) *cnt = 0;
-  }
-  __syncthreads();
-  if (s_last) __threadfence();
-  return s_last != 0;
+// Cluster: barrier over every thread of every CTA (release / acquire), and
+// loads from a peer CTA's shared memory.
+__device__ __forceinline__ void tc_cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t tc_peer(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float4 tc_ld_peer4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
+               : "memory");
+  return v;
 }
 
 // ---------------------------------------------------------------------------
@@ -281,7 +252,8 @@ __device__ bool tc_last_of_tile(int* cnt, int nsplit) {
 // tensor-core task t (rows up to the task's token count rounded to 16 are
 // zero). K step kb of every row lives in slab kb (rtot rows of 128 bytes).
 // act_sh[row] = the power-of-two exponent the row was scaled by.
-// One warp per row: the row's largest magnitude, then its scaled fp16 values.
+// One warp per row and 1024-column chunk (blockIdx.z): the row's largest
+// magnitude (over the whole row), then the chunk's scaled fp16 values.
 // ---------------------------------------------------------------------------
 template <int BITS, bool F32>
 __global__ void __launch_bounds__(256) k_tc_act(const Plan* __restrict__ plan, int B, int K,
@@ -333,9 +305,10 @@ __global__ void __launch_bounds__(256) k_tc_act(const Plan* __restrict__ plan, i
     sh = 14 - e;
     sh = sh > 126 ? 126 : (sh < -126 ? -126 : sh);
   }
-  if (lane == 0) act_sh[row] = sh;
+  if (lane == 0 && blockIdx.z == 0) act_sh[row] = sh;
   const float sc = exp2i(sh);
-  for (int b = lane; b < nblk; b += 32) {
+  const int b1 = min(nblk, ((int)blockIdx.z + 1) * 64);
+  for (int b = (int)blockIdx.z * 64 + lane; b < b1; b += 32) {
     float v[16];
     load16(b, v);
     __half h[16];
@@ -352,217 +325,270 @@ __global__ void __launch_bounds__(256) k_tc_act(const Plan* __restrict__ plan, i
 }
 
 // ---------------------------------------------------------------------------
-// The GEMM. NA = 2: gate and up (silu(gate) * up); NA = 1: down.
-// blockIdx.x = 128-row tile x nsplit K ranges, blockIdx.y = tensor-core task.
+// The GEMM, one weight matrix of 128-row tiles. Gate/up (GU): tile t holds
+// gate rows [64t, 64t+64) in its rows 0-63 and the same up rows in rows
+// 64-127, so silu(gate) * up is formed where the tile's sums meet; down: 128
+// rows of the down matrix.
+// blockIdx.x = tile x nsplit K ranges (a cluster per tile), blockIdx.y = task.
 // ---------------------------------------------------------------------------
 struct TcMaps {
-  CUtensorMap q[2][2];   // [routed pool, shared expert][matrix]: codes, [expert][row][bytes]
+  CUtensorMap q[2][2];   // [routed pool, shared expert][gate or down, up]: codes, [expert][row][bytes]
   CUtensorMap sb[2][2];  // the matrices' scale/bias rows, same views
 };
 struct TcArgs {
   const Plan* plan;
   int B, K;
-  int rows;        // output rows of each matrix
+  int rows;        // output rows (f for gate/up, d for down)
   int y0[2][2];    // first row of matrix i in its map's expert region ([routed, shared][i])
   int kcols;       // input columns
-  int nsplit;
+  int nsplit;      // K splits = cluster size
+  int g, stages, abufs;  // K steps per copy stage, copy stages, fp16 A tiles
+  int sbw;               // scale/bias bytes per row and stage (32, or 16 for rows of 4 groups)
   const unsigned char* act;
   const int* act_sh;
   int rtot;
   float* out;      // H (gate/up) or Y (down), rows (token*nslot + slot)
   int nslot;
   Ctrl* ctrl;
-  float* part;
-  int* cnt;
 };
 
-__host__ __device__ inline int tc_stages(int npad) { return npad <= 128 ? 4 : 3; }
-__host__ __device__ inline size_t tc_gemm_smem(int na, int bits, int npad) {
-  const int stage = na * kTcM * (kTcBK * bits / 8) + npad * 128;
-  return 1024 + (size_t)tc_stages(npad) * stage + 2 * na * kTcM * 16 + 2 * na * kTcM * kTcBK * 2;
+constexpr int kTcHead = 2048;  // barriers, tensor-memory address, flags, the tokens' unscale factors
+constexpr int kTcSbBox = 32;   // scale/bias bytes per row and stage: the 8 groups from the stage's first aligned 4
+// Shared memory of one CTA: head, `stages` copy stages (codes, scale/bias
+// pairs, activation slabs of g K steps), `abufs` fp16 A tiles.
+__host__ __device__ inline size_t tc_gemm_smem(int bits, int npad, int g, int stages, int abufs) {
+  const size_t stage = (size_t)kTcM * g * (kTcBK * bits / 8) + kTcM * kTcSbBox + (size_t)g * npad * 128;
+  return kTcHead + stages * stage + (size_t)abufs * kTcM * kTcBK * 2;
 }
 
-template <int BITS, int NA>
+// One CTA: one tile over one K range; the cluster's CTAs (cluster rank = K
+// split) cover the whole K. K step j lives in copy stage (j / g) % stages.
+//   warp 0 (one thread): copies a stage's g K steps once the MMAs of the
+//     stage's previous use have released it (codes and scale/bias by TMA,
+//     activation slabs by bulk copy);
+//   warps 2-17: dequantise step j's codes into A tile j % abufs (after the
+//     MMAs of step j - abufs released it) and arrive on its `aready` barrier;
+//   warp 1 (one thread): issues step j's MMAs once its A tile is complete,
+//     commits them to the A tile's `afree` barrier and, at a stage's last
+//     step, to the stage's `empty` barrier.
+// Epilogue, per 64 token columns: every CTA copies its partial sums from
+// tensor memory to shared memory; after a cluster barrier CTA r adds its
+// share of the rows over every split in split order (deterministic), undoes
+// the tokens' scales, applies silu(gate)*up (gate/up), stores.
+template <int BITS, bool GU>
 __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant__ TcMaps maps, const TcArgs a) {
   extern __shared__ __align__(1024) unsigned char smem[];
   constexpr int qb = kTcBK * BITS / 8;  // code bytes of one row and K step
   constexpr int kA = kTcM * kTcBK * 2;  // bytes of one fp16 A tile
-  if ((int)blockIdx.y >= a.plan->nbig) return;
+  if ((int)blockIdx.y >= a.plan->nbig) return;  // the same for every CTA of a cluster
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tc_smem(smem) & 1023) {  // the swizzled copies need a 1024-byte aligned base (same for every CTA)
+    if (tid == 0) atomicExch(&a.ctrl->status, BGQ_ERR_CUDA);
+    return;
+  }
   const BigTask bt = plan_big(a.plan, a.B, a.K)[blockIdx.y];
   const int npad = (bt.ntok + 15) & ~15;
-  const int tid = threadIdx.x, warp = tid >> 5;
   const int tile = blockIdx.x / a.nsplit, split = blockIdx.x - tile * a.nsplit;
-  const int m0 = tile * kTcM;
-  const int S = tc_stages(npad);
+  const int G = a.g, S = a.stages, nA = a.abufs;
+  const int cb = G * qb;                                  // code bytes of a row in one stage
+  const int o_sb = kTcM * cb, o_act = o_sb + kTcM * a.sbw;
+  const int stage_bytes = o_act + G * npad * 128;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);  // [4] stage landed
   uint64_t* empty = full + kTcMaxStages;               // [4] stage read by its MMAs
-  uint64_t* adone = empty + kTcMaxStages;              // [2] A tile read by its MMAs
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(adone + 2);
+  uint64_t* aready = empty + kTcMaxStages;             // [3] A tile dequantised
+  uint64_t* afree = aready + 3;                        // [3] A tile read by its MMAs
+  uint64_t* mdone = afree + 3;                         // every MMA complete
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(mdone + 1);
   int* s_fail = reinterpret_cast<int*>(tslot + 1);
-  const int stage_bytes = NA * kTcM * qb + npad * 128;
-  unsigned char* stages = smem + 1024;
-  unsigned char* sbring = stages + S * stage_bytes;       // [2 groups of 4 K steps][NA][128 rows][16 B]
-  unsigned char* atiles = sbring + 2 * NA * kTcM * 16;    // [2][NA][kA]
+  float* s_un = reinterpret_cast<float*>(smem + 1024);  // [256] 2^-sh of each token
+  unsigned char* stages = smem + kTcHead;
+  unsigned char* atiles = stages + S * stage_bytes;  // [nA][kA]
   const int which = bt.expert < 0 ? 1 : 0, ez = bt.expert < 0 ? 0 : bt.expert;
   const int nkt = a.kcols / kTcBK;
   const int kb0 = nkt * split / a.nsplit, nk = nkt * (split + 1) / a.nsplit - kb0;
+  const int nst = (nk + G - 1) / G;  // copy stages of this CTA's K range
   uint32_t ncols = 32;
-  while ((int)ncols < NA * npad) ncols <<= 1;
+  while ((int)ncols < npad) ncols <<= 1;
   if (tid == 0) {
     for (int i = 0; i < kTcMaxStages; ++i) {
       tc_mbar_init(&full[i]);
       tc_mbar_init(&empty[i]);
     }
-    tc_mbar_init(&adone[0]);
-    tc_mbar_init(&adone[1]);
+    for (int i = 0; i < 3; ++i) {
+      tc_mbar_init(&aready[i], kTcDq / 32);  // one arrival per dequantising warp
+      tc_mbar_init(&afree[i]);
+    }
+    tc_mbar_init(mdone);
     *s_fail = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 0) tmem_alloc(tslot, ncols);
+  __syncthreads();
+  // the copies start at once; warp 1 allocates tensor memory meanwhile
+  if (warp == 0) {
+    if (lane > 0)
+      for (int n = lane - 1; n < npad; n += 31) s_un[n] = exp2i(-a.act_sh[bt.pad + n]);  // read in the epilogue
+    if (lane == 0) {
+      const bool sh = which == 1;
+      const CUtensorMap* mq0 = sh ? &maps.q[1][0] : &maps.q[0][0];
+      const CUtensorMap* mq1 = sh ? &maps.q[1][1] : &maps.q[0][1];
+      const CUtensorMap* ms0 = sh ? &maps.sb[1][0] : &maps.sb[0][0];
+      const CUtensorMap* ms1 = sh ? &maps.sb[1][1] : &maps.sb[0][1];
+      const int y00 = sh ? a.y0[1][0] : a.y0[0][0], y01 = sh ? a.y0[1][1] : a.y0[0][1];
+      for (int u = 0; u < nst; ++u) {
+        const int s = u % S, kb = kb0 + u * G, gs = min(G, nk - u * G);
+        if (u >= S && !tc_mbar_wait(&empty[s], (uint32_t)((u / S - 1) & 1), kTcTimeoutNs)) {
+          *s_fail = 1;
+          break;
+        }
+        unsigned char* st = stages + s * stage_bytes;
+        // a box is always copied whole (zero past the matrix's end)
+        tc_expect(&full[s], (uint32_t)(o_act + gs * npad * 128));
+        if (GU) {  // 64 gate rows, then the same 64 up rows
+          const int y = tile * (kTcM / 2);
+          tc_tma3(st, mq0, kb * qb, y00 + y, ez, &full[s]);
+          tc_tma3(st + (kTcM / 2) * cb, mq1, kb * qb, y01 + y, ez, &full[s]);
+          tc_tma3(st + o_sb, ms0, (kb >> 2) * 16, y00 + y, ez, &full[s]);
+          tc_tma3(st + o_sb + (kTcM / 2) * a.sbw, ms1, (kb >> 2) * 16, y01 + y, ez, &full[s]);
+        } else {
+          const int y = y00 + tile * kTcM;
+          tc_tma3(st, mq0, kb * qb, y, ez, &full[s]);
+          tc_tma3(st + o_sb, ms0, (kb >> 2) * 16, y, ez, &full[s]);
+        }
+        for (int t = 0; t < gs; ++t)
+          tc_bulk(st + o_act + t * npad * 128, a.act + ((size_t)(kb + t) * a.rtot + bt.pad) * 128,
+                  (uint32_t)npad * 128, &full[s]);
+      }
+    }
+  } else if (warp == 1) {
+    tmem_alloc(tslot, ncols);
+    tc_fence_before();
+    __syncwarp();
+    tc_fence_after();
+    const uint32_t tbase = *tslot;
+    if (lane == 0) {
+      const uint32_t idesc = tc_idesc(npad);
+      for (int j = 0; j < nk; ++j) {
+        const int u = j / G, t = j - u * G, s = u % S, b = j % nA;
+        if (!tc_mbar_wait(&aready[b], (uint32_t)((j / nA) & 1), kTcTimeoutNs) ||
+            !tc_mbar_wait(&full[s], (uint32_t)((u / S) & 1), kTcTimeoutNs)) {
+          *s_fail = 1;
+          break;
+        }
+        tc_fence_after();
+        const unsigned char* bs = stages + s * stage_bytes + o_act + t * npad * 128;
+        const unsigned char* at = atiles + b * kA;
+#pragma unroll
+        for (int kk = 0; kk < kTcBK / 16; ++kk)
+          tc_mma(tbase, tc_desc(at + kk * 256), tc_desc(bs + kk * 256), idesc, (j | kk) ? 1u : 0u);
+        tc_commit(&afree[b]);
+        if (t == G - 1 || j == nk - 1) tc_commit(&empty[s]);
+      }
+      tc_commit(mdone);  // tracks every MMA this thread issued
+    }
+  } else {
+    // warp w of the 16 dequantises rows 8w..8w+7, lane l row 8w + l%8, quarter l/8
+    const int e = tid - 64, rr = ((e >> 5) << 3) | (lane & 7), qt = lane >> 3;
+    // the codes arrive swizzled (16-byte chunk c of row r at c ^ ((r*cb/128) % (cb/16)), cb >= 32)
+    const int swz = cb >= 32 ? ((rr * cb) >> 7) & (cb / 16 - 1) : 0;
+    for (int j = 0; j < nk; ++j) {
+      const int u = j / G, t = j - u * G, s = u % S, b = j % nA, kb = kb0 + j;
+      // lane 0 waits for the stage and the A tile, the warp follows
+      int okw = 1;
+      if (lane == 0)
+        okw = tc_mbar_wait(&full[s], (uint32_t)((u / S) & 1), kTcTimeoutNs) &&
+              (j < nA || tc_mbar_wait(&afree[b], (uint32_t)((j / nA - 1) & 1), kTcTimeoutNs));
+      if (!__shfl_sync(0xffffffffu, okw, 0)) {
+        *s_fail = 1;
+        break;
+      }
+      const unsigned char* st = stages + s * stage_bytes;
+      const int ks = (kb0 + u * G) & ~3;  // first group of the stage's scale/bias box
+      const uint32_t sbw = *reinterpret_cast<const uint32_t*>(st + o_sb + rr * a.sbw + (kb - ks) * 4);
+      const int x = t * qb + qt * (qb / 4);  // this quarter's first code byte in the row
+      dequant_quarter<BITS>(reinterpret_cast<const uint32_t*>(st + rr * cb + ((((x >> 4) ^ swz) << 4) | (x & 15))), sbw,
+                            atiles + b * kA, rr, qt);
+      tc_fence_proxy();  // this thread's tile stores, visible to the tensor core
+      __syncwarp();
+      if (lane == 0) tc_arrive(&aready[b]);
+    }
+  }
+  // every MMA has completed before tensor memory is read (bounded)
+  if (warp >= 2 && !tc_mbar_wait(mdone, 0, kTcTimeoutNs)) *s_fail = 1;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  const bool ok = *s_fail == 0;
   const uint32_t tbase = *tslot;
-  const uint32_t idesc = tc_idesc(npad);
-  // thread 0: K step kb0 + j into stage j % S (scale/bias rows of four K
-  // steps at a time, at the first step of each group in the range)
-  auto issue = [&](int j) {
-    const int kb = kb0 + j, s = j % S;
-    unsigned char* st = stages + s * stage_bytes;
-    const bool with_sb = j == 0 || (kb & 3) == 0;
-    tc_expect(&full[s], (uint32_t)(NA * kTcM * qb + npad * 128 + (with_sb ? NA * kTcM * 16 : 0)));
-#pragma unroll
-    for (int i = 0; i < NA; ++i) {
-      const int y = a.y0[which][i] + m0;
-      tc_tma3(st + i * kTcM * qb, &maps.q[which][i], kb * qb, y, ez, &full[s]);
-      if (with_sb) tc_tma3(sbring + (((kb >> 2) & 1) * NA + i) * kTcM * 16, &maps.sb[which][i], (kb >> 2) * 16, y, ez,
-                           &full[s]);
-    }
-    tc_bulk(st + NA * kTcM * qb, a.act + ((size_t)kb * a.rtot + bt.pad) * 128, (uint32_t)npad * 128, &full[s]);
-  };
-  int issued = 0;
-  if (tid == 0)
-    for (; issued < S - 1 && issued < nk; ++issued) issue(issued);
-  const int rr = tid & (kTcM - 1), hf = tid >> 7;  // the row this thread dequantises, and which half of its codes
-  int j = 0;
-  for (; j < nk; ++j) {
-    const int kb = kb0 + j, s = j % S;
-    if (tid == 0 && issued < nk) {
-      // the stage of step j + S - 1 was last read by the MMAs of step j - 1
-      if (j >= 1 && !tc_mbar_wait(&empty[(j - 1) % S], (uint32_t)(((j - 1) / S) & 1), kTcTimeoutNs)) *s_fail = 1;
-      else issue(issued++);
-    }
-    if (!tc_mbar_wait(&full[s], (uint32_t)((j / S) & 1), kTcTimeoutNs)) *s_fail = 1;
-    if (j >= 2 && !tc_mbar_wait(&adone[j & 1], (uint32_t)(((j - 2) >> 1) & 1), kTcTimeoutNs)) *s_fail = 1;
-    const unsigned char* st = stages + s * stage_bytes;
-    unsigned char* at = atiles + (j & 1) * NA * kA;
-#pragma unroll
-    for (int i = 0; i < NA; ++i) {
-      const uint32_t sbw =
-          *reinterpret_cast<const uint32_t*>(sbring + (((kb >> 2) & 1) * NA + i) * kTcM * 16 + rr * 16 + (kb & 3) * 4);
-      dequant_half<BITS>(reinterpret_cast<const uint32_t*>(st + i * kTcM * qb + rr * qb + hf * (qb / 2)), sbw,
-                         at + i * kA, rr, hf);
-    }
-    tc_fence_proxy();
-    __syncthreads();
-    if (*s_fail) break;
-    if (tid == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < kTcBK / 16; ++kk) {
-        const uint64_t bd = tc_desc(st + NA * kTcM * qb + kk * 256);
-#pragma unroll
-        for (int i = 0; i < NA; ++i)
-          tc_mma(tbase + i * npad, tc_desc(at + i * kA + kk * 256), bd, idesc, (j | kk) ? 1u : 0u);
-      }
-      tc_commit(&adone[j & 1]);
-      tc_commit(&empty[s]);
-    }
+  if (!ok && tid == 0) {
+    tc_fail(a.ctrl);
+    // bounded waits for copies still in flight before the shared memory is released
+    for (int i = 0; i < S; ++i) tc_mbar_wait(&full[i], 0, kTcTimeoutNs / 8) || tc_mbar_wait(&full[i], 1, 1000);
   }
-  bool ok = *s_fail == 0;
-  // the last commit covers every MMA
-  if (ok && !tc_mbar_wait(&adone[(nk - 1) & 1], (uint32_t)(((nk - 1) >> 1) & 1), kTcTimeoutNs)) ok = false;
-  const size_t pc = (size_t)plan_max_pairs(a.B, a.K);
+  // epilogue (every CTA of the cluster takes the same passes and barriers)
+  float* P = reinterpret_cast<float*>(stages);  // [kTcChunk tokens][128 rows] partial sums
+  const uint32_t p_sa = tc_smem(P);
+  const int orows = GU ? kTcM / 2 : kTcM;             // output rows of the tile
+  const int rs = orows / a.nsplit, r0 = split * rs;  // this CTA's output rows of the reduction
+  const int m0 = tile * orows;
+  const size_t row_stride = (size_t)a.rows;
   const int* ptok = plan_ptok(a.plan, a.B, a.K) + bt.first;
   const int* pslot = plan_pslot(a.plan, a.B, a.K) + bt.first;
-  if (ok && warp < 4) {  // warp w reads tensor-memory lanes 32w..32w+31
-    tc_fence_after();
-    const int row = m0 + warp * 32 + (tid & 31);
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    for (int c0 = 0; c0 < npad; c0 += 8) {
-      float acc[NA][8];
+  for (int c0 = 0; c0 < npad; c0 += kTcChunk) {
+    const int cw = min(kTcChunk, npad - c0);
+    if (ok && warp >= 2) {  // warp w reads tensor-memory lanes 32(w%4)..+31, a quarter (w-2)/4 of the columns
+      const int sub = warp & 3, part = (warp - 2) >> 2;
+      const int row = sub * 32 + lane;
+      for (int c = part * 8; c < cw; c += 32) {
+        float v[8];
+        tmem_ld8(tbase + ((uint32_t)(sub * 32) << 16) + c0 + c, v);
 #pragma unroll
-      for (int i = 0; i < NA; ++i) tmem_ld8(tbase + lane_off + i * npad + c0, acc[i]);
-      if (row < a.rows) {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int n = c0 + u;
-          if (n >= bt.ntok) continue;
-          const float un = exp2i(-a.act_sh[bt.pad + n]);  // the token's scale, undone exactly
-          if (NA == 2) {
-            const float g = acc[0][u] * un, up = acc[NA - 1][u] * un;
-            if (a.nsplit == 1) {
-              a.out[((size_t)ptok[n] * a.nslot + pslot[n]) * a.rows + row] = g / (1.f + expf(-g)) * up;
-            } else {  // partial sums of this K range: [split][pair][gate, up][row]
-              float* pp = a.part + (((size_t)split * pc + bt.first + n) * 2) * a.rows + row;
-              pp[0] = g;
-              pp[a.rows] = up;
-            }
-          } else {
-            const float y = acc[0][u] * un;
-            if (a.nsplit == 1)
-              a.out[((size_t)ptok[n] * a.nslot + pslot[n]) * a.rows + row] = y;
-            else  // [split][pair][row]
-              a.part[((size_t)split * pc + bt.first + n) * a.rows + row] = y;
-          }
-        }
+        for (int k = 0; k < 8; ++k) P[(c + k) * kTcM + row] = v[k];
       }
     }
-  } else if (!ok && tid == 0) {
-    tc_fail(a.ctrl);
-    // bounded waits for the copies and MMAs in flight before the memory is released
-    for (int i = 0; i < S; ++i) tc_mbar_wait(&full[i], 0, kTcTimeoutNs / 8) || tc_mbar_wait(&full[i], 1, 1000);
-    tc_mbar_wait(&adone[0], 0, kTcTimeoutNs / 8);
+    tc_cluster_sync();
+    const int nq = rs / 4;  // row quads of this CTA
+    for (int it = tid; it < cw * nq; it += kTcThreads) {
+      const int c = it / nq, rq = r0 + 4 * (it - c * nq), n = c0 + c;
+      if (!ok || n >= bt.ntok || m0 + rq >= a.rows) continue;
+      const uint32_t off0 = p_sa + (uint32_t)((c * kTcM + rq) * 4);
+      const uint32_t offu = off0 + (uint32_t)(kTcM / 2) * 4;  // the matching up rows (gate/up)
+      // eight splits' loads in flight at once, each added in split order
+      float4 g = make_float4(0.f, 0.f, 0.f, 0.f), w = g;
+      for (int q0 = 0; q0 < a.nsplit; q0 += 8) {
+        float4 gq[8], wq[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (q0 + k < a.nsplit) {
+            gq[k] = tc_ld_peer4(tc_peer(off0, (uint32_t)(q0 + k)));
+            if (GU) wq[k] = tc_ld_peer4(tc_peer(offu, (uint32_t)(q0 + k)));
+          }
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (q0 + k < a.nsplit) {
+            g.x += gq[k].x; g.y += gq[k].y; g.z += gq[k].z; g.w += gq[k].w;
+            if (GU) {
+              w.x += wq[k].x; w.y += wq[k].y; w.z += wq[k].z; w.w += wq[k].w;
+            }
+          }
+      }
+      const float un = s_un[n];  // the token's scale, undone exactly
+      float4 h;
+      if (GU) {
+        const float gx = g.x * un, gy = g.y * un, gz = g.z * un, gw = g.w * un;
+        h.x = gx / (1.f + expf(-gx)) * (w.x * un);
+        h.y = gy / (1.f + expf(-gy)) * (w.y * un);
+        h.z = gz / (1.f + expf(-gz)) * (w.z * un);
+        h.w = gw / (1.f + expf(-gw)) * (w.w * un);
+      } else {
+        h = make_float4(g.x * un, g.y * un, g.z * un, g.w * un);
+      }
+      *reinterpret_cast<float4*>(a.out + ((size_t)ptok[n] * a.nslot + pslot[n]) * row_stride + m0 + rq) = h;
+    }
+    tc_cluster_sync();  // peers are done reading before the next pass overwrites P (or the CTA exits)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_free(tbase, ncols);
-  if (!ok || a.nsplit == 1) return;
-  if (tc_last_of_tile(a.cnt + (size_t)blockIdx.y * gridDim.x / a.nsplit + tile, a.nsplit)) {
-    // the tile's last CTA: partial sums in split order (then silu(gate) * up);
-    // four consecutive rows per thread, every split's loads in flight at once
-    const int per = NA == 2 ? 2 : 1;
-    for (int i = tid; i < (kTcM / 4) * bt.ntok; i += kTcThreads) {
-      const int n = i / (kTcM / 4), row = m0 + 4 * (i - n * (kTcM / 4));
-      if (row >= a.rows) continue;  // rows is a multiple of 64
-      const float4* pp = reinterpret_cast<const float4*>(a.part + ((size_t)bt.first + n) * per * a.rows + row);
-      const size_t qs = pc * per * a.rows / 4, us = a.rows / 4;
-      float4 gq[kTcMaxSplit], uq[kTcMaxSplit];
-#pragma unroll
-      for (int q = 0; q < kTcMaxSplit; ++q)
-        if (q < a.nsplit) {
-          gq[q] = __ldcg(pp + q * qs);
-          if (NA == 2) uq[q] = __ldcg(pp + q * qs + us);
-        }
-      float4 g = gq[0], u = NA == 2 ? uq[0] : gq[0];
-#pragma unroll
-      for (int q = 1; q < kTcMaxSplit; ++q)
-        if (q < a.nsplit) {
-          g.x += gq[q].x; g.y += gq[q].y; g.z += gq[q].z; g.w += gq[q].w;
-          if (NA == 2) {
-            u.x += uq[q].x; u.y += uq[q].y; u.z += uq[q].z; u.w += uq[q].w;
-          }
-        }
-      float4 h = g;
-      if (NA == 2) {
-        h.x = g.x / (1.f + expf(-g.x)) * u.x;
-        h.y = g.y / (1.f + expf(-g.y)) * u.y;
-        h.z = g.z / (1.f + expf(-g.z)) * u.z;
-        h.w = g.w / (1.f + expf(-g.w)) * u.w;
-      }
-      *reinterpret_cast<float4*>(a.out + ((size_t)ptok[n] * a.nslot + pslot[n]) * a.rows + row) = h;
-    }
-  }
+  if (warp == 1) tmem_free(tbase, ncols);
 }
 
 // ---------------------------------------------------------------------------
@@ -573,28 +599,67 @@ static int tc_npad_max(int B) {
   return (n + 15) & ~15;
 }
 
-// K splits: about eight 64-column steps per CTA for gate/up (d columns), four
-// for down (f columns), at most eight splits.
-static int tc_split_gu(int d) {
-  const int n = d / kTcBK / 8;
-  return n < 1 ? 1 : (n > kTcMaxSplit ? kTcMaxSplit : n);
+// Clusters of n CTAs of this kernel the device can hold at once (asked once
+// per device, kernel, shared-memory size and n).
+static int tc_max_clusters(const void* kern, size_t smem, int n) {
+  struct Entry {
+    int dev;
+    const void* kern;
+    size_t smem;
+    int n, count;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> seen;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Entry& e : seen)
+    if (e.dev == dev && e.kern == kern && e.smem == smem && e.n == n) return e.count;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = (unsigned)n;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int count = 0;
+  if (cudaOccupancyMaxActiveClusters(&count, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    count = 0;
+  }
+  seen.push_back(Entry{dev, kern, smem, n, count});
+  return count;
 }
-static int tc_split_dn(int f) {
-  const int n = f / kTcBK / 4;
-  return n < 1 ? 1 : (n > kTcMaxSplit ? kTcMaxSplit : n);
+
+// K splits (the cluster size): the largest of 8, 4, 2 for which every tile's
+// cluster is resident at once (no CTA waits for a second wave) and every CTA
+// keeps at least two K steps; else 1.
+static int tc_nsplit(const void* kern, size_t smem, int tiles, int kcols) {
+  const int nkt = kcols / kTcBK;
+  for (int n = kTcMaxSplit; n > 1; n >>= 1)
+    if (n * 2 <= nkt && tiles <= tc_max_clusters(kern, smem, n)) return n;
+  return 1;
+}
+// Pipeline shape within 227 KB of shared memory: the most K steps per copy
+// stage (fewer, wider TMA boxes; at most the row's K steps), then the most
+// stages, then A tiles.
+static bool tc_pick(int bits, int npad, int nkt, int& g, int& stages, int& abufs) {
+  for (int gg : {4, 2, 1})
+    for (int ss : {3, 2})
+      for (int aa : {3, 2})
+        if (gg <= nkt && tc_gemm_smem(bits, npad, gg, ss, aa) <= 227 * 1024) {
+          g = gg;
+          stages = ss;
+          abufs = aa;
+          return true;
+        }
+  return false;
 }
 static size_t tc_up256(size_t n) { return (n + 255) & ~(size_t)255; }
-
-size_t tc_split_part_bytes(int d, int f, int B, int K) {
-  const size_t pc = (size_t)plan_max_pairs(B, K);
-  const size_t pg = (size_t)tc_split_gu(d) * pc * 2 * f, pd = (size_t)tc_split_dn(f) * pc * d;
-  return tc_up256((pg > pd ? pg : pd) * 4);
-}
-constexpr int kTcCntBatch = 256;  // the largest batch of any call
-size_t tc_split_cnt_bytes(int d, int f, int K) {
-  const size_t tiles = (size_t)((d > f ? d : f) + kTcM - 1) / kTcM;
-  return tc_up256(tiles * plan_max_big(kTcCntBatch, K) * 4);
-}
 // Rows of the staged activations: every task's tokens rounded up to 16.
 int tc_act_rows(int B, int K) { return ((plan_max_pairs(B, K) + 15 * plan_max_big(B, K)) + 15) & ~15; }
 size_t tc_act_bytes(int d, int f, int B, int K) {
@@ -622,26 +687,34 @@ static EncodeTiledFn encode_tiled() {
 }
 
 // A 3-D byte view [nexp][rows][row_bytes] of `base` (experts `estride` bytes
-// apart), in boxes of box_bytes x 128 rows x 1 expert.
+// apart), in boxes of box_bytes x box_rows rows x 1 expert.
 static bool make_map(CUtensorMap* m, const void* base, int row_bytes, int rows, int nexp, long long estride,
-                     int box_bytes) {
+                     int box_bytes, int box_rows, bool swizzle = false) {
   const EncodeTiledFn enc = encode_tiled();
   if (!enc || !base || (uintptr_t)base % 16 || row_bytes % 16 || estride % 16 || box_bytes % 16) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)row_bytes, (cuuint64_t)rows, (cuuint64_t)nexp};
   const cuuint64_t strides[2] = {(cuuint64_t)row_bytes, (cuuint64_t)estride};
-  const cuuint32_t box[3] = {(cuuint32_t)box_bytes, (cuuint32_t)kTcM, 1};
+  const cuuint32_t box[3] = {(cuuint32_t)box_bytes, (cuuint32_t)box_rows, 1};
   const cuuint32_t es[3] = {1, 1, 1};
+  // swizzled: the box's 16-byte chunks XOR-permuted over the box width (32, 64 or 128 bytes)
+  CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_NONE;
+  if (swizzle && box_bytes == 128) sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  if (swizzle && box_bytes == 64) sw = CU_TENSOR_MAP_SWIZZLE_64B;
+  if (swizzle && box_bytes == 32) sw = CU_TENSOR_MAP_SWIZZLE_32B;
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Tensor maps of the gate/up (gu) or down matrices of the routed pool and the
-// shared expert. y0 receives each matrix's first row in its map's expert region.
-static bool tc_maps(const ExpertSet& es, bool gu, TcMaps& M, int (&y0)[2][2]) {
+// shared expert, in boxes of g K steps (codes) or sbw bytes (scale/bias)
+// by 64 (gate/up) or 128 (down) rows. y0 receives each matrix's first row in
+// its map's expert region.
+static bool tc_maps(const ExpertSet& es, bool gu, int g, int sbw, TcMaps& M, int (&y0)[2][2]) {
   const int d = es.d, f = es.f, bits = es.bits;
   const int kc = gu ? d : f, rows = gu ? f : d;
-  const int rb = kc * bits / 8, sbb = (kc / kGroup) * 4, qb = kTcBK * bits / 8;
+  const int rb = kc * bits / 8, sbb = (kc / kGroup) * 4, qb = g * kTcBK * bits / 8;
+  const int br = gu ? kTcM / 2 : kTcM;
   const long long mw = (long long)d * f * bits / 32, mg = (long long)d * f / kGroup * 2;
   memset(&M, 0, sizeof(M));
   // the shared expert (or the one explicit expert): each matrix its own view
@@ -650,8 +723,8 @@ static bool tc_maps(const ExpertSet& es, bool gu, TcMaps& M, int (&y0)[2][2]) {
   const void* ss[2] = {gu ? (const void*)es.shared.gate_sb : (const void*)es.shared.down_sb,
                        (const void*)es.shared.up_sb};
   for (int i = 0; i < (gu ? 2 : 1); ++i) {
-    if (!make_map(&M.q[1][i], sq[i], rb, rows, 1, (long long)rb * rows, qb)) return false;
-    if (!make_map(&M.sb[1][i], ss[i], sbb, rows, 1, (long long)sbb * rows, 16)) return false;
+    if (!make_map(&M.q[1][i], sq[i], rb, rows, 1, (long long)rb * rows, qb, br, true)) return false;
+    if (!make_map(&M.sb[1][i], ss[i], sbb, rows, 1, (long long)sbb * rows, sbw, br)) return false;
     y0[1][i] = 0;
   }
   if (!es.pool_q) {  // no routed pool: never used
@@ -669,8 +742,8 @@ static bool tc_maps(const ExpertSet& es, bool gu, TcMaps& M, int (&y0)[2][2]) {
   const int region = gu ? 3 * f : d;
   // nexp: enough experts to cover any index the plan can name (the pool's rows are all in range)
   const int nexp = 1024;
-  if (!make_map(&M.q[0][0], pq, rb, region, nexp, es.q_stride * 4, qb)) return false;
-  if (!make_map(&M.sb[0][0], ps, sbb, region, nexp, es.sb_stride * 2, 16)) return false;
+  if (!make_map(&M.q[0][0], pq, rb, region, nexp, es.q_stride * 4, qb, br, true)) return false;
+  if (!make_map(&M.sb[0][0], ps, sbb, region, nexp, es.sb_stride * 2, sbw, br)) return false;
   M.q[0][1] = M.q[0][0];
   M.sb[0][1] = M.sb[0][0];
   y0[0][0] = 0;
@@ -682,64 +755,75 @@ static bool tc_maps(const ExpertSet& es, bool gu, TcMaps& M, int (&y0)[2][2]) {
 bool tc_layer_ok(const ExpertSet& es) {
   TcMaps M;
   int y0[2][2];
-  return encode_tiled() != nullptr && tc_maps(es, true, M, y0) && tc_maps(es, false, M, y0);
+  return encode_tiled() != nullptr && tc_maps(es, true, 1, 16, M, y0) && tc_maps(es, false, 1, 16, M, y0);
 }
 
 template <int BITS>
 static cudaError_t tc_run(const ExpertSet& es, bool gu, const Plan* plan, int B, int K, const void* src, float* out,
-                          int nslot, Ctrl* ctrl, const TcSplit& sp, cudaStream_t s) {
-  TcMaps M;
+                          int nslot, Ctrl* ctrl, unsigned char* act, cudaStream_t s) {
   TcArgs a{};
-  if (!tc_maps(es, gu, M, a.y0)) return cudaErrorInvalidValue;
   const int nbig_max = plan_max_big(B, K);
   const int npad = tc_npad_max(B);
+  const int kc = gu ? es.d : es.f;
+  if (!tc_pick(BITS, npad, kc / kTcBK, a.g, a.stages, a.abufs)) return cudaErrorInvalidValue;
+  a.sbw = (kc / kGroup) * 4 >= kTcSbBox ? kTcSbBox : 16;  // a box never wider than the row
+  TcMaps M;
+  if (!tc_maps(es, gu, a.g, a.sbw, M, a.y0)) return cudaErrorInvalidValue;
   a.plan = plan;
   a.B = B;
   a.K = K;
   a.rows = gu ? es.f : es.d;
   a.kcols = gu ? es.d : es.f;
-  a.nsplit = gu ? tc_split_gu(es.d) : tc_split_dn(es.f);
   a.rtot = tc_act_rows(B, K);
-  a.act = sp.act;
-  a.act_sh = reinterpret_cast<const int*>(sp.act + tc_up256((size_t)a.rtot * (((es.d > es.f ? es.d : es.f)) / kTcBK) * 128));
+  a.act = act;
+  a.act_sh = reinterpret_cast<const int*>(act + tc_up256((size_t)a.rtot * (((es.d > es.f ? es.d : es.f)) / kTcBK) * 128));
   a.out = out;
   a.nslot = nslot;
   a.ctrl = ctrl;
-  a.part = sp.part;
-  a.cnt = sp.cnt;
   int* act_sh = const_cast<int*>(a.act_sh);
   // stage the activations once
-  dim3 ga(nbig_max, (npad + 7) / 8);
+  dim3 ga(nbig_max, (npad + 7) / 8, (a.kcols + 1023) / 1024);
   if (gu)
-    k_tc_act<BITS, false><<<ga, 256, 0, s>>>(plan, B, K, src, nslot, a.kcols, sp.act, act_sh, a.rtot);
+    k_tc_act<BITS, false><<<ga, 256, 0, s>>>(plan, B, K, src, nslot, a.kcols, act, act_sh, a.rtot);
   else
-    k_tc_act<BITS, true><<<ga, 256, 0, s>>>(plan, B, K, src, nslot, a.kcols, sp.act, act_sh, a.rtot);
+    k_tc_act<BITS, true><<<ga, 256, 0, s>>>(plan, B, K, src, nslot, a.kcols, act, act_sh, a.rtot);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const size_t sm = tc_gemm_smem(gu ? 2 : 1, BITS, npad);
-  void* kern = gu ? (void*)k_tc_gemm<BITS, 2> : (void*)k_tc_gemm<BITS, 1>;
+  const size_t sm = tc_gemm_smem(BITS, npad, a.g, a.stages, a.abufs);
+  void* kern = gu ? (void*)k_tc_gemm<BITS, true> : (void*)k_tc_gemm<BITS, false>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.rows + kTcM - 1) / kTcM * a.nsplit, nbig_max);
-  if (gu)
-    k_tc_gemm<BITS, 2><<<grid, kTcThreads, sm, s>>>(M, a);
-  else
-    k_tc_gemm<BITS, 1><<<grid, kTcThreads, sm, s>>>(M, a);
-  return cudaGetLastError();
+  const int tiles = gu ? (a.rows + kTcM / 2 - 1) / (kTcM / 2) : (a.rows + kTcM - 1) / kTcM;
+  a.nsplit = tc_nsplit(kern, sm, tiles, a.kcols);
+  // one cluster per tile and task: its CTAs are the tile's K splits
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(tiles * a.nsplit, nbig_max);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = sm;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = (unsigned)a.nsplit;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (gu) return cudaLaunchKernelEx(&cfg, k_tc_gemm<BITS, true>, M, a);
+  return cudaLaunchKernelEx(&cfg, k_tc_gemm<BITS, false>, M, a);
 }
 
 cudaError_t launch_gateup_tc(const ExpertSet& es, const Plan* plan, int B, int K, const uint16_t* x, float* H,
-                             int nslot, Ctrl* ctrl, const TcSplit& sp, cudaStream_t s) {
+                             int nslot, Ctrl* ctrl, unsigned char* act, cudaStream_t s) {
   if (B < kBigTok) return cudaSuccess;  // no task can have 16 tokens
-  return es.bits == 4 ? tc_run<4>(es, true, plan, B, K, x, H, nslot, ctrl, sp, s)
-                      : tc_run<2>(es, true, plan, B, K, x, H, nslot, ctrl, sp, s);
+  return es.bits == 4 ? tc_run<4>(es, true, plan, B, K, x, H, nslot, ctrl, act, s)
+                      : tc_run<2>(es, true, plan, B, K, x, H, nslot, ctrl, act, s);
 }
 
 cudaError_t launch_down_tc(const ExpertSet& es, const Plan* plan, int B, int K, const float* H, float* Y, int nslot,
-                           Ctrl* ctrl, const TcSplit& sp, cudaStream_t s) {
+                           Ctrl* ctrl, unsigned char* act, cudaStream_t s) {
   if (B < kBigTok) return cudaSuccess;
-  return es.bits == 4 ? tc_run<4>(es, false, plan, B, K, H, Y, nslot, ctrl, sp, s)
-                      : tc_run<2>(es, false, plan, B, K, H, Y, nslot, ctrl, sp, s);
+  return es.bits == 4 ? tc_run<4>(es, false, plan, B, K, H, Y, nslot, ctrl, act, s)
+                      : tc_run<2>(es, false, plan, B, K, H, Y, nslot, ctrl, act, s);
 }
 
 }  // namespace bgq

@@ -229,7 +229,7 @@ int32_t moe_layer_forward(const bgq_moe_layer* L, const uint16_t* x, int32_t bat
  * not create them).
  * Same arguments, kernels and results as moe_layer_forward; the scratch memory
  * is a 4 MiB array inside the library (held on every GPU that loads the
- * library until the process exits), enough for batch <= 33 at d_model 4096,
+ * library until the process exits), enough for batch <= 31 at d_model 4096,
  * d_ff 1024, 512 experts, top-4. A call whose moe_layer_workspace_bytes(L,
  * batch) exceeds 4 MiB returns BGQ_ERR_WORKSPACE and launches nothing.
  * Every argument check of moe_layer_forward runs first, in the same order,
@@ -239,9 +239,9 @@ int32_t moe_layer_forward(const bgq_moe_layer* L, const uint16_t* x, int32_t bat
  * first call before any stream capture, and do not call this entry point again
  * after cudaDeviceReset in the same process. Each call clears, on `stream`,
  * the leading bytes of the array that the kernels expect at zero (the
- * 256-byte control block, the batch-1 kernel's (n_experts + 1) tagged logit
- * words and the tensor-core split-K tile counters, each rounded up to 256
- * bytes; their sizes depend on the layer's shape, not on the batch), then runs
+ * 256-byte control block and the batch-1 kernel's (n_experts + 1) tagged
+ * logit words, each rounded up to 256 bytes; their sizes depend on the
+ * layer's shape, not on the batch), then runs
  * the layer. Every other region is written before it is read, so calls of
  * different layer shapes may follow each other, and a call that ended in
  * BGQ_ERR_TIMEOUT needs no clean-up before the next one. All calls on a device

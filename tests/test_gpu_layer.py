@@ -140,8 +140,9 @@ def test_layer_batch_equals_single_bitwise(cuda_device, full_layer):
 
 def test_layer_workspace_reused_across_batches(cuda_device, full_layer):
     """One workspace sized for the largest batch serves calls of several batch
-    sizes (the tensor-core path's split-K counters must be zero at every call,
-    whatever the previous call's layout) and gives the bits of a fresh one."""
+    sizes (every region a call reads is written earlier in the same call or
+    left at zero by the previous one, whatever its layout) and gives the bits
+    of a fresh one."""
     shape, L, t = full_layer
     ws = lib.workspace(lib.moe_layer_workspace_bytes(L, 100), cuda_device)
     for B in (100, 64, 1, 100, 64):

@@ -61,16 +61,17 @@ def test_noalloc_rejects_batches_beyond_the_fixed_scratch(cuda_device):
 
 def test_noalloc_alternating_shapes_reach_the_tensor_core_path(cuda_device):
     """The fixed array is shared by calls of every layer shape. The regions
-    that must start at zero (control block, tagged logits, tensor-core split-K
-    counters) sit at shape-dependent places, so one shape's logits can land
-    where another shape keeps its counters. Alternate shapes, including a
-    batch-64 call whose shared expert runs on the tensor cores with split K,
-    and compare every call with moe_layer_forward on a fresh zeroed workspace."""
+    that must start at zero (control block, tagged logits) have
+    shape-dependent sizes, and every other region sits at a shape-dependent
+    place, so one shape's leftovers land in another shape's scratch. Alternate
+    shapes, including batch-64 calls whose shared expert runs on the tensor
+    cores with split K, and compare every call with moe_layer_forward on a
+    fresh zeroed workspace."""
     K = 4
-    full = layer(cuda_device, 512, 4096, 1024, K, seed=13)   # 4 MiB-class call, batch 33
-    tiny = layer(cuda_device, 8, 256, 128, K, seed=14)       # its logits overlap tc's counters
+    full = layer(cuda_device, 512, 4096, 1024, K, seed=13)   # 4 MiB-class call, batch 31
+    tiny = layer(cuda_device, 8, 256, 128, K, seed=14)       # its logits overlap tc's scratch
     tc = layer(cuda_device, 16, 512, 256, K, seed=15)        # batch 64: the tensor-core path
-    seq = [(full, 4096, 33), (tiny, 256, 20), (tc, 512, 64), (tc, 512, 1), (full, 4096, 1), (tc, 512, 64),
+    seq = [(full, 4096, 31), (tiny, 256, 20), (tc, 512, 64), (tc, 512, 1), (full, 4096, 1), (tc, 512, 64),
            (tiny, 256, 3), (tc, 512, 100)]
     for i, (L, d, B) in enumerate(seq):
         x = synth.activations(13, 200 + i, B, d, device=cuda_device)
