@@ -247,6 +247,9 @@ def workload_name(args, bits=None) -> str:
     if args.workload == "expert":
         return (f"moe_expert_swiglu: one SwiGLU expert (gate/up 1024x4096, down 4096x1024), 4-bit, group 64, "
                 f"batch {args.batch}, ring of {args.ring} experts")
+    if args.workload == "chain":
+        return (f"bgq_gemv_chain: rmsnorm (bf16 weight), then 4-bit 4096x4096 projection, then 4-bit 4096x4096 "
+                f"o_proj + residual, group 64, batch {args.batch}, one persistent launch, ring of {args.ring} chains")
     if args.workload == "gemv8":
         return (f"q8_gemv: {args.rows}x{args.cols} 8-bit codes, " +
                 ("one bf16 scale+bias per row" if args.per_row else "group 64 bf16 scale+bias") +
@@ -692,6 +695,57 @@ def run_expert(args):
     return 0
 
 
+def run_chain(args):
+    """bgq_gemv_chain (rmsnorm, a 4096x4096 4-bit projection, a 4096x4096 4-bit
+    o_proj + residual, one persistent launch) per step, cycling through a ring
+    of distinct chains larger than L2."""
+    import torch
+
+    from bit_group_quantized_gb300 import lib, synth
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    lib.load()
+    d, B = 4096, max(1, min(args.batch, 8))
+    mat_bytes = d * d // 2 + d * d // 64 * 4
+    R = args.ring = max(args.ring, -(-400_000_000 // (2 * mat_bytes)))
+    chains, xs, outs = [], [], []
+    for r in range(R):
+        mats = []
+        for i in range(2):
+            q, sb = synth.qmatrix(args.seed + 7 * r + i, d, d, 4, device=dev)
+            mats.append(lib.QMatrix(q, sb, d, d, 4))
+        chains.append(mats)
+        xs.append(synth.activations(args.seed, 2000 + r, B, d, device=dev))
+        outs.append(torch.empty((B, d), dtype=torch.bfloat16, device=dev))
+    rho = synth.rho(args.seed, 0, d, device=dev)
+    ws = lib.workspace(lib.gemv_chain_workspace_bytes(chains[0], B), dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def body():
+        for r in range(R):
+            lib.gemv_chain(chains[r], xs[r], norm=True, rho=rho, residual=True, ws=ws, out=outs[r], stream=stream)
+
+    n_rep = max(1, args.steps // R)
+    clocks = ClockSampler(0)
+    ms = _timed_graph(torch, stream, body, n_rep, args.warmup) / R
+    clock = clocks.stop()
+    nbytes = 2 * mat_bytes + d * 2 + 2 * B * d * 2  # weights, rho, x in, out
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+    print(json.dumps({
+        "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": 1, "steps": n_rep * R,
+        "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u4 codes x s24 fixed-point x (dp4a), f32 accumulate", "data": "synthetic",
+        "config": {"workload": workload_name(args), "us_per_chain": round(ms * 1000, 3), "bytes": nbytes,
+                   "batch": B, "l2": f"ring of {R} chains ({R * 2 * mat_bytes / 1e6:.0f} MB) cycled, larger than L2"},
+        "roofline": {"bound": "hbm", "kernel": "k_gemv_chain (whole chain, one launch)", "achieved": round(gbs, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4), "peak_kind": peak_kind,
+                     "traffic": None},
+        "clocks": clock}), flush=True)
+    return 0
+
+
 def run_gemv8(args):
     """q8_gemv (int8 weights, rows x cols, batch B) per step, cycling through a
     ring of distinct matrices larger than L2 (4 x 129 MB at least)."""
@@ -741,7 +795,8 @@ def main():
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="stack4", choices=["stack4", "stack2", "layer", "expert", "gemv", "gemv8", "host"])
+    ap.add_argument("--workload", default="stack4", choices=["stack4", "stack2", "layer", "expert", "gemv", "gemv8", "host",
+                                                             "chain"])
     ap.add_argument("--variant", type=int, default=0, help="gemv: 0 integer (production), 1 standard, "
                                                             "2 reordered (the page's fma form), 3 hoisted fp32")
     ap.add_argument("--ring", type=int, default=8, help="layer/gemv: distinct weight copies cycled through")
@@ -771,6 +826,8 @@ def main():
         return run_expert(args)
     if args.workload == "host":
         return run_host(args)
+    if args.workload == "chain":
+        return run_chain(args)
     return run_ours(args)
 
 

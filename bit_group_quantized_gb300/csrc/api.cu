@@ -263,7 +263,7 @@ const char* bgq_status_string(int32_t s) {
   }
 }
 
-int32_t bgq_abi_version(void) { return 101; }
+int32_t bgq_abi_version(void) { return 102; }
 
 static int32_t gemv_common(const bgq_qmatrix* W, const uint16_t* x, uint16_t* y, int32_t batch, int32_t variant,
                            int want_bits, void* stream) {
@@ -483,6 +483,58 @@ int32_t bgq_residual_add(float* h, const float* delta, int64_t n, void* stream) 
   if (!h || !delta || n < 0) return BGQ_ERR_INVALID_ARG;
   if (n == 0) return BGQ_OK;
   return cuda_status(launch_residual_add(h, delta, n, st(stream)));
+}
+
+static int chain_check(const bgq_qmatrix* W, int32_t n, int32_t batch) {
+  if (!W || n < 1 || n > kMaxChain) return BGQ_ERR_INVALID_ARG;
+  if (batch < 1 || batch > 8) return BGQ_ERR_INVALID_ARG;
+  int max_cols = 0;
+  for (int i = 0; i < n; ++i) {
+    int r = check_qmatrix(&W[i]);
+    if (r) return r;
+    if (W[i].bits != W[0].bits) return BGQ_ERR_INVALID_ARG;
+    if (i > 0 && W[i].cols != W[i - 1].rows) return BGQ_ERR_INVALID_ARG;
+    if (W[i].cols > max_cols) max_cols = W[i].cols;
+  }
+  if (chain_smem_bytes(max_cols, W[0].bits, batch) > (size_t)227 * 1024) return BGQ_ERR_UNSUPPORTED;
+  return BGQ_OK;
+}
+// Row stride of the inner steps' outputs: the widest, a multiple of 8 (16-byte rows).
+static int chain_ldb(const bgq_qmatrix* W, int32_t n) {
+  int m = 8;
+  for (int i = 0; i + 1 < n; ++i)
+    if (W[i].rows > m) m = W[i].rows;
+  return (m + 7) & ~7;
+}
+
+size_t bgq_gemv_chain_workspace_bytes(const bgq_qmatrix* W, int32_t n, int32_t batch) {
+  if (chain_check(W, n, batch)) return 0;
+  return sizeof(Ctrl) + 256 + 2 * up256((size_t)batch * chain_ldb(W, n) * 2);
+}
+
+int32_t bgq_gemv_chain(const bgq_qmatrix* W, int32_t n, const uint16_t* x, int32_t batch, int32_t norm,
+                       const uint16_t* rho, float eps, int32_t residual, uint16_t* out, float* out_f32, void* ws,
+                       size_t ws_bytes, void* stream) {
+  int r = chain_check(W, n, batch);
+  if (r) return r;
+  if (!x || !al(x, 16) || (!out && !out_f32) || (out && !al(out, 16)) || (out_f32 && !al(out_f32, 16)))
+    return BGQ_ERR_INVALID_ARG;
+  if (norm && !(eps > 0.f && eps < 1e30f)) return BGQ_ERR_INVALID_ARG;
+  if (residual && W[n - 1].rows != W[0].cols) return BGQ_ERR_INVALID_ARG;
+  if (!ws || !al(ws, 256) || ws_bytes < bgq_gemv_chain_workspace_bytes(W, n, batch)) return BGQ_ERR_WORKSPACE;
+  Carver c(ws);
+  Ctrl* ctrl = c.take<Ctrl>(sizeof(Ctrl));
+  int* counter = c.take<int>(256);
+  const int ldb = chain_ldb(W, n);
+  uint16_t* b0 = c.take<uint16_t>((size_t)batch * ldb * 2);
+  uint16_t* b1 = c.take<uint16_t>((size_t)batch * ldb * 2);
+  ChainStep steps[kMaxChain];
+  for (int i = 0; i < n; ++i)
+    steps[i] = ChainStep{W[i].q, reinterpret_cast<const uint32_t*>(W[i].sb), W[i].rows, W[i].cols};
+  cudaStream_t s = st(stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(Ctrl) + 256, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  return cuda_status(launch_chain(steps, n, W[0].bits, x, batch, norm ? 1 : 0, norm ? rho : nullptr, eps,
+                                  residual ? 1 : 0, out, out_f32, ctrl, counter, b0, b1, ldb, 1000000000ll, s));
 }
 
 size_t moe_stack_workspace_bytes(const bgq_moe_layer* layers, int32_t n_layers) {

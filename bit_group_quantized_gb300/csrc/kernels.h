@@ -106,7 +106,7 @@ cudaError_t launch_qgemv(const QMat& W, const uint16_t* x, int batch, uint16_t* 
                          cudaStream_t s);
 
 // Bytes at the start of a layer workspace that must be zero before a call:
-// control block, tagged logits and split-K counters (api.cu).
+// control block and tagged logits (api.cu).
 size_t layer_zero_prefix_bytes(const bgq_moe_layer* L);
 // moe_layer_forward's argument checks, split around its workspace check
 // (api.cu): BGQ_OK or the status moe_layer_forward returns for the same
@@ -192,5 +192,20 @@ cudaError_t launch_slot_copy(Plan* plan, int E, const ExpertSet& pool, const Slo
 ExpertSet slot_expert_set(const ExpertSet& pool, const SlotGeo& g, void* slots);
 
 int num_sms();
+
+// A chain of dependent group-quantized GEMVs in one persistent launch (chain.cu).
+constexpr int kMaxChain = 8;
+struct ChainStep {
+  const uint32_t* q;
+  const uint32_t* sb;  // (scale, bias) bf16 pairs, one 32-bit word per group
+  int rows, cols;
+};
+size_t chain_smem_bytes(int max_cols, int bits, int T);
+// steps[0..n), all of `bits`; x bf16 [batch][steps[0].cols], batch 1..8;
+// buf0/buf1 bf16 [batch][ldb] (ldb >= the rows of every inner step); *counter
+// zero at launch.
+cudaError_t launch_chain(const ChainStep* steps, int n, int bits, const uint16_t* x, int batch, int norm,
+                         const uint16_t* rho, float eps, int residual, uint16_t* out, float* out_f32, Ctrl* ctrl,
+                         int* counter, uint16_t* buf0, uint16_t* buf1, int ldb, long long timeout_ns, cudaStream_t s);
 
 }  // namespace bgq

@@ -68,6 +68,8 @@ _SIGS = {
                                         _P]),
     "bgq_rmsnorm": (_I, [_P, _P, _I, _I, C.c_float, _P, _P]),
     "bgq_residual_add": (_I, [_P, _P, C.c_int64, _P]),
+    "bgq_gemv_chain_workspace_bytes": (_S, [C.POINTER(bgq_qmatrix), _I, _I]),
+    "bgq_gemv_chain": (_I, [C.POINTER(bgq_qmatrix), _I, _P, _I, _I, _P, C.c_float, _I, _P, _P, _P, _S, _P]),
     "moe_stack_workspace_bytes": (_S, [C.POINTER(bgq_moe_layer), _I]),
     "moe_stack_decode": (_I, [C.POINTER(bgq_moe_layer), C.POINTER(_P), _I, C.c_float, _P, _P, _P, _P, _P, _S,
                               _P]),
@@ -338,6 +340,38 @@ def bgq_rmsnorm(h: torch.Tensor, rho, eps: float, a=None, stream=None):
 def bgq_residual_add(h: torch.Tensor, delta: torch.Tensor, stream=None):
     _check(load().bgq_residual_add(_ptr(h), _ptr(delta), h.numel(), _stream(stream)), "bgq_residual_add")
     return h
+
+
+def _chain_structs(mats: list):
+    arr = (bgq_qmatrix * len(mats))()
+    for i, m in enumerate(mats):
+        arr[i] = m.struct()
+    return arr
+
+
+def gemv_chain_workspace_bytes(mats: list, batch: int) -> int:
+    return load().bgq_gemv_chain_workspace_bytes(_chain_structs(mats), len(mats), batch)
+
+
+def gemv_chain(mats: list, x: torch.Tensor, norm: bool = False, rho=None, eps: float = 1e-6, residual: bool = False,
+               want_out: bool = True, want_f32: bool = False, ws=None, out=None, out_f32=None, stream=None):
+    """bgq_gemv_chain: v_0 = rmsnorm(x)*rho (norm) or x, v_i = bf16(W_i v_{i-1}), out = W_n v (+ x).
+
+    Returns (out bf16 or None, out_f32 or None), each [batch][mats[-1].rows]."""
+    lib = load()
+    arr = _chain_structs(mats)
+    x2 = x.reshape(-1, mats[0].cols)
+    B = x2.shape[0]
+    rows = mats[-1].rows
+    if want_out and out is None:
+        out = alloc((B, rows), torch.bfloat16, x.device)
+    if want_f32 and out_f32 is None:
+        out_f32 = alloc((B, rows), torch.float32, x.device)
+    if ws is None:
+        ws = workspace(lib.bgq_gemv_chain_workspace_bytes(arr, len(mats), B), x.device)
+    _check(lib.bgq_gemv_chain(arr, len(mats), _ptr(x2), B, int(norm), _ptr(rho), eps, int(residual), _ptr(out),
+                              _ptr(out_f32), _ptr(ws), ws.numel(), _stream(stream)), "bgq_gemv_chain")
+    return out, out_f32
 
 
 class Stack:

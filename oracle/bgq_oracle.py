@@ -30,7 +30,8 @@ index wins ties, a sigmoid-gated shared expert, RMSNorm before each layer).
 Readings of silent points are marked READING.
 
 Parity status: every function below is pinned by ``tests/test_oracle_pins.py``
-(hand-computed cases, closed forms, library special cases, invariants).
+(hand-computed cases, closed forms, library special cases, invariants);
+``gemv_chain`` composes pinned steps and is pinned on its own there too.
 """
 
 from __future__ import annotations
@@ -257,3 +258,30 @@ def stack_token(layers, x0_bits, bits: int, top_k: int, eps: float = 1e-6, force
         all_idx.append(idx)
     x_next = f64_to_bf16_bits(rmsnorm(h, None, eps))
     return x_next, h, all_idx
+
+
+# --------------------------------------------------------- projection chain
+def gemv_chain(mats, bits: int, x_bits, norm: bool = False, rho_bits=None, eps: float = 1e-6,
+               residual: bool = False) -> np.ndarray:
+    """The decoder's projections around the MoE block as a chain of GEMVs.
+
+    [FM] "架构设计：SSD当显存用": each layer runs the attention input
+    projections (CMD1) and o_proj + norm (CMD2) on the GPU. READING: the
+    attention mixing between them is not part of this workload, so the chain
+    feeds each projection's output to the next one:
+        v_0 = bf16(rmsnorm(x) * rho) if norm else x
+        v_i = bf16(W_i v_{i-1}),  i = 1..n-1
+        out = W_n v_{n-1} (+ x if residual)      (float64, before rounding)
+    The bf16 roundings of the inner vectors follow the standalone GEMV, whose
+    output is bf16. mats: [(q_words, sb)], x_bits: bf16 [cols] or [batch][cols].
+    """
+    x = bf16_to_f64(np.asarray(_np(x_bits)))
+    v = x
+    if norm:
+        v = np.stack([round_bf16(rmsnorm(row, rho_bits, eps)) for row in np.atleast_2d(x)])
+        v = v.reshape(x.shape)
+    n = len(mats)
+    for i, (q, sb) in enumerate(mats):
+        y = gemv(np.asarray(_np(q)), np.asarray(_np(sb)), bits, v)
+        v = y if i == n - 1 else round_bf16(y)
+    return x + v if residual else v

@@ -72,7 +72,7 @@ def test_q8_gemv_validation(lib):
 def test_status_strings(lib):
     assert lib.status_string(0) == "ok"
     assert "workspace" in lib.status_string(5)
-    assert lib.load().bgq_abi_version() == 101
+    assert lib.load().bgq_abi_version() == 102
 
 
 FAKE = 0x10000000  # 256-byte aligned, never dereferenced: validation fails first
@@ -231,3 +231,46 @@ def test_noalloc_rejects_what_the_workspace_entry_point_rejects(lib):
     assert L.moe_layer_workspace_bytes(C.byref(Ls), 36) > (4 << 20)
     assert L.moe_layer_forward_noalloc(C.byref(Ls), FAKE, 36, FAKE, None, None, None, None, None) == \
         lib.ERR_WORKSPACE
+
+
+def test_gemv_chain_validation(lib):
+    L = lib.load()
+
+    def chain(*mats):
+        arr = (lib.bgq_qmatrix * len(mats))()
+        for i, m in enumerate(mats):
+            arr[i] = m
+        return arr
+
+    good = chain(qmat(lib, rows=4096, cols=4096), qmat(lib, rows=4096, cols=4096))
+    ws_bytes = L.bgq_gemv_chain_workspace_bytes(good, 2, 1)
+    assert ws_bytes >= 512 + 2 * 4096 * 2
+
+    def call(W, n, x=FAKE, batch=1, norm=1, eps=1e-6, residual=1, out=FAKE, out_f32=None, ws=FAKE, nbytes=ws_bytes):
+        return L.bgq_gemv_chain(W, n, x, batch, norm, None, eps, residual, out, out_f32, ws, nbytes, None)
+
+    assert call(None, 2) == lib.ERR_INVALID_ARG
+    assert call(good, 0) == lib.ERR_INVALID_ARG
+    assert call(good, 9) == lib.ERR_INVALID_ARG
+    assert call(good, 2, x=None) == lib.ERR_INVALID_ARG
+    assert call(good, 2, x=FAKE + 2) == lib.ERR_INVALID_ARG  # misaligned x
+    assert call(good, 2, out=None) == lib.ERR_INVALID_ARG  # no output at all
+    assert call(good, 2, batch=0) == lib.ERR_INVALID_ARG
+    assert call(good, 2, batch=9) == lib.ERR_INVALID_ARG
+    assert call(good, 2, eps=0.0) == lib.ERR_INVALID_ARG  # norm needs eps > 0
+    assert call(good, 2, ws=None) == lib.ERR_WORKSPACE
+    assert call(good, 2, nbytes=ws_bytes - 1) == lib.ERR_WORKSPACE
+    # each step's columns are the previous step's rows
+    bad = chain(qmat(lib, rows=4096, cols=4096), qmat(lib, rows=4096, cols=2048))
+    assert call(bad, 2) == lib.ERR_INVALID_ARG
+    assert L.bgq_gemv_chain_workspace_bytes(bad, 2, 1) == 0
+    # mixed bits
+    assert call(chain(qmat(lib, rows=4096, cols=4096), qmat(lib, rows=4096, cols=4096, bits=2)), 2) == \
+        lib.ERR_INVALID_ARG
+    # residual needs the last step back at d rows
+    wide = chain(qmat(lib, rows=2048, cols=4096))
+    assert call(wide, 1, nbytes=L.bgq_gemv_chain_workspace_bytes(wide, 1, 1)) == lib.ERR_INVALID_ARG
+    # eight staged inputs of 12288 columns do not fit in shared memory; two do
+    qkv = chain(qmat(lib, rows=12288, cols=4096), qmat(lib, rows=4096, cols=12288))
+    assert call(qkv, 2, batch=8, nbytes=1 << 30) == lib.ERR_UNSUPPORTED
+    assert L.bgq_gemv_chain_workspace_bytes(qkv, 2, 2) > 0

@@ -686,3 +686,60 @@ def test_planted_bf16_truncation_is_caught(monkeypatch):
 
     monkeypatch.setattr(O, "f64_to_bf16_bits", trunc)
     _raises(check_bf16_rounding)
+
+
+# ------------------------------------------------ the projection chain
+def uniform_matrix(rows, cols, code, scale, bias, bits=4):
+    """Every code `code`; group g's (scale, bias) = (scale[g], bias[g]) (scalars broadcast)."""
+    q = pack_rows([[code] * cols for _ in range(rows)], bits)
+    ng = cols // 64
+    s = np.broadcast_to(np.asarray(scale, dtype=np.float64), (ng,))
+    b = np.broadcast_to(np.asarray(bias, dtype=np.float64), (ng,))
+    sb = np.stack([bf16_bits(s), bf16_bits(b)], axis=-1)  # [ng][2]
+    return q, np.broadcast_to(sb, (rows, ng, 2)).copy()
+
+
+def check_chain_closed_forms():
+    rng = np.random.default_rng(5)
+    # one step, no norm, no residual: the GEMV itself
+    q = pack_rows(rng.integers(0, 16, size=(24, 128)), 4)
+    sb = bf16_bits(rng.normal(0, 0.05, size=(24, 2, 2)))
+    xb = bf16_bits(rng.normal(0, 1, size=(3, 128)))
+    assert np.array_equal(O.gemv_chain([(q, sb)], 4, xb), O.gemv(q, sb, 4, O.bf16_to_f64(xb)))
+    # the inner vector is rounded to bf16: step 1 gives 64/64 + 64 * 2^-16 = 1 + 2^-10 per row,
+    # whose bf16 is 1, so the all-ones step 2 sums 64 ones (64.0625 unrounded)
+    W1 = uniform_matrix(64, 128, 0, 0.0, [1.0 / 64, 2.0 ** -16])
+    W2 = uniform_matrix(8, 64, 1, 1.0, 0.0)
+    ones = bf16_bits(np.ones(128))
+    assert np.array_equal(O.gemv_chain([W1], 4, ones), np.full(64, 1 + 2.0 ** -10))
+    assert np.array_equal(O.gemv_chain([W1, W2], 4, ones), np.full(8, 64.0))
+    # the norm: a constant 3 normalises to bf16(3 / sqrt(9 + eps)) = 1 (0.5 with rho = 0.5)
+    threes = bf16_bits(np.full((2, 64), 3.0))
+    Wsum = uniform_matrix(64, 64, 1, 1.0, 0.0)
+    assert np.array_equal(O.gemv_chain([Wsum], 4, threes, norm=True), np.full((2, 64), 64.0))
+    half = bf16_bits(np.full(64, 0.5))
+    assert np.array_equal(O.gemv_chain([Wsum], 4, threes, norm=True, rho_bits=half), np.full((2, 64), 32.0))
+    # the residual adds x itself (not the normalised input)
+    assert np.array_equal(O.gemv_chain([Wsum], 4, threes, norm=True, residual=True), np.full((2, 64), 67.0))
+    # zero weights: the residual chain returns x
+    Wz = uniform_matrix(64, 64, 5, 0.0, 0.0)
+    xr = bf16_bits(rng.normal(0, 1, size=(2, 64)))
+    assert np.array_equal(O.gemv_chain([Wz, Wz], 4, xr, residual=True), O.bf16_to_f64(xr))
+    # 2-bit codes: all code 3 with scale 1 over 128 ones sums to 384
+    W2b = uniform_matrix(4, 128, 3, 1.0, 0.0, bits=2)
+    assert np.array_equal(O.gemv_chain([W2b], 2, ones), np.full(4, 384.0))
+
+
+def test_chain_closed_forms():
+    check_chain_closed_forms()
+
+
+def test_planted_unrounded_chain_vector_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "round_bf16", lambda v: np.asarray(v, dtype=np.float64))
+    _raises(check_chain_closed_forms)
+
+
+def test_planted_chain_norm_without_rho_is_caught(monkeypatch):
+    good = O.rmsnorm
+    monkeypatch.setattr(O, "rmsnorm", lambda h, rho, eps=1e-6: good(h, None, eps))
+    _raises(check_chain_closed_forms)
