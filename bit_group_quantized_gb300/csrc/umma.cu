@@ -434,9 +434,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
       const CUtensorMap* ms0 = sh ? &maps.sb[1][0] : &maps.sb[0][0];
       const CUtensorMap* ms1 = sh ? &maps.sb[1][1] : &maps.sb[0][1];
       const int y00 = sh ? a.y0[1][0] : a.y0[0][0], y01 = sh ? a.y0[1][1] : a.y0[0][1];
-      for (int u = 0; u < nst; ++u) {
-        const int s = u % S, kb = kb0 + u * G, gs = min(G, nk - u * G);
-        if (u >= S && !tc_mbar_wait(&empty[s], (uint32_t)((u / S - 1) & 1), kTcTimeoutNs)) {
+      // stage s = u % S and the parity of its previous use, kept incrementally
+      // (no integer division in the per-step loops)
+      int s = 0;
+      uint32_t epar = 1;
+      for (int u = 0, kb = kb0; u < nst; ++u, kb += G) {
+        const int gs = min(G, nk - u * G);
+        if (u >= S && !tc_mbar_wait(&empty[s], epar, kTcTimeoutNs)) {
           *s_fail = 1;
           break;
         }
@@ -457,6 +461,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
         for (int t = 0; t < gs; ++t)
           tc_bulk(st + o_act + t * npad * 128, a.act + ((size_t)(kb + t) * a.rtot + bt.pad) * 128,
                   (uint32_t)npad * 128, &full[s]);
+        if (++s == S) {
+          s = 0;
+          epar ^= 1;
+        }
       }
     }
   } else if (warp == 1) {
@@ -467,10 +475,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
     const uint32_t tbase = *tslot;
     if (lane == 0) {
       const uint32_t idesc = tc_idesc(npad);
+      int t = 0, s = 0, b = 0;  // step in stage, stage, A tile
+      uint32_t fpar = 0, apar = 0;
       for (int j = 0; j < nk; ++j) {
-        const int u = j / G, t = j - u * G, s = u % S, b = j % nA;
-        if (!tc_mbar_wait(&aready[b], (uint32_t)((j / nA) & 1), kTcTimeoutNs) ||
-            !tc_mbar_wait(&full[s], (uint32_t)((u / S) & 1), kTcTimeoutNs)) {
+        if (!tc_mbar_wait(&aready[b], apar, kTcTimeoutNs) || !tc_mbar_wait(&full[s], fpar, kTcTimeoutNs)) {
           *s_fail = 1;
           break;
         }
@@ -482,6 +490,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
           tc_mma(tbase, tc_desc(at + kk * 256), tc_desc(bs + kk * 256), idesc, (j | kk) ? 1u : 0u);
         tc_commit(&afree[b]);
         if (t == G - 1 || j == nk - 1) tc_commit(&empty[s]);
+        if (++b == nA) {
+          b = 0;
+          apar ^= 1;
+        }
+        if (++t == G) {
+          t = 0;
+          if (++s == S) {
+            s = 0;
+            fpar ^= 1;
+          }
+        }
       }
       tc_commit(mdone);  // tracks every MMA this thread issued
     }
@@ -490,19 +509,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
     const int e = tid - 64, rr = ((e >> 5) << 3) | (lane & 7), qt = lane >> 3;
     // the codes arrive swizzled (16-byte chunk c of row r at c ^ ((r*cb/128) % (cb/16)), cb >= 32)
     const int swz = cb >= 32 ? ((rr * cb) >> 7) & (cb / 16 - 1) : 0;
-    for (int j = 0; j < nk; ++j) {
-      const int u = j / G, t = j - u * G, s = u % S, b = j % nA, kb = kb0 + j;
-      // lane 0 waits for the stage and the A tile, the warp follows
+    int t = 0, s = 0, b = 0, ks = kb0 & ~3;  // step in stage, stage, A tile, the stage's first sb group
+    uint32_t fpar = 0, apar = 0;
+    for (int j = 0, kb = kb0; j < nk; ++j, ++kb) {
+      // lane 0 waits for the stage and the A tile (freed by the MMAs of step j - nA), the warp follows
       int okw = 1;
       if (lane == 0)
-        okw = tc_mbar_wait(&full[s], (uint32_t)((u / S) & 1), kTcTimeoutNs) &&
-              (j < nA || tc_mbar_wait(&afree[b], (uint32_t)((j / nA - 1) & 1), kTcTimeoutNs));
+        okw = tc_mbar_wait(&full[s], fpar, kTcTimeoutNs) && (j < nA || tc_mbar_wait(&afree[b], apar ^ 1u, kTcTimeoutNs));
       if (!__shfl_sync(0xffffffffu, okw, 0)) {
         *s_fail = 1;
         break;
       }
       const unsigned char* st = stages + s * stage_bytes;
-      const int ks = (kb0 + u * G) & ~3;  // first group of the stage's scale/bias box
       const uint32_t sbw = *reinterpret_cast<const uint32_t*>(st + o_sb + rr * a.sbw + (kb - ks) * 4);
       const int x = t * qb + qt * (qb / 4);  // this quarter's first code byte in the row
       dequant_quarter<BITS>(reinterpret_cast<const uint32_t*>(st + rr * cb + ((((x >> 4) ^ swz) << 4) | (x & 15))), sbw,
@@ -510,6 +528,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
       tc_fence_proxy();  // this thread's tile stores, visible to the tensor core
       __syncwarp();
       if (lane == 0) tc_arrive(&aready[b]);
+      if (++b == nA) {
+        b = 0;
+        apar ^= 1;
+      }
+      if (++t == G) {
+        t = 0;
+        ks = (kb + 1) & ~3;
+        if (++s == S) {
+          s = 0;
+          fpar ^= 1;
+        }
+      }
     }
   }
   // every MMA has completed before tensor memory is read (bounded)
