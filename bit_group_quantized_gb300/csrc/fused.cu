@@ -819,32 +819,68 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
       }
     }
     stamp<TRACE>(P, l, 3);
-    // the layer input as 24-bit fixed point for the gate/up rows
+    // the layer input as 24-bit fixed point for the gate/up rows (its closing
+    // barrier also orders the reset of the failure flag before the logits poll)
+    if (tid == 0) misc[kFail] = 0;
     stage_x24<BITS>(StridedSrc<uint16_t>{a_s, d}, 1, d, sta);
     stamp<TRACE>(P, l, 12);
 
     // ---------------- S: selection from the complete logits (every CTA)
+    constexpr int kSelMaxK = 8;  // the largest top_k the kernel takes
+    // Thread tid polls the tagged words of rows tid, tid + 512 (, tid + 1024)
+    // and keeps the logits in registers as order-preserving keys; every warp
+    // selects its own top K (larger key first, lower index on equal keys) and
+    // warp 0 merges the warps' candidates the same way: the top K of the
+    // union lie among every part's top K, so set and order equal a selection
+    // over all logits at once (the router kernel's block_topk).
     {
-      float* lg_s = reinterpret_cast<float*>(S.B);  // the router rows are done; phase B's copies follow
-      const unsigned tag = (unsigned)l + 1u;        // the words are zero when a launch starts
+      int* ck = reinterpret_cast<int*>(S.B);  // [16][K] candidate keys (the router rows are done;
+      int* ci = ck + kFWarps * kSelMaxK;      // [16][K] their rows       phase B's copies follow)
+      const unsigned tag = (unsigned)l + 1u;  // the words are zero when a launch starts
       const int nrows = E + (has_gate ? 1 : 0);
-      if (tid == 0) misc[kFail] = 0;
-      __syncthreads();
-      for (int e = tid; e < nrows; e += kFThreads) {
+      int key[3];
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        const int row = tid + j * kFThreads;
+        key[j] = INT_MIN;
+        if (row >= nrows) continue;
         unsigned long long v;
         unsigned long long t0 = 0;
-        for (int it = 1; (unsigned)((v = ld_relaxed_u64(P.ltag + e)) >> 32) != tag; ++it) {
+        bool ok = true;
+        for (int it = 1; (unsigned)((v = ld_relaxed_u64(P.ltag + row)) >> 32) != tag; ++it) {
           if ((it & 31) == 0) {
             const unsigned long long t = globaltimer();
             if (t0 == 0) t0 = t;
             if (aborted(ctrl) || (long long)(t - t0) > P.timeout_ns || it > (int)kMaxSpin) {
               if (!aborted(ctrl)) raise_timeout(ctrl);
               misc[kFail] = 1;
+              ok = false;
               break;
             }
           }
         }
-        lg_s[e] = __uint_as_float((unsigned)v);
+        if (!ok) break;
+        const float f = __uint_as_float((unsigned)v);
+        if (row < E)
+          key[j] = fkey(f);
+        else
+          miscf[kL + K] = f;  // the shared-gate logit
+      }
+#pragma unroll 1
+      for (int k = 0; k < K; ++k) {
+        const int m = redux_max(max(key[0], max(key[1], key[2])));
+        int li = INT_MAX;
+#pragma unroll
+        for (int j = 2; j >= 0; --j)
+          if (key[j] == m) li = tid + j * kFThreads;
+        const int bi = redux_min(li);
+#pragma unroll
+        for (int j = 0; j < 3; ++j)
+          if (tid + j * kFThreads == bi) key[j] = INT_MIN;
+        if (lane == 0) {
+          ck[warp * K + k] = m;
+          ci[warp * K + k] = m == INT_MIN ? INT_MAX : bi;
+        }
       }
       __syncthreads();
       if (misc[kFail]) {
@@ -852,8 +888,39 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
         return;
       }
       stamp<TRACE>(P, l, 5);
-      block_topk_select(lg_s, reinterpret_cast<int*>(lg_s + ((E + 4) & ~3)), E, K, has_gate, misc + kIdx,
-                        miscf + kL);
+      if (warp == 0) {
+        const int n = kFWarps * K;  // <= 128: four per lane
+        int kk[4], ii[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int c = lane + 32 * j;
+          kk[j] = c < n ? ck[c] : INT_MIN;
+          ii[j] = c < n ? ci[c] : INT_MAX;
+        }
+        int sel = 0, selk = INT_MIN;
+#pragma unroll 1
+        for (int k = 0; k < K; ++k) {
+          const int m = redux_max(max(max(kk[0], kk[1]), max(kk[2], kk[3])));
+          int li = INT_MAX;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (kk[j] == m) li = min(li, ii[j]);
+          const int bi = redux_min(li);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (ii[j] == bi) kk[j] = INT_MIN;
+          if (lane == k) {
+            sel = bi;
+            selk = m;
+          }
+        }
+        if (lane < K) {
+          misc[kIdx + lane] = sel;
+          miscf[kL + lane] = __int_as_float(selk >= 0 ? selk : selk ^ 0x7fffffff);  // the key's logit
+        }
+        if (lane == 0 && !has_gate) miscf[kL + K] = 0.f;
+      }
+      __syncthreads();
       stamp<TRACE>(P, l, 11);
     }
 
