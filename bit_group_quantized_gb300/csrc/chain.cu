@@ -78,7 +78,7 @@ struct NormSrc {
 
 // Input of the later steps: the previous step's outputs, written by other
 // CTAs, read through L2 only (never from a stale L1 line).
-struct L2Src {
+struct ChainL2Src {
   const uint16_t* x;
   int ld;
   __device__ void load8(int t, int k0, float* v) const {
@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(kChThreads, 1) k_gemv_chain(const __grid_const
       else
         stage_x24<BITS>(StridedSrc<uint16_t>{P.x, d}, T, d, st);
     } else {
-      stage_x24<BITS>(L2Src{P.buf[(k - 1) & 1], P.ldb}, T, W.cols, st);
+      stage_x24<BITS>(ChainL2Src{P.buf[(k - 1) & 1], P.ldb}, T, W.cols, st);
     }
     const bool last = k == P.n - 1;
     const int units = (W.rows + rg.RPP - 1) / rg.RPP;

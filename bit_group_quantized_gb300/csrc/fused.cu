@@ -767,12 +767,16 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
         }
       }
       ss = warp_sum(ss);
-      if (lane == 0) miscf[kRed + warp] = ss;
-      __syncthreads();
-      if (tid == 0) {
-        float s = 0.f;
-        for (int w = 0; w < (l == 0 ? kFWarps : 1); ++w) s += miscf[kRed + w];
-        miscf[kR] = 1.f / sqrtf(s / (float)d + P.eps);
+      if (l == 0) {  // every warp summed part of the input
+        if (lane == 0) miscf[kRed + warp] = ss;
+        __syncthreads();
+        if (tid == 0) {
+          float s = 0.f;
+          for (int w = 0; w < kFWarps; ++w) s += miscf[kRed + w];
+          miscf[kR] = 1.f / sqrtf(s / (float)d + P.eps);
+        }
+      } else if (tid == 0) {  // warp 0 alone summed the previous layer's per-CTA sums
+        miscf[kR] = 1.f / sqrtf(ss / (float)d + P.eps);
       }
       __syncthreads();
       const float r = miscf[kR];
