@@ -33,7 +33,9 @@
 // split order (deterministic). Every mbarrier wait is bounded (on expiry:
 // BGQ_ERR_TIMEOUT in the status word, a bounded wait for the copies in
 // flight, tensor memory freed, return); the cluster barriers are taken by
-// every thread of every CTA on every path.
+// every thread of every CTA on every path. The swizzled copies assume a
+// 1024-byte aligned dynamic shared-memory base; a launch that does not get
+// one writes BGQ_ERR_CUDA to the status word and computes nothing.
 #include <cuda.h>
 
 #include <mutex>

@@ -201,7 +201,13 @@ int32_t moe_route_topk(const uint16_t* router, const uint16_t* shared_gate, cons
  *   h = silu(gate x) * (up x) (fp32, never rounded), y = down h.
  * x: bf16 [batch][d_model]; y (nullable): bf16 [batch][d_model];
  * y_f32 (nullable): fp32 [batch][d_model]. 1 <= batch <= 256.
- * ws: moe_expert_workspace_bytes(e, batch) bytes. */
+ * ws: moe_expert_workspace_bytes(e, batch) bytes.
+ * Paths: batch < 16 runs the integer group dot products (exact sums of the
+ * 24-bit fixed-point inputs); batch >= 16 (device-resident weights whose rows
+ * are 16-byte aligned) the tensor cores, with weights dequantised to fp16
+ * and each token scaled by a power of two into fp16's range (relative error
+ * about 5e-4 beyond the bf16 output rounding). Either path is deterministic;
+ * the two do not give the same bits. */
 size_t moe_expert_workspace_bytes(const bgq_expert* e, int32_t batch);
 int32_t moe_expert_swiglu(const bgq_expert* e, const uint16_t* x, int32_t batch,
                           uint16_t* y, float* y_f32, void* ws, size_t ws_bytes, void* stream);
@@ -210,7 +216,11 @@ int32_t moe_expert_swiglu(const bgq_expert* e, const uint16_t* x, int32_t batch,
  *   out[b] = sum_k w[b][k] * expert_{idx[b][k]}(x[b]) + gamma[b] * shared(x[b]),
  * summed in fp32 in the order k = 0..top_k-1, then the shared expert.
  * For batch > 1 the (token, expert) pairs are grouped by expert so each expert's
- * weights are read once per call.
+ * weights are read once per call; an expert (the shared one included) that
+ * receives 32 or more tokens in a call runs on the tensor cores (see
+ * moe_expert_swiglu), the others on the integer group dot products. A
+ * token's result does not depend on the other tokens of the batch as long as
+ * its experts stay on the same path.
  * x: bf16 [batch][d_model]. out (nullable): bf16 [batch][d_model].
  * out_f32 (nullable): fp32 [batch][d_model] (unrounded). idx_out (nullable):
  * int32 [batch][top_k]. w_out (nullable): fp32 [batch][top_k].
