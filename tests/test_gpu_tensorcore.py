@@ -15,7 +15,12 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("d,f,bits,B", [(4096, 1024, 4, 16), (4096, 1024, 4, 64), (1024, 512, 4, 37),
-                                        (2048, 1024, 2, 24), (512, 256, 4, 130)])
+                                        (2048, 1024, 2, 24), (512, 256, 4, 130),
+                                        # 256 tokens: four 64-column epilogue passes, each between cluster barriers
+                                        (1024, 512, 4, 256), (1024, 512, 2, 200),
+                                        # 3072 x 512: six gate/up K steps per CTA (a copy stage of four,
+                                        # then one of two), two down steps per CTA
+                                        (3072, 512, 4, 48)])
 def test_expert_tensorcore_matches_oracle(cuda_device, d, f, bits, B):
     shape = synth.PoolShape(d, f, 1, bits)
     q, sb = synth.expert_pool_range(91, 0, shape, 0, 1, device=cuda_device)
