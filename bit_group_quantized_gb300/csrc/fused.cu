@@ -497,17 +497,17 @@ __device__ void issue_shared(const FusedParams& P, int l, const FSmem& S) {
 
 // Warp 15: issue layer l's phase-B copies into B (gate/up rows of the selected
 // experts), chunk-major so that chunk 0 lands first; one piece per lane.
-__device__ void issue_B(const FusedParams& P, int l, const FSmem& S) {
+__device__ void issue_B(const FusedParams& P, int l, const FSmem& S, int cb0, int cb1) {
   const FGeo& g = P.g;
   const FusedLayer& L = P.layers[l];
   const int f = P.f, lane = threadIdx.x & 31;
-  const int nB = S.misc[kNB], b = S.misc[kBb];
+  const int b = S.misc[kBb];
   const int* s_idx = S.misc + kIdx;
   fence_proxy_async();
 #pragma unroll 1
-  for (int c0 = 0; c0 < nB; c0 += 8) {
+  for (int c0 = cb0; c0 < cb1; c0 += 8) {
     const int c = c0 + (lane >> 2), piece = lane & 3;
-    if (c < nB) {
+    if (c < cb1) {
       const int start = S.misc[kChB + 2 * c], n = S.misc[kChB + 2 * c + 1];
       uint64_t* m = &S.mB[c];
       if (piece == 0) mbar_expect_tx(m, (uint32_t)n * g.unit);
@@ -929,13 +929,15 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
     }
 
     // ---------------- B: the selected experts' gate/up units (in B)
+    // Copied in two waves: the first half of the chunks at once, the second
+    // half after the shared units, so that the first half lands early and
+    // its units are computed while the rest streams in.
+    const int nB1 = (misc[kNB] + 1) / 2;
     if (warp == kFWarps - 1) {
-      issue_B(P, l, S);  // the last warp: its phase-B units (if any) come last
-      if (TRACE && lane == 0 && misc[kNB] > 0) {  // when the first and the last chunk land
+      issue_B(P, l, S, 0, nB1);  // the last warp: its phase-B units (if any) come last
+      if (TRACE && lane == 0 && misc[kNB] > 0) {  // when the first chunk lands
         mbar_wait(&S.mB[0], par, ctrl, P.timeout_ns);
         stamp<TRACE>(P, l, 14);
-        mbar_wait(&S.mB[misc[kNB] - 1], par, ctrl, P.timeout_ns);
-        stamp<TRACE>(P, l, 15);
       }
     }
     if (warp == 0) {  // the routing weights (used by the combine) while the copies start
@@ -954,7 +956,14 @@ __global__ void __launch_bounds__(kFThreads, 1) k_fused_decode(const __grid_cons
                     P.hk + (size_t)K * f + misc[kS1b], kFWarps - 1 - warp, lane);
     __syncthreads();
     stamp<TRACE>(P, l, 4);
-    if (warp == kFWarps - 2) issue_C<BITS>(P, l, S);
+    if (warp == kFWarps - 2) {
+      issue_B(P, l, S, nB1, misc[kNB]);
+      issue_C<BITS>(P, l, S);
+    }
+    if (TRACE && warp == kFWarps - 1 && lane == 0 && misc[kNB] > 0) {  // when the last chunk lands
+      mbar_wait(&S.mB[misc[kNB] - 1], par, ctrl, P.timeout_ns);
+      stamp<TRACE>(P, l, 15);
+    }
     run_units<BITS>(S.B, misc[kBb], misc[kBe], misc + kChB, misc[kNB], S.mB, par, ctrl, P.timeout_ns, sta, g,
                     P.hk + misc[kBb], warp, lane);  // unit k*f + row
     stamp<TRACE>(P, l, 6);
