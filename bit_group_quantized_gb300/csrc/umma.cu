@@ -480,7 +480,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
       int t = 0, s = 0, b = 0;  // step in stage, stage, A tile
       uint32_t fpar = 0, apar = 0;
       for (int j = 0; j < nk; ++j) {
-        if (!tc_mbar_wait(&aready[b], apar, kTcTimeoutNs) || !tc_mbar_wait(&full[s], fpar, kTcTimeoutNs)) {
+        if (!tc_mbar_wait(&aready[b], apar, kTcTimeoutNs) || (t == 0 && !tc_mbar_wait(&full[s], fpar, kTcTimeoutNs))) {
           *s_fail = 1;
           break;
         }
@@ -516,8 +516,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
     for (int j = 0, kb = kb0; j < nk; ++j, ++kb) {
       // lane 0 waits for the stage and the A tile (freed by the MMAs of step j - nA), the warp follows
       int okw = 1;
+      // (a stage's barrier completes once for all its steps: waited at its first)
       if (lane == 0)
-        okw = tc_mbar_wait(&full[s], fpar, kTcTimeoutNs) && (j < nA || tc_mbar_wait(&afree[b], apar ^ 1u, kTcTimeoutNs));
+        okw = (t > 0 || tc_mbar_wait(&full[s], fpar, kTcTimeoutNs)) &&
+              (j < nA || tc_mbar_wait(&afree[b], apar ^ 1u, kTcTimeoutNs));
       if (!__shfl_sync(0xffffffffu, okw, 0)) {
         *s_fail = 1;
         break;
