@@ -366,12 +366,13 @@ int32_t moe_expert_swiglu(const bgq_expert* e, const uint16_t* x, int32_t batch,
     if (k == Where::kHost) where = Where::kHost;
   }
   const int big_min = where == Where::kHost || !tc_layer_ok(es) ? INT_MAX : kBigTok;  // tensor cores from 16 tokens
-  if (launch_plan_single(plan, batch, big_min, s) != cudaSuccess) return BGQ_ERR_CUDA;
-  if (batch >= big_min) {  // one tensor-core task holds every token: no grouped-GEMV work
-    if (launch_gateup_tc(es, plan, batch, 0, x, H, 1, ctrl, tca, s) != cudaSuccess) return BGQ_ERR_CUDA;
-    if (launch_down_tc(es, plan, batch, 0, H, Y, 1, ctrl, tca, s) != cudaSuccess) return BGQ_ERR_CUDA;
-    return cuda_status(launch_combine(Y, nullptr, nullptr, batch, 0, d, y, y_f32, s));
+  if (batch >= big_min) {
+    // one tensor-core task holds every token: no plan (the kernels take token n, slot 0) and the down
+    // GEMM's epilogue writes y / y_f32 itself, the combine of one slot of weight 1
+    if (launch_gateup_tc(es, nullptr, batch, 0, x, H, 1, ctrl, tca, s) != cudaSuccess) return BGQ_ERR_CUDA;
+    return cuda_status(launch_down_tc(es, nullptr, batch, 0, H, Y, 1, ctrl, tca, y, y_f32, s));
   }
+  if (launch_plan_single(plan, batch, big_min, s) != cudaSuccess) return BGQ_ERR_CUDA;
   if (launch_gateup(es, plan, ntasks, batch, x, H, 1, stage, s) != cudaSuccess) return BGQ_ERR_CUDA;
   return cuda_status(launch_down(es, plan, ntasks, batch, H, Y, 1, stage, Combine{nullptr, nullptr, 0, y, y_f32}, s));
 }
@@ -399,7 +400,8 @@ static int32_t layer_forward_impl(const bgq_moe_layer* L, const uint16_t* x, int
   const bool tc = batch >= big_min;
   if (tc && launch_gateup_tc(es, W.plan, batch, K, x, W.H, K + 1, W.ctrl, W.tca, s) != cudaSuccess) return BGQ_ERR_CUDA;
   // tensor-core tasks first: the grouped down kernel ends with the weighted combine
-  if (tc && launch_down_tc(es, W.plan, batch, K, W.H, W.Y, K + 1, W.ctrl, W.tca, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  if (tc && launch_down_tc(es, W.plan, batch, K, W.H, W.Y, K + 1, W.ctrl, W.tca, nullptr, nullptr, s) != cudaSuccess)
+    return BGQ_ERR_CUDA;
   return cuda_status(
       launch_down(es, W.plan, max_tasks, batch, W.H, W.Y, K + 1, W.stage, Combine{w, gamma, K, out, out_f32}, s));
 }

@@ -135,6 +135,10 @@ cudaError_t launch_plan_single(Plan* plan, int batch, int big_min, cudaStream_t 
 // (tc_act_bytes for a plan of (B, K); written before read). K is split over
 // the CTAs of a cluster, whose partial sums meet in distributed shared
 // memory: no other scratch, nothing left behind between calls.
+// plan == nullptr: one task of all B tokens of the shared-expert view (token
+// n in slot 0; K = 0, nslot = 1). Only then may the down call write bf16 `y`
+// and/or fp32 `y_f32` rows (token-major, d columns) directly instead of Y:
+// the same bits as the combine of that one slot with weight 1.
 size_t tc_act_bytes(int d, int f, int B, int K);
 // Whether the pools of `es` can feed the tensor-core path (tensor-map
 // alignment of the codes and scale/bias rows); host-side check.
@@ -142,7 +146,7 @@ bool tc_layer_ok(const ExpertSet& es);
 cudaError_t launch_gateup_tc(const ExpertSet& es, const Plan* plan, int B, int K, const uint16_t* x, float* H,
                              int nslot, Ctrl* ctrl, unsigned char* act, cudaStream_t s);
 cudaError_t launch_down_tc(const ExpertSet& es, const Plan* plan, int B, int K, const float* H, float* Y, int nslot,
-                           Ctrl* ctrl, unsigned char* act, cudaStream_t s);
+                           Ctrl* ctrl, unsigned char* act, uint16_t* y, float* y_f32, cudaStream_t s);
 
 // Grouped gate/up + SiLU*mul: H[(tok*nslot + slot)*f + row].
 // batch: tokens of x, staged all at once in shared memory when they fit, else

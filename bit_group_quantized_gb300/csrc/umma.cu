@@ -262,8 +262,8 @@ __global__ void __launch_bounds__(256) k_tc_act(const Plan* __restrict__ plan, i
                                                 const void* __restrict__ src, int nslot, int kcols,
                                                 unsigned char* __restrict__ act, int* __restrict__ act_sh, int rtot) {
   const int t = blockIdx.x;
-  if (t >= plan->nbig) return;
-  const BigTask bt = plan_big(plan, B, K)[t];
+  if (t >= (plan ? plan->nbig : 1)) return;
+  const BigTask bt = plan ? plan_big(plan, B, K)[t] : BigTask{-1, B, 0, 0};
   const int npad = (bt.ntok + 15) & ~15;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = blockIdx.y * 8 + warp;
@@ -271,9 +271,10 @@ __global__ void __launch_bounds__(256) k_tc_act(const Plan* __restrict__ plan, i
   const int row = bt.pad + n;
   const bool live = n < bt.ntok;
   size_t srow = 0;
-  if (live) {
-    const int tok = plan_ptok(plan, B, K)[bt.first + n];
-    srow = F32 ? ((size_t)tok * nslot + plan_pslot(plan, B, K)[bt.first + n]) * kcols : (size_t)tok * kcols;
+  if (live) {  // without a plan: token n, slot 0
+    const int tok = plan ? plan_ptok(plan, B, K)[bt.first + n] : n;
+    const int slot = plan ? plan_pslot(plan, B, K)[bt.first + n] : 0;
+    srow = F32 ? ((size_t)tok * nslot + slot) * kcols : (size_t)tok * kcols;
   }
   auto load16 = [&](int b, float (&v)[16]) {
     if (!live) {
@@ -338,7 +339,7 @@ struct TcMaps {
   CUtensorMap sb[2][2];  // the matrices' scale/bias rows, same views
 };
 struct TcArgs {
-  const Plan* plan;
+  const Plan* plan;  // null: one task of every token (B tokens, slot 0) of the shared-expert view
   int B, K;
   int rows;        // output rows (f for gate/up, d for down)
   int y0[2][2];    // first row of matrix i in its map's expert region ([routed, shared][i])
@@ -351,6 +352,8 @@ struct TcArgs {
   int rtot;
   float* out;      // H (gate/up) or Y (down), rows (token*nslot + slot)
   int nslot;
+  uint16_t* y;     // down without a plan: bf16 output rows (token), in place of out when set
+  float* yf;       // down without a plan: fp32 output rows (token), in place of out when set
   Ctrl* ctrl;
 };
 
@@ -382,13 +385,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
   extern __shared__ __align__(1024) unsigned char smem[];
   constexpr int qb = kTcBK * BITS / 8;  // code bytes of one row and K step
   constexpr int kA = kTcM * kTcBK * 2;  // bytes of one fp16 A tile
-  if ((int)blockIdx.y >= a.plan->nbig) return;  // the same for every CTA of a cluster
+  if ((int)blockIdx.y >= (a.plan ? a.plan->nbig : 1)) return;  // the same for every CTA of a cluster
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tc_smem(smem) & 1023) {  // the swizzled copies need a 1024-byte aligned base (same for every CTA)
     if (tid == 0) atomicExch(&a.ctrl->status, BGQ_ERR_CUDA);
     return;
   }
-  const BigTask bt = plan_big(a.plan, a.B, a.K)[blockIdx.y];
+  const BigTask bt = a.plan ? plan_big(a.plan, a.B, a.K)[blockIdx.y] : BigTask{-1, a.B, 0, 0};
   const int npad = (bt.ntok + 15) & ~15;
   const int tile = blockIdx.x / a.nsplit, split = blockIdx.x - tile * a.nsplit;
   const int G = a.g, S = a.stages, nA = a.abufs;
@@ -565,8 +568,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
   const int rs = orows / a.nsplit, r0 = split * rs;  // this CTA's output rows of the reduction
   const int m0 = tile * orows;
   const size_t row_stride = (size_t)a.rows;
-  const int* ptok = plan_ptok(a.plan, a.B, a.K) + bt.first;
-  const int* pslot = plan_pslot(a.plan, a.B, a.K) + bt.first;
+  const int* ptok = a.plan ? plan_ptok(a.plan, a.B, a.K) + bt.first : nullptr;  // null: token n, slot 0
+  const int* pslot = a.plan ? plan_pslot(a.plan, a.B, a.K) + bt.first : nullptr;
   for (int c0 = 0; c0 < npad; c0 += kTcChunk) {
     const int cw = min(kTcChunk, npad - c0);
     if (ok && warp >= 2) {  // warp w reads tensor-memory lanes 32(w%4)..+31, a quarter (w-2)/4 of the columns
@@ -616,7 +619,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
       } else {
         h = make_float4(g.x * un, g.y * un, g.z * un, g.w * un);
       }
-      *reinterpret_cast<float4*>(a.out + ((size_t)ptok[n] * a.nslot + pslot[n]) * row_stride + m0 + rq) = h;
+      if (!GU && (a.y || a.yf)) {  // one slot of weight 1: the combine's fma(1, y, 0), written here
+        h = make_float4(__fadd_rn(h.x, 0.f), __fadd_rn(h.y, 0.f), __fadd_rn(h.z, 0.f), __fadd_rn(h.w, 0.f));
+        const size_t o = (size_t)n * row_stride + m0 + rq;
+        if (a.yf) *reinterpret_cast<float4*>(a.yf + o) = h;
+        if (a.y)
+          *reinterpret_cast<uint2*>(a.y + o) = make_uint2((uint32_t)f2bf(h.x) | ((uint32_t)f2bf(h.y) << 16),
+                                                          (uint32_t)f2bf(h.z) | ((uint32_t)f2bf(h.w) << 16));
+        continue;
+      }
+      const size_t orow = ptok ? (size_t)ptok[n] * a.nslot + pslot[n] : (size_t)n * a.nslot;
+      *reinterpret_cast<float4*>(a.out + orow * row_stride + m0 + rq) = h;
     }
     tc_cluster_sync();  // peers are done reading before the next pass overwrites P (or the CTA exits)
   }
@@ -794,9 +807,9 @@ bool tc_layer_ok(const ExpertSet& es) {
 
 template <int BITS>
 static cudaError_t tc_run(const ExpertSet& es, bool gu, const Plan* plan, int B, int K, const void* src, float* out,
-                          int nslot, Ctrl* ctrl, unsigned char* act, cudaStream_t s) {
+                          int nslot, Ctrl* ctrl, unsigned char* act, uint16_t* y, float* yf, cudaStream_t s) {
   TcArgs a{};
-  const int nbig_max = plan_max_big(B, K);
+  const int nbig_max = plan ? plan_max_big(B, K) : 1;
   const int npad = tc_npad_max(B);
   const int kc = gu ? es.d : es.f;
   if (!tc_pick(BITS, npad, kc / kTcBK, a.g, a.stages, a.abufs)) return cudaErrorInvalidValue;
@@ -813,6 +826,8 @@ static cudaError_t tc_run(const ExpertSet& es, bool gu, const Plan* plan, int B,
   a.act_sh = reinterpret_cast<const int*>(act + tc_up256((size_t)a.rtot * (((es.d > es.f ? es.d : es.f)) / kTcBK) * 128));
   a.out = out;
   a.nslot = nslot;
+  a.y = y;
+  a.yf = yf;
   a.ctrl = ctrl;
   int* act_sh = const_cast<int*>(a.act_sh);
   // stage the activations once
@@ -849,15 +864,16 @@ static cudaError_t tc_run(const ExpertSet& es, bool gu, const Plan* plan, int B,
 cudaError_t launch_gateup_tc(const ExpertSet& es, const Plan* plan, int B, int K, const uint16_t* x, float* H,
                              int nslot, Ctrl* ctrl, unsigned char* act, cudaStream_t s) {
   if (B < kBigTok) return cudaSuccess;  // no task can have 16 tokens
-  return es.bits == 4 ? tc_run<4>(es, true, plan, B, K, x, H, nslot, ctrl, act, s)
-                      : tc_run<2>(es, true, plan, B, K, x, H, nslot, ctrl, act, s);
+  return es.bits == 4 ? tc_run<4>(es, true, plan, B, K, x, H, nslot, ctrl, act, nullptr, nullptr, s)
+                      : tc_run<2>(es, true, plan, B, K, x, H, nslot, ctrl, act, nullptr, nullptr, s);
 }
 
 cudaError_t launch_down_tc(const ExpertSet& es, const Plan* plan, int B, int K, const float* H, float* Y, int nslot,
-                           Ctrl* ctrl, unsigned char* act, cudaStream_t s) {
+                           Ctrl* ctrl, unsigned char* act, uint16_t* y, float* y_f32, cudaStream_t s) {
   if (B < kBigTok) return cudaSuccess;
-  return es.bits == 4 ? tc_run<4>(es, false, plan, B, K, H, Y, nslot, ctrl, act, s)
-                      : tc_run<2>(es, false, plan, B, K, H, Y, nslot, ctrl, act, s);
+  if ((y || y_f32) && plan) return cudaErrorInvalidValue;  // direct output: the one-task form only
+  return es.bits == 4 ? tc_run<4>(es, false, plan, B, K, H, Y, nslot, ctrl, act, y, y_f32, s)
+                      : tc_run<2>(es, false, plan, B, K, H, Y, nslot, ctrl, act, y, y_f32, s);
 }
 
 }  // namespace bgq
