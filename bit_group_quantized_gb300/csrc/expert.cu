@@ -241,6 +241,8 @@ __global__ void __launch_bounds__(kAllThreads, 1)
 k_gateup_all(ExpertSet es, const Plan* __restrict__ plan, const uint16_t* __restrict__ x, int B,
              float* __restrict__ H, int nslot, XStage gst) {
   extern __shared__ __align__(16) unsigned char smem[];
+  pdl_wait();     // launched as a programmatic dependent: nothing is touched before the earlier kernels end
+  pdl_trigger();
   const int d = es.d, f = es.f;
   const RowGeo rg = row_geo(d, BITS);  // LPR == 32, NIT <= kMaxNitE (checked by the launcher)
   // inputs staged here, or (too many tokens for shared memory) read from the
@@ -323,6 +325,8 @@ __global__ void __launch_bounds__(kAllThreads, 1)
 k_down_all(ExpertSet es, const Plan* __restrict__ plan, const float* __restrict__ H, int B,
            float* __restrict__ Y, int nslot, XStage gst, Combine cb) {
   extern __shared__ __align__(16) unsigned char smem[];
+  pdl_wait();  // as k_gateup_all
+  pdl_trigger();
   const int d = es.d, f = es.f;
   const RowGeo rg = row_geo(f, BITS);  // NIT == 1 (checked by the launcher)
   const int T = B * nslot;             // staged vector (tok, slot) at index tok * nslot + slot
@@ -459,10 +463,12 @@ cudaError_t launch_gateup(const ExpertSet& es, const Plan* plan, int max_tasks, 
     }
     if (es.bits == 4) {
       if ((e = set_smem(k_gateup_all<4>, sm)) != cudaSuccess) return e;
-      k_gateup_all<4><<<num_sms(), kAllThreads, sm, s>>>(es, plan, x, batch, H, nslot, gst);
+      e = launch_overlapped(k_gateup_all<4>, num_sms(), kAllThreads, sm, s, es, plan, x, batch, H, nslot, gst);
+      if (e != cudaSuccess) return e;
     } else {
       if ((e = set_smem(k_gateup_all<2>, sm)) != cudaSuccess) return e;
-      k_gateup_all<2><<<num_sms(), kAllThreads, sm, s>>>(es, plan, x, batch, H, nslot, gst);
+      e = launch_overlapped(k_gateup_all<2>, num_sms(), kAllThreads, sm, s, es, plan, x, batch, H, nslot, gst);
+      if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
   }
@@ -499,10 +505,12 @@ cudaError_t launch_down(const ExpertSet& es, const Plan* plan, int max_tasks, in
     }
     if (es.bits == 4) {
       if ((e = set_smem(k_down_all<4>, sm)) != cudaSuccess) return e;
-      k_down_all<4><<<num_sms(), kAllThreads, sm, s>>>(es, plan, H, batch, Y, nslot, gst, cb);
+      e = launch_overlapped(k_down_all<4>, num_sms(), kAllThreads, sm, s, es, plan, H, batch, Y, nslot, gst, cb);
+      if (e != cudaSuccess) return e;
     } else {
       if ((e = set_smem(k_down_all<2>, sm)) != cudaSuccess) return e;
-      k_down_all<2><<<num_sms(), kAllThreads, sm, s>>>(es, plan, H, batch, Y, nslot, gst, cb);
+      e = launch_overlapped(k_down_all<2>, num_sms(), kAllThreads, sm, s, es, plan, H, batch, Y, nslot, gst, cb);
+      if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
   }

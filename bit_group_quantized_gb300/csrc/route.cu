@@ -518,6 +518,7 @@ k_route_coop(const uint16_t* __restrict__ router, const uint16_t* __restrict__ s
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  pdl_trigger();  // every other CTA has left: the grouped kernel behind may take their SMs and wait there
   if (plan) {
     int* s_cnt = reinterpret_cast<int*>(smem);  // plan_scratch_ints(B, K, E) ints
     build_plan(sel_ws, B, K, E, big_min, plan, s_cnt);
@@ -576,6 +577,8 @@ cudaError_t launch_route(const uint16_t* router, const uint16_t* sgate, const ui
 // Plan of one explicit expert over B tokens (slot 0): one tensor-core task for
 // B >= big_min, else grouped-GEMV tasks of up to 8 tokens. Plan sized for (B, 0).
 __global__ void k_plan_single(Plan* plan, int B, int big_min) {
+  pdl_wait();  // an earlier kernel may still read the plan
+  pdl_trigger();
   if (B >= big_min) {
     BigTask* big = plan_big(plan, B, 0);
     int* ptok = plan_ptok(plan, B, 0);
@@ -609,8 +612,7 @@ __global__ void k_plan_single(Plan* plan, int B, int big_min) {
 }
 
 cudaError_t launch_plan_single(Plan* plan, int batch, int big_min, cudaStream_t s) {
-  k_plan_single<<<1, 64, 0, s>>>(plan, batch, big_min);
-  return cudaGetLastError();
+  return launch_overlapped(k_plan_single, 1, 64, 0, s, plan, batch, big_min);
 }
 
 }  // namespace bgq
