@@ -372,9 +372,11 @@ int32_t moe_expert_swiglu(const bgq_expert* e, const uint16_t* x, int32_t batch,
     if (launch_gateup_tc(es, nullptr, batch, 0, x, H, 1, ctrl, tca, s) != cudaSuccess) return BGQ_ERR_CUDA;
     return cuda_status(launch_down_tc(es, nullptr, batch, 0, H, Y, 1, ctrl, tca, y, y_f32, s));
   }
-  if (launch_plan_single(plan, batch, big_min, s) != cudaSuccess) return BGQ_ERR_CUDA;
-  if (launch_gateup(es, plan, ntasks, batch, x, H, 1, stage, s) != cudaSuccess) return BGQ_ERR_CUDA;
-  return cuda_status(launch_down(es, plan, ntasks, batch, H, Y, 1, stage, Combine{nullptr, nullptr, 0, y, y_f32}, s));
+  // grouped GEMVs: the kernels build the tasks themselves where they can, else from a plan kernel
+  const Plan* gp = grouped_planless_ok(es, batch, true) ? nullptr : plan;
+  if (gp && launch_plan_single(plan, batch, big_min, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  if (launch_gateup(es, gp, ntasks, batch, x, H, 1, stage, s) != cudaSuccess) return BGQ_ERR_CUDA;
+  return cuda_status(launch_down(es, gp, ntasks, batch, H, Y, 1, stage, Combine{nullptr, nullptr, 0, y, y_f32}, s));
 }
 
 size_t moe_layer_workspace_bytes(const bgq_moe_layer* L, int32_t max_batch) {

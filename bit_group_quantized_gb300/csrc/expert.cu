@@ -223,10 +223,33 @@ struct GateUpRows {
   uint32_t gs[kMaxNitE], us[kMaxNitE];
 };
 
+// The plan's tasks, or without a plan (one explicit expert over B tokens):
+// tasks of 8 consecutive tokens of the shared-expert view in slot 0, the
+// tasks k_plan_single would build, written to s_task (ends with a block
+// barrier then).
+__device__ __forceinline__ const Task* tasks_of(const Plan* plan, int B, Task* s_task, int& ntasks) {
+  if (plan) {
+    ntasks = plan->ntasks;
+    return plan_tasks(plan);
+  }
+  ntasks = (B + kTaskTok - 1) / kTaskTok;
+  for (int c = threadIdx.x; c < ntasks; c += blockDim.x) {
+    Task& tk = s_task[c];
+    tk.expert = -1;
+    tk.ntok = min(kTaskTok, B - c * kTaskTok);
+    for (int i = 0; i < kTaskTok; ++i) {
+      tk.tok[i] = c * kTaskTok + i;
+      tk.slot[i] = 0;
+    }
+  }
+  __syncthreads();
+  return s_task;
+}
+
 template <int BITS>
-__device__ __forceinline__ void load_gateup(const ExpertSet& es, const Plan* plan, int item, int nr, int r0,
+__device__ __forceinline__ void load_gateup(const ExpertSet& es, const Task* tasks, int item, int nr, int r0,
                                             const RowGeo& rg, int lane, GateUpRows& R) {
-  const Task& tk = plan_tasks(plan)[item / nr];
+  const Task& tk = tasks[item / nr];
   const int row = r0 + item % nr;
   const ExpertRef ex = resolve(es, tk.expert);
   const int wpr = es.d * BITS / 32, gpr = es.d / kGroup;
@@ -241,8 +264,11 @@ __global__ void __launch_bounds__(kAllThreads, 1)
 k_gateup_all(ExpertSet es, const Plan* __restrict__ plan, const uint16_t* __restrict__ x, int B,
              float* __restrict__ H, int nslot, XStage gst) {
   extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ Task s_task[kPlanlessTasks];
   pdl_wait();     // launched as a programmatic dependent: nothing is touched before the earlier kernels end
   pdl_trigger();
+  int ntasks;
+  const Task* tasks = tasks_of(plan, B, s_task, ntasks);
   const int d = es.d, f = es.f;
   const RowGeo rg = row_geo(d, BITS);  // LPR == 32, NIT <= kMaxNitE (checked by the launcher)
   // inputs staged here, or (too many tokens for shared memory) read from the
@@ -255,13 +281,13 @@ k_gateup_all(ExpertSet es, const Plan* __restrict__ plan, const uint16_t* __rest
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const RowSpan rs = cta_rows(f);
   const int nr = rs.e - rs.b;
-  const int total = plan->ntasks * nr;
+  const int total = ntasks * nr;
   GateUpRows cur, nxt;
-  if (warp < total) load_gateup<BITS>(es, plan, warp, nr, rs.b, rg, lane, cur);  // in flight during staging
+  if (warp < total) load_gateup<BITS>(es, tasks, warp, nr, rs.b, rg, lane, cur);  // in flight during staging
   if (local) stage_x24_pairs<BITS>(StridedSrc<uint16_t>{x, d}, B, d, st);  // two code words per thread
   for (int item = warp; item < total; item += kAllWarps) {
-    if (item + kAllWarps < total) load_gateup<BITS>(es, plan, item + kAllWarps, nr, rs.b, rg, lane, nxt);
-    const Task& tk = plan_tasks(plan)[item / nr];
+    if (item + kAllWarps < total) load_gateup<BITS>(es, tasks, item + kAllWarps, nr, rs.b, rg, lane, nxt);
+    const Task& tk = tasks[item / nr];
     const int row = rs.b + item % nr;
     for (int i = 0; i < tk.ntok; ++i) {
       const int t = tk.tok[i];
@@ -302,9 +328,9 @@ __device__ __forceinline__ DownItem down_item(int i, int nch, int nrg) {
 }
 
 template <int BITS>
-__device__ __forceinline__ void load_down(const ExpertSet& es, const Plan* plan, const DownItem& it, int r0, int nrows,
+__device__ __forceinline__ void load_down(const ExpertSet& es, const Task* tasks, const DownItem& it, int r0, int nrows,
                                           const RowGeo& rg, int lp, int rsub, DownRows& R) {
-  const ExpertRef ex = resolve(es, plan_tasks(plan)[it.task].expert);
+  const ExpertRef ex = resolve(es, tasks[it.task].expert);
   const int wpr = es.f * BITS / 32, gpr = es.f / kGroup;
 #pragma unroll
   for (int u = 0; u < kAllRows; ++u) {
@@ -325,8 +351,11 @@ __global__ void __launch_bounds__(kAllThreads, 1)
 k_down_all(ExpertSet es, const Plan* __restrict__ plan, const float* __restrict__ H, int B,
            float* __restrict__ Y, int nslot, XStage gst, Combine cb) {
   extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ Task s_task[kPlanlessTasks];
   pdl_wait();  // as k_gateup_all
   pdl_trigger();
+  int ntasks;
+  const Task* tasks = tasks_of(plan, B, s_task, ntasks);
   const int d = es.d, f = es.f;
   const RowGeo rg = row_geo(f, BITS);  // NIT == 1 (checked by the launcher)
   const int T = B * nslot;             // staged vector (tok, slot) at index tok * nslot + slot
@@ -341,15 +370,15 @@ k_down_all(ExpertSet es, const Plan* __restrict__ plan, const float* __restrict_
   const int nrows = rs.e - rs.b;
   const int nrg = (nrows + rg.RPP - 1) / rg.RPP;
   const int nch = (nrg + kAllRows - 1) / kAllRows;
-  const int total = plan->ntasks * nch;
+  const int total = ntasks * nch;
   DownRows cur, nxt;
-  if (warp < total) load_down<BITS>(es, plan, down_item(warp, nch, nrg), rs.b, nrows, rg, lp, rsub, cur);
+  if (warp < total) load_down<BITS>(es, tasks, down_item(warp, nch, nrg), rs.b, nrows, rg, lp, rsub, cur);
   if (local) stage_x24_pairs<BITS>(StridedSrc<float>{H, f}, T, f, st);
   for (int i = warp; i < total; i += kAllWarps) {
     if (i + kAllWarps < total)
-      load_down<BITS>(es, plan, down_item(i + kAllWarps, nch, nrg), rs.b, nrows, rg, lp, rsub, nxt);
+      load_down<BITS>(es, tasks, down_item(i + kAllWarps, nch, nrg), rs.b, nrows, rg, lp, rsub, nxt);
     const DownItem it = down_item(i, nch, nrg);
-    const Task& tk = plan_tasks(plan)[it.task];
+    const Task& tk = tasks[it.task];
     for (int j = 0; j < tk.ntok; ++j) {
       const int v = tk.tok[j] * nslot + tk.slot[j];
       uint4 xc[4 * Geo<BITS>::kNch];
@@ -445,10 +474,19 @@ static int expert_grid(int max_items) {
   return max_items < g ? (max_items > 0 ? max_items : 1) : g;
 }
 
+bool grouped_planless_ok(const ExpertSet& es, int batch, bool stage_ws) {
+  const RowGeo rg = row_geo(es.d, es.bits), rf = row_geo(es.f, es.bits);
+  if (batch > kPlanlessTasks * kTaskTok) return false;
+  const bool gu = rg.LPR == 32 && rg.NIT <= kMaxNitE && (all_smem(es.d, es.bits, batch) <= kAllSmemMax || stage_ws);
+  const bool dn = rf.NIT == 1 && (all_smem(es.f, es.bits, batch) <= kAllSmemMax || stage_ws);
+  return gu && dn;
+}
+
 cudaError_t launch_gateup(const ExpertSet& es, const Plan* plan, int max_tasks, int batch, const uint16_t* x, float* H,
                           int nslot, unsigned char* stage_ws, cudaStream_t s) {
   RowGeo rg = row_geo(es.d, es.bits);
   const bool fits = all_smem(es.d, es.bits, batch) <= kAllSmemMax;
+  if (!plan && !grouped_planless_ok(es, batch, stage_ws != nullptr)) return cudaErrorInvalidValue;
   if (rg.LPR == 32 && rg.NIT <= kMaxNitE && (fits || stage_ws)) {
     XStage gst{};
     size_t sm = 0;
@@ -491,6 +529,7 @@ cudaError_t launch_down(const ExpertSet& es, const Plan* plan, int max_tasks, in
   RowGeo rg = row_geo(es.f, es.bits);
   const int T = batch * nslot;
   const bool fits = all_smem(es.f, es.bits, T) <= kAllSmemMax;
+  if (!plan && (nslot != 1 || !grouped_planless_ok(es, batch, stage_ws != nullptr))) return cudaErrorInvalidValue;
   if (rg.NIT == 1 && (fits || stage_ws)) {
     XStage gst{};
     size_t sm = 0;

@@ -148,6 +148,13 @@ cudaError_t launch_gateup_tc(const ExpertSet& es, const Plan* plan, int B, int K
 cudaError_t launch_down_tc(const ExpertSet& es, const Plan* plan, int B, int K, const float* H, float* Y, int nslot,
                            Ctrl* ctrl, unsigned char* act, uint16_t* y, float* y_f32, cudaStream_t s);
 
+// plan == nullptr (launch_gateup / launch_down): one explicit expert over all
+// `batch` tokens (tasks of 8 consecutive tokens of the shared-expert view,
+// slot 0, nslot 1), built by the kernels themselves; allowed when
+// grouped_planless_ok() holds (at most kPlanlessTasks tasks and shapes the
+// one-CTA-per-SM kernels take).
+constexpr int kPlanlessTasks = 32;
+bool grouped_planless_ok(const ExpertSet& es, int batch, bool stage_ws);
 // Grouped gate/up + SiLU*mul: H[(tok*nslot + slot)*f + row].
 // batch: tokens of x, staged all at once in shared memory when they fit, else
 // into stage_ws (staged_tokens_bytes(d, bits, batch) bytes of global memory;
