@@ -297,11 +297,21 @@ __global__ void __launch_bounds__(256) k_tc_act(const Plan* __restrict__ plan, i
   };
   const int nblk = kcols / 16;  // 16-column blocks of a row
   float m = 0.f;
-  for (int b = lane; b < nblk; b += 32) {
-    float v[16];
-    load16(b, v);
+  for (int b0 = lane; b0 < nblk; b0 += 32 * 4) {  // four blocks' loads in flight per lane
+    float v[4][16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
+    for (int u = 0; u < 4; ++u) {
+      if (b0 + 32 * u < nblk) {
+        load16(b0 + 32 * u, v[u]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[u][i] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[u][i]));
   }
   m = warp_max(m);
   int sh = 0;  // the largest magnitude times 2^sh lands in [2^14, 2^15)
@@ -312,10 +322,16 @@ __global__ void __launch_bounds__(256) k_tc_act(const Plan* __restrict__ plan, i
   }
   if (lane == 0 && blockIdx.z == 0) act_sh[row] = sh;
   const float sc = exp2i(sh);
-  const int b1 = min(nblk, ((int)blockIdx.z + 1) * 64);
-  for (int b = (int)blockIdx.z * 64 + lane; b < b1; b += 32) {
-    float v[16];
-    load16(b, v);
+  const int b1 = min(nblk, ((int)blockIdx.z + 1) * 64);  // a chunk: two blocks per lane, both loaded first
+  float v2[2][16];
+#pragma unroll
+  for (int u = 0; u < 2; ++u)
+    if ((int)blockIdx.z * 64 + lane + 32 * u < b1) load16((int)blockIdx.z * 64 + lane + 32 * u, v2[u]);
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int b = (int)blockIdx.z * 64 + lane + 32 * u;
+    if (b >= b1) break;
+    const float* v = v2[u];
     __half h[16];
 #pragma unroll
     for (int k = 0; k < 16; ++k) h[tc_slot<BITS>(k)] = __float2half_rn(v[k] * sc);
