@@ -263,7 +263,7 @@ const char* bgq_status_string(int32_t s) {
   }
 }
 
-int32_t bgq_abi_version(void) { return 102; }
+int32_t bgq_abi_version(void) { return 103; }
 
 static int32_t gemv_common(const bgq_qmatrix* W, const uint16_t* x, uint16_t* y, int32_t batch, int32_t variant,
                            int want_bits, void* stream) {
@@ -500,12 +500,14 @@ static int chain_check(const bgq_qmatrix* W, int32_t n, int32_t batch) {
     if (i > 0 && W[i].cols != W[i - 1].rows) return BGQ_ERR_INVALID_ARG;
     if (W[i].cols > max_cols) max_cols = W[i].cols;
   }
-  if (chain_smem_bytes(max_cols, W[0].bits, batch) > (size_t)227 * 1024) return BGQ_ERR_UNSUPPORTED;
+  // every step's GEMV stages at least one token's input in shared memory
+  if (qgemv_int_smem(max_cols, W[0].bits, 1) > (size_t)227 * 1024) return BGQ_ERR_UNSUPPORTED;
   return BGQ_OK;
 }
-// Row stride of the inner steps' outputs: the widest, a multiple of 8 (16-byte rows).
+// Row stride of the intermediate vectors (the normalised input, the inner
+// steps' outputs): the widest, a multiple of 8.
 static int chain_ldb(const bgq_qmatrix* W, int32_t n) {
-  int m = 8;
+  int m = W[0].cols > 8 ? W[0].cols : 8;
   for (int i = 0; i + 1 < n; ++i)
     if (W[i].rows > m) m = W[i].rows;
   return (m + 7) & ~7;
@@ -516,6 +518,12 @@ size_t bgq_gemv_chain_workspace_bytes(const bgq_qmatrix* W, int32_t n, int32_t b
   return sizeof(Ctrl) + 256 + 2 * up256((size_t)batch * chain_ldb(W, n) * 2);
 }
 
+// The chain as programmatic dependent launches of the standalone kernels
+// (RMSNorm, then one GEMV per step, the residual added in the last GEMV's
+// epilogue): each waits for the one before it, and its weight loads start
+// while that one finishes. A single persistent launch with grid-wide waits
+// between the steps was built and measured slower on this GPU (a grid-wide
+// wait on 152 SMs costs more than a dependent launch's boundary).
 int32_t bgq_gemv_chain(const bgq_qmatrix* W, int32_t n, const uint16_t* x, int32_t batch, int32_t norm,
                        const uint16_t* rho, float eps, int32_t residual, uint16_t* out, float* out_f32, void* ws,
                        size_t ws_bytes, void* stream) {
@@ -527,18 +535,27 @@ int32_t bgq_gemv_chain(const bgq_qmatrix* W, int32_t n, const uint16_t* x, int32
   if (residual && W[n - 1].rows != W[0].cols) return BGQ_ERR_INVALID_ARG;
   if (!ws || !al(ws, 256) || ws_bytes < bgq_gemv_chain_workspace_bytes(W, n, batch)) return BGQ_ERR_WORKSPACE;
   Carver c(ws);
-  Ctrl* ctrl = c.take<Ctrl>(sizeof(Ctrl));
-  int* counter = c.take<int>(256);
+  c.take<Ctrl>(sizeof(Ctrl));  // the status word, as in every workspace (nothing here waits on the device)
+  c.take<int>(256);
   const int ldb = chain_ldb(W, n);
-  uint16_t* b0 = c.take<uint16_t>((size_t)batch * ldb * 2);
-  uint16_t* b1 = c.take<uint16_t>((size_t)batch * ldb * 2);
-  ChainStep steps[kMaxChain];
-  for (int i = 0; i < n; ++i)
-    steps[i] = ChainStep{W[i].q, reinterpret_cast<const uint32_t*>(W[i].sb), W[i].rows, W[i].cols};
+  uint16_t* buf[2] = {c.take<uint16_t>((size_t)batch * ldb * 2), c.take<uint16_t>((size_t)batch * ldb * 2)};
   cudaStream_t s = st(stream);
-  if (cudaMemsetAsync(ws, 0, sizeof(Ctrl) + 256, s) != cudaSuccess) return BGQ_ERR_CUDA;
-  return cuda_status(launch_chain(steps, n, W[0].bits, x, batch, norm ? 1 : 0, norm ? rho : nullptr, eps,
-                                  residual ? 1 : 0, out, out_f32, ctrl, counter, b0, b1, ldb, 1000000000ll, s));
+  const uint16_t* cur = x;
+  int k = 0;
+  if (norm) {
+    if (launch_rmsnorm_bf16(x, rho, batch, W[0].cols, eps, buf[0], s) != cudaSuccess) return BGQ_ERR_CUDA;
+    cur = buf[0];
+    k = 1;
+  }
+  for (int i = 0; i < n; ++i) {
+    const bool last = i == n - 1;
+    if (launch_qgemv(qm(&W[i]), cur, batch, last ? out : buf[k], last ? out_f32 : nullptr, 0, s,
+                     last && residual ? x : nullptr) != cudaSuccess)
+      return BGQ_ERR_CUDA;
+    cur = buf[k];  // vectors packed at the step's own row stride
+    k ^= 1;
+  }
+  return BGQ_OK;
 }
 
 size_t moe_stack_workspace_bytes(const bgq_moe_layer* layers, int32_t n_layers) {

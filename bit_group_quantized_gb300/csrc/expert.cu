@@ -598,13 +598,23 @@ cudaError_t launch_combine(const float* Y, const float* w, const float* gamma, i
   return cudaGetLastError();
 }
 
-// One CTA per token: a = bf16(h * (1/sqrt(mean(h^2) + eps)) * rho).
-__global__ void __launch_bounds__(256) k_rmsnorm(const float* __restrict__ h, const uint16_t* __restrict__ rho, int d,
+// One CTA per token: a = bf16(h * (1/sqrt(mean(h^2) + eps)) * rho); h fp32,
+// or bf16 widened exactly (the same bits as on the widened copy). Launched as
+// a programmatic dependent: it waits before touching memory.
+__device__ __forceinline__ float rms_ld(const float* p) { return *p; }
+__device__ __forceinline__ float rms_ld(const uint16_t* p) { return bf16f(*p); }
+template <typename T>
+__global__ void __launch_bounds__(256) k_rmsnorm(const T* __restrict__ h, const uint16_t* __restrict__ rho, int d,
                                                  float eps, uint16_t* __restrict__ a) {
   __shared__ float red[8];
-  const float* ht = h + (size_t)blockIdx.x * d;
+  pdl_wait();
+  pdl_trigger();
+  const T* ht = h + (size_t)blockIdx.x * d;
   float ss = 0.f;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) ss = fmaf(ht[i], ht[i], ss);
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    const float v = rms_ld(ht + i);
+    ss = fmaf(v, v, ss);
+  }
   ss = warp_sum(ss);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
   __syncthreads();
@@ -612,7 +622,7 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const float* __restrict__ h, co
   for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += red[i];
   const float r = 1.f / sqrtf(tot / (float)d + eps);
   for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    float v = ht[i] * r;
+    float v = rms_ld(ht + i) * r;
     if (rho) v *= bf16f(rho[i]);
     a[(size_t)blockIdx.x * d + i] = f2bf(v);
   }
@@ -620,8 +630,11 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const float* __restrict__ h, co
 
 cudaError_t launch_rmsnorm(const float* h, const uint16_t* rho, int batch, int d, float eps, uint16_t* a,
                            cudaStream_t s) {
-  k_rmsnorm<<<batch, 256, 0, s>>>(h, rho, d, eps, a);
-  return cudaGetLastError();
+  return launch_overlapped(k_rmsnorm<float>, batch, 256, 0, s, h, rho, d, eps, a);
+}
+cudaError_t launch_rmsnorm_bf16(const uint16_t* x, const uint16_t* rho, int batch, int d, float eps, uint16_t* a,
+                                cudaStream_t s) {
+  return launch_overlapped(k_rmsnorm<uint16_t>, batch, 256, 0, s, x, rho, d, eps, a);
 }
 
 __global__ void k_residual(float* __restrict__ h, const float* __restrict__ delta, long long n) {

@@ -28,7 +28,8 @@ constexpr int kMaxNit = 4;  // parts per lane held in registers at once
 template <int BITS, int T>
 __global__ void __launch_bounds__(kGemvThreads)
 k_qgemv_int(const uint32_t* __restrict__ q, const uint32_t* __restrict__ sb, int rows, int cols,
-              const uint16_t* __restrict__ x, int ldx, uint16_t* __restrict__ y, float* __restrict__ yf, int ldy) {
+              const uint16_t* __restrict__ x, int ldx, uint16_t* __restrict__ y, float* __restrict__ yf, int ldy,
+              const uint16_t* __restrict__ res) {
   extern __shared__ __align__(16) unsigned char smem[];
   const RowGeo rg = row_geo(cols, BITS);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -90,6 +91,7 @@ k_qgemv_int(const uint32_t* __restrict__ q, const uint32_t* __restrict__ sb, int
   for (int t = 0; t < T; ++t) {
     float v = row_reduce(acc[t], rg.LPR);
     if (valid && lp == 0) {
+      if (res) v += bf16f(res[(size_t)t * ldy + row]);  // a residual input: the fp32 sum, then one rounding
       if (y) y[(size_t)t * ldy + row] = f2bf(v);
       if (yf) yf[(size_t)t * ldy + row] = v;
     }
@@ -192,7 +194,7 @@ size_t qgemv_int_smem(int cols, int bits, int T) { return xstage_bytes(T, cols, 
 
 template <int BITS, int T>
 static cudaError_t launch_int_t(const QMat& W, const uint16_t* x, int ldx, uint16_t* y, float* yf, int ldy,
-                                  cudaStream_t s) {
+                                  const uint16_t* res, cudaStream_t s) {
   RowGeo rg = row_geo(W.cols, BITS);
   int rows_per_cta = kGemvWarps * rg.RPP;
   int grid = (W.rows + rows_per_cta - 1) / rows_per_cta;
@@ -203,21 +205,21 @@ static cudaError_t launch_int_t(const QMat& W, const uint16_t* x, int ldx, uint1
     if (e != cudaSuccess) return e;
   }
   return launch_overlapped(kern, grid, kGemvThreads, sm, s, W.q, reinterpret_cast<const uint32_t*>(W.sb), W.rows,
-                           W.cols, x, ldx, y, yf, ldy);
+                           W.cols, x, ldx, y, yf, ldy, res);
 }
 
 template <int BITS>
 static cudaError_t launch_int_bits(const QMat& W, const uint16_t* x, int ldx, uint16_t* y, float* yf, int ldy,
-                                     int T, cudaStream_t s) {
+                                     const uint16_t* res, int T, cudaStream_t s) {
   switch (T) {
-    case 1: return launch_int_t<BITS, 1>(W, x, ldx, y, yf, ldy, s);
-    case 2: return launch_int_t<BITS, 2>(W, x, ldx, y, yf, ldy, s);
-    case 3: return launch_int_t<BITS, 3>(W, x, ldx, y, yf, ldy, s);
-    case 4: return launch_int_t<BITS, 4>(W, x, ldx, y, yf, ldy, s);
-    case 5: return launch_int_t<BITS, 5>(W, x, ldx, y, yf, ldy, s);
-    case 6: return launch_int_t<BITS, 6>(W, x, ldx, y, yf, ldy, s);
-    case 7: return launch_int_t<BITS, 7>(W, x, ldx, y, yf, ldy, s);
-    default: return launch_int_t<BITS, 8>(W, x, ldx, y, yf, ldy, s);
+    case 1: return launch_int_t<BITS, 1>(W, x, ldx, y, yf, ldy, res, s);
+    case 2: return launch_int_t<BITS, 2>(W, x, ldx, y, yf, ldy, res, s);
+    case 3: return launch_int_t<BITS, 3>(W, x, ldx, y, yf, ldy, res, s);
+    case 4: return launch_int_t<BITS, 4>(W, x, ldx, y, yf, ldy, res, s);
+    case 5: return launch_int_t<BITS, 5>(W, x, ldx, y, yf, ldy, res, s);
+    case 6: return launch_int_t<BITS, 6>(W, x, ldx, y, yf, ldy, res, s);
+    case 7: return launch_int_t<BITS, 7>(W, x, ldx, y, yf, ldy, res, s);
+    default: return launch_int_t<BITS, 8>(W, x, ldx, y, yf, ldy, res, s);
   }
 }
 
@@ -230,18 +232,19 @@ static int qgemv_max_tokens(int cols, int bits) {
 }
 
 cudaError_t launch_qgemv(const QMat& W, const uint16_t* x, int batch, uint16_t* y, float* yf, int variant,
-                         cudaStream_t s) {
+                         cudaStream_t s, const uint16_t* res) {
   const int tmax = variant == 0 ? qgemv_max_tokens(W.cols, W.bits) : 8;
-  if (tmax < 1) return cudaErrorInvalidValue;
+  if (tmax < 1 || (res && variant != 0)) return cudaErrorInvalidValue;
   for (int t0 = 0; t0 < batch; t0 += tmax) {
     int T = batch - t0 < tmax ? batch - t0 : tmax;
     const uint16_t* xt = x + (size_t)t0 * W.cols;
     uint16_t* yt = y ? y + (size_t)t0 * W.rows : nullptr;
     float* yft = yf ? yf + (size_t)t0 * W.rows : nullptr;
+    const uint16_t* rt = res ? res + (size_t)t0 * W.rows : nullptr;
     cudaError_t e;
     if (variant == 0) {
-      e = W.bits == 4 ? launch_int_bits<4>(W, xt, W.cols, yt, yft, W.rows, T, s)
-                      : launch_int_bits<2>(W, xt, W.cols, yt, yft, W.rows, T, s);
+      e = W.bits == 4 ? launch_int_bits<4>(W, xt, W.cols, yt, yft, W.rows, rt, T, s)
+                      : launch_int_bits<2>(W, xt, W.cols, yt, yft, W.rows, rt, T, s);
     } else {
       RowGeo rg = row_geo(W.cols, W.bits);
       int rows_per_cta = kGemvWarps * rg.RPP;

@@ -102,8 +102,10 @@ struct Ctrl {
 static_assert(sizeof(Ctrl) == 256, "control block is 256 bytes");
 
 size_t qgemv_int_smem(int cols, int bits, int T);
+// res (nullable, variant 0): bf16 [batch][rows] added to each fp32 row sum
+// before the outputs are written.
 cudaError_t launch_qgemv(const QMat& W, const uint16_t* x, int batch, uint16_t* y, float* yf, int variant,
-                         cudaStream_t s);
+                         cudaStream_t s, const uint16_t* res = nullptr);
 
 // Bytes at the start of a layer workspace that must be zero before a call:
 // control block and tagged logits (api.cu).
@@ -183,6 +185,8 @@ cudaError_t launch_combine(const float* Y, const float* w, const float* gamma, i
 
 cudaError_t launch_rmsnorm(const float* h, const uint16_t* rho, int batch, int d, float eps, uint16_t* a,
                            cudaStream_t s);
+cudaError_t launch_rmsnorm_bf16(const uint16_t* x, const uint16_t* rho, int batch, int d, float eps, uint16_t* a,
+                                cudaStream_t s);
 cudaError_t launch_residual_add(float* h, const float* delta, long long n, cudaStream_t s);
 cudaError_t launch_widen(const uint16_t* x, float* h, int n, cudaStream_t s);
 
@@ -204,19 +208,7 @@ ExpertSet slot_expert_set(const ExpertSet& pool, const SlotGeo& g, void* slots);
 
 int num_sms();
 
-// A chain of dependent group-quantized GEMVs in one persistent launch (chain.cu).
+// Longest projection chain of bgq_gemv_chain.
 constexpr int kMaxChain = 8;
-struct ChainStep {
-  const uint32_t* q;
-  const uint32_t* sb;  // (scale, bias) bf16 pairs, one 32-bit word per group
-  int rows, cols;
-};
-size_t chain_smem_bytes(int max_cols, int bits, int T);
-// steps[0..n), all of `bits`; x bf16 [batch][steps[0].cols], batch 1..8;
-// buf0/buf1 bf16 [batch][ldb] (ldb >= the rows of every inner step); *counter
-// zero at launch.
-cudaError_t launch_chain(const ChainStep* steps, int n, int bits, const uint16_t* x, int batch, int norm,
-                         const uint16_t* rho, float eps, int residual, uint16_t* out, float* out_f32, Ctrl* ctrl,
-                         int* counter, uint16_t* buf0, uint16_t* buf1, int ldb, long long timeout_ns, cudaStream_t s);
 
 }  // namespace bgq

@@ -139,7 +139,7 @@ typedef struct bgq_moe_layer {
 /* Human-readable name of a status code (static string). */
 const char* bgq_status_string(int32_t status);
 
-/* ABI version of this header (major*100 + minor): 102. */
+/* ABI version of this header (major*100 + minor): 103. */
 int32_t bgq_abi_version(void);
 
 /* Overlapped launch of the GEMVs (q4_gemv, q2_gemv, bgq_qgemv_variant, q8_gemv):
@@ -291,11 +291,11 @@ int32_t bgq_rmsnorm(const float* h, const uint16_t* rho, int32_t batch, int32_t 
 /* h[b] += delta[b] (fp32 residual add between layers), n = batch*d elements. */
 int32_t bgq_residual_add(float* h, const float* delta, int64_t n, void* stream);
 
-/* A chain of dependent group-quantized GEMVs in one persistent launch: the
- * decoder's projections around the MoE block (Flash-MoE page, section
- * "架构设计：SSD当显存用": attention input projections in CMD1, o_proj + norm
- * in CMD2; the attention mixing itself is not part of this library, so each
- * projection feeds the next):
+/* A chain of dependent group-quantized GEMVs: the decoder's projections
+ * around the MoE block (Flash-MoE page, section "架构设计：SSD当显存用":
+ * attention input projections in CMD1, o_proj + norm in CMD2; the attention
+ * mixing itself is not part of this library, so each projection feeds the
+ * next):
  *   v_0 = norm ? bf16(rmsnorm(x) * rho) : x        (rho NULL => 1; as bgq_rmsnorm)
  *   v_i = bf16(W_i v_{i-1}),  i = 1..n-1            (as q4_gemv / q2_gemv)
  *   out_f32 = W_n v_{n-1} (+ x when residual), out = bf16(out_f32)
@@ -303,16 +303,17 @@ int32_t bgq_residual_add(float* h, const float* delta, int64_t n, void* stream);
  * group 64; W[0].cols = d, W[i].cols = W[i-1].rows; residual needs
  * W[n-1].rows = d. x: bf16 [batch][d], 16-byte aligned; out (bf16) and
  * out_f32 (fp32), [batch][W[n-1].rows], nullable but not both, 16-byte
- * aligned. 1 <= batch <= 8, and batch staged inputs of the widest W[i].cols
- * must fit in 227 KB of shared memory (3 bytes per value + 8 per 32 values;
- * 8 tokens at 8192 columns) else BGQ_ERR_UNSUPPORTED. eps > 0 when norm.
+ * aligned. 1 <= batch <= 8; one staged input of the widest W[i].cols must
+ * fit in 227 KB of shared memory (3 bytes per value + 8 per 32 values: up to
+ * about 71,000 columns) else BGQ_ERR_UNSUPPORTED. eps > 0 when norm.
  * ws: bgq_gemv_chain_workspace_bytes(W, n, batch) bytes, 256-byte aligned,
- * written before read (its first 512 bytes are cleared on `stream` by each
- * call). The launch is cooperative (one CTA per SM); the steps are ordered by
- * a bounded grid-wide wait: on expiry BGQ_ERR_TIMEOUT is left in the
- * workspace status word (bgq_read_device_status). The result has the bits of
- * the separate calls (bgq_rmsnorm on the widened x, then q4_gemv per step,
- * the last step's fp32 sum plus x). */
+ * written before read (the intermediate vectors). The steps run as
+ * programmatic dependent launches of the RMSNorm and GEMV kernels on
+ * `stream` (each step's weight loads start while the previous step
+ * finishes; the residual is added in the last GEMV). The result has the bits
+ * of the separate calls (bgq_rmsnorm on the widened x, then q4_gemv per
+ * step, the last step's fp32 sum plus x). As for every GEMV, the weights
+ * must not be written by the kernel just before the call on its stream. */
 size_t bgq_gemv_chain_workspace_bytes(const bgq_qmatrix* W, int32_t n, int32_t batch);
 int32_t bgq_gemv_chain(const bgq_qmatrix* W, int32_t n, const uint16_t* x, int32_t batch, int32_t norm,
                        const uint16_t* rho, float eps, int32_t residual, uint16_t* out, float* out_f32, void* ws,

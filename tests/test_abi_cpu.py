@@ -72,7 +72,7 @@ def test_q8_gemv_validation(lib):
 def test_status_strings(lib):
     assert lib.status_string(0) == "ok"
     assert "workspace" in lib.status_string(5)
-    assert lib.load().bgq_abi_version() == 102
+    assert lib.load().bgq_abi_version() == 103
 
 
 FAKE = 0x10000000  # 256-byte aligned, never dereferenced: validation fails first
@@ -270,7 +270,11 @@ def test_gemv_chain_validation(lib):
     # residual needs the last step back at d rows
     wide = chain(qmat(lib, rows=2048, cols=4096))
     assert call(wide, 1, nbytes=L.bgq_gemv_chain_workspace_bytes(wide, 1, 1)) == lib.ERR_INVALID_ARG
-    # eight staged inputs of 12288 columns do not fit in shared memory; two do
+    # each step's GEMV stages as many inputs per launch as fit in shared
+    # memory, so 12288 columns are taken at any batch; a row so wide that not
+    # even one staged input fits is not
     qkv = chain(qmat(lib, rows=12288, cols=4096), qmat(lib, rows=4096, cols=12288))
-    assert call(qkv, 2, batch=8, nbytes=1 << 30) == lib.ERR_UNSUPPORTED
-    assert L.bgq_gemv_chain_workspace_bytes(qkv, 2, 2) > 0
+    assert L.bgq_gemv_chain_workspace_bytes(qkv, 2, 8) > 0
+    huge = chain(qmat(lib, rows=4096, cols=81920))
+    assert call(huge, 1, batch=1, nbytes=1 << 30) == lib.ERR_UNSUPPORTED
+    assert L.bgq_gemv_chain_workspace_bytes(huge, 1, 1) == 0

@@ -1,5 +1,5 @@
 """GPU parity of bgq_gemv_chain: the decoder's projections around the MoE
-block as a chain of dependent group-quantized GEMVs in one persistent launch.
+block as a chain of dependent group-quantized GEMVs (dependent launches).
 
 Against the fp64 oracle (oracle.gemv_chain, which rounds the inner vectors to
 bf16 as the chain does): bf16 outputs within the workload tolerance
